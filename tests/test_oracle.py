@@ -1,0 +1,358 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself -- closed forms, exact integer sums, library routines, invariants and the
+figures the pages print. No GPU needed."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from recsys_sparse_embedding_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers
+def int_tables(rng, F, rows, D):
+    """Integer-valued fp32 tables (|v| <= 64): every sum below is exact."""
+    return [rng.integers(-64, 65, size=(rows, D)).astype(np.float32) for _ in range(F)]
+
+
+def kjt_from_bags(bags, F, B):
+    """bags[f][b] = list of ids -> key-major lengths / values."""
+    lengths = np.array([len(bags[f][b]) for f in range(F) for b in range(B)], np.int32)
+    values = np.array([i for f in range(F) for b in range(B) for i in bags[f][b]], np.int64)
+    return lengths, values
+
+
+def select_mlp(K1, col, scale, bias=10.0):
+    """MLP whose logit is scale * (x[col] + bias) while x[col] + bias > 0:
+    W1 row 0 picks x[col], W2 row 0 picks h1[0], w3 picks h2[0]."""
+    W1 = np.zeros((256, K1), np.float32)
+    W1[0, col] = 1.0
+    b1 = np.zeros(256, np.float32)
+    b1[0] = bias
+    W2 = np.zeros((64, 256), np.float32)
+    W2[0, 0] = 1.0
+    b2 = np.zeros(64, np.float32)
+    w3 = np.zeros(64, np.float32)
+    w3[0] = scale
+    b3 = np.zeros(1, np.float32)
+    return W1, b1, W2, b2, w3, b3
+
+
+def run_din(tables, lengths, values, B, seq_ids, seq_lengths, mlp, max_len=100,
+            q_feat=(0, 1, 2), seq_table=(0, 1, 2), **kw):
+    return oracle.din(tables, values, lengths, B, q_feat, seq_table, seq_ids, seq_lengths,
+                      max_len, *mlp, **kw)
+
+
+# ---------------------------------------------------------------- offsets
+def test_offsets_all_ones_is_iota():
+    n = 1000
+    off, flags = oracle.offsets(np.ones(n, np.int32))
+    assert flags == 0
+    assert np.array_equal(off, np.arange(n + 1))
+
+
+def test_offsets_hand_case_and_negative_flag():
+    off, flags = oracle.offsets(np.array([2, 0, 3, 1], np.int32))
+    assert list(off) == [0, 2, 2, 5, 6] and flags == 0
+    off, flags = oracle.offsets(np.array([2, -4, 3], np.int32))
+    assert list(off) == [0, 2, 2, 5] and flags == oracle.FLAG_NEG_LENGTH
+
+
+# ---------------------------------------------------------------- pooling
+def test_pool_single_id_bag_is_the_row():
+    rng = np.random.default_rng(1)
+    F, B, D = 4, 9, 16
+    tables = [rng.standard_normal((50, D)).astype(np.float32) for _ in range(F)]
+    ids = rng.integers(0, 50, size=(F, B))
+    bags = [[[int(ids[f, b])] for b in range(B)] for f in range(F)]
+    lengths, values = kjt_from_bags(bags, F, B)
+    pooled, flags = oracle.emb_bag_pool(tables, values, lengths, B)
+    assert flags == 0
+    for b in range(B):
+        for f in range(F):
+            assert np.array_equal(pooled[b, f * D:(f + 1) * D], tables[f][ids[f, b]])
+
+
+def test_pool_integer_tables_exact_and_permutation_invariant():
+    rng = np.random.default_rng(2)
+    F, B, D = 3, 17, 16
+    tables = int_tables(rng, F, 40, D)
+    bags = [[list(rng.integers(0, 40, size=rng.integers(0, 9))) for _ in range(B)]
+            for _ in range(F)]
+    lengths, values = kjt_from_bags(bags, F, B)
+    pooled, flags = oracle.emb_bag_pool(tables, values, lengths, B)
+    assert flags == 0
+    for f in range(F):
+        for b in range(B):
+            want = np.zeros(D, np.int64)
+            for i in bags[f][b]:
+                want += tables[f][i].astype(np.int64)
+            assert np.array_equal(pooled[b, f * D:(f + 1) * D], want.astype(np.float32))
+    perm = [[list(rng.permutation(bags[f][b])) for b in range(B)] for f in range(F)]
+    l2, v2 = kjt_from_bags(perm, F, B)
+    pooled2, _ = oracle.emb_bag_pool(tables, v2, l2, B)
+    assert np.array_equal(pooled, pooled2)
+
+
+def test_pool_empty_bag_zero_and_out_of_range_flag():
+    rng = np.random.default_rng(3)
+    D = 16
+    tables = [rng.standard_normal((10, D)).astype(np.float32) for _ in range(2)]
+    bags = [[[], [3, 10]], [[-1], [2]]]    # empty bag; id 10 and -1 out of range
+    lengths, values = kjt_from_bags(bags, 2, 2)
+    pooled, flags = oracle.emb_bag_pool(tables, values, lengths, 2)
+    assert flags == oracle.FLAG_ID_RANGE
+    assert np.array_equal(pooled[0, :D], np.zeros(D, np.float32))
+    assert np.array_equal(pooled[1, :D], tables[0][3])
+    assert np.array_equal(pooled[0, D:], np.zeros(D, np.float32))
+    assert np.array_equal(pooled[1, D:], tables[1][2])
+
+
+def test_pool_fp32_sum_within_rounding_bound_of_exact_sum():
+    """fp32 left-to-right sum of n terms is within n*eps*sum|terms| of the
+    exact sum (here n <= 8, so well inside 1e-6 * sum|terms|)."""
+    rng = np.random.default_rng(4)
+    F, B, D = 2, 200, 16
+    tables = [rng.standard_normal((100, D)).astype(np.float32) for _ in range(F)]
+    bags = [[list(rng.integers(0, 100, size=rng.integers(1, 9))) for _ in range(B)]
+            for _ in range(F)]
+    lengths, values = kjt_from_bags(bags, F, B)
+    pooled, _ = oracle.emb_bag_pool(tables, values, lengths, B)
+    for f in range(F):
+        for b in range(B):
+            rows = tables[f][bags[f][b]].astype(np.float64)
+            exact = rows.sum(0)
+            bound = 1e-6 * np.abs(rows).sum(0)
+            assert np.all(np.abs(pooled[b, f * D:(f + 1) * D] - exact) <= bound)
+
+
+def test_pool_bf16_table_widens_exactly():
+    rng = np.random.default_rng(5)
+    D = 64
+    t = synth.f32_to_bf16_bits(rng.standard_normal((30, D)).astype(np.float32))
+    bags = [[[7], [29, 0]]]
+    lengths, values = kjt_from_bags(bags, 1, 2)
+    pooled, flags = oracle.emb_bag_pool([t], values, lengths, 2)
+    assert flags == 0
+    rows = synth.bf16_bits_to_f32(t)
+    assert np.array_equal(pooled[0], rows[7])
+    assert np.array_equal(pooled[1], (rows[29] + rows[0]).astype(np.float32))
+
+
+# ---------------------------------------------------------------- MLP
+def test_attn_mlp_matches_library_gemm():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((37, 192))
+    b = synth.generate("tiny", seed=3, nonzero_bias=True)
+    z = oracle.attn_mlp(x, b.W1, b.b1, b.W2, b.b2, b.w3, b.b3)
+    W1, W2 = b.W1.astype(np.float64), b.W2.astype(np.float64)
+    h1 = np.maximum(x @ W1.T + b.b1, 0)
+    h2 = np.maximum(h1 @ W2.T + b.b2, 0)
+    want = h2 @ b.w3.astype(np.float64) + b.b3[0]
+    assert np.allclose(z, want, rtol=1e-12, atol=1e-12)
+
+
+def test_attn_mlp_selection_closed_form():
+    x = np.zeros((3, 192))
+    x[:, 77] = [0.5, -2.0, 3.25]
+    mlp = select_mlp(192, 77, scale=-1.5, bias=0.0)
+    z = oracle.attn_mlp(x, *mlp)
+    assert np.array_equal(z, -1.5 * np.maximum(x[:, 77], 0))
+
+
+def test_attn_mlp_bf16_rounds_h1_to_nearest_even():
+    # h1 = round_bf16(x + 0): 1 + 2^-8 is a tie -> 1; 1 + 3*2^-9 -> 1 + 2^-7
+    x = np.zeros((2, 192))
+    x[:, 5] = [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -9]
+    mlp = select_mlp(192, 5, scale=1.0, bias=0.0)
+    z = oracle.attn_mlp(x, *mlp, bf16_mlp=True)
+    assert list(z) == [1.0, 1 + 2.0 ** -7]
+
+
+# ---------------------------------------------------------------- DIN
+def tiny_din_inputs(rng, L_list, D=16, rows=20, positive=False):
+    F, B = 3, len(L_list)
+    lo = 0.05 if positive else -1.0
+    tables = [rng.uniform(lo, 1.0, size=(rows, D)).astype(np.float32) for _ in range(F)]
+    bags = [[[int(rng.integers(0, rows))] for _ in range(B)] for _ in range(F)]
+    lengths, values = kjt_from_bags(bags, F, B)
+    seq_lengths = np.array(L_list, np.int32)
+    P = int(seq_lengths.sum())
+    seq_ids = rng.integers(0, rows, size=(3, P)).astype(np.int64)
+    return tables, lengths, values, seq_ids, seq_lengths, bags
+
+
+def seq_rows(tables, seq_ids, seq_lengths, b, D=16):
+    off = int(seq_lengths[:b].sum())
+    L = int(seq_lengths[b])
+    return np.stack([np.concatenate([tables[k][seq_ids[k, off + t]] for k in range(3)])
+                     for t in range(L)]).astype(np.float64) if L else np.zeros((0, 3 * D))
+
+
+def test_din_single_position_returns_that_row():
+    rng = np.random.default_rng(7)
+    t, l, v, sid, sl, _ = tiny_din_inputs(rng, [1, 1, 1])
+    mlp = synth.generate("tiny", seed=1, nonzero_bias=True)
+    out, flags = run_din(t, l, v, 3, sid, sl, (mlp.W1, mlp.b1, mlp.W2, mlp.b2, mlp.w3, mlp.b3))
+    assert flags == 0
+    for b in range(3):
+        assert np.array_equal(out[b], seq_rows(t, sid, sl, b)[0])
+
+
+def test_din_zero_w3_gives_mean_and_empty_gives_zero():
+    rng = np.random.default_rng(8)
+    t, l, v, sid, sl, _ = tiny_din_inputs(rng, [4, 0, 7])
+    g = synth.generate("tiny", seed=2, nonzero_bias=True)
+    mlp = (g.W1, g.b1, g.W2, g.b2, np.zeros(64, np.float32), g.b3)
+    out, _ = run_din(t, l, v, 3, sid, sl, mlp)
+    assert np.allclose(out[0], seq_rows(t, sid, sl, 0).mean(0), rtol=0, atol=1e-15)
+    assert np.array_equal(out[1], np.zeros(48))
+    assert np.allclose(out[2], seq_rows(t, sid, sl, 2).mean(0), rtol=0, atol=1e-15)
+
+
+def test_din_identical_positions_return_the_row():
+    rng = np.random.default_rng(9)
+    t, l, v, sid, sl, _ = tiny_din_inputs(rng, [5])
+    sid[:, :] = sid[:, :1]
+    g = synth.generate("tiny", seed=4, nonzero_bias=True)
+    out, _ = run_din(t, l, v, 1, sid, sl, (g.W1, g.b1, g.W2, g.b2, g.w3, g.b3))
+    assert np.allclose(out[0], seq_rows(t, sid, sl, 0)[0], rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("part", [0, 1, 2, 3])
+def test_din_cat_order_two_positions_closed_form(part):
+    """The input is cat[q, s, q - s, q * s]; with an MLP that selects one column
+    of part `part`, two positions have softmax weight sigmoid(c*(x0 - x1))."""
+    rng = np.random.default_rng(10 + part)
+    t, l, v, sid, sl, bags = tiny_din_inputs(rng, [2], positive=True)
+    d = 5
+    c = 3.0
+    mlp = select_mlp(192, part * 48 + d, scale=c, bias=10.0)
+    out, flags = run_din(t, l, v, 1, sid, sl, mlp)
+    assert flags == 0
+    S = seq_rows(t, sid, sl, 0)
+    q = np.concatenate([t[k][bags[k][0][0]] for k in range(3)]).astype(np.float64)
+    xs = [q[d], S[:, d], q[d] - S[:, d], q[d] * S[:, d]][part]
+    xs = np.broadcast_to(xs, (2,))
+    a0 = 1.0 / (1.0 + math.exp(c * (xs[1] - xs[0])))
+    want = a0 * S[0] + (1 - a0) * S[1]
+    assert np.allclose(out[0], want, rtol=1e-13, atol=1e-15)
+
+
+def test_din_query_is_the_pooled_multi_hot_bag():
+    rng = np.random.default_rng(20)
+    D, rows = 16, 20
+    t = [rng.uniform(0.05, 1.0, size=(rows, D)).astype(np.float32) for _ in range(3)]
+    bags = [[[1, 4, 9]], [[2]], [[3, 3]]]
+    l, v = kjt_from_bags(bags, 3, 1)
+    sl = np.array([2], np.int32)
+    sid = rng.integers(0, rows, size=(3, 2)).astype(np.int64)
+    d, c = 16 + 7, 2.0             # a column of the cate (second) block of q * s
+    mlp = select_mlp(192, 3 * 48 + d, scale=c, bias=10.0)
+    out, _ = run_din(t, l, v, 1, sid, sl, mlp)
+    S = seq_rows(t, sid, sl, 0)
+    qd = float(t[1][2][7])
+    a0 = 1.0 / (1.0 + math.exp(c * qd * (S[1, d] - S[0, d])))
+    assert np.allclose(out[0], a0 * S[0] + (1 - a0) * S[1], rtol=1e-13, atol=1e-15)
+    # a multi-hot bag in the query: the q block of target 0 is the bag sum
+    d0 = 3
+    mlp = select_mlp(192, 3 * 48 + d0, scale=c, bias=10.0)
+    out, _ = run_din(t, l, v, 1, sid, sl, mlp)
+    q0 = float(np.float32(np.float32(t[0][1][3] + t[0][4][3]) + t[0][9][3]))
+    a0 = 1.0 / (1.0 + math.exp(c * q0 * (S[1, d0] - S[0, d0])))
+    assert np.allclose(out[0], a0 * S[0] + (1 - a0) * S[1], rtol=1e-13, atol=1e-15)
+
+
+def test_din_padded_equals_jagged_bitwise():
+    b = synth.generate("tiny", seed=5, nonzero_bias=True)
+    jag, f1 = oracle.din_batch(b)
+    pad, f2 = oracle.din_batch(b, padded=True)
+    assert f1 == f2 == 0
+    assert np.array_equal(jag, pad)
+    jag, _ = oracle.din_batch(b, bf16_mlp=True)
+    pad, _ = oracle.din_batch(b, padded=True, bf16_mlp=True)
+    assert np.array_equal(jag, pad)
+
+
+def test_din_weights_sum_to_one_and_permutation_invariance():
+    b = synth.generate("tiny", seed=6, nonzero_bias=True, peaked=True)
+    out, _, lg, wt = oracle.din_batch(b, want_logits=True)
+    L = np.minimum(b.seq_lengths, b.max_len)
+    for i in range(b.B):
+        if L[i] > 0:
+            assert abs(wt[i].sum() - 1.0) < 1e-12
+            assert np.all(wt[i, L[i]:] == 0)
+    # shuffle positions inside each sample
+    rng = np.random.default_rng(0)
+    off = np.concatenate([[0], np.cumsum(b.seq_lengths)])
+    sv = b.seq_values.copy()
+    for i in range(b.B):
+        p = rng.permutation(b.seq_lengths[i]) + off[i]
+        sv[:, off[i]:off[i + 1]] = sv[:, p]
+    b2 = synth.Batch(**{**b.__dict__, "seq_values": sv})
+    out2, _ = oracle.din_batch(b2)
+    assert np.allclose(out, out2, rtol=0, atol=1e-14)
+
+
+def test_din_peaked_softmax_picks_the_argmax_row():
+    rng = np.random.default_rng(21)
+    t, l, v, sid, sl, _ = tiny_din_inputs(rng, [6], positive=True)
+    mlp = select_mlp(192, 48 + 2, scale=400.0, bias=10.0)   # z = 400 * s[2]
+    out, _ = run_din(t, l, v, 1, sid, sl, mlp)
+    S = seq_rows(t, sid, sl, 0)
+    top = np.sort(S[:, 2])
+    if top[-1] - top[-2] > 0.05:     # exp(-400*0.05) ~ 2e-9
+        assert np.allclose(out[0], S[np.argmax(S[:, 2])], rtol=0, atol=1e-7)
+
+
+def test_din_truncation_and_bad_ids():
+    rng = np.random.default_rng(22)
+    t, l, v, sid, sl, _ = tiny_din_inputs(rng, [5, 3])
+    g = synth.generate("tiny", seed=7, nonzero_bias=True)
+    mlp = (g.W1, g.b1, g.W2, g.b2, g.w3, g.b3)
+    full, _ = run_din(t, l, v, 2, sid, sl, mlp, max_len=100)
+    # max_len 3: sample 0 keeps its first 3 positions -- equal to a sample of length 3
+    trunc, flags = run_din(t, l, v, 2, sid, sl, mlp, max_len=3)
+    assert flags & oracle.FLAG_SEQ_TRUNC
+    sid3 = np.concatenate([sid[:, :3], sid[:, 5:]], axis=1)
+    ref, _ = run_din(t, l, v, 2, sid3, np.array([3, 3], np.int32), mlp, max_len=3)
+    assert np.array_equal(trunc, ref)
+    assert np.array_equal(trunc[1], full[1])
+    # an out-of-range seq id gives a zero sub-row and the range flag
+    sid_bad = sid.copy()
+    sid_bad[1, 5] = 10 ** 9
+    bad, flags = run_din(t, l, v, 2, sid_bad, sl, mlp)
+    assert flags & oracle.FLAG_ID_RANGE
+    assert np.array_equal(bad[0], full[0])
+
+
+# ---------------------------------------------------------------- shapes
+def test_workload_shapes_match_the_pages_figures():
+    g = json.load(open(os.path.join(GOLDEN, "taobao_shapes.json")))
+    rows = synth.TAOBAO_ROWS
+    assert sum(rows[:15]) == g["id_feature_vocab_total"]["value"]
+    mb = g["id_feature_vocab_total"]["value"] * g["embedding_dim"]["value"] * 4 / 2 ** 20
+    assert round(mb) == g["embedding_weight_megabytes"]["value"]
+    wl = synth.WORKLOADS["taobao"]
+    assert wl.B == g["batch_size"]["value"] and wl.D == g["embedding_dim"]["value"]
+    assert wl.max_len == g["sequence_cap"]["value"]
+    assert wl.B * 5 * 3 * wl.D == g["seq_elements_real"]["value"]
+    assert wl.B * wl.max_len * 3 * wl.D == g["seq_elements_padded"]["value"]
+    assert wl.K1 == g["attention_input_width"]["value"]
+    assert wl.Q == g["query_width"]["value"]
+    assert [synth.ATTN_N1, synth.ATTN_N2] == g["attn_mlp_hidden"]["value"]
+
+
+def test_generator_is_seeded_and_shaped():
+    a = synth.generate("tiny", seed=11)
+    b = synth.generate("tiny", seed=11)
+    assert np.array_equal(a.values, b.values) and np.array_equal(a.seq_values, b.seq_values)
+    assert a.lengths.size == 16 * 64 and a.values.size == a.lengths.sum()
+    assert a.seq_values.shape == (3, a.seq_lengths.sum())
+    assert a.seq_lengths.min() >= 0 and a.seq_lengths.max() <= 10
