@@ -1,0 +1,397 @@
+"""Throughput of the MultiTowerDIN sparse forward (EmbeddingBag pooling +
+padding-free DIN target attention) on synthetic Taobao-shaped batches.
+
+One step = one din_sparse_fwd call (KJT offsets, pooled gather over 16 tables,
+query, jagged sequence gather, attention MLP on tensor cores, masked softmax,
+weighted sum) over one batch of B=8192 samples already resident in HBM.
+Between timed steps L2 is flushed by writing a buffer larger than L2; each
+step is timed by its own pair of CUDA events, so the flush is not counted.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N>1 runs independent replicas, one per rank (launched by torch.distributed.run);
+the path has no cross-sample exchange, so there is no collective in a step.
+The reference arm (--impl reference) is the CPU oracle, timed on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "taobao"
+METRIC = "samples/sec for sparse fwd (EmbBag+jagged DIN) at B=8192; % of HBM/tensor roofline"
+UNIT = "samples/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "launch.cuh", "fwd_attn_tc.cu"]
+
+
+def workload_desc(B):
+    return ("taobao-shaped MultiTowerDIN sparse fwd: B=%d, 16 fp32 dim-16 tables "
+            "(201 MB, page-1 bucket sizes), Zipf(1.1) ids, 1 id/feature, seq len geometric "
+            "mean 5 cap 100, attn MLP 192-256-64-1 bf16 tensor cores" % B)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    """Measured HBM GB/s and bf16 TFLOP/s (burst, sustained) or the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, pre + k.lower() + ".")
+                elif isinstance(x, (int, float)):
+                    flat[pre[:-1]] = float(x)
+            walk(d)
+            hbm = next((v for k, v in flat.items() if "hbm" in k and "gb" in k), None)
+            tfs = next((v for k, v in flat.items() if "bf16" in k and "tflop" in k
+                        and "sustain" not in k), None)
+            tfs_s = next((v for k, v in flat.items() if "bf16" in k and "sustain" in k), None)
+            if hbm and tfs:
+                return hbm, tfs, tfs_s or tfs, "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def algorithmic_work(batch):
+    """Bytes and FLOPs the method must move / do for one batch (fp32 D=16):
+    deep: 8 B per id + 4 B per bag length + 64 B per row + 1024 B output row;
+    DIN: 24 B of ids + 192 B of rows per valid position, 4 B length, 192 B output;
+    MLP: 2*(192*256 + 256*64 + 64) FLOPs per valid position. Padded positions
+    the method avoids are not counted; MLP weights (131 KB) are not counted."""
+    D = batch.D
+    es = 2 if batch.wl.dtype == "bf16" else 4
+    n_ids = int(batch.values.size)
+    F, B = batch.F, batch.B
+    L = np.minimum(np.maximum(batch.seq_lengths, 0), batch.max_len).astype(np.int64)
+    P = int(L.sum())
+    deep = 8 * n_ids + 4 * F * B + D * es * n_ids + 4 * F * D * B
+    din = 24 * P + 3 * D * es * P + 4 * B + 4 * 3 * D * B
+    K1 = 12 * D
+    flops = 2 * (K1 * 256 + 256 * 64 + 64) * P
+    return deep + din, flops, P
+
+
+def traffic_record():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+        if rec.get("kernel_hash") != kernel_hash():
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "recsys_sparse_embedding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_rate(batch, samples_per_pass, passes, threads):
+    """The oracle as it stands, split over host threads by sample chunks."""
+    import concurrent.futures as cf
+    import oracle
+    chunks = np.array_split(np.arange(samples_per_pass, dtype=np.int32) % batch.B, threads)
+    oracle.lib()
+
+    def work(ch):
+        if ch.size:
+            oracle.pool_batch(batch, ch)
+            oracle.din_batch(batch, ch)
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for _ in range(passes):
+            list(ex.map(work, chunks))
+    dt = time.perf_counter() - t0
+    return samples_per_pass * passes / dt, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from recsys_sparse_embedding_gb300 import synth
+    batch = synth.generate(WORKLOAD, seed=0)
+    threads = os.cpu_count() or 1
+    per_step = 1024
+    for _ in range(args.warmup):
+        cpu_oracle_rate(batch, 64, 1, threads)
+    rate, dt = cpu_oracle_rate(batch, per_step, args.steps, threads)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(batch.B), "B": batch.B,
+                   "reference": "CPU oracle (plain C, fp64 attention), %d host threads" % threads},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "%d samples of the B=%d batch per step" % (per_step, batch.B)},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-sample", type=int, default=8192)
+    ap.add_argument("--cpu-passes", type=int, default=3)
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from recsys_sparse_embedding_gb300 import binding, synth
+    from recsys_sparse_embedding_gb300.device_batch import to_device
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    batch = synth.generate(WORKLOAD, seed=rank)
+    db = to_device(batch, dev)
+    B, D, F = db.B, db.D, db.F
+    mode = binding.DSF_MODE_BF16_TC if args.mode == "bf16" else binding.DSF_MODE_FP32
+    mlp = db.mlp(mode)
+    wsp = binding.Workspace(B, D, device=dev)
+    wsp.prepare(mlp)
+    pooled = torch.empty(B, F * D, device=dev)
+    din = torch.empty(B, 3 * D, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        binding.din_sparse_fwd(db.tables, db.values, db.lengths, db.seq_values, db.seq_lengths,
+                               db.max_len, db.q_feat, db.seq_table, B, mlp, pooled, din, wsp,
+                               status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        st = int(status.item())
+        if st:
+            raise RuntimeError("device status 0x%x during warm-up" % st)
+        graph = None
+        if not args.no_graph:
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    step()
+                g.replay()
+                stream.synchronize()
+                graph = g
+            except Exception as e:  # capture unsupported: time direct launches
+                print("graph capture unavailable: %s" % e, file=sys.stderr)
+                graph = None
+                torch.cuda.synchronize()
+        run = graph.replay if graph is not None else step
+
+        K = args.steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            for i in range(K):
+                flush.fill_(float(i & 7))
+                ev[i][0].record(stream)
+                run()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        times_ms = [a.elapsed_time(b) for a, b in ev]
+        st = int(status.item())
+        total_ms = float(sum(times_ms))
+        if ws > 1:
+            t = torch.tensor([total_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+        value = B * K * ws / (total_ms / 1e3)
+        ms_step = total_ms / K
+
+        # end to end: pinned host inputs -> device, the C-ABI call, results -> host
+        h_in = [x.cpu().pin_memory() for x in (db.values, db.lengths, db.seq_values, db.seq_lengths)]
+        d_in = [torch.empty_like(x, device=dev) for x in h_in]
+        h_out = [torch.empty(pooled.shape, dtype=pooled.dtype).pin_memory(),
+                 torch.empty(din.shape, dtype=din.dtype).pin_memory()]
+        h2d = sum(x.numel() * x.element_size() for x in h_in)
+        d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            binding.din_sparse_fwd(db.tables, d_in[0], d_in[1], d_in[2], d_in[3], db.max_len,
+                                   db.q_feat, db.seq_table, B, mlp, pooled, din, wsp,
+                                   status=status, stream=stream)
+            h_out[0].copy_(pooled, non_blocking=True)
+            h_out[1].copy_(din, non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        E = args.e2e_steps
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(E)]
+        for i in range(E):
+            flush.fill_(float(i & 7))
+            eev[i][0].record(stream)
+            e2e_step()
+            eev[i][1].record(stream)
+        stream.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+        e2e_value = B * E / (e2e_ms / 1e3)
+
+    # roofline of the fused kernel (the only kernel of a step)
+    nbytes, flops, P = algorithmic_work(batch)
+    hbm, tfs, tfs_s, src = peaks()
+    t_s = ms_step / 1e3
+    ach_gbs = nbytes / t_s / 1e9
+    ach_tfs = flops / t_s / 1e12
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = flops / (tfs_s * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    roof = {"bound": bound,
+            "achieved": ach_gbs if bound == "hbm" else ach_tfs,
+            "peak": hbm if bound == "hbm" else tfs_s,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": (ach_gbs / hbm) if bound == "hbm" else (ach_tfs / tfs_s),
+            "traffic": traffic_record(),
+            "peak_source": src,
+            "algorithmic_bytes_per_launch": nbytes,
+            "flops_per_launch": flops,
+            "tensor_achieved_tflops": ach_tfs,
+            "tensor_frac": ach_tfs / tfs_s,
+            "combined_frac": max(t_hbm, t_tc) / t_s,
+            "valid_positions": P}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.skip_cpu:
+        threads = os.cpu_count() or 1
+        rate, dt = cpu_oracle_rate(batch, args.cpu_sample, args.cpu_passes, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "%d passes over %d samples of the B=%d batch (%.1f s wall)"
+               % (args.cpu_passes, args.cpu_sample, B, dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp32+bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(B), "B": B, "mode": args.mode,
+                       "l2": "flushed between steps (512 MB write, not timed)",
+                       "graph": graph is not None, "parallelism": "replicas" if ws > 1 else "1gpu"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "status": st,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

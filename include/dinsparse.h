@@ -1,0 +1,170 @@
+/*
+ * dinsparse.h -- C ABI of the GB300 (sm_103a) MultiTowerDIN sparse forward.
+ *
+ * The path computes, for a batch of B samples:
+ *   (a) EmbeddingBag sum pooling of a KeyedJaggedTensor over F tables:
+ *       pooled[b, f*D:(f+1)*D] = sum of table_f rows over bag (f, b).
+ *       ("MultiTowerDIN: current state analysis", section 3: one [num_buckets, 16]
+ *       table per id feature, sum-pooled lookup; section 2: SparseData(values,
+ *       lengths) becomes a KeyedJaggedTensor.)
+ *   (b) Padding-free DIN target attention:
+ *       q_b    = cat of the pooled bags of the three target features
+ *                (adgroup_id / cate_id / brand; section 1 feature groups),
+ *       s_b,t  = cat of the three sequence sub-feature rows at position t,
+ *                read from the same tables ("MultiTowerDIN: integrating
+ *                DynamicEmb", section 2.4: shared embedding tables),
+ *       x      = cat[q, s, q - s, q * s]          (section 4.2 code block),
+ *       z      = w3 . ReLU(W2 ReLU(W1 x + b1) + b2) + b3
+ *                (attn_mlp hidden [256, 64], then a linear to 1; section 4.2),
+ *       a      = softmax of z over the valid positions t < L_b only
+ *                (section 4.2 mask + softmax; the padding to max_len that the
+ *                pages' flow builds is never materialised here),
+ *       din[b] = sum_t a_t s_b,t                 (section 4.4 weighted sum).
+ *
+ * Conventions for every entry point:
+ *   - All pointers named *_dev or documented "device" are device pointers
+ *     (CUDA global memory); all others are host pointers. Every device buffer
+ *     is allocated and freed by the caller; the library never allocates.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on it. The return value covers argument checks and
+ *     launch errors only; data errors found on the device are OR-ed into
+ *     *status_dev (DSF_FLAG_* bits), which the caller zeroes beforehand.
+ *   - One workspace may serve one stream at a time: two calls that overlap on
+ *     the GPU must not share a workspace (its grid-barrier counter and
+ *     per-block partial sums would race).
+ *   - Device data errors never fault or trap: an id outside [0, rows) or a
+ *     value index past the values array contributes a zero row; a negative
+ *     length counts as zero; a sequence longer than max_len keeps its first
+ *     max_len positions. Each sets its flag bit.
+ */
+#ifndef DINSPARSE_H
+#define DINSPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSF_MAX_TABLES 32
+
+/* Table element types. */
+enum { DSF_F32 = 0, DSF_BF16 = 1 };
+
+/* Attention-MLP arithmetic. BF16_TC: bf16 operands on tcgen05 tensor cores,
+ * fp32 accumulation (the pages' half-precision MLP, "integrating DynamicEmb",
+ * section 3.3). FP32: fp32 CUDA-core arithmetic, a check mode. */
+enum { DSF_MODE_BF16_TC = 0, DSF_MODE_FP32 = 1 };
+
+/* Return codes. */
+enum {
+  DSF_OK = 0,
+  DSF_EINVAL = 1,        /* null pointer, bad size, index out of range ... */
+  DSF_EUNSUPPORTED = 2,  /* a D / dtype / MLP shape this library does not build */
+  DSF_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  DSF_EWORKSPACE = 4     /* workspace missing, too small or misaligned */
+};
+
+/* Bits OR-ed into *status_dev by the kernels. */
+#define DSF_FLAG_ID_RANGE      0x01 /* an id outside [0, rows) (contributes zero) */
+#define DSF_FLAG_NEG_LENGTH    0x02 /* a negative length (counted as zero) */
+#define DSF_FLAG_SEQ_TRUNC     0x04 /* a sequence longer than max_len was cut */
+#define DSF_FLAG_COUNT         0x08 /* lengths sum differs from the values array size */
+#define DSF_FLAG_TIMEOUT       0x10 /* a device wait ran out (about 1 s); outputs invalid */
+#define DSF_FLAG_NOT_PREPARED  0x20 /* dsf_prepare_mlp was not run on this workspace */
+
+/* F embedding tables, one per KJT key, all with the same D and element type.
+ * table_ptrs[f]: device pointer to a row-major [table_rows[f], D] table,
+ * 16-byte aligned. Host arrays of length F. */
+typedef struct {
+  const void* const* table_ptrs;
+  const int64_t* table_rows;
+  int32_t F;      /* 1 .. DSF_MAX_TABLES */
+  int32_t D;      /* 16 or 64 */
+  int32_t dtype;  /* DSF_F32 or DSF_BF16 */
+} dsf_tables;
+
+/* KeyedJaggedTensor of the deep group (section 2: values + lengths).
+ * lengths_dev: int32 [F*B], key-major (the B bags of key 0, then key 1 ...);
+ * values_dev: int64 [n_values], the row ids of all bags in the same order. */
+typedef struct {
+  const int64_t* values_dev;
+  int64_t n_values;
+  const int32_t* lengths_dev;
+} dsf_kjt;
+
+/* The behaviour sequence (section 2: SequenceSparseData(values, seq_lengths)).
+ * values_dev: int64 [3, n_per_key], key-major: sub-feature k's ids are
+ * values_dev[k*n_per_key + j]; the positions of sample b are
+ * j = seq_off[b] .. seq_off[b] + L_b - 1 with seq_off the exclusive scan of
+ * lengths_dev (int32 [B]). max_len: the sequence cap (section 4.1, 100). */
+typedef struct {
+  const int64_t* values_dev;
+  int64_t n_per_key;
+  const int32_t* lengths_dev;
+  int32_t max_len;
+} dsf_seq;
+
+/* The attention MLP, device fp32, PyTorch Linear layout [out, in]:
+ * W1 [N1, K1], b1 [N1], W2 [N2, N1], b2 [N2], w3 [N2], b3 [1].
+ * K1 = 4 * 3 * D, N1 = 256, N2 = 64 (attn_mlp hidden_units [256, 64]). */
+typedef struct {
+  const float *W1, *b1, *W2, *b2, *w3, *b3;
+  int32_t K1, N1, N2;
+  int32_t mode; /* DSF_MODE_BF16_TC or DSF_MODE_FP32 */
+} dsf_mlp;
+
+/* Bytes of workspace needed for batch size B and embedding dim D (packed MLP
+ * weights, per-block partial sums, grid-barrier counter, query buffer).
+ * Returns 0 for unsupported D. */
+size_t dsf_workspace_bytes(int32_t B, int32_t D);
+
+/* Zeroes the workspace's barrier state. Call once after allocating a
+ * workspace (before any other call that uses it). Asynchronous on stream. */
+int dsf_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* Packs the MLP weights into the workspace: bf16 in the tensor-core operand
+ * layout (128-byte swizzled, K-major) and fp32 transposed copies for the check
+ * mode. Call again whenever W1 / W2 change; b1, b2, w3, b3 are read directly at
+ * each forward call. D selects the shape (K1 = 12 * D). */
+int dsf_prepare_mlp(const dsf_mlp* mlp, int32_t D, void* workspace_dev, size_t ws_bytes,
+                    void* stream);
+
+/* (a) EmbeddingBag sum pooling of all F keys.
+ * pooled_dev: fp32 [B, F*D], row-major; bag (f, b) goes to columns
+ * [f*D, (f+1)*D). Each bag is summed in fp32 in value order (an empty bag
+ * gives zeros). B >= 0; B = 0 is a no-op. */
+int emb_bag_pool(const dsf_tables* tables, const dsf_kjt* kjt, int32_t B, float* pooled_dev,
+                 void* workspace_dev, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/* (b) Jagged DIN target attention.
+ * q_feat[3]: KJT keys whose pooled bags form the query (target items).
+ * seq_table[3]: table index of each sequence sub-feature.
+ * din_dev: fp32 [B, 3*D]; a sample with no valid position gets zeros.
+ * logits_dev (nullable): fp32 [n_per_key]; receives z for every valid position
+ * j of the sequence values (positions past max_len are left untouched). */
+int din_jagged_attn(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
+                    const int32_t q_feat[3], const int32_t seq_table[3], int32_t B,
+                    const dsf_mlp* mlp, float* din_dev, float* logits_dev,
+                    void* workspace_dev, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/* (a) + (b) in one launch: pooled_dev as emb_bag_pool, din_dev as
+ * din_jagged_attn, with the query read from the pooled rows. */
+int din_sparse_fwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
+                   const int32_t q_feat[3], const int32_t seq_table[3], int32_t B,
+                   const dsf_mlp* mlp, float* pooled_dev, float* din_dev, float* logits_dev,
+                   void* workspace_dev, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/* Human-readable name of a return code. */
+const char* dsf_status_string(int code);
+
+/* Grid size (CTAs) the forward kernels use on the current device for this
+ * call shape; 0 if unsupported. For diagnostics and benchmarks. */
+int32_t dsf_grid_size(int32_t D, int32_t dtype, int32_t mode, int32_t with_attention);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DINSPARSE_H */

@@ -1,0 +1,225 @@
+"""ctypes binding of libdinsparse.so (include/dinsparse.h).
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels. PyTorch supplies device memory and the stream. There is no CPU
+fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdinsparse.so")
+
+DSF_F32, DSF_BF16 = 0, 1
+DSF_MODE_BF16_TC, DSF_MODE_FP32 = 0, 1
+DSF_OK, DSF_EINVAL, DSF_EUNSUPPORTED, DSF_ECUDA, DSF_EWORKSPACE = 0, 1, 2, 3, 4
+FLAG_ID_RANGE = 0x01
+FLAG_NEG_LENGTH = 0x02
+FLAG_SEQ_TRUNC = 0x04
+FLAG_COUNT = 0x08
+FLAG_TIMEOUT = 0x10
+FLAG_NOT_PREPARED = 0x20
+
+EXPORTS = ["dsf_workspace_bytes", "dsf_workspace_init", "dsf_prepare_mlp", "emb_bag_pool",
+           "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size"]
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+
+class CTables(ctypes.Structure):
+    _fields_ = [("table_ptrs", _vp), ("table_rows", _vp), ("F", _i32), ("D", _i32), ("dtype", _i32)]
+
+
+class CKjt(ctypes.Structure):
+    _fields_ = [("values_dev", _vp), ("n_values", _i64), ("lengths_dev", _vp)]
+
+
+class CSeq(ctypes.Structure):
+    _fields_ = [("values_dev", _vp), ("n_per_key", _i64), ("lengths_dev", _vp), ("max_len", _i32)]
+
+
+class CMlp(ctypes.Structure):
+    _fields_ = [("W1", _vp), ("b1", _vp), ("W2", _vp), ("b2", _vp), ("w3", _vp), ("b3", _vp),
+                ("K1", _i32), ("N1", _i32), ("N2", _i32), ("mode", _i32)]
+
+
+class DsfError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, status_string(code), code))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libdinsparse.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdinsparse.so is not built (run recsys_sparse_embedding_gb300"
+                               ".build.build()); there is no fallback implementation")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        L.dsf_workspace_bytes.argtypes = [_i32, _i32]
+        L.dsf_workspace_bytes.restype = _sz
+        L.dsf_workspace_init.argtypes = [_vp, _sz, _vp]
+        L.dsf_workspace_init.restype = ctypes.c_int
+        L.dsf_prepare_mlp.argtypes = [P(CMlp), _i32, _vp, _sz, _vp]
+        L.dsf_prepare_mlp.restype = ctypes.c_int
+        L.emb_bag_pool.argtypes = [P(CTables), P(CKjt), _i32, _vp, _vp, _sz, _vp, _vp]
+        L.emb_bag_pool.restype = ctypes.c_int
+        L.din_jagged_attn.argtypes = [P(CTables), P(CKjt), P(CSeq), _vp, _vp, _i32, P(CMlp),
+                                      _vp, _vp, _vp, _sz, _vp, _vp]
+        L.din_jagged_attn.restype = ctypes.c_int
+        L.din_sparse_fwd.argtypes = [P(CTables), P(CKjt), P(CSeq), _vp, _vp, _i32, P(CMlp),
+                                     _vp, _vp, _vp, _vp, _sz, _vp, _vp]
+        L.din_sparse_fwd.restype = ctypes.c_int
+        L.dsf_status_string.argtypes = [ctypes.c_int]
+        L.dsf_status_string.restype = ctypes.c_char_p
+        L.dsf_grid_size.argtypes = [_i32, _i32, _i32, _i32]
+        L.dsf_grid_size.restype = _i32
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().dsf_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != DSF_OK:
+        raise DsfError(rc, where)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class EmbeddingTables:
+    """F device tables [rows_f, D], all fp32 or all bf16."""
+
+    def __init__(self, tables: Sequence[torch.Tensor]):
+        self.tables = list(tables)
+        F = len(self.tables)
+        D = int(self.tables[0].shape[1])
+        dt = self.tables[0].dtype
+        for t in self.tables:
+            if t.dim() != 2 or int(t.shape[1]) != D or t.dtype != dt or not t.is_contiguous():
+                raise ValueError("tables must be contiguous [rows, D] with one D and dtype")
+        self.F, self.D = F, D
+        self.dtype = DSF_BF16 if dt == torch.bfloat16 else DSF_F32
+        self._ptrs = (ctypes.c_void_p * F)(*[t.data_ptr() for t in self.tables])
+        self._rows = (ctypes.c_int64 * F)(*[int(t.shape[0]) for t in self.tables])
+        self.c = CTables(ctypes.cast(self._ptrs, _vp), ctypes.cast(self._rows, _vp), F, D, self.dtype)
+
+    @property
+    def rows(self):
+        return [int(t.shape[0]) for t in self.tables]
+
+
+class AttnMLP:
+    """Device fp32 attention MLP in Linear [out, in] layout."""
+
+    def __init__(self, W1, b1, W2, b2, w3, b3, mode: int = DSF_MODE_BF16_TC):
+        self.t = [x.contiguous() for x in (W1, b1, W2, b2, w3.reshape(-1), b3.reshape(-1))]
+        W1, b1, W2, b2, w3, b3 = self.t
+        self.mode = int(mode)
+        self.c = CMlp(W1.data_ptr(), b1.data_ptr(), W2.data_ptr(), b2.data_ptr(), w3.data_ptr(),
+                      b3.data_ptr(), int(W1.shape[1]), int(W1.shape[0]), int(W2.shape[0]), self.mode)
+
+    def with_mode(self, mode: int) -> "AttnMLP":
+        return AttnMLP(*self.t, mode=mode)
+
+
+class Workspace:
+    """Caller-owned scratch for one stream: grid-barrier state, per-CTA partial
+    sums, packed MLP weights and the query buffer."""
+
+    def __init__(self, B: int, D: int, device=None, stream=None):
+        n = int(lib().dsf_workspace_bytes(int(B), int(D)))
+        if n == 0:
+            raise DsfError(DSF_EUNSUPPORTED, "dsf_workspace_bytes")
+        self.B, self.D, self.nbytes = int(B), int(D), n
+        self.buf = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+        _check(lib().dsf_workspace_init(self.buf.data_ptr(), n, _stream_ptr(stream)),
+               "dsf_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def prepare(self, mlp: AttnMLP, stream=None) -> None:
+        _check(lib().dsf_prepare_mlp(ctypes.byref(mlp.c), self.D, self.ptr, self.nbytes,
+                                     _stream_ptr(stream)), "dsf_prepare_mlp")
+
+
+def _kjt(values: torch.Tensor, lengths: torch.Tensor) -> CKjt:
+    return CKjt(values.data_ptr(), int(values.numel()), lengths.data_ptr())
+
+
+def _seq(seq_values: torch.Tensor, seq_lengths: torch.Tensor, max_len: int) -> CSeq:
+    n = int(seq_values.shape[-1]) if seq_values.dim() == 2 else int(seq_values.numel()) // 3
+    return CSeq(seq_values.data_ptr(), n, seq_lengths.data_ptr(), int(max_len))
+
+
+def _i3(x) -> ctypes.Array:
+    return (ctypes.c_int32 * 3)(*[int(v) for v in x])
+
+
+def emb_bag_pool(tables: EmbeddingTables, values: torch.Tensor, lengths: torch.Tensor, B: int,
+                 pooled: torch.Tensor, workspace: Workspace, status: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    kjt = _kjt(values, lengths)
+    _check(lib().emb_bag_pool(ctypes.byref(tables.c), ctypes.byref(kjt), int(B), pooled.data_ptr(),
+                              workspace.ptr, workspace.nbytes, _dptr(status), _stream_ptr(stream)),
+           "emb_bag_pool")
+    return pooled
+
+
+def din_jagged_attn(tables: EmbeddingTables, values: torch.Tensor, lengths: torch.Tensor,
+                    seq_values: torch.Tensor, seq_lengths: torch.Tensor, max_len: int,
+                    q_feat, seq_table, B: int, mlp: AttnMLP, din: torch.Tensor,
+                    workspace: Workspace, logits: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    kjt, seq = _kjt(values, lengths), _seq(seq_values, seq_lengths, max_len)
+    qf, st = _i3(q_feat), _i3(seq_table)
+    _check(lib().din_jagged_attn(ctypes.byref(tables.c), ctypes.byref(kjt), ctypes.byref(seq),
+                                 ctypes.cast(qf, _vp), ctypes.cast(st, _vp), int(B),
+                                 ctypes.byref(mlp.c), din.data_ptr(), _dptr(logits), workspace.ptr,
+                                 workspace.nbytes, _dptr(status), _stream_ptr(stream)),
+           "din_jagged_attn")
+    return din
+
+
+def din_sparse_fwd(tables: EmbeddingTables, values: torch.Tensor, lengths: torch.Tensor,
+                   seq_values: torch.Tensor, seq_lengths: torch.Tensor, max_len: int,
+                   q_feat, seq_table, B: int, mlp: AttnMLP, pooled: torch.Tensor,
+                   din: torch.Tensor, workspace: Workspace, logits: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, stream=None):
+    kjt, seq = _kjt(values, lengths), _seq(seq_values, seq_lengths, max_len)
+    qf, st = _i3(q_feat), _i3(seq_table)
+    _check(lib().din_sparse_fwd(ctypes.byref(tables.c), ctypes.byref(kjt), ctypes.byref(seq),
+                                ctypes.cast(qf, _vp), ctypes.cast(st, _vp), int(B),
+                                ctypes.byref(mlp.c), pooled.data_ptr(), din.data_ptr(),
+                                _dptr(logits), workspace.ptr, workspace.nbytes, _dptr(status),
+                                _stream_ptr(stream)),
+           "din_sparse_fwd")
+    return pooled, din
+
+
+def grid_size(D: int, dtype: int, mode: int, with_attention: bool) -> int:
+    return int(lib().dsf_grid_size(int(D), int(dtype), int(mode), int(bool(with_attention))))

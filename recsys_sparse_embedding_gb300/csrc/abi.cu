@@ -1,0 +1,270 @@
+// C ABI of the sparse forward (declared in include/dinsparse.h): argument
+// validation, workspace layout, MLP weight packing and kernel dispatch. No
+// function here allocates device memory; every buffer belongs to the caller.
+#include <cstdint>
+#include <cstring>
+
+#include "dinsparse.h"
+#include "launch.cuh"
+
+namespace dsf {
+namespace {
+
+constexpr int kCost0 = 4;  // per-sample cost (in sequence positions) of the work split
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t wpack, w1t, w2t, qbuf, total;
+};
+
+WsLayout ws_layout(int32_t B, int32_t D) {
+  WsLayout l{};
+  const size_t K1 = size_t(12) * D;
+  l.wpack = kWsWpackOff;
+  l.w1t = align256(l.wpack + (size_t(kN1) * K1 + size_t(kN2) * kN1) * 2);
+  l.w2t = align256(l.w1t + K1 * kN1 * 4);
+  l.qbuf = align256(l.w2t + size_t(kN1) * kN2 * 4);
+  l.total = align256(l.qbuf + size_t(B > 0 ? B : 0) * 3 * D * 4);
+  return l;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Packs W1 / W2 (fp32, [out, in]) into bf16 K-major 128-byte-swizzled operand
+// blocks and fp32 transposed copies; writes the prepared tag last.
+__global__ void prepare_kernel(const float* __restrict__ W1, const float* __restrict__ W2, int K1,
+                               uint8_t* wpack, float* w1t, float* w2t) {
+  const long long n1 = (long long)kN1 * K1, n2 = (long long)kN2 * kN1;
+  const long long W1B = n1 * 2;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n1 + n2;
+       i += (long long)gridDim.x * blockDim.x) {
+    if (i < n1) {
+      const int n = int(i / K1), k = int(i % K1);
+      const float w = W1[i];
+      *reinterpret_cast<__nv_bfloat16*>(wpack + sw128_offset(n, k, kN1)) = __float2bfloat16_rn(w);
+      w1t[(long long)k * kN1 + n] = w;
+    } else {
+      const long long j = i - n1;
+      const int n = int(j / kN1), k = int(j % kN1);
+      const float w = W2[j];
+      *reinterpret_cast<__nv_bfloat16*>(wpack + W1B + sw128_offset(n, k, kN2)) = __float2bfloat16_rn(w);
+      w2t[(long long)k * kN2 + n] = w;
+    }
+  }
+}
+
+__global__ void tag_kernel(uint32_t* magic, uint32_t tag) { *magic = tag; }
+
+int check_tables(const dsf_tables* t) {
+  if (!t || !t->table_ptrs || !t->table_rows) return DSF_EINVAL;
+  if (t->F < 1 || t->F > DSF_MAX_TABLES) return DSF_EINVAL;
+  if (t->D != 16 && t->D != 64) return DSF_EUNSUPPORTED;
+  if (t->dtype != DSF_F32 && t->dtype != DSF_BF16) return DSF_EUNSUPPORTED;
+  for (int f = 0; f < t->F; ++f) {
+    if (!t->table_ptrs[f] || !aligned(t->table_ptrs[f], 16)) return DSF_EINVAL;
+    if (t->table_rows[f] < 0) return DSF_EINVAL;
+  }
+  return DSF_OK;
+}
+
+int check_kjt(const dsf_kjt* k, int32_t B, int32_t F) {
+  if (!k) return DSF_EINVAL;
+  if (k->n_values < 0) return DSF_EINVAL;
+  if (B > 0 && F > 0 && (!k->lengths_dev || !aligned(k->lengths_dev, 4))) return DSF_EINVAL;
+  if (k->n_values > 0 && (!k->values_dev || !aligned(k->values_dev, 8))) return DSF_EINVAL;
+  return DSF_OK;
+}
+
+int check_seq(const dsf_seq* s, int32_t B) {
+  if (!s) return DSF_EINVAL;
+  if (s->n_per_key < 0 || s->n_per_key > INT32_MAX) return DSF_EINVAL;
+  if (s->max_len < 1 || s->max_len > 65536) return DSF_EINVAL;
+  if (B > 0 && (!s->lengths_dev || !aligned(s->lengths_dev, 4))) return DSF_EINVAL;
+  if (s->n_per_key > 0 && (!s->values_dev || !aligned(s->values_dev, 8))) return DSF_EINVAL;
+  return DSF_OK;
+}
+
+int check_mlp(const dsf_mlp* m, int32_t D) {
+  if (!m || !m->W1 || !m->b1 || !m->W2 || !m->b2 || !m->w3 || !m->b3) return DSF_EINVAL;
+  if (m->K1 != 12 * D || m->N1 != kN1 || m->N2 != kN2) return DSF_EUNSUPPORTED;
+  if (m->mode != DSF_MODE_BF16_TC && m->mode != DSF_MODE_FP32) return DSF_EINVAL;
+  if (m->mode == DSF_MODE_BF16_TC && D != 16) return DSF_EUNSUPPORTED;
+  return DSF_OK;
+}
+
+int check_ws(void* ws, size_t bytes, int32_t B, int32_t D) {
+  if (!ws || !aligned(ws, 256)) return DSF_EWORKSPACE;
+  if (bytes < ws_layout(B, D).total) return DSF_EWORKSPACE;
+  return DSF_OK;
+}
+
+void fill_common(FwdParams& p, const dsf_tables* t, const dsf_kjt* k, int32_t B, void* ws,
+                 int32_t* status) {
+  std::memset(&p, 0, sizeof(p));
+  for (int f = 0; f < t->F; ++f) {
+    p.tables[f] = t->table_ptrs[f];
+    p.rows[f] = t->table_rows[f];
+  }
+  p.F = t->F;
+  p.B = B;
+  p.cost0 = kCost0;
+  p.values = reinterpret_cast<const long long*>(k->values_dev);
+  p.n_values = k->n_values;
+  p.lengths = k->lengths_dev;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.magic = reinterpret_cast<const uint32_t*>(w + kWsMagicOff);
+  p.bar_count = reinterpret_cast<unsigned long long*>(w + kWsCountOff);
+  p.bar_gen = reinterpret_cast<unsigned long long*>(w + kWsGenOff);
+  p.partials = reinterpret_cast<long long*>(w + kWsPartOff);
+  p.status = status;
+}
+
+int map_launch(int rc) {
+  if (rc == 0) return DSF_OK;
+  if (rc == 2) return DSF_EUNSUPPORTED;
+  return DSF_ECUDA;
+}
+
+int run_attention(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
+                  const int32_t q_feat[3], const int32_t seq_table[3], int32_t B,
+                  const dsf_mlp* mlp, float* pooled, float* din, float* logits, void* ws,
+                  size_t ws_bytes, int32_t* status, void* stream) {
+  int rc;
+  if ((rc = check_tables(tables)) != DSF_OK) return rc;
+  if (B < 0 || B > (1 << 24)) return DSF_EINVAL;
+  if ((rc = check_kjt(kjt, B, tables->F)) != DSF_OK) return rc;
+  if ((rc = check_seq(seq, B)) != DSF_OK) return rc;
+  if ((rc = check_mlp(mlp, tables->D)) != DSF_OK) return rc;
+  if (!q_feat || !seq_table) return DSF_EINVAL;
+  for (int k = 0; k < 3; ++k) {
+    if (q_feat[k] < 0 || q_feat[k] >= tables->F) return DSF_EINVAL;
+    if (seq_table[k] < 0 || seq_table[k] >= tables->F) return DSF_EINVAL;
+  }
+  if (!din || !aligned(din, 16)) return DSF_EINVAL;
+  if (pooled && !aligned(pooled, 16)) return DSF_EINVAL;
+  if (logits && !aligned(logits, 4)) return DSF_EINVAL;
+  if ((rc = check_ws(ws, ws_bytes, B, tables->D)) != DSF_OK) return rc;
+  if (B == 0) return DSF_OK;
+  const WsLayout l = ws_layout(B, tables->D);
+  FwdParams p;
+  fill_common(p, tables, kjt, B, ws, status);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.max_len = seq->max_len;
+  p.seq_values = reinterpret_cast<const long long*>(seq->values_dev);
+  p.n_seq = seq->n_per_key;
+  p.seq_lengths = seq->lengths_dev;
+  for (int k = 0; k < 3; ++k) {
+    p.q_feat[k] = q_feat[k];
+    p.seq_table[k] = seq_table[k];
+  }
+  p.pooled = pooled;
+  p.qbuf = reinterpret_cast<float*>(w + l.qbuf);
+  p.din = din;
+  p.logits = logits;
+  p.b1 = mlp->b1;
+  p.b2 = mlp->b2;
+  p.w3 = mlp->w3;
+  p.b3 = mlp->b3;
+  p.wpack = w + l.wpack;
+  p.w1t = reinterpret_cast<const float*>(w + l.w1t);
+  p.w2t = reinterpret_cast<const float*>(w + l.w2t);
+  const bool bf16 = tables->dtype == DSF_BF16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int lrc = mlp->mode == DSF_MODE_BF16_TC ? launch_attn_tc(tables->D, bf16, p, s)
+                                                 : launch_attn_f32(tables->D, bf16, p, s);
+  return map_launch(lrc);
+}
+
+}  // namespace
+}  // namespace dsf
+
+using namespace dsf;
+
+extern "C" {
+
+size_t dsf_workspace_bytes(int32_t B, int32_t D) {
+  if (D != 16 && D != 64) return 0;
+  return ws_layout(B, D).total;
+}
+
+int dsf_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream) {
+  if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < kWsPartOff) return DSF_EWORKSPACE;
+  const cudaError_t e = cudaMemsetAsync(workspace_dev, 0, kWsPartOff, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSF_OK : DSF_ECUDA;
+}
+
+int dsf_prepare_mlp(const dsf_mlp* mlp, int32_t D, void* workspace_dev, size_t ws_bytes, void* stream) {
+  if (D != 16 && D != 64) return DSF_EUNSUPPORTED;
+  if (!mlp || !mlp->W1 || !mlp->W2) return DSF_EINVAL;
+  if (mlp->K1 != 12 * D || mlp->N1 != kN1 || mlp->N2 != kN2) return DSF_EUNSUPPORTED;
+  if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < ws_layout(0, D).total)
+    return DSF_EWORKSPACE;
+  const WsLayout l = ws_layout(0, D);
+  uint8_t* w = static_cast<uint8_t*>(workspace_dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long n = (long long)kN1 * 12 * D + (long long)kN2 * kN1;
+  const int threads = 256;
+  const int blocks = int((n + threads - 1) / threads);
+  prepare_kernel<<<blocks, threads, 0, s>>>(mlp->W1, mlp->W2, 12 * D, w + l.wpack,
+                                            reinterpret_cast<float*>(w + l.w1t),
+                                            reinterpret_cast<float*>(w + l.w2t));
+  tag_kernel<<<1, 1, 0, s>>>(reinterpret_cast<uint32_t*>(w + kWsMagicOff), kMagicBase | uint32_t(D));
+  return cudaGetLastError() == cudaSuccess ? DSF_OK : DSF_ECUDA;
+}
+
+int emb_bag_pool(const dsf_tables* tables, const dsf_kjt* kjt, int32_t B, float* pooled_dev,
+                 void* workspace_dev, size_t ws_bytes, int32_t* status_dev, void* stream) {
+  int rc;
+  if ((rc = check_tables(tables)) != DSF_OK) return rc;
+  if (B < 0 || B > (1 << 24)) return DSF_EINVAL;
+  if ((rc = check_kjt(kjt, B, tables->F)) != DSF_OK) return rc;
+  if (!pooled_dev || !aligned(pooled_dev, 16)) return DSF_EINVAL;
+  if ((rc = check_ws(workspace_dev, ws_bytes, B, tables->D)) != DSF_OK) return rc;
+  if (B == 0) return DSF_OK;
+  FwdParams p;
+  fill_common(p, tables, kjt, B, workspace_dev, status_dev);
+  p.pooled = pooled_dev;
+  p.max_len = 1;
+  return map_launch(launch_pool(tables->D, tables->dtype == DSF_BF16, p,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int din_jagged_attn(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
+                    const int32_t q_feat[3], const int32_t seq_table[3], int32_t B,
+                    const dsf_mlp* mlp, float* din_dev, float* logits_dev, void* workspace_dev,
+                    size_t ws_bytes, int32_t* status_dev, void* stream) {
+  return run_attention(tables, kjt, seq, q_feat, seq_table, B, mlp, nullptr, din_dev, logits_dev,
+                       workspace_dev, ws_bytes, status_dev, stream);
+}
+
+int din_sparse_fwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
+                   const int32_t q_feat[3], const int32_t seq_table[3], int32_t B,
+                   const dsf_mlp* mlp, float* pooled_dev, float* din_dev, float* logits_dev,
+                   void* workspace_dev, size_t ws_bytes, int32_t* status_dev, void* stream) {
+  if (!pooled_dev) return DSF_EINVAL;
+  return run_attention(tables, kjt, seq, q_feat, seq_table, B, mlp, pooled_dev, din_dev, logits_dev,
+                       workspace_dev, ws_bytes, status_dev, stream);
+}
+
+const char* dsf_status_string(int code) {
+  switch (code) {
+    case DSF_OK: return "ok";
+    case DSF_EINVAL: return "invalid argument";
+    case DSF_EUNSUPPORTED: return "unsupported configuration";
+    case DSF_ECUDA: return "CUDA error";
+    case DSF_EWORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int32_t dsf_grid_size(int32_t D, int32_t dtype, int32_t mode, int32_t with_attention) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool bf16 = dtype == DSF_BF16;
+  if (!with_attention) return grid_pool(D, bf16, dev);
+  if (mode == DSF_MODE_BF16_TC) return grid_attn_tc(D, bf16, dev);
+  return grid_attn_f32(D, bf16, dev);
+}
+
+}  // extern "C"

@@ -1,0 +1,22 @@
+// Instantiations of the forward kernel with the fp32 (check-mode) attention MLP.
+#include "launch.cuh"
+
+namespace dsf {
+
+int launch_attn_f32(int D, bool bf16, const FwdParams& p, cudaStream_t s) {
+  if (D == 16 && !bf16) return launch_fwd<Cfg<16, false, 1, true>>(p, s);
+  if (D == 16 && bf16) return launch_fwd<Cfg<16, true, 1, true>>(p, s);
+  if (D == 64 && !bf16) return launch_fwd<Cfg<64, false, 1, true>>(p, s);
+  if (D == 64 && bf16) return launch_fwd<Cfg<64, true, 1, true>>(p, s);
+  return 2;
+}
+
+int grid_attn_f32(int D, bool bf16, int dev) {
+  if (D == 16 && !bf16) return grid_for_device<Cfg<16, false, 1, true>>(dev);
+  if (D == 16 && bf16) return grid_for_device<Cfg<16, true, 1, true>>(dev);
+  if (D == 64 && !bf16) return grid_for_device<Cfg<64, false, 1, true>>(dev);
+  if (D == 64 && bf16) return grid_for_device<Cfg<64, true, 1, true>>(dev);
+  return 0;
+}
+
+}  // namespace dsf

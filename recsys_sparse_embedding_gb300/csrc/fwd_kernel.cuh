@@ -1,0 +1,977 @@
+// Fused MultiTowerDIN sparse forward for sm_103a: KJT offsets scan, sum-pooled
+// EmbeddingBag gather and padding-free DIN target attention in one persistent,
+// cooperatively launched kernel (one CTA per SM when attention is on).
+//
+// Method (pages cited by title and section):
+//   "MultiTowerDIN: current state analysis"
+//     s2   SparseData(values, lengths) -> KeyedJaggedTensor; sequence features
+//          carry (values, seq_lengths)
+//     s3   one [num_buckets, 16] table per id feature, sum-pooled bags
+//     s4.1 the sequence is padded to 100 in the pages' flow; here only the
+//          valid positions are ever gathered or computed
+//     s4.2 attention input cat[q, s, q - s, q * s]; attn_mlp 256 -> 64, linear
+//          to 1, mask + softmax, weighted sum
+//     s4.4 shapes [B,48] query, [B,100,192] input, [B,48] output
+//   "MultiTowerDIN: integrating DynamicEmb"
+//     s2.4 sequence sub-features share the target features' tables
+//     s3.3 lookup in fp32, MLP in half precision (bf16 here)
+//
+// Work split. Every CTA redundantly scans seq_lengths and takes a contiguous
+// sample range balanced by cost = cost0 + valid positions. It pools all F bags
+// of its own samples (so each pooled row is written by one CTA) and then runs
+// attention for the same samples, so the query never crosses CTAs. The only
+// cross-CTA exchange is the per-feature length total of each CTA's samples,
+// needed to place its bags in the key-major values array: one grid barrier
+// (bounded wait), split so that the first sequence tile's gather is in flight
+// while it completes.
+#pragma once
+#include <cstdint>
+#include <type_traits>
+
+#include "dinsparse.h"
+#include "ptx.cuh"
+
+namespace dsf {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSB = 128;            // samples per batch inside a CTA
+constexpr int kMaxF = 32;           // tables
+constexpr int kMaxG = 1024;         // grid size limit (rows of the partials table)
+constexpr int kN1 = 256, kN2 = 64;  // attn_mlp hidden units
+constexpr int kMaxBagLen = 1 << 19; // longer bags are clamped (flagged)
+
+// Workspace layout (bytes). The header holds the prepared-weights tag and the
+// grid barrier (arrival count and generation).
+constexpr size_t kWsHdr = 0;
+constexpr size_t kWsMagicOff = 0;
+constexpr size_t kWsCountOff = 64;
+constexpr size_t kWsGenOff = 128;
+constexpr size_t kWsPartOff = 256;
+constexpr size_t kWsPartBytes = size_t(kMaxG) * kMaxF * 8;
+constexpr size_t kWsWpackOff = kWsPartOff + kWsPartBytes;
+constexpr uint32_t kMagicBase = 0x44534600u;  // 'DSF\0' | D
+
+struct FwdParams {
+  const void* tables[kMaxF];
+  long long rows[kMaxF];
+  int F, B, max_len, cost0;
+  const long long* values;
+  long long n_values;
+  const int* lengths;
+  const long long* seq_values;
+  long long n_seq;
+  const int* seq_lengths;
+  int q_feat[3], seq_table[3];
+  float* pooled;   // [B, F*D] or null
+  float* qbuf;     // [B, 3D] query buffer when pooled is null
+  float* din;      // [B, 3D] (attention)
+  float* logits;   // [n_seq] or null
+  const float *b1, *b2, *w3, *b3;
+  const uint8_t* wpack;  // bf16 W1 | W2 in the swizzled operand layout
+  const float* w1t;      // fp32 W1^T [K1][256]
+  const float* w2t;      // fp32 W2^T [256][64]
+  const uint32_t* magic;
+  unsigned long long* bar_count;
+  unsigned long long* bar_gen;
+  long long* partials;   // [G][F]
+  int* status;
+};
+
+// ------------------------------------------------------------------ config
+template <int D_, bool BF16_, int MODE_, bool ATTN_>
+struct Cfg {
+  static constexpr int D = D_;
+  static constexpr bool BF16 = BF16_;  // table element type
+  static constexpr int MODE = MODE_;   // 0: bf16 tcgen05 MLP, 1: fp32 CUDA-core MLP
+  static constexpr bool ATTN = ATTN_;
+  static constexpr int ES = BF16 ? 2 : 4;
+  static constexpr int ROWB = D * ES;          // bytes per table row
+  static constexpr int LPB = ROWB / 16;        // lanes per row (16 B each)
+  static constexpr int EPL = 16 / ES;          // elements per 16-B piece
+  static constexpr int Q = 3 * D;
+  static constexpr int K1 = 4 * Q;
+  static constexpr int TM = MODE == 0 ? 128 : 64;  // rows per attention tile
+  static constexpr int SROWB = Q * ES;             // bytes per S row
+  static_assert(D % 8 == 0, "D must be a multiple of 8");
+
+  // pool region: staging rows then the bag offsets
+  static constexpr int POOL_STAGE_BYTES = 47 * 1024;
+  static constexpr int POOL_CAP = POOL_STAGE_BYTES / ROWB;
+  static constexpr int POOL_OFFS_BYTES = (kMaxF * kSB + 1) * 4;
+  static constexpr int POOL_BYTES = POOL_STAGE_BYTES + POOL_OFFS_BYTES;
+
+  // tensor-core mode
+  static constexpr int W1B = kN1 * K1 * 2;
+  static constexpr int W2B = kN2 * kN1 * 2;
+  static constexpr int XB = TM * K1 * 2;
+  static constexpr int H1B = TM * kN1 * 2;
+  // fp32 mode
+  static constexpr int H1S = kN1 + 4;  // padded fp32 row stride
+  static constexpr int QTB = TM * Q * 4;
+  static constexpr int H1FB = TM * H1S * 4;
+
+  static constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+  // byte offsets from the 1024-aligned smem base
+  static constexpr int W1_OFF = 0;
+  static constexpr int W2_OFF = (ATTN && MODE == 0) ? W1_OFF + W1B : 0;
+  static constexpr int ACT_OFF = (ATTN && MODE == 0) ? W2_OFF + W2B : 0;
+  static constexpr int ACT_BYTES =
+      !ATTN ? POOL_BYTES : (MODE == 0 ? cmax(cmax(XB, H1B), POOL_BYTES) : cmax(H1FB, POOL_BYTES));
+  static constexpr int QT_OFF = ACT_OFF + ACT_BYTES;                   // fp32 mode only
+  static constexpr int S_OFF = QT_OFF + ((ATTN && MODE == 1) ? QTB : 0);
+  static constexpr int S_BYTES = ATTN ? TM * SROWB : 0;
+  static constexpr int MISC_OFF = (S_OFF + S_BYTES + 127) / 128 * 128;
+};
+
+template <int Q>
+struct Misc {
+  float b1[kN1];
+  float b2[kN2];
+  float w3[kN2];
+  float z[128];
+  float red[4][128];
+  float carry[2][4 + 192];     // softmax state: m, l, -, -, acc[Q]
+  float pcarry[2][64];         // pooling carry of a bag that spans windows
+  int row_samp[128];
+  int row_j[128];
+  int rp[kSB + 4];             // valid-row prefix of the batch's samples
+  long long so[kSB];           // first sequence value index of each sample
+  long long fcur[kMaxF];       // next global value index of feature f for this CTA
+  long long ft[kMaxF];
+  long long fpre[kMaxF];
+  long long scan64[2][kWarps + 2];
+  uint64_t mbar_w;
+  uint64_t mbar_mma;
+  unsigned int tmem_base;
+  int abort_;
+  int sb0, sb1;
+  long long seq_cur;           // seq value index of the next batch's first sample
+  unsigned long long gen0;
+};
+
+template <class C>
+constexpr int smem_bytes() {
+  return C::MISC_OFF + int(sizeof(Misc<C::Q>)) + 1024;  // + alignment slack
+}
+
+// ------------------------------------------------------------------ helpers
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Exclusive scan of two int64 values over the block. Contains __syncthreads.
+__device__ __forceinline__ void block_scan2(long long a, long long b, long long (*scr)[kWarps + 2],
+                                            long long& ea, long long& eb, long long& ta,
+                                            long long& tb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long ia = warp_incl_scan(a), ib = warp_incl_scan(b);
+  if (lane == 31) {
+    scr[0][warp] = ia;
+    scr[1][warp] = ib;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    long long wa = lane < kWarps ? scr[0][lane] : 0;
+    long long wb = lane < kWarps ? scr[1][lane] : 0;
+    long long xa = warp_incl_scan(wa), xb = warp_incl_scan(wb);
+    if (lane < kWarps) {
+      scr[0][lane] = xa - wa;
+      scr[1][lane] = xb - wb;
+    }
+    if (lane == kWarps - 1) {
+      scr[0][kWarps] = xa;
+      scr[1][kWarps] = xb;
+    }
+  }
+  __syncthreads();
+  ea = scr[0][warp] + ia - a;
+  eb = scr[1][warp] + ib - b;
+  ta = scr[0][kWarps];
+  tb = scr[1][kWarps];
+  __syncthreads();
+}
+
+// Largest i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
+template <typename T>
+__device__ __forceinline__ int upper_index(const T* a, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)a[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void flag(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float4 ldcg4(const float* p) {
+  return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+// 16-byte piece of a staged row (fp32 or bf16) widened to EPL floats.
+template <bool BF16>
+__device__ __forceinline__ void widen16(const uint8_t* src, float* out) {
+  const uint4 v = *reinterpret_cast<const uint4*>(src);
+  if constexpr (BF16) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+    out[0] = __uint_as_float(v.x);
+    out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z);
+    out[3] = __uint_as_float(v.w);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float s_elem(const uint8_t* S, int srowb, int r, int d) {
+  if constexpr (BF16) {
+    const uint16_t h = *reinterpret_cast<const uint16_t*>(S + r * srowb + d * 2);
+    return __uint_as_float(uint32_t(h) << 16);
+  } else {
+    return *reinterpret_cast<const float*>(S + r * srowb + d * 4);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using M = Misc<C::Q>;
+  M* ms = reinterpret_cast<M*>(sm + C::MISC_OFF);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int F = p.F, B = p.B;
+  constexpr int D = C::D, Q = C::Q;
+  int local_flags = 0;
+
+  // ---------------------------------------------------------------- prologue
+  bool attn_ok = C::ATTN;
+  if (tid == 0) {
+    ms->abort_ = 0;
+    if constexpr (C::ATTN && C::MODE == 0) {
+      mbar_init(&ms->mbar_w, 1);
+      mbar_init(&ms->mbar_mma, 1);
+      fence_mbarrier_init();
+    }
+  }
+  if constexpr (C::ATTN) {
+    const uint32_t magic = *p.magic;
+    attn_ok = magic == (kMagicBase | uint32_t(D));
+    if (tid == 0 && !attn_ok && cta == 0) flag(p.status, DSF_FLAG_NOT_PREPARED);
+    if constexpr (C::MODE == 0) {
+      if (warp == 0) {
+        tmem_alloc(&ms->tmem_base, 512);
+        tmem_relinquish();
+        tc_fence_before();
+      }
+    }
+    if (tid < kN1) ms->b1[tid] = p.b1[tid];
+    if (tid < kN2) {
+      ms->b2[tid] = p.b2[tid];
+      ms->w3[tid] = p.w3[tid];
+    }
+  }
+  __syncthreads();
+  if constexpr (C::ATTN && C::MODE == 0) {
+    tc_fence_after();
+    if (tid == 0 && attn_ok) {
+      // stage the packed bf16 weights (bulk copies, 16 KB pieces)
+      mbar_arrive_expect_tx(&ms->mbar_w, C::W1B + C::W2B);
+      for (int off = 0; off < C::W1B + C::W2B; off += 16384) {
+        const int nbytes = min(16384, C::W1B + C::W2B - off);
+        bulk_g2s(sm + C::W1_OFF + off, p.wpack + off, nbytes, &ms->mbar_w);
+      }
+    }
+  }
+  const float b3 = C::ATTN ? p.b3[0] : 0.f;
+
+  // ---------------------------------------------------------------- partition
+  int sb0, sb1;
+  if constexpr (C::ATTN) {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int t0 = min(B, tid * per), t1 = min(B, t0 + per);
+    long long csum = 0;
+    for (int b = t0; b < t1; ++b) {
+      const int L = p.seq_lengths[b];
+      const int Lv = min(max(L, 0), p.max_len);
+      csum += p.cost0 + Lv;
+    }
+    long long cex, dummy, ctot, dt;
+    block_scan2(csum, 0, ms->scan64, cex, dummy, ctot, dt);
+    const long long lo0 = (long long)cta * ctot / G;
+    const long long lo1 = (long long)(cta + 1) * ctot / G;
+    long long n0 = 0, n1 = 0, run = cex, lsum0 = 0;
+    for (int b = t0; b < t1; ++b) {
+      const int L = p.seq_lengths[b];
+      const int Lf = max(L, 0);
+      const int Lv = min(Lf, p.max_len);
+      if (run < lo0) { ++n0; lsum0 += Lf; }
+      if (run < lo1) ++n1;
+      run += p.cost0 + Lv;
+    }
+    long long e0, e1, s0a, s1a;
+    block_scan2(n0, n1, ms->scan64, e0, e1, s0a, s1a);
+    long long el, ed, ltot, dt2;
+    block_scan2(lsum0, 0, ms->scan64, el, ed, ltot, dt2);
+    sb0 = int(s0a);
+    sb1 = int(s1a);
+    if (tid == 0) ms->seq_cur = ltot;
+  } else {
+    sb0 = int((long long)cta * B / G);
+    sb1 = int((long long)(cta + 1) * B / G);
+  }
+  const int ns = sb1 - sb0;
+
+  // ---------------------------------------------------------------- per-feature totals
+  for (int f = warp; f < F; f += kWarps) {
+    long long s = 0;
+    for (int i = lane; i < ns; i += 32) {
+      int l = p.lengths[(long long)f * B + sb0 + i];
+      if (l < 0) { local_flags |= DSF_FLAG_NEG_LENGTH; l = 0; }
+      if (l > kMaxBagLen) { local_flags |= DSF_FLAG_COUNT; l = kMaxBagLen; }
+      s += l;
+    }
+    s = warp_sum(s);
+    if (lane == 0) {
+      ms->ft[f] = s;
+      p.partials[(long long)cta * F + f] = s;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // arrive on the grid barrier (generation-counting, reset by the last arrival)
+    const unsigned long long gen = ld_acquire_u64(p.bar_gen);
+    ms->gen0 = gen;
+    __threadfence();
+    const unsigned long long old = atomicAdd(p.bar_count, 1ull);
+    if (old == (unsigned long long)(G - 1)) {
+      atomicExch(p.bar_count, 0ull);
+      __threadfence();
+      atomicAdd(p.bar_gen, 1ull);
+    }
+  }
+
+  // ---------------------------------------------------------------- batch setup
+  // Valid-row prefix rp[] and sequence value offsets so[] for samples [bs, be).
+  auto setup_batch = [&](int bs, int be) {
+    const int nb = be - bs;
+    long long lv = 0, lf = 0;
+    if (tid < nb) {
+      const int L = p.seq_lengths[bs + tid];
+      if (L < 0) local_flags |= DSF_FLAG_NEG_LENGTH;
+      if (L > p.max_len) local_flags |= DSF_FLAG_SEQ_TRUNC;
+      lf = max(L, 0);
+      lv = min(lf, (long long)p.max_len);
+    }
+    long long ev, ef, tv, tf;
+    block_scan2(lv, lf, ms->scan64, ev, ef, tv, tf);
+    if (tid < nb) {
+      ms->rp[tid] = int(ev);
+      ms->so[tid] = ms->seq_cur + ef;
+    }
+    if (tid == 0) ms->rp[nb] = int(tv);
+    __syncthreads();
+    if (tid == 0) ms->seq_cur += tf;
+    __syncthreads();
+  };
+
+  // Row metadata and cp.async gather of the sequence rows of tile [t0, t0+n).
+  auto gather_tile = [&](int t0, int n, int nb) {
+    uint8_t* S = sm + C::S_OFF;
+    if (tid < C::TM) {
+      if (tid < n) {
+        const int r = t0 + tid;
+        const int i = upper_index(ms->rp, nb + 1, r);
+        ms->row_samp[tid] = i;
+        const long long j = ms->so[i] + (r - ms->rp[i]);
+        ms->row_j[tid] = j < p.n_seq ? int(j) : -1;
+      } else {
+        ms->row_samp[tid] = 0;
+        ms->row_j[tid] = -1;
+      }
+    }
+    __syncthreads();
+    for (int item = tid; item < 3 * n; item += kThreads) {
+      const int r = item / 3, k = item - 3 * r;
+      const int j = ms->row_j[r];
+      const int tb = p.seq_table[k];
+      const uint8_t* base = static_cast<const uint8_t*>(p.tables[tb]);
+      bool ok = false;
+      long long id = 0;
+      if (j >= 0) {
+        id = p.seq_values[(long long)k * p.n_seq + j];
+        ok = id >= 0 && id < p.rows[tb];
+        if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
+      } else {
+        local_flags |= DSF_FLAG_COUNT;
+      }
+      uint8_t* dst = S + r * C::SROWB + k * C::ROWB;
+      const uint8_t* src = ok ? base + id * C::ROWB : base;
+#pragma unroll
+      for (int q = 0; q < C::LPB; ++q) cp_async_16(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+
+  int first_nb = 0;
+  bool prefetched = false;
+  if constexpr (C::ATTN) {
+    if (ns > 0) {
+      const int be = min(sb0 + kSB, sb1);
+      first_nb = be - sb0;
+      setup_batch(sb0, be);
+      if (attn_ok && ms->rp[first_nb] > 0) {
+        gather_tile(0, min(C::TM, ms->rp[first_nb]), first_nb);
+        prefetched = true;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- barrier wait
+  if (tid == 0) {
+    bool ok = true;
+    if (ld_acquire_u64(p.bar_gen) == ms->gen0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u64(p.bar_gen) == ms->gen0) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) { ok = false; break; }
+        __nanosleep(64);
+      }
+    }
+    ms->abort_ = ok ? 0 : 1;
+  }
+  __syncthreads();
+  const bool aborted = ms->abort_ != 0;
+  if (aborted) {
+    if (tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
+  } else {
+    // base value index of each feature for this CTA's samples
+    for (int f = warp; f < F; f += kWarps) {
+      long long tot = 0, pre = 0;
+      for (int c2 = lane; c2 < G; c2 += 32) {
+        const long long v = __ldcg(&p.partials[(long long)c2 * F + f]);
+        tot += v;
+        if (c2 < cta) pre += v;
+      }
+      tot = warp_sum(tot);
+      pre = warp_sum(pre);
+      if (lane == 0) {
+        ms->fpre[f] = pre;
+        ms->ft[f] = tot;
+      }
+    }
+    __syncthreads();
+    if (tid < F) {
+      long long base = ms->fpre[tid];
+      for (int f = 0; f < tid; ++f) base += ms->ft[f];
+      ms->fcur[tid] = base;
+    }
+    if (tid == 0 && cta == 0) {
+      long long total = 0;
+      for (int f = 0; f < F; ++f) total += ms->ft[f];
+      if (total != p.n_values) local_flags |= DSF_FLAG_COUNT;
+    }
+    __syncthreads();
+  }
+
+  // ---------------------------------------------------------------- batches
+  const bool pool_all = p.pooled != nullptr;
+  const float* qsrc = pool_all ? p.pooled : p.qbuf;
+  const long long qstride = pool_all ? (long long)F * D : Q;
+  int qcol[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) qcol[k] = pool_all ? p.q_feat[k] * D : k * D;
+  auto want_feature = [&](int f) -> bool {
+    if (pool_all) return true;
+    return f == p.q_feat[0] || f == p.q_feat[1] || f == p.q_feat[2];
+  };
+  uint32_t mma_phase = 0;
+  bool weights_ready = false;
+  bool tc_fail = false;
+
+  for (int bs = sb0; !aborted && bs < sb1; bs += kSB) {
+    const int be = min(bs + kSB, sb1);
+    const int nb = be - bs;
+    if (C::ATTN && bs != sb0) setup_batch(bs, be);
+
+    // ------------------------------------------------------------ pooling
+    {
+      uint8_t* stage = sm + C::ACT_OFF;
+      uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::POOL_STAGE_BYTES);
+      const int nbag = F * nb;
+      const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
+      const int g0 = tid * per;
+      int loc[8];
+      long long s = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        loc[k] = 0;
+        const int g = g0 + k;
+        if (k < per && g < nbag) {
+          const int f = g / nb, i = g - f * nb;
+          int l = p.lengths[(long long)f * B + bs + i];
+          l = min(max(l, 0), kMaxBagLen);
+          loc[k] = l;
+          s += l;
+        }
+      }
+      long long ex, d0, tot, d1;
+      block_scan2(s, 0, ms->scan64, ex, d0, tot, d1);
+      {
+        long long run = ex;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int g = g0 + k;
+          if (k < per && g < nbag) {
+            offs[g] = uint32_t(run);
+            run += loc[k];
+          }
+        }
+        if (tid == 0) offs[nbag] = uint32_t(tot);
+      }
+      __syncthreads();
+      const long long U = tot;
+      int widx = 0;
+      for (long long w0 = 0; w0 < U; w0 += C::POOL_CAP, ++widx) {
+        const long long w1 = min(U, w0 + (long long)C::POOL_CAP);
+        for (long long u = w0 + tid; u < w1; u += kThreads) {
+          const int g = upper_index(offs, nbag + 1, u);
+          const int f = g / nb;
+          if (!want_feature(f)) continue;
+          const long long gv = ms->fcur[f] + (u - (long long)offs[f * nb]);
+          const uint8_t* tbase = static_cast<const uint8_t*>(p.tables[f]);
+          bool ok = false;
+          long long id = 0;
+          if (gv < p.n_values) {
+            id = p.values[gv];
+            ok = id >= 0 && id < p.rows[f];
+            if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
+          } else {
+            local_flags |= DSF_FLAG_COUNT;
+          }
+          uint8_t* dst = stage + (u - w0) * C::ROWB;
+          const uint8_t* src = ok ? tbase + id * C::ROWB : tbase;
+#pragma unroll
+          for (int q = 0; q < C::LPB; ++q) cp_async_16(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+        // sum the bags that intersect [w0, w1), in value order
+        const int ga = upper_index(offs, nbag + 1, w0);
+        const int gb = upper_index(offs, nbag + 1, w1 - 1);
+        float* cin = ms->pcarry[widx & 1];
+        float* cout = ms->pcarry[(widx + 1) & 1];
+        const int grp = tid / C::LPB, sub = tid - grp * C::LPB;
+        constexpr int NGRP = kThreads / C::LPB;
+        for (int g = ga + grp; g <= gb; g += NGRP) {
+          const long long a = offs[g], e = offs[g + 1];
+          if (a == e) continue;
+          const int f = g / nb;
+          if (!want_feature(f)) continue;
+          float acc[C::EPL];
+          if (a < w0) {
+#pragma unroll
+            for (int q = 0; q < C::EPL; ++q) acc[q] = cin[sub * C::EPL + q];
+          } else {
+#pragma unroll
+            for (int q = 0; q < C::EPL; ++q) acc[q] = 0.f;
+          }
+          const long long lo = a < w0 ? w0 : a, hi = e < w1 ? e : w1;
+          for (long long u = lo; u < hi; ++u) {
+            float v[C::EPL];
+            widen16<C::BF16>(stage + (u - w0) * C::ROWB + sub * 16, v);
+#pragma unroll
+            for (int q = 0; q < C::EPL; ++q) acc[q] += v[q];
+          }
+          if (e <= w1) {
+            const int i = g - f * nb;
+            const long long b = bs + i;
+            if (pool_all) {
+              float* o = p.pooled + b * F * D + f * D + sub * C::EPL;
+#pragma unroll
+              for (int q = 0; q < C::EPL; q += 4)
+                *reinterpret_cast<float4*>(o + q) = make_float4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 3; ++k) {
+                if (p.q_feat[k] != f) continue;
+                float* o = p.qbuf + b * Q + k * D + sub * C::EPL;
+#pragma unroll
+                for (int q = 0; q < C::EPL; q += 4)
+                  *reinterpret_cast<float4*>(o + q) = make_float4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < C::EPL; ++q) cout[sub * C::EPL + q] = acc[q];
+          }
+        }
+        __syncthreads();
+      }
+      // empty bags
+      for (int g = tid; g < nbag; g += kThreads) {
+        if (offs[g] != offs[g + 1]) continue;
+        const int f = g / nb, i = g - f * nb;
+        if (!want_feature(f)) continue;
+        const long long b = bs + i;
+        if (pool_all) {
+          float* o = p.pooled + b * F * D + f * D;
+          for (int q = 0; q < D; q += 4) *reinterpret_cast<float4*>(o + q) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          for (int k = 0; k < 3; ++k) {
+            if (p.q_feat[k] != f) continue;
+            float* o = p.qbuf + b * Q + k * D;
+            for (int q = 0; q < D; q += 4) *reinterpret_cast<float4*>(o + q) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+      __syncthreads();
+      if (tid < F) ms->fcur[tid] += (long long)offs[(tid + 1) * nb] - (long long)offs[tid * nb];
+      __syncthreads();
+    }
+
+    if constexpr (C::ATTN) {
+      if (!attn_ok || tc_fail) continue;
+      // samples without a valid position get zeros
+      for (int i = tid; i < nb; i += kThreads) {
+        if (ms->rp[i] != ms->rp[i + 1]) continue;
+        float* o = p.din + (long long)(bs + i) * Q;
+        for (int d = 0; d < Q; d += 4) *reinterpret_cast<float4*>(o + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      const int R = ms->rp[nb];
+      int tix = 0;
+      for (int t0 = 0; t0 < R && !tc_fail; t0 += C::TM, ++tix) {
+        const int n = min(C::TM, R - t0);
+        if (!(prefetched && bs == sb0 && t0 == 0)) gather_tile(t0, n, nb);
+        cp_async_wait_all();
+        __syncthreads();
+        const uint8_t* S = sm + C::S_OFF;
+
+        if constexpr (C::MODE == 0) {
+          // ---------------------------------------------- x = cat[q, s, q-s, q*s] -> bf16 tile
+          uint8_t* X = sm + C::ACT_OFF;
+          constexpr int OCT = Q / 8;
+          for (int item = tid; item < C::TM * OCT; item += kThreads) {
+            const int r = item / OCT, o = item - r * OCT;
+            uint4 ch[4];
+            if (r < n) {
+              const long long b = bs + ms->row_samp[r];
+              const int d0 = o * 8, k = d0 / D, dd = d0 - k * D;
+              const float* qp = qsrc + b * qstride + qcol[k] + dd;
+              const float4 qa = ldcg4(qp), qb = ldcg4(qp + 4);
+              const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+              float sv[8];
+              if constexpr (C::BF16) {
+                widen16<true>(S + r * C::SROWB + d0 * 2, sv);
+              } else {
+                widen16<false>(S + r * C::SROWB + d0 * 4, sv);
+                widen16<false>(S + r * C::SROWB + d0 * 4 + 16, sv + 4);
+              }
+              uint32_t w[4][4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float q0 = qv[2 * e], q1 = qv[2 * e + 1], s0 = sv[2 * e], s1 = sv[2 * e + 1];
+                w[0][e] = pack_bf16x2(q0, q1);
+                w[1][e] = pack_bf16x2(s0, s1);
+                w[2][e] = pack_bf16x2(q0 - s0, q1 - s1);
+                w[3][e] = pack_bf16x2(q0 * s0, q1 * s1);
+              }
+#pragma unroll
+              for (int part = 0; part < 4; ++part) ch[part] = make_uint4(w[part][0], w[part][1], w[part][2], w[part][3]);
+            } else {
+#pragma unroll
+              for (int part = 0; part < 4; ++part) ch[part] = make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {
+              const uint32_t kk = uint32_t(part * Q + o * 8);
+              *reinterpret_cast<uint4*>(X + sw128_offset(uint32_t(r), kk, C::TM)) = ch[part];
+            }
+          }
+          fence_proxy_async_smem();
+          __syncthreads();
+          const uint32_t tbase = ms->tmem_base;
+          if (tid == 0) {
+            bool ok = true;
+            if (!weights_ready) ok = mbar_wait(&ms->mbar_w, 0);
+            weights_ready = weights_ready || ok;
+            if (ok) {
+              tc_fence_after();
+              constexpr uint32_t IDESC1 = idesc_bf16_f32(128, kN1);
+              const uint32_t xa = smem_u32(X), wa = smem_u32(sm + C::W1_OFF);
+#pragma unroll
+              for (int kk = 0; kk < C::K1 / 16; ++kk) {
+                const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+                tc_mma_f16(tbase, sw128_kmajor_desc(xa + kb * C::TM * 128 + ko),
+                           sw128_kmajor_desc(wa + kb * kN1 * 128 + ko), IDESC1, kk > 0);
+              }
+              tc_commit(&ms->mbar_mma);
+            } else {
+              ms->abort_ = 2;
+            }
+          }
+          __syncthreads();
+          if (ms->abort_ == 2) { tc_fail = true; break; }
+          // one thread waits for the MMAs, the block learns the outcome together
+          if (tid == 0) ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
+          mma_phase ^= 1u;
+          __syncthreads();
+          if (ms->abort_ == 3) { tc_fail = true; break; }
+          tc_fence_after();
+          // ---------------------------------------------- epilogue 1: h1 = ReLU(acc + b1) -> bf16
+          {
+            const int lq = warp & 3, cg = warp >> 2;
+            const int row = lq * 32 + lane;
+            const uint32_t ta = tbase + (uint32_t(lq * 32) << 16) + uint32_t(cg * 64);
+            float v[64];
+            tmem_ld16(ta, v);
+            tmem_ld16(ta + 16, v + 16);
+            tmem_ld16(ta + 32, v + 32);
+            tmem_ld16(ta + 48, v + 48);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = cg * 64 + c8 * 8 + 2 * e;
+                const float h0 = fmaxf(v[c8 * 8 + 2 * e] + ms->b1[col], 0.f);
+                const float h1 = fmaxf(v[c8 * 8 + 2 * e + 1] + ms->b1[col + 1], 0.f);
+                w[e] = pack_bf16x2(h0, h1);
+              }
+              *reinterpret_cast<uint4*>(X + sw128_offset(uint32_t(row), uint32_t(cg * 64 + c8 * 8), C::TM)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncthreads();
+          if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t IDESC2 = idesc_bf16_f32(128, kN2);
+            const uint32_t ha = smem_u32(X), wa = smem_u32(sm + C::W2_OFF);
+#pragma unroll
+            for (int kk = 0; kk < kN1 / 16; ++kk) {
+              const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+              tc_mma_f16(tbase + kN1, sw128_kmajor_desc(ha + kb * C::TM * 128 + ko),
+                         sw128_kmajor_desc(wa + kb * kN2 * 128 + ko), IDESC2, kk > 0);
+            }
+            tc_commit(&ms->mbar_mma);
+            ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
+          }
+          mma_phase ^= 1u;
+          __syncthreads();
+          if (ms->abort_ == 3) { tc_fail = true; break; }
+          tc_fence_after();
+          // ---------------------------------------------- epilogue 2: z = w3 . ReLU(acc + b2) + b3
+          {
+            const int lq = warp & 3, cg = warp >> 2;
+            const int row = lq * 32 + lane;
+            float v[16];
+            tmem_ld16(tbase + (uint32_t(lq * 32) << 16) + uint32_t(kN1 + cg * 16), v);
+            tmem_ld_wait();
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = cg * 16 + e;
+              part += fmaxf(v[e] + ms->b2[col], 0.f) * ms->w3[col];
+            }
+            ms->red[cg][row] = part;
+          }
+          tc_fence_before();
+          __syncthreads();
+          if (tid < C::TM) ms->z[tid] = ((ms->red[0][tid] + ms->red[1][tid]) + (ms->red[2][tid] + ms->red[3][tid])) + b3;
+          __syncthreads();
+        } else {
+          // ---------------------------------------------- fp32 check mode
+          float* QT = reinterpret_cast<float*>(sm + C::QT_OFF);
+          float* H1 = reinterpret_cast<float*>(sm + C::ACT_OFF);
+          constexpr int Q4 = Q / 4;
+          for (int item = tid; item < C::TM * Q4; item += kThreads) {
+            const int r = item / Q4, o = item - r * Q4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < n) {
+              const long long b = bs + ms->row_samp[r];
+              const int d0 = o * 4, k = d0 / D, dd = d0 - k * D;
+              v = ldcg4(qsrc + b * qstride + qcol[k] + dd);
+            }
+            *reinterpret_cast<float4*>(QT + r * Q + o * 4) = v;
+          }
+          __syncthreads();
+          {
+            // layer 1: thread = 4 rows x 8 units
+            const int rg = warp, ug = lane;
+            float acc[4][8];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+              for (int u = 0; u < 8; ++u) acc[a][u] = 0.f;
+            auto run_part = [&](auto part_tag) {
+              constexpr int PART = decltype(part_tag)::value;
+              for (int d = 0; d < Q; ++d) {
+                const float* wp = p.w1t + (long long)(PART * Q + d) * kN1 + ug * 8;
+                const float4 wa = __ldg(reinterpret_cast<const float4*>(wp));
+                const float4 wb = __ldg(reinterpret_cast<const float4*>(wp + 4));
+                const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                  const int r = rg * 4 + a;
+                  const float qv = QT[r * Q + d];
+                  const float sv = s_elem<C::BF16>(S, C::SROWB, r, d);
+                  float x;
+                  if constexpr (PART == 0) x = qv;
+                  else if constexpr (PART == 1) x = sv;
+                  else if constexpr (PART == 2) x = qv - sv;
+                  else x = qv * sv;
+#pragma unroll
+                  for (int u = 0; u < 8; ++u) acc[a][u] = fmaf(x, w[u], acc[a][u]);
+                }
+              }
+            };
+            run_part(std::integral_constant<int, 0>{});
+            run_part(std::integral_constant<int, 1>{});
+            run_part(std::integral_constant<int, 2>{});
+            run_part(std::integral_constant<int, 3>{});
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                H1[(rg * 4 + a) * C::H1S + ug * 8 + u] = fmaxf(acc[a][u] + ms->b1[ug * 8 + u], 0.f);
+          }
+          __syncthreads();
+          {
+            // layer 2 + score: thread = 1 row x 8 units
+            const int r = tid >> 3, u2 = tid & 7;
+            float a2[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a2[u] = 0.f;
+            for (int k = 0; k < kN1; ++k) {
+              const float h = H1[r * C::H1S + k];
+              const float* wp = p.w2t + (long long)k * kN2 + u2 * 8;
+              const float4 wa = __ldg(reinterpret_cast<const float4*>(wp));
+              const float4 wb = __ldg(reinterpret_cast<const float4*>(wp + 4));
+              a2[0] = fmaf(h, wa.x, a2[0]); a2[1] = fmaf(h, wa.y, a2[1]);
+              a2[2] = fmaf(h, wa.z, a2[2]); a2[3] = fmaf(h, wa.w, a2[3]);
+              a2[4] = fmaf(h, wb.x, a2[4]); a2[5] = fmaf(h, wb.y, a2[5]);
+              a2[6] = fmaf(h, wb.z, a2[6]); a2[7] = fmaf(h, wb.w, a2[7]);
+            }
+            float part = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) part += fmaxf(a2[u] + ms->b2[u2 * 8 + u], 0.f) * ms->w3[u2 * 8 + u];
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            part += __shfl_xor_sync(0xffffffffu, part, 4);
+            if (u2 == 0 && r < C::TM) ms->z[r] = part + b3;
+          }
+          __syncthreads();
+        }
+
+        // ---------------------------------------------- masked softmax + weighted sum
+        {
+          const int ia = ms->row_samp[0], ib = ms->row_samp[n - 1];
+          float* cin = ms->carry[tix & 1];
+          float* cout = ms->carry[(tix + 1) & 1];
+          if (p.logits) {
+            for (int r = tid; r < n; r += kThreads) {
+              const int j = ms->row_j[r];
+              if (j >= 0) p.logits[j] = ms->z[r];
+            }
+          }
+          __syncthreads();
+          for (int si = ia + warp; si <= ib; si += kWarps) {
+            const int ra = ms->rp[si], re = ms->rp[si + 1];
+            const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
+            if (r1 <= r0) continue;
+            const bool has_in = ra < t0, has_out = re > t0 + n;
+            float m = -INFINITY;
+            for (int r = r0 + lane; r < r1; r += 32) m = fmaxf(m, ms->z[r]);
+            m = warp_max(m);
+            if (has_in) m = fmaxf(m, cin[0]);
+            float l = 0.f;
+            for (int r = r0 + lane; r < r1; r += 32) {
+              const float e = expf(ms->z[r] - m);
+              ms->z[r] = e;
+              l += e;
+            }
+            l = warp_sum(l);
+            float sc = 0.f;
+            if (has_in) {
+              sc = expf(cin[0] - m);
+              l += cin[1] * sc;
+            }
+            __syncwarp();
+            const long long b = bs + si;
+            for (int d = lane; d < Q; d += 32) {
+              float acc = has_in ? cin[4 + d] * sc : 0.f;
+              for (int r = r0; r < r1; ++r) acc = fmaf(ms->z[r], s_elem<C::BF16>(S, C::SROWB, r, d), acc);
+              if (has_out) cout[4 + d] = acc;
+              else p.din[b * Q + d] = acc / l;
+            }
+            if (has_out && lane == 0) {
+              cout[0] = m;
+              cout[1] = l;
+            }
+          }
+          __syncthreads();
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- cleanup
+  cp_async_wait_all();
+  if constexpr (C::ATTN && C::MODE == 0) {
+    if (tid == 0 && attn_ok && !weights_ready) {
+      if (!mbar_wait(&ms->mbar_w, 0)) local_flags |= DSF_FLAG_TIMEOUT;
+    }
+    if (tid == 0 && ms->abort_ == 3) {
+      // an MMA group did not complete in time: give it one more bounded wait
+      // before the accumulator columns are released
+      mbar_wait(&ms->mbar_mma, mma_phase ^ 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(ms->tmem_base, 512);
+    }
+  }
+  if (tc_fail && tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
+  // one status write per warp
+  local_flags = __reduce_or_sync(0xffffffffu, local_flags);
+  if (lane == 0 && local_flags) flag(p.status, local_flags);
+}
+
+}  // namespace dsf
