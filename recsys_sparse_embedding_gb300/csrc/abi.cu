@@ -70,7 +70,7 @@ int check_tables(const dsf_tables* t) {
 
 int check_kjt(const dsf_kjt* k, int32_t B, int32_t F) {
   if (!k) return DSF_EINVAL;
-  if (k->n_values < 0) return DSF_EINVAL;
+  if (k->n_values < 0 || k->n_values > INT32_MAX) return DSF_EINVAL;
   if (B > 0 && F > 0 && (!k->lengths_dev || !aligned(k->lengths_dev, 4))) return DSF_EINVAL;
   if (k->n_values > 0 && (!k->values_dev || !aligned(k->values_dev, 8))) return DSF_EINVAL;
   return DSF_OK;
@@ -87,6 +87,7 @@ int check_seq(const dsf_seq* s, int32_t B) {
 
 int check_mlp(const dsf_mlp* m, int32_t D) {
   if (!m || !m->W1 || !m->b1 || !m->W2 || !m->b2 || !m->w3 || !m->b3) return DSF_EINVAL;
+  if (!aligned(m->b1, 16) || !aligned(m->b2, 16) || !aligned(m->w3, 16)) return DSF_EINVAL;
   if (m->K1 != 12 * D || m->N1 != kN1 || m->N2 != kN2) return DSF_EUNSUPPORTED;
   if (m->mode != DSF_MODE_BF16_TC && m->mode != DSF_MODE_FP32) return DSF_EINVAL;
   if (m->mode == DSF_MODE_BF16_TC && D != 16) return DSF_EUNSUPPORTED;
@@ -114,9 +115,9 @@ void fill_common(FwdParams& p, const dsf_tables* t, const dsf_kjt* k, int32_t B,
   p.lengths = k->lengths_dev;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.magic = reinterpret_cast<const uint32_t*>(w + kWsMagicOff);
-  p.bar_count = reinterpret_cast<unsigned long long*>(w + kWsCountOff);
-  p.bar_gen = reinterpret_cast<unsigned long long*>(w + kWsGenOff);
-  p.partials = reinterpret_cast<long long*>(w + kWsPartOff);
+  p.done = reinterpret_cast<unsigned long long*>(w + kWsDoneOff);
+  p.epoch = reinterpret_cast<unsigned int*>(w + kWsEpochOff);
+  p.partials = reinterpret_cast<unsigned long long*>(w + kWsPartOff);
   p.status = status;
 }
 
@@ -189,8 +190,8 @@ size_t dsf_workspace_bytes(int32_t B, int32_t D) {
 }
 
 int dsf_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream) {
-  if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < kWsPartOff) return DSF_EWORKSPACE;
-  const cudaError_t e = cudaMemsetAsync(workspace_dev, 0, kWsPartOff, static_cast<cudaStream_t>(stream));
+  if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < kWsWpackOff) return DSF_EWORKSPACE;
+  const cudaError_t e = cudaMemsetAsync(workspace_dev, 0, kWsWpackOff, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSF_OK : DSF_ECUDA;
 }
 

@@ -16,14 +16,16 @@
 //     s2.4 sequence sub-features share the target features' tables
 //     s3.3 lookup in fp32, MLP in half precision (bf16 here)
 //
-// Work split. Every CTA redundantly scans seq_lengths and takes a contiguous
-// sample range balanced by cost = cost0 + valid positions. It pools all F bags
-// of its own samples (so each pooled row is written by one CTA) and then runs
-// attention for the same samples, so the query never crosses CTAs. The only
-// cross-CTA exchange is the per-feature length total of each CTA's samples,
-// needed to place its bags in the key-major values array: one grid barrier
-// (bounded wait), split so that the first sequence tile's gather is in flight
-// while it completes.
+// Work split. Every CTA stages seq_lengths in shared memory, scans it and
+// takes a contiguous sample range balanced by cost = cost0 + valid positions.
+// It pools all F bags of its own samples (so each pooled row is written by one
+// CTA) and then runs attention for the same samples, so the query never
+// crosses CTAs. The only cross-CTA exchange is the per-feature length total of
+// each CTA's samples, needed to place its bags in the key-major values array.
+// Each CTA publishes its totals tagged with the launch epoch; a CTA that needs
+// them polls the tagged words themselves (bounded wait), so the exchange costs
+// one round trip once the last CTA has published. The first sequence tile's
+// gather is in flight meanwhile. The epoch advances when the last CTA exits.
 #pragma once
 #include <cstdint>
 #include <type_traits>
@@ -41,12 +43,11 @@ constexpr int kMaxG = 1024;         // grid size limit (rows of the partials tab
 constexpr int kN1 = 256, kN2 = 64;  // attn_mlp hidden units
 constexpr int kMaxBagLen = 1 << 19; // longer bags are clamped (flagged)
 
-// Workspace layout (bytes). The header holds the prepared-weights tag and the
-// grid barrier (arrival count and generation).
-constexpr size_t kWsHdr = 0;
+// Workspace layout (bytes). The header holds the prepared-weights tag, the
+// launch epoch and the exit counter that advances it.
 constexpr size_t kWsMagicOff = 0;
-constexpr size_t kWsCountOff = 64;
-constexpr size_t kWsGenOff = 128;
+constexpr size_t kWsDoneOff = 64;
+constexpr size_t kWsEpochOff = 128;
 constexpr size_t kWsPartOff = 256;
 constexpr size_t kWsPartBytes = size_t(kMaxG) * kMaxF * 8;
 constexpr size_t kWsWpackOff = kWsPartOff + kWsPartBytes;
@@ -72,9 +73,9 @@ struct FwdParams {
   const float* w1t;      // fp32 W1^T [K1][256]
   const float* w2t;      // fp32 W2^T [256][64]
   const uint32_t* magic;
-  unsigned long long* bar_count;
-  unsigned long long* bar_gen;
-  long long* partials;   // [G][F]
+  unsigned long long* done;      // CTAs that finished this launch
+  unsigned int* epoch;           // launch counter, tags the partials
+  unsigned long long* partials;  // [G][F]: (epoch + 1) << 32 | length total
   int* status;
 };
 
@@ -87,19 +88,16 @@ struct Cfg {
   static constexpr bool ATTN = ATTN_;
   static constexpr int ES = BF16 ? 2 : 4;
   static constexpr int ROWB = D * ES;          // bytes per table row
-  static constexpr int LPB = ROWB / 16;        // lanes per row (16 B each)
-  static constexpr int EPL = 16 / ES;          // elements per 16-B piece
+  static constexpr int LPB = ROWB / 16;        // 16-byte pieces per row
+  static constexpr int EPL = 16 / ES;          // elements per 16-byte piece
   static constexpr int Q = 3 * D;
   static constexpr int K1 = 4 * Q;
   static constexpr int TM = MODE == 0 ? 128 : 64;  // rows per attention tile
   static constexpr int SROWB = Q * ES;             // bytes per S row
   static_assert(D % 8 == 0, "D must be a multiple of 8");
 
-  // pool region: staging rows then the bag offsets
-  static constexpr int POOL_STAGE_BYTES = 47 * 1024;
-  static constexpr int POOL_CAP = POOL_STAGE_BYTES / ROWB;
-  static constexpr int POOL_OFFS_BYTES = (kMaxF * kSB + 1) * 4;
-  static constexpr int POOL_BYTES = POOL_STAGE_BYTES + POOL_OFFS_BYTES;
+  // pool region: bag offsets at its end (F*nb+1 words), staging rows before
+  static constexpr int POOL_BYTES = 64 * 1024;
 
   // tensor-core mode
   static constexpr int W1B = kN1 * K1 * 2;
@@ -119,41 +117,46 @@ struct Cfg {
   static constexpr int ACT_OFF = (ATTN && MODE == 0) ? W2_OFF + W2B : 0;
   static constexpr int ACT_BYTES =
       !ATTN ? POOL_BYTES : (MODE == 0 ? cmax(cmax(XB, H1B), POOL_BYTES) : cmax(H1FB, POOL_BYTES));
-  static constexpr int QT_OFF = ACT_OFF + ACT_BYTES;                   // fp32 mode only
+  static constexpr int QT_OFF = ACT_OFF + ACT_BYTES;  // fp32 mode only
   static constexpr int S_OFF = QT_OFF + ((ATTN && MODE == 1) ? QTB : 0);
   static constexpr int S_BYTES = ATTN ? TM * SROWB : 0;
   static constexpr int MISC_OFF = (S_OFF + S_BYTES + 127) / 128 * 128;
+  // values a thread stages per pooling window
+  static constexpr int VPT = (ACT_BYTES / ROWB + kThreads - 1) / kThreads;
+  // seq_lengths staged per chunk of the partition scan
+  static constexpr int SEQ_CHUNK = ACT_BYTES / 4;
 };
 
-template <int Q>
+template <int D, int Q>
 struct Misc {
   float b1[kN1];
   float b2[kN2];
   float w3[kN2];
   float z[128];
   float red[4][128];
-  float carry[2][4 + 192];     // softmax state: m, l, -, -, acc[Q]
-  float pcarry[2][64];         // pooling carry of a bag that spans windows
+  float carry[2][4 + Q];       // softmax state: m, l, -, -, acc[Q]
+  float pcarry[2][D];          // pooling carry of a bag that spans windows
   int row_samp[128];
   int row_j[128];
   int rp[kSB + 4];             // valid-row prefix of the batch's samples
-  long long so[kSB];           // first sequence value index of each sample
+  int so[kSB];                 // first sequence value index of each sample
   long long fcur[kMaxF];       // next global value index of feature f for this CTA
   long long ft[kMaxF];
   long long fpre[kMaxF];
   long long scan64[2][kWarps + 2];
+  long long red3[3][kWarps];
+  long long wtot[2][kWarps];
   uint64_t mbar_w;
   uint64_t mbar_mma;
   unsigned int tmem_base;
   int abort_;
-  int sb0, sb1;
   long long seq_cur;           // seq value index of the next batch's first sample
-  unsigned long long gen0;
+  unsigned int epoch;
 };
 
 template <class C>
 constexpr int smem_bytes() {
-  return C::MISC_OFF + int(sizeof(Misc<C::Q>)) + 1024;  // + alignment slack
+  return C::MISC_OFF + int(sizeof(Misc<C::D, C::Q>)) + 1024;  // + alignment slack
 }
 
 // ------------------------------------------------------------------ helpers
@@ -213,6 +216,29 @@ __device__ __forceinline__ void block_scan2(long long a, long long b, long long 
   __syncthreads();
 }
 
+// Block-wide sums of three int64 values. Contains __syncthreads.
+__device__ __forceinline__ void block_sum3(long long& a, long long& b, long long& c,
+                                           long long (*scr)[kWarps]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  c = warp_sum(c);
+  if (lane == 0) {
+    scr[0][warp] = a;
+    scr[1][warp] = b;
+    scr[2][warp] = c;
+  }
+  __syncthreads();
+  a = b = c = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    a += scr[0][w];
+    b += scr[1][w];
+    c += scr[2][w];
+  }
+  __syncthreads();
+}
+
 // Largest i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
 template <typename T>
 __device__ __forceinline__ int upper_index(const T* a, int n, long long x) {
@@ -262,13 +288,21 @@ __device__ __forceinline__ float s_elem(const uint8_t* S, int srowb, int r, int 
   }
 }
 
+// One gathered sequence sub-row of a tile, held in registers between the id
+// load and the row copy.
+struct SeqItem {
+  long long id;
+  int r, k, i, j;
+  bool valid;
+};
+
 // ------------------------------------------------------------------ kernel
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using M = Misc<C::Q>;
+  using M = Misc<C::D, C::Q>;
   M* ms = reinterpret_cast<M*>(sm + C::MISC_OFF);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -277,36 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   int local_flags = 0;
 
   // ---------------------------------------------------------------- prologue
+  // Nothing here waits on global memory: the prepared tag is read into a
+  // register for later, the biases and the weights are copied asynchronously.
   bool attn_ok = C::ATTN;
+  const uint32_t magic = C::ATTN ? *p.magic : 0u;
   if (tid == 0) {
     ms->abort_ = 0;
+    ms->epoch = *p.epoch;
     if constexpr (C::ATTN && C::MODE == 0) {
       mbar_init(&ms->mbar_w, 1);
       mbar_init(&ms->mbar_mma, 1);
       fence_mbarrier_init();
-    }
-  }
-  if constexpr (C::ATTN) {
-    const uint32_t magic = *p.magic;
-    attn_ok = magic == (kMagicBase | uint32_t(D));
-    if (tid == 0 && !attn_ok && cta == 0) flag(p.status, DSF_FLAG_NOT_PREPARED);
-    if constexpr (C::MODE == 0) {
-      if (warp == 0) {
-        tmem_alloc(&ms->tmem_base, 512);
-        tmem_relinquish();
-        tc_fence_before();
-      }
-    }
-    if (tid < kN1) ms->b1[tid] = p.b1[tid];
-    if (tid < kN2) {
-      ms->b2[tid] = p.b2[tid];
-      ms->w3[tid] = p.w3[tid];
-    }
-  }
-  __syncthreads();
-  if constexpr (C::ATTN && C::MODE == 0) {
-    tc_fence_after();
-    if (tid == 0 && attn_ok) {
       // stage the packed bf16 weights (bulk copies, 16 KB pieces)
       mbar_arrive_expect_tx(&ms->mbar_w, C::W1B + C::W2B);
       for (int off = 0; off < C::W1B + C::W2B; off += 16384) {
@@ -315,72 +330,160 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       }
     }
   }
-  const float b3 = C::ATTN ? p.b3[0] : 0.f;
+  if constexpr (C::ATTN) {
+    if constexpr (C::MODE == 0) {
+      __syncwarp();
+      if (warp == 0) {
+        tmem_alloc(&ms->tmem_base, 512);
+        tmem_relinquish();
+        tc_fence_before();
+      }
+    }
+    // biases: 16-byte pieces of b1 [256], b2 [64], w3 [64]
+    if (tid < kN1 / 4) cp_async_16_ca(ms->b1 + 4 * tid, p.b1 + 4 * tid, 16u);
+    else if (tid < kN1 / 4 + kN2 / 4) cp_async_16_ca(ms->b2 + 4 * (tid - kN1 / 4), p.b2 + 4 * (tid - kN1 / 4), 16u);
+    else if (tid < kN1 / 4 + kN2 / 2) cp_async_16_ca(ms->w3 + 4 * (tid - kN1 / 4 - kN2 / 4), p.w3 + 4 * (tid - kN1 / 4 - kN2 / 4), 16u);
+  }
+  __syncthreads();
+  if constexpr (C::ATTN && C::MODE == 0) tc_fence_after();
+  const float b3 = C::ATTN ? __ldg(p.b3) : 0.f;
 
   // ---------------------------------------------------------------- partition
+  // Sample b belongs to CTA c when its exclusive cost prefix lies in
+  // [c*Ctot/G, (c+1)*Ctot/G); every CTA computes the same split. seq_lengths
+  // is staged in shared memory; each warp sums a contiguous run of samples and
+  // only the warps whose run contains a boundary scan it sample by sample.
   int sb0, sb1;
   if constexpr (C::ATTN) {
-    const int per = (B + kThreads - 1) / kThreads;
-    const int t0 = min(B, tid * per), t1 = min(B, t0 + per);
-    long long csum = 0;
-    for (int b = t0; b < t1; ++b) {
-      const int L = p.seq_lengths[b];
-      const int Lv = min(max(L, 0), p.max_len);
-      csum += p.cost0 + Lv;
+    int* sl = reinterpret_cast<int*>(sm + C::ACT_OFF);
+    constexpr int CH = C::SEQ_CHUNK;
+    const bool single = B <= CH;
+    auto cost_of = [&](int L) -> long long { return p.cost0 + min(max(L, 0), p.max_len); };
+    auto stage = [&](int c0, int n) {
+      for (int i = tid; i < n; i += kThreads) cp_async_4(sl + i, p.seq_lengths + c0 + i);
+      cp_async_commit();
+      cp_async_wait_all();
+      __syncthreads();
+    };
+    // per-warp totals of the staged chunk (cost and full lengths) into ms->wtot
+    auto warp_totals = [&](int n, int& a, int& e) {
+      const int pw = ((n + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+      a = min(n, warp * pw);
+      e = min(n, a + pw);
+      long long wc = 0, wl = 0;
+      for (int i = a + lane; i < e; i += 32) {
+        const int L = sl[i];
+        wc += cost_of(L);
+        wl += max(L, 0);
+      }
+      wc = warp_sum(wc);
+      wl = warp_sum(wl);
+      if (lane == 0) {
+        ms->wtot[0][warp] = wc;
+        ms->wtot[1][warp] = wl;
+      }
+      __syncthreads();
+    };
+    long long ctot = 0;
+    int a = 0, e = 0;
+    if (single) {
+      stage(0, B);
+      warp_totals(B, a, e);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) ctot += ms->wtot[0][w];
+    } else {
+      long long csum = 0;
+      for (int c0 = 0; c0 < B; c0 += CH) {
+        const int n = min(CH, B - c0);
+        stage(c0, n);
+        for (int i = tid; i < n; i += kThreads) csum += cost_of(sl[i]);
+        __syncthreads();
+      }
+      long long u0 = 0, u1 = 0;
+      ctot = csum;
+      block_sum3(ctot, u0, u1, ms->red3);
     }
-    long long cex, dummy, ctot, dt;
-    block_scan2(csum, 0, ms->scan64, cex, dummy, ctot, dt);
     const long long lo0 = (long long)cta * ctot / G;
     const long long lo1 = (long long)(cta + 1) * ctot / G;
-    long long n0 = 0, n1 = 0, run = cex, lsum0 = 0;
-    for (int b = t0; b < t1; ++b) {
-      const int L = p.seq_lengths[b];
-      const int Lf = max(L, 0);
-      const int Lv = min(Lf, p.max_len);
-      if (run < lo0) { ++n0; lsum0 += Lf; }
-      if (run < lo1) ++n1;
-      run += p.cost0 + Lv;
+    long long n0 = 0, n1 = 0, l0 = 0, run = 0;
+    for (int c0 = 0; c0 < B; c0 += CH) {
+      const int n = min(CH, B - c0);
+      if (!single) {
+        stage(c0, n);
+        warp_totals(n, a, e);
+      }
+      long long wp = run, chunk_tot = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const long long v = ms->wtot[0][w];
+        if (w < warp) wp += v;
+        chunk_tot += v;
+      }
+      const long long wc = ms->wtot[0][warp], wl = ms->wtot[1][warp];
+      // samples with exclusive prefix below each boundary
+      const bool cross0 = wp < lo0 && lo0 < wp + wc;
+      const bool cross1 = wp < lo1 && lo1 < wp + wc;
+      if (lane == 0) {
+        if (wp + wc <= lo0) { n0 += e - a; l0 += wl; }
+        if (wp + wc <= lo1) n1 += e - a;
+      }
+      if (cross0 || cross1) {
+        long long rr = wp;
+        for (int i = a; i < e; i += 32) {
+          const int idx = i + lane;
+          long long c = 0, lf = 0;
+          if (idx < e) {
+            const int L = sl[idx];
+            lf = max(L, 0);
+            c = p.cost0 + min(lf, (long long)p.max_len);
+          }
+          const long long inc = warp_incl_scan(c);
+          const long long ex = rr + inc - c;
+          if (idx < e) {
+            if (cross0 && ex < lo0) { ++n0; l0 += lf; }
+            if (cross1 && ex < lo1) ++n1;
+          }
+          rr += __shfl_sync(0xffffffffu, inc, 31);
+        }
+      }
+      run += chunk_tot;
+      __syncthreads();
     }
-    long long e0, e1, s0a, s1a;
-    block_scan2(n0, n1, ms->scan64, e0, e1, s0a, s1a);
-    long long el, ed, ltot, dt2;
-    block_scan2(lsum0, 0, ms->scan64, el, ed, ltot, dt2);
-    sb0 = int(s0a);
-    sb1 = int(s1a);
-    if (tid == 0) ms->seq_cur = ltot;
+    block_sum3(n0, n1, l0, ms->red3);
+    sb0 = int(n0);
+    sb1 = int(n1);
+    if (tid == 0) ms->seq_cur = l0;
   } else {
     sb0 = int((long long)cta * B / G);
     sb1 = int((long long)(cta + 1) * B / G);
   }
+  attn_ok = C::ATTN && magic == (kMagicBase | uint32_t(D));
+  if (C::ATTN && tid == 0 && !attn_ok && cta == 0) flag(p.status, DSF_FLAG_NOT_PREPARED);
   const int ns = sb1 - sb0;
+  const unsigned long long tag = (unsigned long long)(ms->epoch + 1u) << 32;
 
   // ---------------------------------------------------------------- per-feature totals
   for (int f = warp; f < F; f += kWarps) {
     long long s = 0;
-    for (int i = lane; i < ns; i += 32) {
-      int l = p.lengths[(long long)f * B + sb0 + i];
-      if (l < 0) { local_flags |= DSF_FLAG_NEG_LENGTH; l = 0; }
-      if (l > kMaxBagLen) { local_flags |= DSF_FLAG_COUNT; l = kMaxBagLen; }
-      s += l;
+    const int* lp = p.lengths + (long long)f * B + sb0;
+    for (int i0 = 0; i0 < ns; i0 += 128) {
+      int l[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * 32 + lane;
+        l[k] = i < ns ? lp[i] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        int v = l[k];
+        if (v < 0) { local_flags |= DSF_FLAG_NEG_LENGTH; v = 0; }
+        if (v > kMaxBagLen) { local_flags |= DSF_FLAG_COUNT; v = kMaxBagLen; }
+        s += v;
+      }
     }
     s = warp_sum(s);
-    if (lane == 0) {
-      ms->ft[f] = s;
-      p.partials[(long long)cta * F + f] = s;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    // arrive on the grid barrier (generation-counting, reset by the last arrival)
-    const unsigned long long gen = ld_acquire_u64(p.bar_gen);
-    ms->gen0 = gen;
-    __threadfence();
-    const unsigned long long old = atomicAdd(p.bar_count, 1ull);
-    if (old == (unsigned long long)(G - 1)) {
-      atomicExch(p.bar_count, 0ull);
-      __threadfence();
-      atomicAdd(p.bar_gen, 1ull);
-    }
+    if (s > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; s = 0x7fffffffll; }
+    if (lane == 0) st_relaxed_u64(&p.partials[(long long)cta * F + f], tag | (unsigned long long)s);
   }
 
   // ---------------------------------------------------------------- batch setup
@@ -399,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     block_scan2(lv, lf, ms->scan64, ev, ef, tv, tf);
     if (tid < nb) {
       ms->rp[tid] = int(ev);
-      ms->so[tid] = ms->seq_cur + ef;
+      const long long so = ms->seq_cur + ef;
+      ms->so[tid] = so < p.n_seq ? int(so) : int(p.n_seq);
     }
     if (tid == 0) ms->rp[nb] = int(tv);
     __syncthreads();
@@ -407,82 +511,95 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     __syncthreads();
   };
 
-  // Row metadata and cp.async gather of the sequence rows of tile [t0, t0+n).
-  auto gather_tile = [&](int t0, int n, int nb) {
-    uint8_t* S = sm + C::S_OFF;
-    if (tid < C::TM) {
-      if (tid < n) {
-        const int r = t0 + tid;
-        const int i = upper_index(ms->rp, nb + 1, r);
-        ms->row_samp[tid] = i;
-        const long long j = ms->so[i] + (r - ms->rp[i]);
-        ms->row_j[tid] = j < p.n_seq ? int(j) : -1;
-      } else {
-        ms->row_samp[tid] = 0;
-        ms->row_j[tid] = -1;
-      }
+  // Id load of this thread's sub-row of tile [t0, t0+n): item = tid -> (row, key).
+  auto seq_ids = [&](int t0, int n, int nb) -> SeqItem {
+    SeqItem it;
+    it.valid = tid < 3 * n;
+    it.id = -1;
+    it.r = tid / 3;
+    it.k = tid - 3 * it.r;
+    it.i = 0;
+    it.j = -1;
+    if (it.valid) {
+      const int rr = t0 + it.r;
+      it.i = upper_index(ms->rp, nb + 1, rr);
+      const long long j = (long long)ms->so[it.i] + (rr - ms->rp[it.i]);
+      it.j = j < p.n_seq ? int(j) : -1;
+      if (it.j >= 0) it.id = p.seq_values[(long long)it.k * p.n_seq + it.j];
     }
-    __syncthreads();
-    for (int item = tid; item < 3 * n; item += kThreads) {
-      const int r = item / 3, k = item - 3 * r;
-      const int j = ms->row_j[r];
-      const int tb = p.seq_table[k];
+    return it;
+  };
+  // Row metadata and the row copy (L1-allocating cp.async) of a prefetched item.
+  auto seq_rows = [&](const SeqItem& it) {
+    if (it.valid) {
+      if (it.k == 0) {
+        ms->row_samp[it.r] = it.i;
+        ms->row_j[it.r] = it.j;
+      }
+      const int tb = p.seq_table[it.k];
       const uint8_t* base = static_cast<const uint8_t*>(p.tables[tb]);
       bool ok = false;
-      long long id = 0;
-      if (j >= 0) {
-        id = p.seq_values[(long long)k * p.n_seq + j];
-        ok = id >= 0 && id < p.rows[tb];
+      if (it.j >= 0) {
+        ok = it.id >= 0 && it.id < p.rows[tb];
         if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
       } else {
         local_flags |= DSF_FLAG_COUNT;
       }
-      uint8_t* dst = S + r * C::SROWB + k * C::ROWB;
-      const uint8_t* src = ok ? base + id * C::ROWB : base;
+      uint8_t* dst = sm + C::S_OFF + it.r * C::SROWB + it.k * C::ROWB;
+      const uint8_t* src = ok ? base + it.id * C::ROWB : base;
 #pragma unroll
-      for (int q = 0; q < C::LPB; ++q) cp_async_16(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
+      for (int q = 0; q < C::LPB; ++q) cp_async_16_ca(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
     }
     cp_async_commit();
   };
 
-  int first_nb = 0;
   bool prefetched = false;
   if constexpr (C::ATTN) {
     if (ns > 0) {
       const int be = min(sb0 + kSB, sb1);
-      first_nb = be - sb0;
       setup_batch(sb0, be);
-      if (attn_ok && ms->rp[first_nb] > 0) {
-        gather_tile(0, min(C::TM, ms->rp[first_nb]), first_nb);
+      if (attn_ok && ms->rp[be - sb0] > 0) {
+        const SeqItem it = seq_ids(0, min(C::TM, ms->rp[be - sb0]), be - sb0);
+        seq_rows(it);
         prefetched = true;
       }
     }
   }
 
-  // ---------------------------------------------------------------- barrier wait
-  if (tid == 0) {
+  // ---------------------------------------------------------------- exchange
+  // Every CTA's per-feature totals, read once they carry this launch's tag.
+  {
     bool ok = true;
-    if (ld_acquire_u64(p.bar_gen) == ms->gen0) {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_u64(p.bar_gen) == ms->gen0) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) { ok = false; break; }
-        __nanosleep(64);
-      }
-    }
-    ms->abort_ = ok ? 0 : 1;
-  }
-  __syncthreads();
-  const bool aborted = ms->abort_ != 0;
-  if (aborted) {
-    if (tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
-  } else {
-    // base value index of each feature for this CTA's samples
     for (int f = warp; f < F; f += kWarps) {
       long long tot = 0, pre = 0;
-      for (int c2 = lane; c2 < G; c2 += 32) {
-        const long long v = __ldcg(&p.partials[(long long)c2 * F + f]);
-        tot += v;
-        if (c2 < cta) pre += v;
+      for (int c0 = 0; c0 < G && ok; c0 += 256) {
+        unsigned long long v[8];
+        uint64_t t0 = 0;
+        while (true) {
+          bool all = true;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c2 = c0 + k * 32 + lane;
+            v[k] = c2 < G ? ld_relaxed_u64(&p.partials[(long long)c2 * F + f]) : tag;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) all = all && ((v[k] & 0xffffffff00000000ull) == tag);
+          if (__all_sync(0xffffffffu, all)) break;
+          if (t0 == 0) {
+            t0 = globaltimer_ns();
+          } else if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c2 = c0 + k * 32 + lane;
+          const long long x = c2 < G ? (long long)(v[k] & 0xffffffffull) : 0;
+          tot += x;
+          if (c2 < cta) pre += x;
+        }
       }
       tot = warp_sum(tot);
       pre = warp_sum(pre);
@@ -491,7 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         ms->ft[f] = tot;
       }
     }
-    __syncthreads();
+    if (!ok && lane == 0) ms->abort_ = 1;
+  }
+  __syncthreads();
+  const bool aborted = ms->abort_ != 0;
+  if (aborted) {
+    if (tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
+  } else {
     if (tid < F) {
       long long base = ms->fpre[tid];
       for (int f = 0; f < tid; ++f) base += ms->ft[f];
@@ -527,24 +650,28 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 
     // ------------------------------------------------------------ pooling
     {
-      uint8_t* stage = sm + C::ACT_OFF;
-      uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::POOL_STAGE_BYTES);
       const int nbag = F * nb;
+      const int offs_bytes = ((nbag + 1) * 4 + 15) / 16 * 16;
+      uint8_t* stage = sm + C::ACT_OFF;
+      uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::ACT_BYTES - offs_bytes);
+      const int cap = (C::ACT_BYTES - offs_bytes) / C::ROWB;
       const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
       const int g0 = tid * per;
       int loc[8];
-      long long s = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         loc[k] = 0;
         const int g = g0 + k;
         if (k < per && g < nbag) {
           const int f = g / nb, i = g - f * nb;
-          int l = p.lengths[(long long)f * B + bs + i];
-          l = min(max(l, 0), kMaxBagLen);
-          loc[k] = l;
-          s += l;
+          loc[k] = p.lengths[(long long)f * B + bs + i];
         }
+      }
+      long long s = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        loc[k] = min(max(loc[k], 0), kMaxBagLen);
+        s += loc[k];
       }
       long long ex, d0, tot, d1;
       block_scan2(s, 0, ms->scan64, ex, d0, tot, d1);
@@ -563,27 +690,43 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       __syncthreads();
       const long long U = tot;
       int widx = 0;
-      for (long long w0 = 0; w0 < U; w0 += C::POOL_CAP, ++widx) {
-        const long long w1 = min(U, w0 + (long long)C::POOL_CAP);
-        for (long long u = w0 + tid; u < w1; u += kThreads) {
-          const int g = upper_index(offs, nbag + 1, u);
-          const int f = g / nb;
-          if (!want_feature(f)) continue;
-          const long long gv = ms->fcur[f] + (u - (long long)offs[f * nb]);
-          const uint8_t* tbase = static_cast<const uint8_t*>(p.tables[f]);
-          bool ok = false;
-          long long id = 0;
-          if (gv < p.n_values) {
-            id = p.values[gv];
-            ok = id >= 0 && id < p.rows[f];
-            if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
-          } else {
-            local_flags |= DSF_FLAG_COUNT;
+      for (long long w0 = 0; w0 < U; w0 += cap, ++widx) {
+        const long long w1 = min(U, w0 + (long long)cap);
+        // ids first (all loads in flight), then the row copies
+        long long idv[C::VPT];
+        int fv[C::VPT];
+        bool inw[C::VPT];
+#pragma unroll
+        for (int k = 0; k < C::VPT; ++k) {
+          const long long u = w0 + tid + (long long)k * kThreads;
+          inw[k] = false;
+          idv[k] = -1;
+          fv[k] = 0;
+          if (u < w1) {
+            const int g = upper_index(offs, nbag + 1, u);
+            const int f = g / nb;
+            fv[k] = f;
+            if (want_feature(f)) {
+              inw[k] = true;
+              const long long gv = ms->fcur[f] + (u - (long long)offs[f * nb]);
+              if (gv < p.n_values) idv[k] = p.values[gv];
+              else local_flags |= DSF_FLAG_COUNT;
+            }
           }
+        }
+#pragma unroll
+        for (int k = 0; k < C::VPT; ++k) {
+          if (!inw[k]) continue;
+          const long long u = w0 + tid + (long long)k * kThreads;
+          const int f = fv[k];
+          const uint8_t* tbase = static_cast<const uint8_t*>(p.tables[f]);
+          const long long id = idv[k];
+          const bool ok = id >= 0 && id < p.rows[f];
+          if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
           uint8_t* dst = stage + (u - w0) * C::ROWB;
           const uint8_t* src = ok ? tbase + id * C::ROWB : tbase;
 #pragma unroll
-          for (int q = 0; q < C::LPB; ++q) cp_async_16(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
+          for (int q = 0; q < C::LPB; ++q) cp_async_16_ca(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
         }
         cp_async_commit();
         cp_async_wait_all();
@@ -672,11 +815,20 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       }
       const int R = ms->rp[nb];
       int tix = 0;
+      if (R > 0 && !(prefetched && bs == sb0)) {
+        const SeqItem it = seq_ids(0, min(C::TM, R), nb);
+        seq_rows(it);
+      }
       for (int t0 = 0; t0 < R && !tc_fail; t0 += C::TM, ++tix) {
         const int n = min(C::TM, R - t0);
-        if (!(prefetched && bs == sb0 && t0 == 0)) gather_tile(t0, n, nb);
         cp_async_wait_all();
         __syncthreads();
+        // ids of the next tile: loads in flight while this tile computes
+        const int t1 = t0 + C::TM;
+        const bool has_next = t1 < R;
+        SeqItem nxt;
+        nxt.valid = false;
+        if (has_next) nxt = seq_ids(t1, min(C::TM, R - t1), nb);
         const uint8_t* S = sm + C::S_OFF;
 
         if constexpr (C::MODE == 0) {
@@ -738,17 +890,15 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
                            sw128_kmajor_desc(wa + kb * kN1 * 128 + ko), IDESC1, kk > 0);
               }
               tc_commit(&ms->mbar_mma);
+              // one thread waits for the MMAs, the block learns the outcome together
+              ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
             } else {
               ms->abort_ = 2;
             }
           }
-          __syncthreads();
-          if (ms->abort_ == 2) { tc_fail = true; break; }
-          // one thread waits for the MMAs, the block learns the outcome together
-          if (tid == 0) ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
           mma_phase ^= 1u;
           __syncthreads();
-          if (ms->abort_ == 3) { tc_fail = true; break; }
+          if (ms->abort_ != 0) { tc_fail = true; break; }
           tc_fence_after();
           // ---------------------------------------------- epilogue 1: h1 = ReLU(acc + b1) -> bf16
           {
@@ -793,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           }
           mma_phase ^= 1u;
           __syncthreads();
-          if (ms->abort_ == 3) { tc_fail = true; break; }
+          if (ms->abort_ != 0) { tc_fail = true; break; }
           tc_fence_after();
           // ---------------------------------------------- epilogue 2: z = w3 . ReLU(acc + b2) + b3
           {
@@ -899,18 +1049,28 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         }
 
         // ---------------------------------------------- masked softmax + weighted sum
+        // Per sample segment of the tile (a warp each): running max m and sum l
+        // over its valid rows (merged with the state carried from the previous
+        // tile), z[r] <- exp(z[r] - m). Then one thread per (segment, d)
+        // accumulates sum_r exp(z_r - m) s[r][d] in row order.
         {
           const int ia = ms->row_samp[0], ib = ms->row_samp[n - 1];
+          const int nseg = ib - ia + 1;
           float* cin = ms->carry[tix & 1];
           float* cout = ms->carry[(tix + 1) & 1];
+          float* seg_sc = ms->red[0];   // scale of the carried-in state
+          float* seg_inv = ms->red[1];  // 1 / l, or 0 when the segment carries out
+          float* seg_m = ms->red[2];
+          float* seg_l = ms->red[3];
           if (p.logits) {
             for (int r = tid; r < n; r += kThreads) {
               const int j = ms->row_j[r];
               if (j >= 0) p.logits[j] = ms->z[r];
             }
+            __syncthreads();
           }
-          __syncthreads();
-          for (int si = ia + warp; si <= ib; si += kWarps) {
+          for (int g = warp; g < nseg; g += kWarps) {
+            const int si = ia + g;
             const int ra = ms->rp[si], re = ms->rp[si + 1];
             const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
             if (r1 <= r0) continue;
@@ -921,31 +1081,44 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             if (has_in) m = fmaxf(m, cin[0]);
             float l = 0.f;
             for (int r = r0 + lane; r < r1; r += 32) {
-              const float e = expf(ms->z[r] - m);
-              ms->z[r] = e;
-              l += e;
+              const float ez = expf(ms->z[r] - m);
+              ms->z[r] = ez;
+              l += ez;
             }
             l = warp_sum(l);
-            float sc = 0.f;
-            if (has_in) {
-              sc = expf(cin[0] - m);
-              l += cin[1] * sc;
+            if (lane == 0) {
+              const float sc = has_in ? expf(cin[0] - m) : 0.f;
+              if (has_in) l += cin[1] * sc;
+              seg_sc[g] = sc;
+              seg_inv[g] = has_out ? 0.f : 1.f / l;
+              seg_m[g] = m;
+              seg_l[g] = l;
             }
-            __syncwarp();
-            const long long b = bs + si;
-            for (int d = lane; d < Q; d += 32) {
-              float acc = has_in ? cin[4 + d] * sc : 0.f;
-              for (int r = r0; r < r1; ++r) acc = fmaf(ms->z[r], s_elem<C::BF16>(S, C::SROWB, r, d), acc);
-              if (has_out) cout[4 + d] = acc;
-              else p.din[b * Q + d] = acc / l;
-            }
-            if (has_out && lane == 0) {
-              cout[0] = m;
-              cout[1] = l;
+          }
+          __syncthreads();
+          for (int item = tid; item < nseg * Q; item += kThreads) {
+            const int g = item / Q, d = item - g * Q;
+            const int si = ia + g;
+            const int ra = ms->rp[si], re = ms->rp[si + 1];
+            const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
+            if (r1 <= r0) continue;
+            const bool has_in = ra < t0, has_out = re > t0 + n;
+            float acc = has_in ? cin[4 + d] * seg_sc[g] : 0.f;
+            for (int r = r0; r < r1; ++r) acc = fmaf(ms->z[r], s_elem<C::BF16>(S, C::SROWB, r, d), acc);
+            if (has_out) {
+              cout[4 + d] = acc;
+              if (d == 0) {
+                cout[0] = seg_m[g];
+                cout[1] = seg_l[g];
+              }
+            } else {
+              p.din[(long long)(bs + si) * Q + d] = acc * seg_inv[g];
             }
           }
           __syncthreads();
         }
+        // the next tile's rows: S and the row metadata are free again
+        if (has_next) seq_rows(nxt);
       }
     }
   }
@@ -969,6 +1142,17 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
   }
   if (tc_fail && tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
+  // the last CTA to finish advances the epoch for the next launch
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned long long old = atomicAdd(p.done, 1ull);
+    if (old == (unsigned long long)(G - 1)) {
+      atomicExch(p.done, 0ull);
+      __threadfence();
+      atomicExch(p.epoch, ms->epoch + 1u);
+    }
+  }
   // one status write per warp
   local_flags = __reduce_or_sync(0xffffffffu, local_flags);
   if (lane == 0 && local_flags) flag(p.status, local_flags);
