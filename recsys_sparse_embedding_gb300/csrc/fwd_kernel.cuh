@@ -428,22 +428,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         if (wp + wc <= lo1) n1 += e - a;
       }
       if (cross0 || cross1) {
-        long long rr = wp;
-        for (int i = a; i < e; i += 32) {
-          const int idx = i + lane;
-          long long c = 0, lf = 0;
-          if (idx < e) {
-            const int L = sl[idx];
-            lf = max(L, 0);
-            c = p.cost0 + min(lf, (long long)p.max_len);
-          }
-          const long long inc = warp_incl_scan(c);
-          const long long ex = rr + inc - c;
-          if (idx < e) {
-            if (cross0 && ex < lo0) { ++n0; l0 += lf; }
-            if (cross1 && ex < lo1) ++n1;
-          }
-          rr += __shfl_sync(0xffffffffu, inc, 31);
+        // each lane a contiguous run; one warp scan of the run totals
+        const int run_len = (e - a + 31) / 32;
+        const int la = min(e, a + lane * run_len), le = min(e, la + run_len);
+        int lsum = 0;
+        for (int i = la; i < le; ++i) lsum += int(cost_of(sl[i]));
+        long long rr = wp + (warp_incl_scan(lsum) - lsum);
+        for (int i = la; i < le; ++i) {
+          const int L = sl[i];
+          const long long lf = max(L, 0);
+          if (cross0 && rr < lo0) { ++n0; l0 += lf; }
+          if (cross1 && rr < lo1) ++n1;
+          rr += cost_of(L);
         }
       }
       run += chunk_tot;
@@ -483,7 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
     s = warp_sum(s);
     if (s > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; s = 0x7fffffffll; }
-    if (lane == 0) st_relaxed_u64(&p.partials[(long long)cta * F + f], tag | (unsigned long long)s);
+    if (lane == 0) {
+      st_relaxed_u64(&p.partials[(long long)cta * F + f], tag | (unsigned long long)s);
+      __threadfence();  // push the tagged total out to L2 now
+    }
   }
 
   // ---------------------------------------------------------------- batch setup
@@ -554,13 +553,14 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   };
 
   bool prefetched = false;
+  SeqItem first_item;
+  first_item.valid = false;
   if constexpr (C::ATTN) {
     if (ns > 0) {
       const int be = min(sb0 + kSB, sb1);
       setup_batch(sb0, be);
       if (attn_ok && ms->rp[be - sb0] > 0) {
-        const SeqItem it = seq_ids(0, min(C::TM, ms->rp[be - sb0]), be - sb0);
-        seq_rows(it);
+        first_item = seq_ids(0, min(C::TM, ms->rp[be - sb0]), be - sb0);
         prefetched = true;
       }
     }
@@ -610,6 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
     if (!ok && lane == 0) ms->abort_ = 1;
   }
+  // the first tile's row copies go out once the exchange no longer competes
+  // with them for the load pipeline
+  if (C::ATTN && prefetched) seq_rows(first_item);
   __syncthreads();
   const bool aborted = ms->abort_ != 0;
   if (aborted) {
@@ -651,6 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     // ------------------------------------------------------------ pooling
     {
       const int nbag = F * nb;
+      // g / nb as a multiply-shift, exact for g < 4097 and nb <= 128
+      const unsigned int nb_recip = ((1u << 20) + unsigned(nb) - 1u) / unsigned(nb);
+      auto feat_of = [&](int g) -> int { return int((unsigned(g) * nb_recip) >> 20); };
       const int offs_bytes = ((nbag + 1) * 4 + 15) / 16 * 16;
       uint8_t* stage = sm + C::ACT_OFF;
       uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::ACT_BYTES - offs_bytes);
@@ -704,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           fv[k] = 0;
           if (u < w1) {
             const int g = upper_index(offs, nbag + 1, u);
-            const int f = g / nb;
+            const int f = feat_of(g);
             fv[k] = f;
             if (want_feature(f)) {
               inw[k] = true;
@@ -741,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         for (int g = ga + grp; g <= gb; g += NGRP) {
           const long long a = offs[g], e = offs[g + 1];
           if (a == e) continue;
-          const int f = g / nb;
+          const int f = feat_of(g);
           if (!want_feature(f)) continue;
           float acc[C::EPL];
           if (a < w0) {
