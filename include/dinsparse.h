@@ -156,6 +156,25 @@ int din_sparse_fwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* 
                    const dsf_mlp* mlp, float* pooled_dev, float* din_dev, float* logits_dev,
                    void* workspace_dev, size_t ws_bytes, int32_t* status_dev, void* stream);
 
+/* (a) EmbeddingBag sum pooling, as emb_bag_pool, for callers that cannot
+ * allocate device memory -- for instance a serving runtime whose device memory
+ * belongs to its own arena allocator, or code that runs inside a stream
+ * capture, where cudaMalloc is not permitted. The pages have no counterpart to
+ * this entry point; it exists only for such callers.
+ * It takes no workspace: the cross-CTA exchange state (a header and one partial
+ * sum per CTA and table) lives in a fixed 262,400-byte array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits. Limits: F <= DSF_MAX_TABLES (32) and a kernel grid of at most 1024
+ * CTAs (larger devices get DSF_EUNSUPPORTED); B is not limited by the array.
+ * The first call on a device, made with that device current, looks up the
+ * array's device address and clears it on `stream`; make that first call
+ * before any stream capture. Every call shares the one array and leaves it
+ * ready for the next call, so calls that overlap on the GPU (for instance on
+ * two streams) race: serialise them. Allocates nothing (no cudaMalloc or
+ * cudaFree, no allocating library call). */
+int emb_bag_pool_noalloc(const dsf_tables* tables, const dsf_kjt* kjt, int32_t B,
+                         float* pooled_dev, int32_t* status_dev, void* stream);
+
 /* Human-readable name of a return code. */
 const char* dsf_status_string(int code);
 

@@ -26,7 +26,8 @@ FLAG_TIMEOUT = 0x10
 FLAG_NOT_PREPARED = 0x20
 
 EXPORTS = ["dsf_workspace_bytes", "dsf_workspace_init", "dsf_prepare_mlp", "emb_bag_pool",
-           "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size"]
+           "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size",
+           "emb_bag_pool_noalloc"]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.din_sparse_fwd.restype = ctypes.c_int
         L.dsf_status_string.argtypes = [ctypes.c_int]
         L.dsf_status_string.restype = ctypes.c_char_p
+        L.emb_bag_pool_noalloc.argtypes = [P(CTables), P(CKjt), _i32, _vp, _vp, _vp]
+        L.emb_bag_pool_noalloc.restype = ctypes.c_int
         L.dsf_grid_size.argtypes = [_i32, _i32, _i32, _i32]
         L.dsf_grid_size.restype = _i32
         _lib = L
@@ -187,6 +190,18 @@ def emb_bag_pool(tables: EmbeddingTables, values: torch.Tensor, lengths: torch.T
     _check(lib().emb_bag_pool(ctypes.byref(tables.c), ctypes.byref(kjt), int(B), pooled.data_ptr(),
                               workspace.ptr, workspace.nbytes, _dptr(status), _stream_ptr(stream)),
            "emb_bag_pool")
+    return pooled
+
+
+def emb_bag_pool_noalloc(tables: EmbeddingTables, values: torch.Tensor, lengths: torch.Tensor,
+                         B: int, pooled: torch.Tensor, status: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """emb_bag_pool without a workspace, for callers that cannot allocate
+    device memory; its scratch is a fixed array inside the library."""
+    kjt = _kjt(values, lengths)
+    _check(lib().emb_bag_pool_noalloc(ctypes.byref(tables.c), ctypes.byref(kjt), int(B),
+                                      pooled.data_ptr(), _dptr(status), _stream_ptr(stream)),
+           "emb_bag_pool_noalloc")
     return pooled
 
 

@@ -3,6 +3,7 @@
 // function here allocates device memory; every buffer belongs to the caller.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "dinsparse.h"
 #include "launch.cuh"
@@ -266,6 +267,73 @@ int32_t dsf_grid_size(int32_t D, int32_t dtype, int32_t mode, int32_t with_atten
   if (!with_attention) return grid_pool(D, bf16, dev);
   if (mode == DSF_MODE_BF16_TC) return grid_attn_tc(D, bf16, dev);
   return grid_attn_f32(D, bf16, dev);
+}
+
+// ---------------------------------------------------------------------------
+// EmbeddingBag pooling without a caller workspace.
+//
+// For callers that cannot allocate device memory, e.g. a serving runtime whose
+// device memory is owned by its own arena allocator, or code that runs while a
+// stream is being captured, where cudaMalloc is not allowed. The pooling
+// kernel's only scratch is the exchange state (workspace header plus the
+// per-CTA partial sums); here it lives in one fixed array compiled into the
+// library instead. Host code must not use the array's name as a device
+// address: its address is looked up per device at first use.
+
+}  // extern "C"
+
+namespace dsf {
+namespace {
+
+// Header + partials for up to kMaxG CTAs x kMaxF tables: 262,400 bytes held on
+// every device that loads the library, until the process exits.
+constexpr size_t kStaticScratchBytes = kWsWpackOff;
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, cleared on the
+// first call for that device (the clear is queued on `stream`).
+int static_scratch(int dev, cudaStream_t stream, void** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return DSF_ECUDA;
+    if (cudaMemsetAsync(ptr, 0, kStaticScratchBytes, stream) != cudaSuccess) return DSF_ECUDA;
+    g_static_ptr[dev] = ptr;
+  }
+  *out = g_static_ptr[dev];
+  return DSF_OK;
+}
+
+}  // namespace
+}  // namespace dsf
+
+extern "C" {
+
+int emb_bag_pool_noalloc(const dsf_tables* tables, const dsf_kjt* kjt, int32_t B,
+                         float* pooled_dev, int32_t* status_dev, void* stream) {
+  int rc;
+  if ((rc = check_tables(tables)) != DSF_OK) return rc;
+  if (B < 0 || B > (1 << 24)) return DSF_EINVAL;
+  if ((rc = check_kjt(kjt, B, tables->F)) != DSF_OK) return rc;
+  if (!pooled_dev || !aligned(pooled_dev, 16)) return DSF_EINVAL;
+  if (B == 0) return DSF_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSF_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DSF_EUNSUPPORTED;
+  const bool bf16 = tables->dtype == DSF_BF16;
+  const int G = grid_pool(tables->D, bf16, dev);
+  if (G <= 0 || G > kMaxG) return DSF_EUNSUPPORTED;  // scratch holds kMaxG CTAs
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if ((rc = static_scratch(dev, s, &scratch)) != DSF_OK) return rc;
+  FwdParams p;
+  fill_common(p, tables, kjt, B, scratch, status_dev);
+  p.pooled = pooled_dev;
+  p.max_len = 1;
+  return map_launch(launch_pool(tables->D, bf16, p, s));
 }
 
 }  // extern "C"
