@@ -11,8 +11,6 @@
 namespace dsf {
 namespace {
 
-constexpr int kCost0 = 4;  // per-sample cost (in sequence positions) of the work split
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
@@ -110,7 +108,6 @@ void fill_common(FwdParams& p, const dsf_tables* t, const dsf_kjt* k, int32_t B,
   }
   p.F = t->F;
   p.B = B;
-  p.cost0 = kCost0;
   p.values = reinterpret_cast<const long long*>(k->values_dev);
   p.n_values = k->n_values;
   p.lengths = k->lengths_dev;

@@ -16,9 +16,8 @@
 //     s2.4 sequence sub-features share the target features' tables
 //     s3.3 lookup in fp32, MLP in half precision (bf16 here)
 //
-// Work split. Every CTA stages seq_lengths in shared memory, scans it and
-// takes a contiguous sample range balanced by cost = cost0 + valid positions.
-// It pools all F bags of its own samples (so each pooled row is written by one
+// Work split. CTA c takes the contiguous samples [c*B/G, (c+1)*B/G). It pools
+// all F bags of its own samples (so each pooled row is written by one
 // CTA) and then runs attention for the same samples, so the query never
 // crosses CTAs. The only cross-CTA exchange is the per-feature length total of
 // each CTA's samples, needed to place its bags in the key-major values array.
@@ -56,7 +55,7 @@ constexpr uint32_t kMagicBase = 0x44534600u;  // 'DSF\0' | D
 struct FwdParams {
   const void* tables[kMaxF];
   long long rows[kMaxF];
-  int F, B, max_len, cost0;
+  int F, B, max_len;
   const long long* values;
   long long n_values;
   const int* lengths;
@@ -75,7 +74,7 @@ struct FwdParams {
   const uint32_t* magic;
   unsigned long long* done;      // CTAs that finished this launch
   unsigned int* epoch;           // launch counter, tags the partials
-  unsigned long long* partials;  // [G][F]: (epoch + 1) << 32 | length total
+  unsigned long long* partials;  // [G][kMaxF]: (epoch + 1) << 32 | length total
   int* status;
 };
 
@@ -93,7 +92,10 @@ struct Cfg {
   static constexpr int Q = 3 * D;
   static constexpr int K1 = 4 * Q;
   static constexpr int TM = MODE == 0 ? 128 : 64;  // rows per attention tile
-  static constexpr int SROWB = Q * ES;             // bytes per S row
+  // bytes per S row; the tensor-core mode pads each row by 16 bytes so that a
+  // warp reading one 16-byte piece of 32 consecutive rows hits every bank
+  static constexpr int SROWB = Q * ES + (MODE == 0 ? 16 : 0);
+  static constexpr int QROW = Q + 4;               // floats per q-tile row (padded)
   static_assert(D % 8 == 0, "D must be a multiple of 8");
 
   // pool region: bag offsets at its end (F*nb+1 words), staging rows before
@@ -111,20 +113,29 @@ struct Cfg {
 
   static constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-  // byte offsets from the 1024-aligned smem base
+  // Byte offsets from the 1024-aligned smem base. In the tensor-core mode the
+  // attention input x and h1 live in tensor memory, and the sequence rows S are
+  // double-buffered: [W1 | W2 | ACT | S1 | S0 | misc]. Pooling stages rows in
+  // ACT and S1 (S1 is free then: only the first tile is in flight, in S0).
+  static constexpr bool TWO_S = ATTN && MODE == 0;
   static constexpr int W1_OFF = 0;
   static constexpr int W2_OFF = (ATTN && MODE == 0) ? W1_OFF + W1B : 0;
   static constexpr int ACT_OFF = (ATTN && MODE == 0) ? W2_OFF + W2B : 0;
   static constexpr int ACT_BYTES =
-      !ATTN ? POOL_BYTES : (MODE == 0 ? cmax(cmax(XB, H1B), POOL_BYTES) : cmax(H1FB, POOL_BYTES));
+      !ATTN ? POOL_BYTES : (MODE == 0 ? 36 * 1024 : cmax(H1FB, POOL_BYTES));
   static constexpr int QT_OFF = ACT_OFF + ACT_BYTES;  // fp32 mode only
-  static constexpr int S_OFF = QT_OFF + ((ATTN && MODE == 1) ? QTB : 0);
   static constexpr int S_BYTES = ATTN ? TM * SROWB : 0;
+  static constexpr int S1_OFF = QT_OFF + ((ATTN && MODE == 1) ? QTB : 0);
+  static constexpr int S_OFF = S1_OFF + (TWO_S ? S_BYTES : 0);  // buffer 0
   static constexpr int MISC_OFF = (S_OFF + S_BYTES + 127) / 128 * 128;
+  static constexpr int POOL_AVAIL = ACT_BYTES + (TWO_S ? S_BYTES : 0);
   // values a thread stages per pooling window
-  static constexpr int VPT = (ACT_BYTES / ROWB + kThreads - 1) / kThreads;
-  // seq_lengths staged per chunk of the partition scan
-  static constexpr int SEQ_CHUNK = ACT_BYTES / 4;
+  static constexpr int VPT = (POOL_AVAIL / ROWB + kThreads - 1) / kThreads;
+  // tensor-memory columns: layer-1 accumulator (h1 packed over its first half),
+  // layer-2 accumulator, the bf16 x tile
+  static constexpr uint32_t TM_ACC1 = 0, TM_ACC2 = kN1, TM_X = kN1 + kN2;
+  static_assert(!(ATTN && MODE == 0) || TM_X + K1 / 2 <= 512, "tensor memory columns");
+  static_assert(!(ATTN && MODE == 0) || TM * QROW * 4 <= ACT_BYTES, "q tile");
 };
 
 template <int D, int Q>
@@ -136,8 +147,8 @@ struct Misc {
   float red[4][128];
   float carry[2][4 + Q];       // softmax state: m, l, -, -, acc[Q]
   float pcarry[2][D];          // pooling carry of a bag that spans windows
-  int row_samp[128];
-  int row_j[128];
+  int row_samp[2][128];         // per S buffer: sample of each tile row
+  int row_j[2][128];            // per S buffer: sequence value index of each row
   int rp[kSB + 4];             // valid-row prefix of the batch's samples
   int so[kSB];                 // first sequence value index of each sample
   long long fcur[kMaxF];       // next global value index of feature f for this CTA
@@ -145,7 +156,6 @@ struct Misc {
   long long fpre[kMaxF];
   long long scan64[2][kWarps + 2];
   long long red3[3][kWarps];
-  long long wtot[2][kWarps];
   uint64_t mbar_w;
   uint64_t mbar_mma;
   unsigned int tmem_base;
@@ -288,14 +298,6 @@ __device__ __forceinline__ float s_elem(const uint8_t* S, int srowb, int r, int 
   }
 }
 
-// One gathered sequence sub-row of a tile, held in registers between the id
-// load and the row copy.
-struct SeqItem {
-  long long id;
-  int r, k, i, j;
-  bool valid;
-};
-
 // ------------------------------------------------------------------ kernel
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -349,110 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   const float b3 = C::ATTN ? __ldg(p.b3) : 0.f;
 
   // ---------------------------------------------------------------- partition
-  // Sample b belongs to CTA c when its exclusive cost prefix lies in
-  // [c*Ctot/G, (c+1)*Ctot/G); every CTA computes the same split. seq_lengths
-  // is staged in shared memory; each warp sums a contiguous run of samples and
-  // only the warps whose run contains a boundary scan it sample by sample.
-  int sb0, sb1;
-  if constexpr (C::ATTN) {
-    int* sl = reinterpret_cast<int*>(sm + C::ACT_OFF);
-    constexpr int CH = C::SEQ_CHUNK;
-    const bool single = B <= CH;
-    auto cost_of = [&](int L) -> long long { return p.cost0 + min(max(L, 0), p.max_len); };
-    auto stage = [&](int c0, int n) {
-      for (int i = tid; i < n; i += kThreads) cp_async_4(sl + i, p.seq_lengths + c0 + i);
-      cp_async_commit();
-      cp_async_wait_all();
-      __syncthreads();
-    };
-    // per-warp totals of the staged chunk (cost and full lengths) into ms->wtot
-    auto warp_totals = [&](int n, int& a, int& e) {
-      const int pw = ((n + kWarps * 32 - 1) / (kWarps * 32)) * 32;
-      a = min(n, warp * pw);
-      e = min(n, a + pw);
-      long long wc = 0, wl = 0;
-      for (int i = a + lane; i < e; i += 32) {
-        const int L = sl[i];
-        wc += cost_of(L);
-        wl += max(L, 0);
-      }
-      wc = warp_sum(wc);
-      wl = warp_sum(wl);
-      if (lane == 0) {
-        ms->wtot[0][warp] = wc;
-        ms->wtot[1][warp] = wl;
-      }
-      __syncthreads();
-    };
-    long long ctot = 0;
-    int a = 0, e = 0;
-    if (single) {
-      stage(0, B);
-      warp_totals(B, a, e);
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) ctot += ms->wtot[0][w];
-    } else {
-      long long csum = 0;
-      for (int c0 = 0; c0 < B; c0 += CH) {
-        const int n = min(CH, B - c0);
-        stage(c0, n);
-        for (int i = tid; i < n; i += kThreads) csum += cost_of(sl[i]);
-        __syncthreads();
-      }
-      long long u0 = 0, u1 = 0;
-      ctot = csum;
-      block_sum3(ctot, u0, u1, ms->red3);
-    }
-    const long long lo0 = (long long)cta * ctot / G;
-    const long long lo1 = (long long)(cta + 1) * ctot / G;
-    long long n0 = 0, n1 = 0, l0 = 0, run = 0;
-    for (int c0 = 0; c0 < B; c0 += CH) {
-      const int n = min(CH, B - c0);
-      if (!single) {
-        stage(c0, n);
-        warp_totals(n, a, e);
-      }
-      long long wp = run, chunk_tot = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const long long v = ms->wtot[0][w];
-        if (w < warp) wp += v;
-        chunk_tot += v;
-      }
-      const long long wc = ms->wtot[0][warp], wl = ms->wtot[1][warp];
-      // samples with exclusive prefix below each boundary
-      const bool cross0 = wp < lo0 && lo0 < wp + wc;
-      const bool cross1 = wp < lo1 && lo1 < wp + wc;
-      if (lane == 0) {
-        if (wp + wc <= lo0) { n0 += e - a; l0 += wl; }
-        if (wp + wc <= lo1) n1 += e - a;
-      }
-      if (cross0 || cross1) {
-        // each lane a contiguous run; one warp scan of the run totals
-        const int run_len = (e - a + 31) / 32;
-        const int la = min(e, a + lane * run_len), le = min(e, la + run_len);
-        int lsum = 0;
-        for (int i = la; i < le; ++i) lsum += int(cost_of(sl[i]));
-        long long rr = wp + (warp_incl_scan(lsum) - lsum);
-        for (int i = la; i < le; ++i) {
-          const int L = sl[i];
-          const long long lf = max(L, 0);
-          if (cross0 && rr < lo0) { ++n0; l0 += lf; }
-          if (cross1 && rr < lo1) ++n1;
-          rr += cost_of(L);
-        }
-      }
-      run += chunk_tot;
-      __syncthreads();
-    }
-    block_sum3(n0, n1, l0, ms->red3);
-    sb0 = int(n0);
-    sb1 = int(n1);
-    if (tid == 0) ms->seq_cur = l0;
-  } else {
-    sb0 = int((long long)cta * B / G);
-    sb1 = int((long long)(cta + 1) * B / G);
-  }
+  // Equal sample counts per CTA: no cross-CTA work is needed to place them.
+  const int sb0 = int((long long)cta * B / G);
+  const int sb1 = int((long long)(cta + 1) * B / G);
   attn_ok = C::ATTN && magic == (kMagicBase | uint32_t(D));
   if (C::ATTN && tid == 0 && !attn_ok && cta == 0) flag(p.status, DSF_FLAG_NOT_PREPARED);
   const int ns = sb1 - sb0;
@@ -480,9 +381,29 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     s = warp_sum(s);
     if (s > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; s = 0x7fffffffll; }
     if (lane == 0) {
-      st_relaxed_u64(&p.partials[(long long)cta * F + f], tag | (unsigned long long)s);
+      st_relaxed_u64(&p.partials[(long long)cta * kMaxF + f], tag | (unsigned long long)s);
       __threadfence();  // push the tagged total out to L2 now
     }
+  }
+
+  // ---------------------------------------------------------------- sequence offset
+  // First sequence value index of sample sb0: sum of the full lengths before it.
+  if constexpr (C::ATTN) {
+    long long acc = 0;
+    for (int b0 = 0; b0 < sb0; b0 += 4 * kThreads) {
+      int l[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int b = b0 + k * kThreads + tid;
+        l[k] = b < sb0 ? p.seq_lengths[b] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc += max(l[k], 0);
+    }
+    long long u0 = 0, u1 = 0;
+    block_sum3(acc, u0, u1, ms->red3);
+    if (tid == 0) ms->seq_cur = acc;
+    __syncthreads();
   }
 
   // ---------------------------------------------------------------- batch setup
@@ -511,108 +432,173 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   };
 
   // Id load of this thread's sub-row of tile [t0, t0+n): item = tid -> (row, key).
-  auto seq_ids = [&](int t0, int n, int nb) -> SeqItem {
-    SeqItem it;
-    it.valid = tid < 3 * n;
-    it.id = -1;
-    it.r = tid / 3;
-    it.k = tid - 3 * it.r;
-    it.i = 0;
-    it.j = -1;
-    if (it.valid) {
-      const int rr = t0 + it.r;
-      it.i = upper_index(ms->rp, nb + 1, rr);
-      const long long j = (long long)ms->so[it.i] + (rr - ms->rp[it.i]);
-      it.j = j < p.n_seq ? int(j) : -1;
-      if (it.j >= 0) it.id = p.seq_values[(long long)it.k * p.n_seq + it.j];
-    }
-    return it;
+  // Sequence rows of a tile [t0, t0+n): thread tid < 3n owns sub-row
+  // (r = tid/3, key k = tid%3). Only its id is kept in a register between the
+  // id load and the row copy; the rest is recomputed from rp[] / so[].
+  struct RowSlot { int r, k, i, j; };
+  auto row_slot = [&](int t0, int nb) -> RowSlot {
+    RowSlot rs;
+    rs.r = tid / 3;
+    rs.k = tid - 3 * rs.r;
+    const int rr = t0 + rs.r;
+    rs.i = upper_index(ms->rp, nb + 1, rr);
+    const long long j = (long long)ms->so[rs.i] + (rr - ms->rp[rs.i]);
+    rs.j = j < p.n_seq ? int(j) : -1;
+    return rs;
   };
-  // Row metadata and the row copy (L1-allocating cp.async) of a prefetched item.
-  auto seq_rows = [&](const SeqItem& it) {
-    if (it.valid) {
-      if (it.k == 0) {
-        ms->row_samp[it.r] = it.i;
-        ms->row_j[it.r] = it.j;
+  auto seq_ids = [&](int t0, int n, int nb) -> long long {
+    long long id = -1;
+    if (tid < 3 * n) {
+      const RowSlot rs = row_slot(t0, nb);
+      if (rs.j >= 0) id = p.seq_values[(long long)rs.k * p.n_seq + rs.j];
+    }
+    return id;
+  };
+  auto s_buf = [&](int buf) -> uint8_t* { return sm + (buf ? C::S1_OFF : C::S_OFF); };
+  // Row metadata and the row copy (L1-allocating cp.async) of a prefetched id.
+  auto seq_rows = [&](long long id, int t0, int n, int nb, int buf) {
+    if (tid < 3 * n) {
+      const RowSlot rs = row_slot(t0, nb);
+      if (rs.k == 0) {
+        ms->row_samp[buf][rs.r] = rs.i;
+        ms->row_j[buf][rs.r] = rs.j;
       }
-      const int tb = p.seq_table[it.k];
+      const int tb = p.seq_table[rs.k];
       const uint8_t* base = static_cast<const uint8_t*>(p.tables[tb]);
       bool ok = false;
-      if (it.j >= 0) {
-        ok = it.id >= 0 && it.id < p.rows[tb];
+      if (rs.j >= 0) {
+        ok = id >= 0 && id < p.rows[tb];
         if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
       } else {
         local_flags |= DSF_FLAG_COUNT;
       }
-      uint8_t* dst = sm + C::S_OFF + it.r * C::SROWB + it.k * C::ROWB;
-      const uint8_t* src = ok ? base + it.id * C::ROWB : base;
+      uint8_t* dst = s_buf(buf) + rs.r * C::SROWB + rs.k * C::ROWB;
+      const uint8_t* src = ok ? base + id * C::ROWB : base;
 #pragma unroll
       for (int q = 0; q < C::LPB; ++q) cp_async_16_ca(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
     }
     cp_async_commit();
   };
+  // The query slices of a tile's rows into the q tile (tensor-core mode):
+  // ACT + r*Q floats, part k at k*D, read back from this CTA's own pooled (or
+  // query-buffer) rows.
+  auto q_rows = [&](int t0, int n, int nb, int bs) {
+    if constexpr (C::TWO_S) {
+      if (tid < 3 * n) {
+        const RowSlot rs = row_slot(t0, nb);
+        const bool pa = p.pooled != nullptr;
+        const float* src = (pa ? p.pooled : p.qbuf) +
+                           (long long)(bs + rs.i) * (pa ? (long long)F * D : Q) +
+                           (pa ? p.q_feat[rs.k] * D : rs.k * D);
+        float* dst = reinterpret_cast<float*>(sm + C::ACT_OFF) + rs.r * C::QROW + rs.k * D;
+#pragma unroll
+        for (int q = 0; q < D / 4; ++q) cp_async_16_ca(dst + 4 * q, src + 4 * q, 16u);
+      }
+      cp_async_commit();
+    }
+  };
 
   bool prefetched = false;
-  SeqItem first_item;
-  first_item.valid = false;
+  long long first_id = -1, second_id = -1;
+  int first_n = 0, second_n = 0;
   if constexpr (C::ATTN) {
     if (ns > 0) {
       const int be = min(sb0 + kSB, sb1);
       setup_batch(sb0, be);
-      if (attn_ok && ms->rp[be - sb0] > 0) {
-        first_item = seq_ids(0, min(C::TM, ms->rp[be - sb0]), be - sb0);
+      const int R0 = ms->rp[be - sb0];
+      if (attn_ok && R0 > 0) {
+        first_n = min(C::TM, R0);
+        first_id = seq_ids(0, first_n, be - sb0);
+        if (C::TWO_S && R0 > C::TM) {
+          second_n = min(C::TM, R0 - C::TM);
+          second_id = seq_ids(C::TM, second_n, be - sb0);
+        }
         prefetched = true;
       }
     }
   }
 
   // ---------------------------------------------------------------- exchange
-  // Every CTA's per-feature totals, read once they carry this launch's tag.
+  // Every CTA's per-feature totals, read as whole 256-byte rows (16 threads per
+  // row, 16 bytes each) once all of them carry this launch's tag. Thread t
+  // always holds features 2*(t%16) and 2*(t%16)+1.
   {
+    const int jp = tid & 15;                 // feature pair
+    const int f0 = 2 * jp, f1 = f0 + 1;
+    const bool w0 = f0 < F, w1 = f1 < F;
+    long long tot0 = 0, tot1 = 0, pre0 = 0, pre1 = 0;
     bool ok = true;
-    for (int f = warp; f < F; f += kWarps) {
-      long long tot = 0, pre = 0;
-      for (int c0 = 0; c0 < G && ok; c0 += 256) {
-        unsigned long long v[8];
-        uint64_t t0 = 0;
-        while (true) {
-          bool all = true;
+    uint64_t t0 = 0;
+    for (int r0 = 0; r0 < G; r0 += kThreads / 16 * 4) {
+      unsigned long long v[4][2];
+      while (true) {
+        bool ready = true;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int c2 = c0 + k * 32 + lane;
-            v[k] = c2 < G ? ld_relaxed_u64(&p.partials[(long long)c2 * F + f]) : tag;
+        for (int k = 0; k < 4; ++k) {
+          const int c = r0 + k * (kThreads / 16) + (tid >> 4);
+          if (c < G) {
+            const ulonglong2 x = ld_relaxed_u64x2(&p.partials[(long long)c * kMaxF + f0]);
+            v[k][0] = x.x;
+            v[k][1] = x.y;
+            ready = ready && (!w0 || (x.x & 0xffffffff00000000ull) == tag) &&
+                    (!w1 || (x.y & 0xffffffff00000000ull) == tag);
+          } else {
+            v[k][0] = v[k][1] = tag;
           }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) all = all && ((v[k] & 0xffffffff00000000ull) == tag);
-          if (__all_sync(0xffffffffu, all)) break;
-          if (t0 == 0) {
-            t0 = globaltimer_ns();
-          } else if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          __nanosleep(64);
         }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c2 = c0 + k * 32 + lane;
-          const long long x = c2 < G ? (long long)(v[k] & 0xffffffffull) : 0;
-          tot += x;
-          if (c2 < cta) pre += x;
+        if (__syncthreads_and(ready)) break;
+        if (t0 == 0) t0 = globaltimer_ns();
+        if (__syncthreads_or(globaltimer_ns() - t0 > kWaitLimitNs)) {
+          ok = false;
+          break;
         }
+        __nanosleep(64);
       }
-      tot = warp_sum(tot);
-      pre = warp_sum(pre);
-      if (lane == 0) {
-        ms->fpre[f] = pre;
-        ms->ft[f] = tot;
+      if (!ok) break;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = r0 + k * (kThreads / 16) + (tid >> 4);
+        if (c >= G) continue;
+        const long long x0 = w0 ? (long long)(v[k][0] & 0xffffffffull) : 0;
+        const long long x1 = w1 ? (long long)(v[k][1] & 0xffffffffull) : 0;
+        tot0 += x0;
+        tot1 += x1;
+        if (c < cta) {
+          pre0 += x0;
+          pre1 += x1;
+        }
       }
     }
-    if (!ok && lane == 0) ms->abort_ = 1;
+    // the two rows a warp reads share feature pairs: fold lanes l and l+16
+    tot0 += __shfl_xor_sync(0xffffffffu, tot0, 16);
+    tot1 += __shfl_xor_sync(0xffffffffu, tot1, 16);
+    pre0 += __shfl_xor_sync(0xffffffffu, pre0, 16);
+    pre1 += __shfl_xor_sync(0xffffffffu, pre1, 16);
+    long long* red = reinterpret_cast<long long*>(sm + C::ACT_OFF);  // [kWarps][16][4]
+    if (lane < 16) {
+      long long* o = red + (warp * 16 + lane) * 4;
+      o[0] = tot0;
+      o[1] = tot1;
+      o[2] = pre0;
+      o[3] = pre1;
+    }
+    if (!ok && tid == 0) ms->abort_ = 1;
+    __syncthreads();
+    if (tid < F) {
+      const int j = tid >> 1, h = tid & 1;
+      long long tot = 0, pre = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        tot += red[(w * 16 + j) * 4 + h];
+        pre += red[(w * 16 + j) * 4 + 2 + h];
+      }
+      ms->ft[tid] = tot;
+      ms->fpre[tid] = pre;
+    }
   }
   // the first tile's row copies go out once the exchange no longer competes
   // with them for the load pipeline
-  if (C::ATTN && prefetched) seq_rows(first_item);
+  if (C::ATTN && prefetched) seq_rows(first_id, 0, first_n, min(sb0 + kSB, sb1) - sb0, 0);
   __syncthreads();
   const bool aborted = ms->abort_ != 0;
   if (aborted) {
@@ -633,11 +619,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 
   // ---------------------------------------------------------------- batches
   const bool pool_all = p.pooled != nullptr;
-  const float* qsrc = pool_all ? p.pooled : p.qbuf;
-  const long long qstride = pool_all ? (long long)F * D : Q;
-  int qcol[3];
-#pragma unroll
-  for (int k = 0; k < 3; ++k) qcol[k] = pool_all ? p.q_feat[k] * D : k * D;
   auto want_feature = [&](int f) -> bool {
     if (pool_all) return true;
     return f == p.q_feat[0] || f == p.q_feat[1] || f == p.q_feat[2];
@@ -659,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       auto feat_of = [&](int g) -> int { return int((unsigned(g) * nb_recip) >> 20); };
       const int offs_bytes = ((nbag + 1) * 4 + 15) / 16 * 16;
       uint8_t* stage = sm + C::ACT_OFF;
-      uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::ACT_BYTES - offs_bytes);
-      const int cap = (C::ACT_BYTES - offs_bytes) / C::ROWB;
+      uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::POOL_AVAIL - offs_bytes);
+      const int cap = (C::POOL_AVAIL - offs_bytes) / C::ROWB;
       const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
       const int g0 = tid * per;
       int loc[8];
@@ -820,143 +801,241 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         for (int d = 0; d < Q; d += 4) *reinterpret_cast<float4*>(o + d) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       const int R = ms->rp[nb];
-      int tix = 0;
-      if (R > 0 && !(prefetched && bs == sb0)) {
-        const SeqItem it = seq_ids(0, min(C::TM, R), nb);
-        seq_rows(it);
-      }
-      for (int t0 = 0; t0 < R && !tc_fail; t0 += C::TM, ++tix) {
-        const int n = min(C::TM, R - t0);
-        cp_async_wait_all();
-        __syncthreads();
-        // ids of the next tile: loads in flight while this tile computes
-        const int t1 = t0 + C::TM;
-        const bool has_next = t1 < R;
-        SeqItem nxt;
-        nxt.valid = false;
-        if (has_next) nxt = seq_ids(t1, min(C::TM, R - t1), nb);
-        const uint8_t* S = sm + C::S_OFF;
+      const int T = (R + C::TM - 1) / C::TM;  // tiles of this batch
+      if (!C::TWO_S && T > 0 && !(prefetched && bs == sb0))
+        seq_rows(seq_ids(0, min(C::TM, R), nb), 0, min(C::TM, R), nb, 0);
+      if (T == 0) continue;
 
-        if constexpr (C::MODE == 0) {
-          // ---------------------------------------------- x = cat[q, s, q-s, q*s] -> bf16 tile
-          uint8_t* X = sm + C::ACT_OFF;
-          constexpr int OCT = Q / 8;
-          for (int item = tid; item < C::TM * OCT; item += kThreads) {
-            const int r = item / OCT, o = item - r * OCT;
-            uint4 ch[4];
-            if (r < n) {
-              const long long b = bs + ms->row_samp[r];
-              const int d0 = o * 8, k = d0 / D, dd = d0 - k * D;
-              const float* qp = qsrc + b * qstride + qcol[k] + dd;
-              const float4 qa = ldcg4(qp), qb = ldcg4(qp + 4);
-              const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-              float sv[8];
-              if constexpr (C::BF16) {
-                widen16<true>(S + r * C::SROWB + d0 * 2, sv);
-              } else {
-                widen16<false>(S + r * C::SROWB + d0 * 4, sv);
-                widen16<false>(S + r * C::SROWB + d0 * 4 + 16, sv + 4);
+      // masked softmax + weighted sum of tile [t0, t0+n) held in S buffer `buf`
+      auto softmax_tile = [&](int t0, int n, int tix, int buf) {
+        const uint8_t* S = s_buf(buf);
+          // ---------------------------------------------- masked softmax + weighted sum
+          // Per sample segment of the tile (a warp each): running max m and sum l
+          // over its valid rows (merged with the state carried from the previous
+          // tile), z[r] <- exp(z[r] - m). Then one thread per (segment, d)
+          // accumulates sum_r exp(z_r - m) s[r][d] in row order.
+          {
+            const int ia = ms->row_samp[buf][0], ib = ms->row_samp[buf][n - 1];
+            const int nseg = ib - ia + 1;
+            float* cin = ms->carry[tix & 1];
+            float* cout = ms->carry[(tix + 1) & 1];
+            float* seg_sc = ms->red[0];   // scale of the carried-in state
+            float* seg_inv = ms->red[1];  // 1 / l, or 0 when the segment carries out
+            float* seg_m = ms->red[2];
+            float* seg_l = ms->red[3];
+            if (p.logits) {
+              for (int r = tid; r < n; r += kThreads) {
+                const int j = ms->row_j[buf][r];
+                if (j >= 0) p.logits[j] = ms->z[r];
               }
-              uint32_t w[4][4];
+              __syncthreads();
+            }
+            for (int g = warp; g < nseg; g += kWarps) {
+              const int si = ia + g;
+              const int ra = ms->rp[si], re = ms->rp[si + 1];
+              const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
+              if (r1 <= r0) continue;
+              const bool has_in = ra < t0, has_out = re > t0 + n;
+              float m = -INFINITY;
+              for (int r = r0 + lane; r < r1; r += 32) m = fmaxf(m, ms->z[r]);
+              m = warp_max(m);
+              if (has_in) m = fmaxf(m, cin[0]);
+              float l = 0.f;
+              for (int r = r0 + lane; r < r1; r += 32) {
+                const float ez = expf(ms->z[r] - m);
+                ms->z[r] = ez;
+                l += ez;
+              }
+              l = warp_sum(l);
+              if (lane == 0) {
+                const float sc = has_in ? expf(cin[0] - m) : 0.f;
+                if (has_in) l += cin[1] * sc;
+                seg_sc[g] = sc;
+                seg_inv[g] = has_out ? 0.f : 1.f / l;
+                seg_m[g] = m;
+                seg_l[g] = l;
+              }
+            }
+            __syncthreads();
+            for (int item = tid; item < nseg * Q; item += kThreads) {
+              const int g = item / Q, d = item - g * Q;
+              const int si = ia + g;
+              const int ra = ms->rp[si], re = ms->rp[si + 1];
+              const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
+              if (r1 <= r0) continue;
+              const bool has_in = ra < t0, has_out = re > t0 + n;
+              float acc = has_in ? cin[4 + d] * seg_sc[g] : 0.f;
+              for (int r = r0; r < r1; ++r) acc = fmaf(ms->z[r], s_elem<C::BF16>(S, C::SROWB, r, d), acc);
+              if (has_out) {
+                cout[4 + d] = acc;
+                if (d == 0) {
+                  cout[0] = seg_m[g];
+                  cout[1] = seg_l[g];
+                }
+              } else {
+                p.din[(long long)(bs + si) * Q + d] = acc * seg_inv[g];
+              }
+            }
+            __syncthreads();
+          }
+      };
+
+      if constexpr (C::MODE == 0) {
+        // ---------------------------------------------------------- pipelined tiles
+        // Per tile k: wait layer 1 (k); epilogue 1 (h1 -> TMEM); issue layer 2 (k);
+        // build x (k+1) while it runs; wait layer 2; epilogue 2 (z); issue layer 1
+        // (k+1); softmax (k) while it runs; copy the rows and query slices of tile
+        // k+2 into the freed buffers. Rows run two tiles ahead, their ids three.
+        const uint32_t tbase = ms->tmem_base;
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+        const float* QS = reinterpret_cast<const float*>(sm + C::ACT_OFF);  // q tile [TM][Q]
+        // x tile -> tensor memory: warp w builds part w/4 of cat[q, s, q-s, q*s]
+        // for rows 32*(w%4) .. +31, 8 dims (4 packed columns) at a time
+        auto build_x = [&](int n, int buf) {
+          const uint8_t* S = s_buf(buf);
+          const int part = warp >> 2;
+          const int r = (warp & 3) * 32 + lane;
+          const bool live = r < n;
+          const float* qrow = QS + r * C::QROW;
+          const uint8_t* srow = S + r * C::SROWB;
+          const uint32_t xa = tbase + lane_base + C::TM_X + uint32_t(part * (Q / 2));
+#pragma unroll 2
+          for (int c = 0; c < Q / 8; ++c) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (live) {
+              float qv[8], sv[8];
+              if (part != 1) {
+                const float4 a = *reinterpret_cast<const float4*>(qrow + c * 8);
+                const float4 b2 = *reinterpret_cast<const float4*>(qrow + c * 8 + 4);
+                qv[0] = a.x; qv[1] = a.y; qv[2] = a.z; qv[3] = a.w;
+                qv[4] = b2.x; qv[5] = b2.y; qv[6] = b2.z; qv[7] = b2.w;
+              }
+              if (part != 0) {
+#pragma unroll
+                for (int i = 0; i < 8 / C::EPL; ++i)
+                  widen16<C::BF16>(srow + (c * 8 + i * C::EPL) * C::ES, sv + i * C::EPL);
+              }
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float q0 = qv[2 * e], q1 = qv[2 * e + 1], s0 = sv[2 * e], s1 = sv[2 * e + 1];
-                w[0][e] = pack_bf16x2(q0, q1);
-                w[1][e] = pack_bf16x2(s0, s1);
-                w[2][e] = pack_bf16x2(q0 - s0, q1 - s1);
-                w[3][e] = pack_bf16x2(q0 * s0, q1 * s1);
+                float x0, x1;
+                if (part == 0) { x0 = qv[2 * e]; x1 = qv[2 * e + 1]; }
+                else if (part == 1) { x0 = sv[2 * e]; x1 = sv[2 * e + 1]; }
+                else if (part == 2) { x0 = qv[2 * e] - sv[2 * e]; x1 = qv[2 * e + 1] - sv[2 * e + 1]; }
+                else { x0 = qv[2 * e] * sv[2 * e]; x1 = qv[2 * e + 1] * sv[2 * e + 1]; }
+                w[e] = pack_bf16x2(x0, x1);
               }
-#pragma unroll
-              for (int part = 0; part < 4; ++part) ch[part] = make_uint4(w[part][0], w[part][1], w[part][2], w[part][3]);
-            } else {
-#pragma unroll
-              for (int part = 0; part < 4; ++part) ch[part] = make_uint4(0u, 0u, 0u, 0u);
             }
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-              const uint32_t kk = uint32_t(part * Q + o * 8);
-              *reinterpret_cast<uint4*>(X + sw128_offset(uint32_t(r), kk, C::TM)) = ch[part];
-            }
+            tmem_st4(xa + uint32_t(c * 4), w);
           }
-          fence_proxy_async_smem();
-          __syncthreads();
-          const uint32_t tbase = ms->tmem_base;
-          if (tid == 0) {
-            bool ok = true;
-            if (!weights_ready) ok = mbar_wait(&ms->mbar_w, 0);
-            weights_ready = weights_ready || ok;
-            if (ok) {
-              tc_fence_after();
-              constexpr uint32_t IDESC1 = idesc_bf16_f32(128, kN1);
-              const uint32_t xa = smem_u32(X), wa = smem_u32(sm + C::W1_OFF);
+          tmem_st_wait();
+        };
+        auto issue_l1 = [&]() {  // thread 0
+          tc_fence_after();
+          constexpr uint32_t IDESC1 = idesc_bf16_f32(128, kN1);
+          const uint32_t wa = smem_u32(sm + C::W1_OFF);
 #pragma unroll
-              for (int kk = 0; kk < C::K1 / 16; ++kk) {
-                const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
-                tc_mma_f16(tbase, sw128_kmajor_desc(xa + kb * C::TM * 128 + ko),
-                           sw128_kmajor_desc(wa + kb * kN1 * 128 + ko), IDESC1, kk > 0);
-              }
-              tc_commit(&ms->mbar_mma);
-              // one thread waits for the MMAs, the block learns the outcome together
-              ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
-            } else {
-              ms->abort_ = 2;
-            }
+          for (int kk = 0; kk < C::K1 / 16; ++kk) {
+            const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+            tc_mma_f16_ts(tbase + C::TM_ACC1, tbase + C::TM_X + uint32_t(kk * 8),
+                          sw128_kmajor_desc(wa + kb * kN1 * 128 + ko), IDESC1, kk > 0);
           }
+          tc_commit(&ms->mbar_mma);
+        };
+        // h1 of hidden units [64g, 64g+64) sits packed in accumulator columns
+        // [64g, 64g+32): K-step kk of layer 2 reads columns 64(kk/4) + 8(kk%4)
+        auto issue_l2 = [&]() {  // thread 0
+          tc_fence_after();
+          constexpr uint32_t IDESC2 = idesc_bf16_f32(128, kN2);
+          const uint32_t wa = smem_u32(sm + C::W2_OFF);
+#pragma unroll
+          for (int kk = 0; kk < kN1 / 16; ++kk) {
+            const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+            tc_mma_f16_ts(tbase + C::TM_ACC2, tbase + C::TM_ACC1 + kb * 64 + uint32_t((kk & 3) * 8),
+                          sw128_kmajor_desc(wa + kb * kN2 * 128 + ko), IDESC2, kk > 0);
+          }
+          tc_commit(&ms->mbar_mma);
+        };
+        // one thread waits for the MMAs, the block learns the outcome together
+        auto wait_mma = [&]() -> bool {
+          if (tid == 0) ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
           mma_phase ^= 1u;
           __syncthreads();
-          if (ms->abort_ != 0) { tc_fail = true; break; }
+          if (ms->abort_ != 0) return false;
           tc_fence_after();
-          // ---------------------------------------------- epilogue 1: h1 = ReLU(acc + b1) -> bf16
+          return true;
+        };
+
+        // prologue: rows of tile 0 are in S0 (or on their way); its query slices
+        // and the rows of tile 1 go out now, then x (0) and layer 1 (0)
+        auto tile_n = [&](int kt) { return min(C::TM, R - kt * C::TM); };
+        long long id1 = -1, nxt = -1;
+        if (prefetched && bs == sb0) {
+          id1 = second_id;
+        } else {
+          seq_rows(seq_ids(0, tile_n(0), nb), 0, tile_n(0), nb, 0);
+          if (T > 1) id1 = seq_ids(C::TM, tile_n(1), nb);
+        }
+        q_rows(0, tile_n(0), nb, bs);
+        if (T > 1) seq_rows(id1, C::TM, tile_n(1), nb, 1);
+        if (T > 2) nxt = seq_ids(2 * C::TM, tile_n(2), nb);
+        // wait for the rows and query slices of tile 0; tile 1's rows may stay in flight
+        if (T > 1) cp_async_wait_group<1>();
+        else cp_async_wait_all();
+        __syncthreads();
+        build_x(min(C::TM, R), 0);
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          bool ok = true;
+          if (!weights_ready) ok = mbar_wait(&ms->mbar_w, 0);
+          weights_ready = weights_ready || ok;
+          if (ok) issue_l1();
+          else ms->abort_ = 2;
+        }
+        if (T > 1) q_rows(C::TM, tile_n(1), nb, bs);  // x (0) is done reading the q tile
+        __syncthreads();
+        if (ms->abort_ != 0) tc_fail = true;
+
+        for (int k = 0; k < T && !tc_fail; ++k) {
+          const int buf = k & 1;
+          const int t0 = k * C::TM, n = min(C::TM, R - t0);
+          // ---- layer 1 (k) done: epilogue 1, h1 packed back into TMEM
+          if (!wait_mma()) { tc_fail = true; break; }
           {
-            const int lq = warp & 3, cg = warp >> 2;
-            const int row = lq * 32 + lane;
-            const uint32_t ta = tbase + (uint32_t(lq * 32) << 16) + uint32_t(cg * 64);
-            float v[64];
-            tmem_ld16(ta, v);
-            tmem_ld16(ta + 16, v + 16);
-            tmem_ld16(ta + 32, v + 32);
-            tmem_ld16(ta + 48, v + 48);
-            tmem_ld_wait();
+            const int cg = warp >> 2;
+            const uint32_t ta = tbase + lane_base + C::TM_ACC1 + uint32_t(cg * 64);
+#pragma unroll 1
+            for (int qq = 0; qq < 4; ++qq) {
+              float v[16];
+              tmem_ld16(ta + qq * 16, v);
+              tmem_ld_wait();
+              uint32_t h[8];
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int col = cg * 64 + c8 * 8 + 2 * e;
-                const float h0 = fmaxf(v[c8 * 8 + 2 * e] + ms->b1[col], 0.f);
-                const float h1 = fmaxf(v[c8 * 8 + 2 * e + 1] + ms->b1[col + 1], 0.f);
-                w[e] = pack_bf16x2(h0, h1);
+              for (int e = 0; e < 8; ++e) {
+                const int col = cg * 64 + qq * 16 + 2 * e;
+                h[e] = pack_bf16x2(fmaxf(v[2 * e] + ms->b1[col], 0.f), fmaxf(v[2 * e + 1] + ms->b1[col + 1], 0.f));
               }
-              *reinterpret_cast<uint4*>(X + sw128_offset(uint32_t(row), uint32_t(cg * 64 + c8 * 8), C::TM)) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
+              // columns [64cg + 8qq, +8) were read by this warp already
+              tmem_st8(ta + qq * 8, h);
             }
+            tmem_st_wait();
           }
           tc_fence_before();
-          fence_proxy_async_smem();
           __syncthreads();
-          if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t IDESC2 = idesc_bf16_f32(128, kN2);
-            const uint32_t ha = smem_u32(X), wa = smem_u32(sm + C::W2_OFF);
-#pragma unroll
-            for (int kk = 0; kk < kN1 / 16; ++kk) {
-              const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
-              tc_mma_f16(tbase + kN1, sw128_kmajor_desc(ha + kb * C::TM * 128 + ko),
-                         sw128_kmajor_desc(wa + kb * kN2 * 128 + ko), IDESC2, kk > 0);
-            }
-            tc_commit(&ms->mbar_mma);
-            ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
+          if (tid == 0) issue_l2();
+          // ---- x of tile k+1 while layer 2 (k) runs
+          if (k + 1 < T) {
+            cp_async_wait_all();
+            __syncthreads();
+            build_x(min(C::TM, R - t0 - C::TM), buf ^ 1);
+            tc_fence_before();
           }
-          mma_phase ^= 1u;
-          __syncthreads();
-          if (ms->abort_ != 0) { tc_fail = true; break; }
-          tc_fence_after();
-          // ---------------------------------------------- epilogue 2: z = w3 . ReLU(acc + b2) + b3
+          // ---- layer 2 (k) done: epilogue 2, z = w3 . ReLU(acc + b2) + b3
+          if (!wait_mma()) { tc_fail = true; break; }
           {
-            const int lq = warp & 3, cg = warp >> 2;
-            const int row = lq * 32 + lane;
+            const int cg = warp >> 2;
             float v[16];
-            tmem_ld16(tbase + (uint32_t(lq * 32) << 16) + uint32_t(kN1 + cg * 16), v);
+            tmem_ld16(tbase + lane_base + C::TM_ACC2 + uint32_t(cg * 16), v);
             tmem_ld_wait();
             float part = 0.f;
 #pragma unroll
@@ -964,167 +1043,122 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               const int col = cg * 16 + e;
               part += fmaxf(v[e] + ms->b2[col], 0.f) * ms->w3[col];
             }
-            ms->red[cg][row] = part;
+            ms->red[cg][(warp & 3) * 32 + lane] = part;
           }
           tc_fence_before();
           __syncthreads();
           if (tid < C::TM) ms->z[tid] = ((ms->red[0][tid] + ms->red[1][tid]) + (ms->red[2][tid] + ms->red[3][tid])) + b3;
+          // ---- layer 1 (k+1) runs during the softmax of tile k
+          if (tid == 0 && k + 1 < T) issue_l1();
           __syncthreads();
-        } else {
-          // ---------------------------------------------- fp32 check mode
-          float* QT = reinterpret_cast<float*>(sm + C::QT_OFF);
-          float* H1 = reinterpret_cast<float*>(sm + C::ACT_OFF);
-          constexpr int Q4 = Q / 4;
-          for (int item = tid; item < C::TM * Q4; item += kThreads) {
-            const int r = item / Q4, o = item - r * Q4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < n) {
-              const long long b = bs + ms->row_samp[r];
-              const int d0 = o * 4, k = d0 / D, dd = d0 - k * D;
-              v = ldcg4(qsrc + b * qstride + qcol[k] + dd);
-            }
-            *reinterpret_cast<float4*>(QT + r * Q + o * 4) = v;
+          softmax_tile(t0, n, k, buf);
+          // ---- rows and query slices of tile k+2 into the freed buffers
+          if (k + 2 < T) {
+            seq_rows(nxt, t0 + 2 * C::TM, tile_n(k + 2), nb, buf);
+            q_rows(t0 + 2 * C::TM, tile_n(k + 2), nb, bs);
+            if (k + 3 < T) nxt = seq_ids(t0 + 3 * C::TM, tile_n(k + 3), nb);
           }
-          __syncthreads();
-          {
-            // layer 1: thread = 4 rows x 8 units
-            const int rg = warp, ug = lane;
-            float acc[4][8];
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-              for (int u = 0; u < 8; ++u) acc[a][u] = 0.f;
-            auto run_part = [&](auto part_tag) {
-              constexpr int PART = decltype(part_tag)::value;
-              for (int d = 0; d < Q; ++d) {
-                const float* wp = p.w1t + (long long)(PART * Q + d) * kN1 + ug * 8;
-                const float4 wa = __ldg(reinterpret_cast<const float4*>(wp));
-                const float4 wb = __ldg(reinterpret_cast<const float4*>(wp + 4));
-                const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                  const int r = rg * 4 + a;
-                  const float qv = QT[r * Q + d];
-                  const float sv = s_elem<C::BF16>(S, C::SROWB, r, d);
-                  float x;
-                  if constexpr (PART == 0) x = qv;
-                  else if constexpr (PART == 1) x = sv;
-                  else if constexpr (PART == 2) x = qv - sv;
-                  else x = qv * sv;
-#pragma unroll
-                  for (int u = 0; u < 8; ++u) acc[a][u] = fmaf(x, w[u], acc[a][u]);
-                }
-              }
-            };
-            run_part(std::integral_constant<int, 0>{});
-            run_part(std::integral_constant<int, 1>{});
-            run_part(std::integral_constant<int, 2>{});
-            run_part(std::integral_constant<int, 3>{});
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                H1[(rg * 4 + a) * C::H1S + ug * 8 + u] = fmaxf(acc[a][u] + ms->b1[ug * 8 + u], 0.f);
-          }
-          __syncthreads();
-          {
-            // layer 2 + score: thread = 1 row x 8 units
-            const int r = tid >> 3, u2 = tid & 7;
-            float a2[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) a2[u] = 0.f;
-            for (int k = 0; k < kN1; ++k) {
-              const float h = H1[r * C::H1S + k];
-              const float* wp = p.w2t + (long long)k * kN2 + u2 * 8;
-              const float4 wa = __ldg(reinterpret_cast<const float4*>(wp));
-              const float4 wb = __ldg(reinterpret_cast<const float4*>(wp + 4));
-              a2[0] = fmaf(h, wa.x, a2[0]); a2[1] = fmaf(h, wa.y, a2[1]);
-              a2[2] = fmaf(h, wa.z, a2[2]); a2[3] = fmaf(h, wa.w, a2[3]);
-              a2[4] = fmaf(h, wb.x, a2[4]); a2[5] = fmaf(h, wb.y, a2[5]);
-              a2[6] = fmaf(h, wb.z, a2[6]); a2[7] = fmaf(h, wb.w, a2[7]);
-            }
-            float part = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) part += fmaxf(a2[u] + ms->b2[u2 * 8 + u], 0.f) * ms->w3[u2 * 8 + u];
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            part += __shfl_xor_sync(0xffffffffu, part, 4);
-            if (u2 == 0 && r < C::TM) ms->z[r] = part + b3;
-          }
-          __syncthreads();
         }
-
-        // ---------------------------------------------- masked softmax + weighted sum
-        // Per sample segment of the tile (a warp each): running max m and sum l
-        // over its valid rows (merged with the state carried from the previous
-        // tile), z[r] <- exp(z[r] - m). Then one thread per (segment, d)
-        // accumulates sum_r exp(z_r - m) s[r][d] in row order.
-        {
-          const int ia = ms->row_samp[0], ib = ms->row_samp[n - 1];
-          const int nseg = ib - ia + 1;
-          float* cin = ms->carry[tix & 1];
-          float* cout = ms->carry[(tix + 1) & 1];
-          float* seg_sc = ms->red[0];   // scale of the carried-in state
-          float* seg_inv = ms->red[1];  // 1 / l, or 0 when the segment carries out
-          float* seg_m = ms->red[2];
-          float* seg_l = ms->red[3];
-          if (p.logits) {
-            for (int r = tid; r < n; r += kThreads) {
-              const int j = ms->row_j[r];
-              if (j >= 0) p.logits[j] = ms->z[r];
+      } else {
+        // ---------------------------------------------------------- sequential tiles (fp32)
+        for (int t0 = 0, tix = 0; t0 < R; t0 += C::TM, ++tix) {
+          const int n = min(C::TM, R - t0);
+          cp_async_wait_all();
+          __syncthreads();
+          const int t1 = t0 + C::TM;
+          const bool has_next = t1 < R;
+          long long nxt = -1;
+          if (has_next) nxt = seq_ids(t1, min(C::TM, R - t1), nb);
+          const uint8_t* S = s_buf(0);
+          const float* qsrc = pool_all ? p.pooled : p.qbuf;
+          const long long qstride = pool_all ? (long long)F * D : Q;
+          {
+            // ---------------------------------------------- fp32 check mode
+            float* QT = reinterpret_cast<float*>(sm + C::QT_OFF);
+            float* H1 = reinterpret_cast<float*>(sm + C::ACT_OFF);
+            constexpr int Q4 = Q / 4;
+            for (int item = tid; item < C::TM * Q4; item += kThreads) {
+              const int r = item / Q4, o = item - r * Q4;
+              float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (r < n) {
+                const long long b = bs + ms->row_samp[0][r];
+                const int d0 = o * 4, k = d0 / D, dd = d0 - k * D;
+                v = ldcg4(qsrc + b * qstride + (pool_all ? p.q_feat[k] * D : k * D) + dd);
+              }
+              *reinterpret_cast<float4*>(QT + r * Q + o * 4) = v;
             }
             __syncthreads();
-          }
-          for (int g = warp; g < nseg; g += kWarps) {
-            const int si = ia + g;
-            const int ra = ms->rp[si], re = ms->rp[si + 1];
-            const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
-            if (r1 <= r0) continue;
-            const bool has_in = ra < t0, has_out = re > t0 + n;
-            float m = -INFINITY;
-            for (int r = r0 + lane; r < r1; r += 32) m = fmaxf(m, ms->z[r]);
-            m = warp_max(m);
-            if (has_in) m = fmaxf(m, cin[0]);
-            float l = 0.f;
-            for (int r = r0 + lane; r < r1; r += 32) {
-              const float ez = expf(ms->z[r] - m);
-              ms->z[r] = ez;
-              l += ez;
+            {
+              // layer 1: thread = 4 rows x 8 units
+              const int rg = warp, ug = lane;
+              float acc[4][8];
+  #pragma unroll
+              for (int a = 0; a < 4; ++a)
+  #pragma unroll
+                for (int u = 0; u < 8; ++u) acc[a][u] = 0.f;
+              auto run_part = [&](auto part_tag) {
+                constexpr int PART = decltype(part_tag)::value;
+                for (int d = 0; d < Q; ++d) {
+                  const float* wp = p.w1t + (long long)(PART * Q + d) * kN1 + ug * 8;
+                  const float4 wa = __ldg(reinterpret_cast<const float4*>(wp));
+                  const float4 wb = __ldg(reinterpret_cast<const float4*>(wp + 4));
+                  const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+  #pragma unroll
+                  for (int a = 0; a < 4; ++a) {
+                    const int r = rg * 4 + a;
+                    const float qv = QT[r * Q + d];
+                    const float sv = s_elem<C::BF16>(S, C::SROWB, r, d);
+                    float x;
+                    if constexpr (PART == 0) x = qv;
+                    else if constexpr (PART == 1) x = sv;
+                    else if constexpr (PART == 2) x = qv - sv;
+                    else x = qv * sv;
+  #pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[a][u] = fmaf(x, w[u], acc[a][u]);
+                  }
+                }
+              };
+              run_part(std::integral_constant<int, 0>{});
+              run_part(std::integral_constant<int, 1>{});
+              run_part(std::integral_constant<int, 2>{});
+              run_part(std::integral_constant<int, 3>{});
+  #pragma unroll
+              for (int a = 0; a < 4; ++a)
+  #pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  H1[(rg * 4 + a) * C::H1S + ug * 8 + u] = fmaxf(acc[a][u] + ms->b1[ug * 8 + u], 0.f);
             }
-            l = warp_sum(l);
-            if (lane == 0) {
-              const float sc = has_in ? expf(cin[0] - m) : 0.f;
-              if (has_in) l += cin[1] * sc;
-              seg_sc[g] = sc;
-              seg_inv[g] = has_out ? 0.f : 1.f / l;
-              seg_m[g] = m;
-              seg_l[g] = l;
-            }
-          }
-          __syncthreads();
-          for (int item = tid; item < nseg * Q; item += kThreads) {
-            const int g = item / Q, d = item - g * Q;
-            const int si = ia + g;
-            const int ra = ms->rp[si], re = ms->rp[si + 1];
-            const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
-            if (r1 <= r0) continue;
-            const bool has_in = ra < t0, has_out = re > t0 + n;
-            float acc = has_in ? cin[4 + d] * seg_sc[g] : 0.f;
-            for (int r = r0; r < r1; ++r) acc = fmaf(ms->z[r], s_elem<C::BF16>(S, C::SROWB, r, d), acc);
-            if (has_out) {
-              cout[4 + d] = acc;
-              if (d == 0) {
-                cout[0] = seg_m[g];
-                cout[1] = seg_l[g];
+            __syncthreads();
+            {
+              // layer 2 + score: thread = 1 row x 8 units
+              const int r = tid >> 3, u2 = tid & 7;
+              float a2[8];
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) a2[u] = 0.f;
+              for (int k = 0; k < kN1; ++k) {
+                const float h = H1[r * C::H1S + k];
+                const float* wp = p.w2t + (long long)k * kN2 + u2 * 8;
+                const float4 wa = __ldg(reinterpret_cast<const float4*>(wp));
+                const float4 wb = __ldg(reinterpret_cast<const float4*>(wp + 4));
+                a2[0] = fmaf(h, wa.x, a2[0]); a2[1] = fmaf(h, wa.y, a2[1]);
+                a2[2] = fmaf(h, wa.z, a2[2]); a2[3] = fmaf(h, wa.w, a2[3]);
+                a2[4] = fmaf(h, wb.x, a2[4]); a2[5] = fmaf(h, wb.y, a2[5]);
+                a2[6] = fmaf(h, wb.z, a2[6]); a2[7] = fmaf(h, wb.w, a2[7]);
               }
-            } else {
-              p.din[(long long)(bs + si) * Q + d] = acc * seg_inv[g];
+              float part = 0.f;
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) part += fmaxf(a2[u] + ms->b2[u2 * 8 + u], 0.f) * ms->w3[u2 * 8 + u];
+              part += __shfl_xor_sync(0xffffffffu, part, 1);
+              part += __shfl_xor_sync(0xffffffffu, part, 2);
+              part += __shfl_xor_sync(0xffffffffu, part, 4);
+              if (u2 == 0 && r < C::TM) ms->z[r] = part + b3;
             }
+            __syncthreads();
+
           }
-          __syncthreads();
+          softmax_tile(t0, n, tix, 0);
+          if (has_next) seq_rows(nxt, t1, min(C::TM, R - t1), nb, 0);
         }
-        // the next tile's rows: S and the row metadata are free again
-        if (has_next) seq_rows(nxt);
       }
     }
   }
