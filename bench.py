@@ -226,7 +226,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-sample", type=int, default=8192)
-    ap.add_argument("--cpu-passes", type=int, default=3)
+    ap.add_argument("--cpu-passes", type=int, default=8)
     ap.add_argument("--skip-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
