@@ -89,7 +89,7 @@ int check_mlp(const dsf_mlp* m, int32_t D) {
   if (!aligned(m->b1, 16) || !aligned(m->b2, 16) || !aligned(m->w3, 16)) return DSF_EINVAL;
   if (m->K1 != 12 * D || m->N1 != kN1 || m->N2 != kN2) return DSF_EUNSUPPORTED;
   if (m->mode != DSF_MODE_BF16_TC && m->mode != DSF_MODE_FP32) return DSF_EINVAL;
-  if (m->mode == DSF_MODE_BF16_TC && D != 16) return DSF_EUNSUPPORTED;
+
   return DSF_OK;
 }
 
@@ -135,6 +135,8 @@ int run_attention(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* s
   if ((rc = check_kjt(kjt, B, tables->F)) != DSF_OK) return rc;
   if ((rc = check_seq(seq, B)) != DSF_OK) return rc;
   if ((rc = check_mlp(mlp, tables->D)) != DSF_OK) return rc;
+  // the tensor-core MLP with D = 64 is built for bf16 tables only
+  if (mlp->mode == DSF_MODE_BF16_TC && tables->D == 64 && tables->dtype != DSF_BF16) return DSF_EUNSUPPORTED;
   if (!q_feat || !seq_table) return DSF_EINVAL;
   for (int k = 0; k < 3; ++k) {
     if (q_feat[k] < 0 || q_feat[k] >= tables->F) return DSF_EINVAL;

@@ -117,12 +117,22 @@ struct Cfg {
   // attention input x and h1 live in tensor memory, and the sequence rows S are
   // double-buffered: [W1 | W2 | ACT | S1 | S0 | misc]. Pooling stages rows in
   // ACT and S1 (S1 is free then: only the first tile is in flight, in S0).
-  static constexpr bool TWO_S = ATTN && MODE == 0;
-  static constexpr int W1_OFF = 0;
-  static constexpr int W2_OFF = (ATTN && MODE == 0) ? W1_OFF + W1B : 0;
-  static constexpr int ACT_OFF = (ATTN && MODE == 0) ? W2_OFF + W2B : 0;
+  // With D = 64 the 768-wide W1 does not fit: it streams through a ring of
+  // W1_STAGES K-blocks (64 wide, 32 KB) and x is built one K-block at a time in
+  // a two-slot smem ring: [W2 | W1 ring | x ring | S | misc]; pooling stages in
+  // the W1 and x rings.
+  static constexpr bool STREAM = ATTN && MODE == 0 && D == 64;
+  static constexpr bool TWO_S = ATTN && MODE == 0 && !STREAM;
+  static constexpr int W1_STAGES = 3;
+  static constexpr int W1KB = kN1 * 128;     // one 64-wide K-block of W1
+  static constexpr int XKB = TM * 128;       // one 64-wide K-block of x
+  static constexpr int W1_OFF = STREAM ? W2B : 0;
+  static constexpr int W2_OFF = STREAM ? 0 : ((ATTN && MODE == 0) ? W1_OFF + W1B : 0);
+  static constexpr int XR_OFF = W1_OFF + W1_STAGES * W1KB;  // stream mode
+  static constexpr int ACT_OFF = STREAM ? W1_OFF : ((ATTN && MODE == 0) ? W2_OFF + W2B : 0);
   static constexpr int ACT_BYTES =
-      !ATTN ? POOL_BYTES : (MODE == 0 ? 36 * 1024 : cmax(H1FB, POOL_BYTES));
+      !ATTN ? POOL_BYTES
+            : (STREAM ? W1_STAGES * W1KB + 2 * XKB : (MODE == 0 ? 36 * 1024 : cmax(H1FB, POOL_BYTES)));
   static constexpr int QT_OFF = ACT_OFF + ACT_BYTES;  // fp32 mode only
   static constexpr int S_BYTES = ATTN ? TM * SROWB : 0;
   static constexpr int S1_OFF = QT_OFF + ((ATTN && MODE == 1) ? QTB : 0);
@@ -134,8 +144,8 @@ struct Cfg {
   // tensor-memory columns: layer-1 accumulator (h1 packed over its first half),
   // layer-2 accumulator, the bf16 x tile
   static constexpr uint32_t TM_ACC1 = 0, TM_ACC2 = kN1, TM_X = kN1 + kN2;
-  static_assert(!(ATTN && MODE == 0) || TM_X + K1 / 2 <= 512, "tensor memory columns");
-  static_assert(!(ATTN && MODE == 0) || TM * QROW * 4 <= ACT_BYTES, "q tile");
+  static_assert(!TWO_S || TM_X + K1 / 2 <= 512, "tensor memory columns");
+  static_assert(!TWO_S || TM * QROW * 4 <= ACT_BYTES, "q tile");
 };
 
 template <int D, int Q>
@@ -158,6 +168,8 @@ struct Misc {
   long long red3[3][kWarps];
   uint64_t mbar_w;
   uint64_t mbar_mma;
+  uint64_t mbar_full[3];       // W1 K-block landed in ring slot (stream mode)
+  uint64_t mbar_done[3];       // MMAs reading ring slot finished (stream mode)
   unsigned int tmem_base;
   int abort_;
   long long seq_cur;           // seq value index of the next batch's first sample
@@ -323,12 +335,22 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     if constexpr (C::ATTN && C::MODE == 0) {
       mbar_init(&ms->mbar_w, 1);
       mbar_init(&ms->mbar_mma, 1);
+      if constexpr (C::STREAM) {
+        for (int i = 0; i < 3; ++i) {
+          mbar_init(&ms->mbar_full[i], 1);
+          mbar_init(&ms->mbar_done[i], 1);
+        }
+      }
       fence_mbarrier_init();
-      // stage the packed bf16 weights (bulk copies, 16 KB pieces)
-      mbar_arrive_expect_tx(&ms->mbar_w, C::W1B + C::W2B);
-      for (int off = 0; off < C::W1B + C::W2B; off += 16384) {
-        const int nbytes = min(16384, C::W1B + C::W2B - off);
-        bulk_g2s(sm + C::W1_OFF + off, p.wpack + off, nbytes, &ms->mbar_w);
+      // stage the packed bf16 weights (bulk copies, 16 KB pieces): W1 | W2, or
+      // only W2 when W1 streams
+      const int w_src = C::STREAM ? C::W1B : 0;
+      const int w_bytes = C::STREAM ? C::W2B : C::W1B + C::W2B;
+      uint8_t* w_dst = sm + (C::STREAM ? C::W2_OFF : C::W1_OFF);
+      mbar_arrive_expect_tx(&ms->mbar_w, w_bytes);
+      for (int off = 0; off < w_bytes; off += 16384) {
+        const int nbytes = min(16384, w_bytes - off);
+        bulk_g2s(w_dst + off, p.wpack + w_src + off, nbytes, &ms->mbar_w);
       }
     }
   }
@@ -624,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     return f == p.q_feat[0] || f == p.q_feat[1] || f == p.q_feat[2];
   };
   uint32_t mma_phase = 0;
+  uint32_t gk = 0;  // W1 K-blocks consumed so far (stream mode)
   bool weights_ready = false;
   bool tc_fail = false;
 
@@ -880,7 +903,163 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           }
       };
 
-      if constexpr (C::MODE == 0) {
+      if constexpr (C::STREAM) {
+        // ---------------------------------------------------------- streamed W1 (D = 64)
+        // Per tile: 12 K-blocks of layer 1. x K-block kb (part kb/3 of
+        // cat[q, s, q-s, q*s], dims (kb%3)*64..+64) is built in x-ring slot kb%2;
+        // W1 K-block kb arrives in W1-ring slot gk%3 by bulk copy (gk counts
+        // blocks over the whole launch). Thread 0 issues each block's 4 MMAs,
+        // commits them to the slot's done barrier and refills the slot of the
+        // previous block once its MMAs are done.
+        const uint32_t tbase = ms->tmem_base;
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+        const bool pa = p.pooled != nullptr;
+        const float* qsrc = pa ? p.pooled : p.qbuf;
+        const long long qstride = pa ? (long long)F * D : Q;
+        constexpr int NKB = C::K1 / 64;
+        auto load_w1 = [&](uint32_t g) {  // thread 0
+          const int slot = int(g % 3u), blk = int(g % uint32_t(NKB));
+          mbar_arrive_expect_tx(&ms->mbar_full[slot], C::W1KB);
+          for (int off = 0; off < C::W1KB; off += 16384)
+            bulk_g2s(sm + C::W1_OFF + slot * C::W1KB + off, p.wpack + (size_t)blk * C::W1KB + off, 16384,
+                     &ms->mbar_full[slot]);
+        };
+        for (int t0 = 0, tix = 0; t0 < R && !tc_fail; t0 += C::TM, ++tix) {
+          const int n = min(C::TM, R - t0);
+          cp_async_wait_all();
+          __syncthreads();
+          const int t1 = t0 + C::TM;
+          const bool has_next = t1 < R;
+          long long nxt = -1;
+          if (has_next) nxt = seq_ids(t1, min(C::TM, R - t1), nb);
+          const uint8_t* S = s_buf(0);
+          if (tid == 0) {
+            load_w1(gk);
+            load_w1(gk + 1);
+          }
+          for (int kb = 0; kb < NKB; ++kb, ++gk) {
+            uint8_t* X = sm + C::XR_OFF + (kb & 1) * C::XKB;
+            const int part = kb / 3, k = kb % 3;
+            for (int item = tid; item < C::TM * 8; item += kThreads) {
+              const int r = item >> 3, c = item & 7;
+              uint4 out = make_uint4(0u, 0u, 0u, 0u);
+              if (r < n) {
+                const long long b = bs + ms->row_samp[0][r];
+                float qv[8], sv[8];
+                if (part != 1) {
+                  const float* qp = qsrc + b * qstride + (pa ? p.q_feat[k] * D : k * D) + c * 8;
+                  const float4 a = *reinterpret_cast<const float4*>(qp);
+                  const float4 a2 = *reinterpret_cast<const float4*>(qp + 4);
+                  qv[0] = a.x; qv[1] = a.y; qv[2] = a.z; qv[3] = a.w;
+                  qv[4] = a2.x; qv[5] = a2.y; qv[6] = a2.z; qv[7] = a2.w;
+                }
+                if (part != 0) widen16<true>(S + r * C::SROWB + (k * 64 + c * 8) * 2, sv);
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float x0, x1;
+                  if (part == 0) { x0 = qv[2 * e]; x1 = qv[2 * e + 1]; }
+                  else if (part == 1) { x0 = sv[2 * e]; x1 = sv[2 * e + 1]; }
+                  else if (part == 2) { x0 = qv[2 * e] - sv[2 * e]; x1 = qv[2 * e + 1] - sv[2 * e + 1]; }
+                  else { x0 = qv[2 * e] * sv[2 * e]; x1 = qv[2 * e + 1] * sv[2 * e + 1]; }
+                  w[e] = pack_bf16x2(x0, x1);
+                }
+                out = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+              *reinterpret_cast<uint4*>(X + sw128_offset(uint32_t(r), uint32_t(c * 8), C::TM)) = out;
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+              const int slot = int(gk % 3u);
+              bool ok = mbar_wait(&ms->mbar_full[slot], (gk / 3u) & 1u);
+              if (ok) {
+                tc_fence_after();
+                constexpr uint32_t IDESC1 = idesc_bf16_f32(128, kN1);
+                const uint32_t xa = smem_u32(X), wa = smem_u32(sm + C::W1_OFF + slot * C::W1KB);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc_mma_f16(tbase + C::TM_ACC1, sw128_kmajor_desc(xa + kk * 32), sw128_kmajor_desc(wa + kk * 32),
+                             IDESC1, (kb > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&ms->mbar_done[slot]);
+                if (kb >= 1) ok = mbar_wait(&ms->mbar_done[(gk - 1u) % 3u], ((gk - 1u) / 3u) & 1u);
+                if (ok && kb + 2 < NKB) load_w1(gk + 2u);
+              }
+              ms->abort_ = ok ? 0 : 3;
+            }
+            __syncthreads();
+            if (ms->abort_ != 0) { tc_fail = true; break; }
+          }
+          if (tc_fail) break;
+          // all of layer 1 done (the last block's commit covers every earlier MMA)
+          if (tid == 0) {
+            bool ok = mbar_wait(&ms->mbar_done[(gk - 1u) % 3u], ((gk - 1u) / 3u) & 1u);
+            if (ok && !weights_ready) ok = mbar_wait(&ms->mbar_w, 0);
+            weights_ready = weights_ready || ok;
+            ms->abort_ = ok ? 0 : 3;
+          }
+          __syncthreads();
+          if (ms->abort_ != 0) { tc_fail = true; break; }
+          tc_fence_after();
+          // epilogue 1: h1 packed in place over the first half of each group's columns
+          {
+            const int cg = warp >> 2;
+            const uint32_t ta = tbase + lane_base + C::TM_ACC1 + uint32_t(cg * 64);
+#pragma unroll 1
+            for (int qq = 0; qq < 4; ++qq) {
+              float v[16];
+              tmem_ld16(ta + qq * 16, v);
+              tmem_ld_wait();
+              uint32_t h[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int col = cg * 64 + qq * 16 + 2 * e;
+                h[e] = pack_bf16x2(fmaxf(v[2 * e] + ms->b1[col], 0.f), fmaxf(v[2 * e + 1] + ms->b1[col + 1], 0.f));
+              }
+              tmem_st8(ta + qq * 8, h);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          __syncthreads();
+          if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t IDESC2 = idesc_bf16_f32(128, kN2);
+            const uint32_t wa = smem_u32(sm + C::W2_OFF);
+#pragma unroll
+            for (int kk = 0; kk < kN1 / 16; ++kk) {
+              const uint32_t kb2 = kk >> 2, ko = (kk & 3) * 32;
+              tc_mma_f16_ts(tbase + C::TM_ACC2, tbase + C::TM_ACC1 + kb2 * 64 + uint32_t((kk & 3) * 8),
+                            sw128_kmajor_desc(wa + kb2 * kN2 * 128 + ko), IDESC2, kk > 0);
+            }
+            tc_commit(&ms->mbar_mma);
+            ms->abort_ = mbar_wait(&ms->mbar_mma, mma_phase) ? 0 : 3;
+          }
+          mma_phase ^= 1u;
+          __syncthreads();
+          if (ms->abort_ != 0) { tc_fail = true; break; }
+          tc_fence_after();
+          {
+            const int cg = warp >> 2;
+            float v[16];
+            tmem_ld16(tbase + lane_base + C::TM_ACC2 + uint32_t(cg * 16), v);
+            tmem_ld_wait();
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = cg * 16 + e;
+              part += fmaxf(v[e] + ms->b2[col], 0.f) * ms->w3[col];
+            }
+            ms->red[cg][(warp & 3) * 32 + lane] = part;
+          }
+          tc_fence_before();
+          __syncthreads();
+          if (tid < C::TM) ms->z[tid] = ((ms->red[0][tid] + ms->red[1][tid]) + (ms->red[2][tid] + ms->red[3][tid])) + b3;
+          __syncthreads();
+          softmax_tile(t0, n, tix, 0);
+          if (has_next) seq_rows(nxt, t1, min(C::TM, R - t1), nb, 0);
+        }
+      } else if constexpr (C::MODE == 0) {
         // ---------------------------------------------------------- pipelined tiles
         // Per tile k: wait layer 1 (k); epilogue 1 (h1 -> TMEM); issue layer 2 (k);
         // build x (k+1) while it runs; wait layer 2; epilogue 2 (z); issue layer 1
@@ -1173,6 +1352,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       // an MMA group did not complete in time: give it one more bounded wait
       // before the accumulator columns are released
       mbar_wait(&ms->mbar_mma, mma_phase ^ 1u);
+      if constexpr (C::STREAM) {
+        if (gk > 0) mbar_wait(&ms->mbar_done[(gk - 1u) % 3u], ((gk - 1u) / 3u) & 1u);
+        for (uint32_t g = gk; g < gk + 2u; ++g) mbar_wait(&ms->mbar_full[g % 3u], (g / 3u) & 1u);
+      }
     }
     tc_fence_before();
     __syncthreads();

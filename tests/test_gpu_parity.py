@@ -106,9 +106,15 @@ def test_gather_stress_full_size_sampled():
     check_batch(b, samples=sample_ids(b.B, 160), check_logits=False)
 
 
-def test_wide_bf16_tables_fp32_mode():
+def test_wide_bf16_tables_both_modes():
+    # D = 64: the tensor-core path streams W1 through the smem ring
     b = synth.generate("wide_bf16", seed=0, B=512, nonzero_bias=True)
-    check_batch(b, modes=(F32,))
+    check_batch(b)
+
+
+def test_wide_bf16_full_size_sampled():
+    b = synth.generate("wide_bf16", seed=0)
+    check_batch(b, samples=sample_ids(b.B, 160), check_logits=False)
 
 
 def test_entry_points_agree():
