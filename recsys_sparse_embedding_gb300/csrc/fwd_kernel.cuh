@@ -41,6 +41,7 @@ constexpr int kMaxF = 32;           // tables
 constexpr int kMaxG = 1024;         // grid size limit (rows of the partials table)
 constexpr int kN1 = 256, kN2 = 64;  // attn_mlp hidden units
 constexpr int kMaxBagLen = 1 << 19; // longer bags are clamped (flagged)
+constexpr int kShortBag = 16;       // batches whose bags all fit pool directly
 
 // Workspace layout (bytes). The header holds the prepared-weights tag, the
 // launch epoch and the exit counter that advances it.
@@ -281,10 +282,14 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
   return __ldcg(reinterpret_cast<const float4*>(p));
 }
 
-// 16-byte piece of a staged row (fp32 or bf16) widened to EPL floats.
+// 16 bytes of a read-only table row, through the non-coherent path.
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// 16-byte piece of a row (fp32 or bf16) widened to EPL floats.
 template <bool BF16>
-__device__ __forceinline__ void widen16(const uint8_t* src, float* out) {
-  const uint4 v = *reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void widen16v(const uint4 v, float* out) {
   if constexpr (BF16) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -298,6 +303,11 @@ __device__ __forceinline__ void widen16(const uint8_t* src, float* out) {
     out[2] = __uint_as_float(v.z);
     out[3] = __uint_as_float(v.w);
   }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void widen16(const uint8_t* src, float* out) {
+  widen16v<BF16>(*reinterpret_cast<const uint4*>(src), out);
 }
 
 template <bool BF16>
@@ -381,8 +391,104 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   const int ns = sb1 - sb0;
   const unsigned long long tag = (unsigned long long)(ms->epoch + 1u) << 32;
 
+  // ---------------------------------------------------------------- pooling helpers
+  // Bag offsets of a batch of nb samples live at the end of the pool region
+  // (F*nb+1 words); value rows are staged before them, `cap` rows per window.
+  const bool pool_all = p.pooled != nullptr;
+  auto want_feature = [&](int f) -> bool {
+    if (pool_all) return true;
+    return f == p.q_feat[0] || f == p.q_feat[1] || f == p.q_feat[2];
+  };
+  auto pool_offs = [&](int nb) -> uint32_t* {
+    const int offs_bytes = ((F * nb + 1) * 4 + 15) / 16 * 16;
+    return reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::POOL_AVAIL - offs_bytes);
+  };
+  auto pool_cap = [&](int nb) -> int {
+    const int offs_bytes = ((F * nb + 1) * 4 + 15) / 16 * 16;
+    return (C::POOL_AVAIL - offs_bytes) / C::ROWB;
+  };
+  // bag g -> feature g / nb as a multiply-shift, exact for g < 4097, nb <= 128
+  auto nb_recip_of = [](int nb) -> unsigned { return ((1u << 20) + unsigned(nb) - 1u) / unsigned(nb); };
+  // Exclusive scan of the batch's bag lengths (key-major bags g = f*nb + i)
+  // into offs; returns the batch's value count and whether any bag holds more
+  // than kShortBag values. Contains barriers.
+  auto pool_scan = [&](int bs, int nb, bool& longbag) -> long long {
+    const int nbag = F * nb;
+    uint32_t* offs = pool_offs(nb);
+    const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
+    const int g0 = tid * per;
+    int loc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      loc[k] = 0;
+      const int g = g0 + k;
+      if (k < per && g < nbag) {
+        const int f = g / nb, i = g - f * nb;
+        loc[k] = p.lengths[(long long)f * B + bs + i];
+      }
+    }
+    long long sum = 0;
+    bool lng = false;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (loc[k] < 0) { local_flags |= DSF_FLAG_NEG_LENGTH; loc[k] = 0; }
+      if (loc[k] > kMaxBagLen) { local_flags |= DSF_FLAG_COUNT; loc[k] = kMaxBagLen; }
+      lng = lng || loc[k] > kShortBag;
+      sum += loc[k];
+    }
+    long long ex, d0, tot, d1;
+    block_scan2(sum, 0, ms->scan64, ex, d0, tot, d1);
+    long long run = ex;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int g = g0 + k;
+      if (k < per && g < nbag) {
+        offs[g] = uint32_t(run);
+        run += loc[k];
+      }
+    }
+    if (tid == 0) offs[nbag] = uint32_t(tot);
+    longbag = __syncthreads_or(lng) != 0;
+    return tot;
+  };
+  // For the values [w0, w1) of a window: bag -> (feature, index within the
+  // feature's values of this batch), kept in each value's own staging slot
+  // until its id is loaded.
+  auto pool_map = [&](int nb, long long w0, long long w1) {
+    const uint32_t* offs = pool_offs(nb);
+    const unsigned rcp = nb_recip_of(nb);
+    for (long long u = w0 + tid; u < w1; u += kThreads) {
+      const int g = upper_index(offs, F * nb + 1, u);
+      const int f = int((unsigned(g) * rcp) >> 20);
+      *reinterpret_cast<int2*>(sm + C::ACT_OFF + (u - w0) * C::ROWB) =
+          make_int2(f, int(u - (long long)offs[f * nb]));
+    }
+  };
+
   // ---------------------------------------------------------------- per-feature totals
-  for (int f = warp; f < F; f += kWarps) {
+  // The first batch's bag offsets (and its first window's value map) are made
+  // here, before the exchange; a CTA with a single batch publishes its totals
+  // straight from them.
+  long long U0 = 0;
+  bool long0 = false;
+  const int nb0 = min(kSB, ns);
+  if (ns > 0) U0 = pool_scan(sb0, nb0, long0);
+  if (tid < kMaxF) {
+    ms->ft[tid] = 0;
+    ms->fpre[tid] = 0;
+  }
+  if (ns <= kSB) {
+    if (tid < F) {
+      long long t = 0;
+      if (ns > 0) {
+        const uint32_t* offs = pool_offs(ns);
+        t = (long long)offs[(tid + 1) * ns] - (long long)offs[tid * ns];
+      }
+      if (t > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; t = 0x7fffffffll; }
+      st_relaxed_u64(&p.partials[(long long)cta * kMaxF + tid], tag | (unsigned long long)t);
+      __threadfence();
+    }
+  } else for (int f = warp; f < F; f += kWarps) {
     long long s = 0;
     const int* lp = p.lengths + (long long)f * B + sb0;
     for (int i0 = 0; i0 < ns; i0 += 128) {
@@ -407,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       __threadfence();  // push the tagged total out to L2 now
     }
   }
+  if (ns > 0 && long0) pool_map(nb0, 0, min(U0, (long long)pool_cap(nb0)));
 
   // ---------------------------------------------------------------- sequence offset
   // First sequence value index of sample sb0: sum of the full lengths before it.
@@ -501,6 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
     cp_async_commit();
   };
+  // L2 prefetch of the rows behind a prefetched id (thread tid < 3n holds key
+  // tid % 3 of row tid / 3, or -1).
+  auto seq_prefetch = [&](long long id) {
+    if (id < 0) return;
+    const int tb = p.seq_table[tid % 3];
+    if (id >= p.rows[tb]) return;
+    const uint8_t* row = static_cast<const uint8_t*>(p.tables[tb]) + id * C::ROWB;
+#pragma unroll
+    for (int o = 0; o < C::ROWB; o += 128) prefetch_l2(row + o);
+  };
   // The query slices of a tile's rows into the q tile (tensor-core mode):
   // ACT + r*Q floats, part k at k*D, read back from this CTA's own pooled (or
   // query-buffer) rows.
@@ -519,6 +636,41 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       cp_async_commit();
     }
   };
+
+  // Exchange of every CTA's per-feature totals: row c of the partials holds
+  // CTA c's tagged totals. Thread t reads 16 bytes (features f0 = 2*(t%TPR) and
+  // f0+1) of row t/TPR + k*RPP for each of NSLOT slots; TPR = 8 threads per
+  // row when F <= 16 (a 128-byte line), else 16. The first pass is issued
+  // here and checked after the batch setup, whose work hides its latency.
+  const int xsh = F <= 16 ? 3 : 4;
+  const int xjp = tid & ((1 << xsh) - 1);
+  const int xf0 = 2 * xjp;
+  const bool xw0 = xf0 < F, xw1 = xf0 + 1 < F;
+  const int xrpp = kThreads >> xsh;
+  constexpr int NSLOT = 5;
+  unsigned long long xv[NSLOT][2];
+  auto exch_issue = [&](int r0) {
+#pragma unroll
+    for (int k = 0; k < NSLOT; ++k) {
+      const int c = r0 + k * xrpp + (tid >> xsh);
+      if (c < G && xw0) {
+        const ulonglong2 x = ld_relaxed_u64x2(&p.partials[(long long)c * kMaxF + xf0]);
+        xv[k][0] = x.x;
+        xv[k][1] = x.y;
+      } else {
+        xv[k][0] = xv[k][1] = tag;
+      }
+    }
+  };
+  auto exch_ready = [&]() -> bool {
+    bool ready = true;
+#pragma unroll
+    for (int k = 0; k < NSLOT; ++k)
+      ready = ready && (!xw0 || (xv[k][0] & 0xffffffff00000000ull) == tag) &&
+              (!xw1 || (xv[k][1] & 0xffffffff00000000ull) == tag);
+    return ready;
+  };
+  exch_issue(0);
 
   bool prefetched = false;
   long long first_id = -1, second_id = -1;
@@ -541,48 +693,31 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   }
 
   // ---------------------------------------------------------------- exchange
-  // Every CTA's per-feature totals, read as whole 256-byte rows (16 threads per
-  // row, 16 bytes each) once all of them carry this launch's tag. Thread t
-  // always holds features 2*(t%16) and 2*(t%16)+1.
+  // Wait until every row read carries this launch's tag, then sum the totals
+  // (all rows) and the prefix (rows of CTAs before this one) per feature.
   {
-    const int jp = tid & 15;                 // feature pair
-    const int f0 = 2 * jp, f1 = f0 + 1;
-    const bool w0 = f0 < F, w1 = f1 < F;
     long long tot0 = 0, tot1 = 0, pre0 = 0, pre1 = 0;
     bool ok = true;
     uint64_t t0 = 0;
-    for (int r0 = 0; r0 < G; r0 += kThreads / 16 * 4) {
-      unsigned long long v[4][2];
+    for (int r0 = 0; r0 < G; r0 += xrpp * NSLOT) {
+      if (r0 > 0) exch_issue(r0);
       while (true) {
-        bool ready = true;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = r0 + k * (kThreads / 16) + (tid >> 4);
-          if (c < G) {
-            const ulonglong2 x = ld_relaxed_u64x2(&p.partials[(long long)c * kMaxF + f0]);
-            v[k][0] = x.x;
-            v[k][1] = x.y;
-            ready = ready && (!w0 || (x.x & 0xffffffff00000000ull) == tag) &&
-                    (!w1 || (x.y & 0xffffffff00000000ull) == tag);
-          } else {
-            v[k][0] = v[k][1] = tag;
-          }
-        }
-        if (__syncthreads_and(ready)) break;
+        if (__syncthreads_and(exch_ready())) break;
         if (t0 == 0) t0 = globaltimer_ns();
         if (__syncthreads_or(globaltimer_ns() - t0 > kWaitLimitNs)) {
           ok = false;
           break;
         }
         __nanosleep(64);
+        exch_issue(r0);
       }
       if (!ok) break;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = r0 + k * (kThreads / 16) + (tid >> 4);
+      for (int k = 0; k < NSLOT; ++k) {
+        const int c = r0 + k * xrpp + (tid >> xsh);
         if (c >= G) continue;
-        const long long x0 = w0 ? (long long)(v[k][0] & 0xffffffffull) : 0;
-        const long long x1 = w1 ? (long long)(v[k][1] & 0xffffffffull) : 0;
+        const long long x0 = xw0 ? (long long)(xv[k][0] & 0xffffffffull) : 0;
+        const long long x1 = xw1 ? (long long)(xv[k][1] & 0xffffffffull) : 0;
         tot0 += x0;
         tot1 += x1;
         if (c < cta) {
@@ -591,32 +726,24 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         }
       }
     }
-    // the two rows a warp reads share feature pairs: fold lanes l and l+16
-    tot0 += __shfl_xor_sync(0xffffffffu, tot0, 16);
-    tot1 += __shfl_xor_sync(0xffffffffu, tot1, 16);
-    pre0 += __shfl_xor_sync(0xffffffffu, pre0, 16);
-    pre1 += __shfl_xor_sync(0xffffffffu, pre1, 16);
-    long long* red = reinterpret_cast<long long*>(sm + C::ACT_OFF);  // [kWarps][16][4]
-    if (lane < 16) {
-      long long* o = red + (warp * 16 + lane) * 4;
-      o[0] = tot0;
-      o[1] = tot1;
-      o[2] = pre0;
-      o[3] = pre1;
+    // the rows a warp reads share feature pairs: fold lanes l, l + TPR, ...
+    for (int off = 1 << xsh; off < 32; off <<= 1) {
+      tot0 += __shfl_xor_sync(0xffffffffu, tot0, off);
+      tot1 += __shfl_xor_sync(0xffffffffu, tot1, off);
+      pre0 += __shfl_xor_sync(0xffffffffu, pre0, off);
+      pre1 += __shfl_xor_sync(0xffffffffu, pre1, off);
+    }
+    if (lane < (1 << xsh)) {
+      if (xw0) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&ms->ft[xf0]), (unsigned long long)tot0);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&ms->fpre[xf0]), (unsigned long long)pre0);
+      }
+      if (xw1) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&ms->ft[xf0 + 1]), (unsigned long long)tot1);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&ms->fpre[xf0 + 1]), (unsigned long long)pre1);
+      }
     }
     if (!ok && tid == 0) ms->abort_ = 1;
-    __syncthreads();
-    if (tid < F) {
-      const int j = tid >> 1, h = tid & 1;
-      long long tot = 0, pre = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        tot += red[(w * 16 + j) * 4 + h];
-        pre += red[(w * 16 + j) * 4 + 2 + h];
-      }
-      ms->ft[tid] = tot;
-      ms->fpre[tid] = pre;
-    }
   }
   // the first tile's row copies go out once the exchange no longer competes
   // with them for the load pipeline
@@ -640,11 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   }
 
   // ---------------------------------------------------------------- batches
-  const bool pool_all = p.pooled != nullptr;
-  auto want_feature = [&](int f) -> bool {
-    if (pool_all) return true;
-    return f == p.q_feat[0] || f == p.q_feat[1] || f == p.q_feat[2];
-  };
   uint32_t mma_phase = 0;
   uint32_t gk = 0;  // W1 K-blocks consumed so far (stream mode)
   bool weights_ready = false;
@@ -658,50 +780,93 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     // ------------------------------------------------------------ pooling
     {
       const int nbag = F * nb;
-      // g / nb as a multiply-shift, exact for g < 4097 and nb <= 128
-      const unsigned int nb_recip = ((1u << 20) + unsigned(nb) - 1u) / unsigned(nb);
+      const unsigned nb_recip = nb_recip_of(nb);
       auto feat_of = [&](int g) -> int { return int((unsigned(g) * nb_recip) >> 20); };
-      const int offs_bytes = ((nbag + 1) * 4 + 15) / 16 * 16;
       uint8_t* stage = sm + C::ACT_OFF;
-      uint32_t* offs = reinterpret_cast<uint32_t*>(sm + C::ACT_OFF + C::POOL_AVAIL - offs_bytes);
-      const int cap = (C::POOL_AVAIL - offs_bytes) / C::ROWB;
-      const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
-      const int g0 = tid * per;
-      int loc[8];
+      uint32_t* offs = pool_offs(nb);
+      const int cap = pool_cap(nb);
+      bool longbag = long0;
+      const long long tot = bs == sb0 ? U0 : pool_scan(bs, nb, longbag);
+      const long long U = longbag ? tot : 0;  // staged windows only for long bags
+      if (!longbag) {
+        // Direct: one thread per (bag, 16*PPT-byte part), bags in sample-major
+        // order, two in flight per thread; ids then rows straight from global
+        // memory, summed in value order, stored as one contiguous piece.
+        constexpr int PPT = C::LPB < 4 ? C::LPB : 4;
+        constexpr int TPB = C::LPB / PPT;
+        constexpr int EPT = PPT * C::EPL;
+        const int nitems = nbag * TPB;
+        const unsigned f_recip = ((1u << 20) + unsigned(F) - 1u) / unsigned(F);
+        for (int it0 = 0; it0 < nitems; it0 += 2 * kThreads) {
+          long long va[2], ve[2], id[2];
+          int fk[2], ik[2], pk[2];
+          bool live[2];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        loc[k] = 0;
-        const int g = g0 + k;
-        if (k < per && g < nbag) {
-          const int f = g / nb, i = g - f * nb;
-          loc[k] = p.lengths[(long long)f * B + bs + i];
-        }
-      }
-      long long s = 0;
+          for (int k = 0; k < 2; ++k) {
+            const int item = it0 + k * kThreads + tid;
+            const int bi = item / TPB;
+            pk[k] = item - bi * TPB;
+            ik[k] = int((unsigned(bi) * f_recip) >> 20);
+            fk[k] = bi - ik[k] * F;
+            live[k] = item < nitems && want_feature(fk[k]);
+            va[k] = ve[k] = 0;
+            id[k] = -1;
+            if (live[k]) {
+              const int g = fk[k] * nb + ik[k];
+              const uint32_t lo = offs[g], hi = offs[g + 1];
+              va[k] = ms->fcur[fk[k]] + (long long)(lo - offs[fk[k] * nb]);
+              ve[k] = va[k] + (long long)(hi - lo);
+              if (va[k] < ve[k]) {
+                if (ve[k] <= p.n_values) id[k] = __ldg(p.values + va[k]);
+                else { local_flags |= DSF_FLAG_COUNT; ve[k] = va[k]; }
+              }
+            }
+          }
+          float acc[2][EPT];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        loc[k] = min(max(loc[k], 0), kMaxBagLen);
-        s += loc[k];
-      }
-      long long ex, d0, tot, d1;
-      block_scan2(s, 0, ms->scan64, ex, d0, tot, d1);
-      {
-        long long run = ex;
+          for (int k = 0; k < 2; ++k) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int g = g0 + k;
-          if (k < per && g < nbag) {
-            offs[g] = uint32_t(run);
-            run += loc[k];
+            for (int q = 0; q < EPT; ++q) acc[k][q] = 0.f;
+            for (long long u = va[k]; u < ve[k]; ++u) {
+              const long long v = u == va[k] ? id[k] : __ldg(p.values + u);
+              if (v < 0 || v >= p.rows[fk[k]]) { local_flags |= DSF_FLAG_ID_RANGE; continue; }
+              const uint8_t* src = static_cast<const uint8_t*>(p.tables[fk[k]]) + v * C::ROWB + pk[k] * PPT * 16;
+#pragma unroll
+              for (int q = 0; q < PPT; ++q) {
+                float x[C::EPL];
+                widen16v<C::BF16>(ldg16(src + 16 * q), x);
+#pragma unroll
+                for (int e = 0; e < C::EPL; ++e) acc[k][q * C::EPL + e] += x[e];
+              }
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (!live[k]) continue;
+            const long long b = bs + ik[k];
+            auto put = [&](float* o) {
+#pragma unroll
+              for (int q = 0; q < EPT; q += 4)
+                *reinterpret_cast<float4*>(o + q) = make_float4(acc[k][q], acc[k][q + 1], acc[k][q + 2], acc[k][q + 3]);
+            };
+            if (pool_all) {
+              put(p.pooled + b * F * D + fk[k] * D + pk[k] * EPT);
+            } else {
+              for (int j = 0; j < 3; ++j)
+                if (p.q_feat[j] == fk[k]) put(p.qbuf + b * Q + j * D + pk[k] * EPT);
+            }
           }
         }
-        if (tid == 0) offs[nbag] = uint32_t(tot);
       }
-      __syncthreads();
-      const long long U = tot;
       int widx = 0;
       for (long long w0 = 0; w0 < U; w0 += cap, ++widx) {
         const long long w1 = min(U, w0 + (long long)cap);
+        // value -> (feature, index) map in the staging slots (the first window
+        // of the first batch was mapped before the exchange)
+        if (!(bs == sb0 && widx == 0)) {
+          pool_map(nb, w0, w1);
+          __syncthreads();
+        }
         // ids first (all loads in flight), then the row copies
         long long idv[C::VPT];
         int fv[C::VPT];
@@ -713,12 +878,12 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           idv[k] = -1;
           fv[k] = 0;
           if (u < w1) {
-            const int g = upper_index(offs, nbag + 1, u);
-            const int f = feat_of(g);
+            const int2 fl = *reinterpret_cast<const int2*>(stage + (u - w0) * C::ROWB);
+            const int f = fl.x;
             fv[k] = f;
             if (want_feature(f)) {
               inw[k] = true;
-              const long long gv = ms->fcur[f] + (u - (long long)offs[f * nb]);
+              const long long gv = ms->fcur[f] + fl.y;
               if (gv < p.n_values) idv[k] = p.values[gv];
               else local_flags |= DSF_FLAG_COUNT;
             }
@@ -794,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         __syncthreads();
       }
       // empty bags
-      for (int g = tid; g < nbag; g += kThreads) {
+      for (int g = tid; longbag && g < nbag; g += kThreads) {
         if (offs[g] != offs[g + 1]) continue;
         const int f = g / nb, i = g - f * nb;
         if (!want_feature(f)) continue;
@@ -829,78 +994,99 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         seq_rows(seq_ids(0, min(C::TM, R), nb), 0, min(C::TM, R), nb, 0);
       if (T == 0) continue;
 
-      // masked softmax + weighted sum of tile [t0, t0+n) held in S buffer `buf`
-      auto softmax_tile = [&](int t0, int n, int tix, int buf) {
+      // masked softmax + weighted sum of tile [t0, t0+n) held in S buffer `buf`.
+      // (1) Per sample segment of the tile, a group of 8 lanes: the running max
+      // m over its valid rows (merged with the state carried from the previous
+      // tile), z[r] <- exp(z[r] - m) and l = sum of those. (2) One thread per
+      // (segment, d): sum_r exp(z_r - m) s[r][d] over the segment's rows with
+      // four interleaved partial sums. A segment that continues into the next
+      // tile hands (m, l, acc) on. With skip0, warp 0 takes no part (its thread
+      // 0 is issuing MMAs).
+      auto softmax_tile = [&](int t0, int n, int tix, int buf, bool skip0) {
         const uint8_t* S = s_buf(buf);
-          // ---------------------------------------------- masked softmax + weighted sum
-          // Per sample segment of the tile (a warp each): running max m and sum l
-          // over its valid rows (merged with the state carried from the previous
-          // tile), z[r] <- exp(z[r] - m). Then one thread per (segment, d)
-          // accumulates sum_r exp(z_r - m) s[r][d] in row order.
-          {
-            const int ia = ms->row_samp[buf][0], ib = ms->row_samp[buf][n - 1];
-            const int nseg = ib - ia + 1;
-            float* cin = ms->carry[tix & 1];
-            float* cout = ms->carry[(tix + 1) & 1];
-            float* seg_sc = ms->red[0];   // scale of the carried-in state
-            float* seg_inv = ms->red[1];  // 1 / l, or 0 when the segment carries out
-            float* seg_m = ms->red[2];
-            float* seg_l = ms->red[3];
-            if (p.logits) {
-              for (int r = tid; r < n; r += kThreads) {
-                const int j = ms->row_j[buf][r];
-                if (j >= 0) p.logits[j] = ms->z[r];
-              }
-              __syncthreads();
-            }
-            for (int g = warp; g < nseg; g += kWarps) {
-              const int si = ia + g;
-              const int ra = ms->rp[si], re = ms->rp[si + 1];
-              const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
-              if (r1 <= r0) continue;
-              const bool has_in = ra < t0, has_out = re > t0 + n;
-              float m = -INFINITY;
-              for (int r = r0 + lane; r < r1; r += 32) m = fmaxf(m, ms->z[r]);
-              m = warp_max(m);
-              if (has_in) m = fmaxf(m, cin[0]);
-              float l = 0.f;
-              for (int r = r0 + lane; r < r1; r += 32) {
-                const float ez = expf(ms->z[r] - m);
-                ms->z[r] = ez;
-                l += ez;
-              }
-              l = warp_sum(l);
-              if (lane == 0) {
-                const float sc = has_in ? expf(cin[0] - m) : 0.f;
-                if (has_in) l += cin[1] * sc;
-                seg_sc[g] = sc;
-                seg_inv[g] = has_out ? 0.f : 1.f / l;
-                seg_m[g] = m;
-                seg_l[g] = l;
-              }
-            }
-            __syncthreads();
-            for (int item = tid; item < nseg * Q; item += kThreads) {
-              const int g = item / Q, d = item - g * Q;
-              const int si = ia + g;
-              const int ra = ms->rp[si], re = ms->rp[si + 1];
-              const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
-              if (r1 <= r0) continue;
-              const bool has_in = ra < t0, has_out = re > t0 + n;
-              float acc = has_in ? cin[4 + d] * seg_sc[g] : 0.f;
-              for (int r = r0; r < r1; ++r) acc = fmaf(ms->z[r], s_elem<C::BF16>(S, C::SROWB, r, d), acc);
-              if (has_out) {
-                cout[4 + d] = acc;
-                if (d == 0) {
-                  cout[0] = seg_m[g];
-                  cout[1] = seg_l[g];
-                }
-              } else {
-                p.din[(long long)(bs + si) * Q + d] = acc * seg_inv[g];
-              }
-            }
-            __syncthreads();
+        const int ia = ms->row_samp[buf][0], ib = ms->row_samp[buf][n - 1];
+        const int nseg = ib - ia + 1;
+        const float* cin = ms->carry[tix & 1];
+        float* cout = ms->carry[(tix + 1) & 1];
+        float* z = ms->z;
+        float* seg_sc = ms->red[0];   // scale of the carried-in state
+        float* seg_inv = ms->red[1];  // 1 / l, or 0 when the segment carries out
+        float* seg_m = ms->red[2];
+        float* seg_l = ms->red[3];
+        const int t_lo = skip0 ? 32 : 0;
+        if (p.logits) {
+          for (int r = tid; r < n; r += kThreads) {
+            const int j = ms->row_j[buf][r];
+            if (j >= 0) p.logits[j] = z[r];
           }
+          __syncthreads();
+        }
+        if (tid >= t_lo) {
+          const int gl = lane & 7;
+          const unsigned gmask = 0xffu << (lane & 24);
+          const int ngrp = (kThreads - t_lo) >> 3;
+          for (int g = (tid - t_lo) >> 3; g < nseg; g += ngrp) {
+            const int si = ia + g;
+            const int ra = ms->rp[si], re = ms->rp[si + 1];
+            const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
+            if (r1 <= r0) continue;
+            const bool has_in = ra < t0, has_out = re > t0 + n;
+            float m = -INFINITY;
+            for (int r = r0 + gl; r < r1; r += 8) m = fmaxf(m, z[r]);
+            m = fmaxf(m, __shfl_xor_sync(gmask, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(gmask, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(gmask, m, 1));
+            if (has_in) m = fmaxf(m, cin[0]);
+            float l = 0.f;
+            for (int r = r0 + gl; r < r1; r += 8) {
+              const float e = expf(z[r] - m);
+              z[r] = e;
+              l += e;
+            }
+            l += __shfl_xor_sync(gmask, l, 4);
+            l += __shfl_xor_sync(gmask, l, 2);
+            l += __shfl_xor_sync(gmask, l, 1);
+            if (gl == 0) {
+              const float sc = has_in ? expf(cin[0] - m) : 0.f;
+              if (has_in) l += cin[1] * sc;
+              seg_sc[g] = sc;
+              seg_inv[g] = has_out ? 0.f : 1.f / l;
+              seg_m[g] = m;
+              seg_l[g] = l;
+            }
+          }
+        }
+        __syncthreads();
+        const int stride = kThreads - t_lo;
+        for (int item = tid - t_lo; item >= 0 && item < nseg * Q; item += stride) {
+          const int g = item / Q, d = item - g * Q;
+          const int si = ia + g;
+          const int ra = ms->rp[si], re = ms->rp[si + 1];
+          const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
+          if (r1 <= r0) continue;
+          const bool has_in = ra < t0, has_out = re > t0 + n;
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          int r = r0;
+          for (; r + 4 <= r1; r += 4) {
+            a0 = fmaf(z[r], s_elem<C::BF16>(S, C::SROWB, r, d), a0);
+            a1 = fmaf(z[r + 1], s_elem<C::BF16>(S, C::SROWB, r + 1, d), a1);
+            a2 = fmaf(z[r + 2], s_elem<C::BF16>(S, C::SROWB, r + 2, d), a2);
+            a3 = fmaf(z[r + 3], s_elem<C::BF16>(S, C::SROWB, r + 3, d), a3);
+          }
+          for (; r < r1; ++r) a0 = fmaf(z[r], s_elem<C::BF16>(S, C::SROWB, r, d), a0);
+          float acc = (a0 + a1) + (a2 + a3);
+          if (has_in) acc = fmaf(cin[4 + d], seg_sc[g], acc);
+          if (has_out) {
+            cout[4 + d] = acc;
+            if (d == 0) {
+              cout[0] = seg_m[g];
+              cout[1] = seg_l[g];
+            }
+          } else {
+            p.din[(long long)(bs + si) * Q + d] = acc * seg_inv[g];
+          }
+        }
+        __syncthreads();
       };
 
       if constexpr (C::STREAM) {
@@ -940,10 +1126,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           for (int kb = 0; kb < NKB; ++kb, ++gk) {
             uint8_t* X = sm + C::XR_OFF + (kb & 1) * C::XKB;
             const int part = kb / 3, k = kb % 3;
-            for (int item = tid; item < C::TM * 8; item += kThreads) {
+            for (int item = tid; item < n * 8; item += kThreads) {
               const int r = item >> 3, c = item & 7;
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
-              if (r < n) {
+              {
                 const long long b = bs + ms->row_samp[0][r];
                 float qv[8], sv[8];
                 if (part != 1) {
@@ -1002,7 +1188,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           if (ms->abort_ != 0) { tc_fail = true; break; }
           tc_fence_after();
           // epilogue 1: h1 packed in place over the first half of each group's columns
-          {
+          if ((warp & 3) * 32 < n) {
             const int cg = warp >> 2;
             const uint32_t ta = tbase + lane_base + C::TM_ACC1 + uint32_t(cg * 64);
 #pragma unroll 1
@@ -1039,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           __syncthreads();
           if (ms->abort_ != 0) { tc_fail = true; break; }
           tc_fence_after();
-          {
+          if ((warp & 3) * 32 < n) {
             const int cg = warp >> 2;
             float v[16];
             tmem_ld16(tbase + lane_base + C::TM_ACC2 + uint32_t(cg * 16), v);
@@ -1056,7 +1242,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           __syncthreads();
           if (tid < C::TM) ms->z[tid] = ((ms->red[0][tid] + ms->red[1][tid]) + (ms->red[2][tid] + ms->red[3][tid])) + b3;
           __syncthreads();
-          softmax_tile(t0, n, tix, 0);
+          softmax_tile(t0, n, tix, 0, false);
           if (has_next) seq_rows(nxt, t1, min(C::TM, R - t1), nb, 0);
         }
       } else if constexpr (C::MODE == 0) {
@@ -1071,6 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         // x tile -> tensor memory: warp w builds part w/4 of cat[q, s, q-s, q*s]
         // for rows 32*(w%4) .. +31, 8 dims (4 packed columns) at a time
         auto build_x = [&](int n, int buf) {
+          if ((warp & 3) * 32 >= n) return;  // rows past the tile end are never read back
           const uint8_t* S = s_buf(buf);
           const int part = warp >> 2;
           const int r = (warp & 3) * 32 + lane;
@@ -1180,7 +1367,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           const int t0 = k * C::TM, n = min(C::TM, R - t0);
           // ---- layer 1 (k) done: epilogue 1, h1 packed back into TMEM
           if (!wait_mma()) { tc_fail = true; break; }
-          {
+          if ((warp & 3) * 32 < n) {
             const int cg = warp >> 2;
             const uint32_t ta = tbase + lane_base + C::TM_ACC1 + uint32_t(cg * 64);
 #pragma unroll 1
@@ -1199,19 +1386,22 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             }
             tmem_st_wait();
           }
+          // rows of tile k+2 into L2 now: their copy into S (after the softmax
+          // of tile k frees the buffer) then hits L2
+          if (k + 2 < T) seq_prefetch(nxt);
+          // (the rows and query slices of tile k+1 have landed too)
+          cp_async_wait_all();
           tc_fence_before();
           __syncthreads();
           if (tid == 0) issue_l2();
           // ---- x of tile k+1 while layer 2 (k) runs
           if (k + 1 < T) {
-            cp_async_wait_all();
-            __syncthreads();
             build_x(min(C::TM, R - t0 - C::TM), buf ^ 1);
             tc_fence_before();
           }
           // ---- layer 2 (k) done: epilogue 2, z = w3 . ReLU(acc + b2) + b3
           if (!wait_mma()) { tc_fail = true; break; }
-          {
+          if ((warp & 3) * 32 < n) {
             const int cg = warp >> 2;
             float v[16];
             tmem_ld16(tbase + lane_base + C::TM_ACC2 + uint32_t(cg * 16), v);
@@ -1227,10 +1417,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           tc_fence_before();
           __syncthreads();
           if (tid < C::TM) ms->z[tid] = ((ms->red[0][tid] + ms->red[1][tid]) + (ms->red[2][tid] + ms->red[3][tid])) + b3;
-          // ---- layer 1 (k+1) runs during the softmax of tile k
-          if (tid == 0 && k + 1 < T) issue_l1();
           __syncthreads();
-          softmax_tile(t0, n, k, buf);
+          // ---- layer 1 (k+1) runs during the softmax of tile k (warp 0 issues it)
+          if (tid == 0 && k + 1 < T) issue_l1();
+          softmax_tile(t0, n, k, buf, k + 1 < T);
           // ---- rows and query slices of tile k+2 into the freed buffers
           if (k + 2 < T) {
             seq_rows(nxt, t0 + 2 * C::TM, tile_n(k + 2), nb, buf);
@@ -1335,7 +1525,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             __syncthreads();
 
           }
-          softmax_tile(t0, n, tix, 0);
+          softmax_tile(t0, n, tix, 0, false);
           if (has_next) seq_rows(nxt, t1, min(C::TM, R - t1), nb, 0);
         }
       }

@@ -73,6 +73,11 @@ __device__ __forceinline__ void cp_async_16_ca(void* smem_dst, const void* gmem_
                "l"(gmem_src), "r"(src_bytes)
                : "memory");
 }
+// Bring the 128-byte line holding p into L2 (a hint; callers pass only
+// addresses inside their buffers).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // 4-byte copy (no alignment beyond 4 bytes needed).
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
@@ -245,6 +250,15 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ ulonglong2 ld_relaxed_u64x2(const unsigned long long* p) {
   ulonglong2 v;
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+  return v;
+}
+
+// Weak 16-byte load from L2 (not cached in L1), re-issued on every call: the
+// polling loads of the tagged exchange (each 8-byte word carries its own tag,
+// so a stale word is simply read again).
+__device__ __forceinline__ ulonglong2 ld_cg_u64x2(const unsigned long long* p) {
+  ulonglong2 v;
+  asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
   return v;
 }
 
