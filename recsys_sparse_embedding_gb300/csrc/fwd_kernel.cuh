@@ -36,7 +36,7 @@ namespace dsf {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSB = 128;            // samples per batch inside a CTA
+constexpr int kSB = 128;            // samples per batch inside a CTA (<= 256: uint8 row metadata)
 constexpr int kMaxF = 32;           // tables
 constexpr int kMaxG = 1024;         // grid size limit (rows of the partials table)
 constexpr int kN1 = 256, kN2 = 64;  // attn_mlp hidden units
@@ -146,7 +146,7 @@ struct Cfg {
   // layer-2 accumulator, the bf16 x tile
   static constexpr uint32_t TM_ACC1 = 0, TM_ACC2 = kN1, TM_X = kN1 + kN2;
   static_assert(!TWO_S || TM_X + K1 / 2 <= 512, "tensor memory columns");
-  static_assert(!TWO_S || TM * QROW * 4 <= ACT_BYTES, "q tile");
+  static_assert(!TWO_S || kSB * QROW * 4 <= ACT_BYTES, "query slices of a batch");
 };
 
 template <int D, int Q>
@@ -158,8 +158,7 @@ struct Misc {
   float red[4][128];
   float carry[2][4 + Q];       // softmax state: m, l, -, -, acc[Q]
   float pcarry[2][D];          // pooling carry of a bag that spans windows
-  int row_samp[2][128];         // per S buffer: sample of each tile row
-  int row_j[2][128];            // per S buffer: sequence value index of each row
+  uint8_t row_samp[4][128];     // per tile (ring of 4): sample (in the batch) of each row
   int rp[kSB + 4];             // valid-row prefix of the batch's samples
   int so[kSB];                 // first sequence value index of each sample
   long long fcur[kMaxF];       // next global value index of feature f for this CTA
@@ -560,48 +559,37 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     __syncthreads();
   };
 
-  // Id load of this thread's sub-row of tile [t0, t0+n): item = tid -> (row, key).
   // Sequence rows of a tile [t0, t0+n): thread tid < 3n owns sub-row
-  // (r = tid/3, key k = tid%3). Only its id is kept in a register between the
-  // id load and the row copy; the rest is recomputed from rp[] / so[].
-  struct RowSlot { int r, k, i, j; };
-  auto row_slot = [&](int t0, int nb) -> RowSlot {
-    RowSlot rs;
-    rs.r = tid / 3;
-    rs.k = tid - 3 * rs.r;
-    const int rr = t0 + rs.r;
-    rs.i = upper_index(ms->rp, nb + 1, rr);
-    const long long j = (long long)ms->so[rs.i] + (rr - ms->rp[rs.i]);
-    rs.j = j < p.n_seq ? int(j) : -1;
-    return rs;
-  };
+  // (r = tid/3, key k = tid%3). seq_ids finds the row's sample (written once
+  // per tile to the ring slot (t0/TM) % 4 by the k = 0 thread) and value index
+  // and loads the id; only the id stays in a register until the row copy.
+  // kNoRow marks a thread without a row.
+  constexpr long long kNoRow = (long long)(~0ull >> 1) * -1 - 1;
   auto seq_ids = [&](int t0, int n, int nb) -> long long {
-    long long id = -1;
+    long long id = kNoRow;
     if (tid < 3 * n) {
-      const RowSlot rs = row_slot(t0, nb);
-      if (rs.j >= 0) id = p.seq_values[(long long)rs.k * p.n_seq + rs.j];
+      const int r = tid / 3, k = tid - 3 * r;
+      const int rr = t0 + r;
+      const int i = upper_index(ms->rp, nb + 1, rr);
+      const long long jj = (long long)ms->so[i] + (rr - ms->rp[i]);
+      const int j = jj < p.n_seq ? int(jj) : -1;
+      if (k == 0) ms->row_samp[(t0 / C::TM) & 3][r] = uint8_t(i);
+      if (j >= 0) id = p.seq_values[(long long)k * p.n_seq + j];
+      else local_flags |= DSF_FLAG_COUNT;
     }
     return id;
   };
   auto s_buf = [&](int buf) -> uint8_t* { return sm + (buf ? C::S1_OFF : C::S_OFF); };
-  // Row metadata and the row copy (L1-allocating cp.async) of a prefetched id.
-  auto seq_rows = [&](long long id, int t0, int n, int nb, int buf) {
+  // The row copy (L1-allocating cp.async) behind a prefetched id; a thread
+  // whose row has no value (or an id out of range) zero-fills its piece.
+  auto seq_rows = [&](long long id, int n, int buf) {
     if (tid < 3 * n) {
-      const RowSlot rs = row_slot(t0, nb);
-      if (rs.k == 0) {
-        ms->row_samp[buf][rs.r] = rs.i;
-        ms->row_j[buf][rs.r] = rs.j;
-      }
-      const int tb = p.seq_table[rs.k];
+      const int r = tid / 3, k = tid - 3 * r;
+      const int tb = p.seq_table[k];
       const uint8_t* base = static_cast<const uint8_t*>(p.tables[tb]);
-      bool ok = false;
-      if (rs.j >= 0) {
-        ok = id >= 0 && id < p.rows[tb];
-        if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
-      } else {
-        local_flags |= DSF_FLAG_COUNT;
-      }
-      uint8_t* dst = s_buf(buf) + rs.r * C::SROWB + rs.k * C::ROWB;
+      const bool ok = id >= 0 && id < p.rows[tb];
+      if (!ok && id != kNoRow) local_flags |= DSF_FLAG_ID_RANGE;
+      uint8_t* dst = s_buf(buf) + r * C::SROWB + k * C::ROWB;
       const uint8_t* src = ok ? base + id * C::ROWB : base;
 #pragma unroll
       for (int q = 0; q < C::LPB; ++q) cp_async_16_ca(dst + 16 * q, src + 16 * q, ok ? 16u : 0u);
@@ -618,25 +606,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 #pragma unroll
     for (int o = 0; o < C::ROWB; o += 128) prefetch_l2(row + o);
   };
-  // The query slices of a tile's rows into the q tile (tensor-core mode):
-  // ACT + r*Q floats, part k at k*D, read back from this CTA's own pooled (or
-  // query-buffer) rows.
-  auto q_rows = [&](int t0, int n, int nb, int bs) {
-    if constexpr (C::TWO_S) {
-      if (tid < 3 * n) {
-        const RowSlot rs = row_slot(t0, nb);
-        const bool pa = p.pooled != nullptr;
-        const float* src = (pa ? p.pooled : p.qbuf) +
-                           (long long)(bs + rs.i) * (pa ? (long long)F * D : Q) +
-                           (pa ? p.q_feat[rs.k] * D : rs.k * D);
-        float* dst = reinterpret_cast<float*>(sm + C::ACT_OFF) + rs.r * C::QROW + rs.k * D;
-#pragma unroll
-        for (int q = 0; q < D / 4; ++q) cp_async_16_ca(dst + 4 * q, src + 4 * q, 16u);
-      }
-      cp_async_commit();
-    }
-  };
-
   // Exchange of every CTA's per-feature totals: row c of the partials holds
   // CTA c's tagged totals. Thread t reads 16 bytes (features f0 = 2*(t%TPR) and
   // f0+1) of row t/TPR + k*RPP for each of NSLOT slots; TPR = 8 threads per
@@ -747,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   }
   // the first tile's row copies go out once the exchange no longer competes
   // with them for the load pipeline
-  if (C::ATTN && prefetched) seq_rows(first_id, 0, first_n, min(sb0 + kSB, sb1) - sb0, 0);
+  if (C::ATTN && prefetched) seq_rows(first_id, first_n, 0);
   __syncthreads();
   const bool aborted = ms->abort_ != 0;
   if (aborted) {
@@ -822,13 +791,29 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               }
             }
           }
+          // first value of both bags: all row loads in flight before the adds
+          // (a bag without a usable first value reads row 0 and adds nothing)
           float acc[2][EPT];
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
+            const bool has = va[k] < ve[k];
+            const bool ok = has && id[k] >= 0 && id[k] < p.rows[fk[k]];
+            if (has && !ok) local_flags |= DSF_FLAG_ID_RANGE;
+            const uint8_t* src = static_cast<const uint8_t*>(p.tables[fk[k]]) + (ok ? id[k] : 0) * C::ROWB +
+                                 pk[k] * PPT * 16;
 #pragma unroll
-            for (int q = 0; q < EPT; ++q) acc[k][q] = 0.f;
-            for (long long u = va[k]; u < ve[k]; ++u) {
-              const long long v = u == va[k] ? id[k] : __ldg(p.values + u);
+            for (int q = 0; q < PPT; ++q) {
+              float x[C::EPL];
+              widen16v<C::BF16>(ldg16(src + 16 * q), x);
+#pragma unroll
+              for (int e = 0; e < C::EPL; ++e) acc[k][q * C::EPL + e] = 0.f + (ok ? x[e] : 0.f);
+            }
+          }
+          // the rest of each bag, in value order
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            for (long long u = va[k] + 1; u < ve[k]; ++u) {
+              const long long v = __ldg(p.values + u);
               if (v < 0 || v >= p.rows[fk[k]]) { local_flags |= DSF_FLAG_ID_RANGE; continue; }
               const uint8_t* src = static_cast<const uint8_t*>(p.tables[fk[k]]) + v * C::ROWB + pk[k] * PPT * 16;
 #pragma unroll
@@ -854,6 +839,12 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             } else {
               for (int j = 0; j < 3; ++j)
                 if (p.q_feat[j] == fk[k]) put(p.qbuf + b * Q + j * D + pk[k] * EPT);
+            }
+            if constexpr (C::TWO_S) {
+              // the batch's query slices for the attention tiles
+              for (int j = 0; j < 3; ++j)
+                if (p.q_feat[j] == fk[k])
+                  put(reinterpret_cast<float*>(sm + C::ACT_OFF) + ik[k] * C::QROW + j * D + pk[k] * EPT);
             }
           }
         }
@@ -976,6 +967,20 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         }
       }
       __syncthreads();
+      if constexpr (C::TWO_S) {
+        if (longbag) {
+          // staged pooling wrote the query slices to global memory only
+          constexpr int P4 = D / 4;
+          for (int it = tid; it < nb * 3 * P4; it += kThreads) {
+            const int i = it / (3 * P4), rem = it - i * 3 * P4, j = rem / P4, q = rem - j * P4;
+            const float* src = pool_all ? p.pooled + (long long)(bs + i) * F * D + p.q_feat[j] * D
+                                        : p.qbuf + (long long)(bs + i) * Q + j * D;
+            cp_async_16_ca(reinterpret_cast<float*>(sm + C::ACT_OFF) + i * C::QROW + j * D + 4 * q, src + 4 * q, 16u);
+          }
+          cp_async_commit();
+          cp_async_wait_all();
+        }
+      }
       if (tid < F) ms->fcur[tid] += (long long)offs[(tid + 1) * nb] - (long long)offs[tid * nb];
       __syncthreads();
     }
@@ -991,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       const int R = ms->rp[nb];
       const int T = (R + C::TM - 1) / C::TM;  // tiles of this batch
       if (!C::TWO_S && T > 0 && !(prefetched && bs == sb0))
-        seq_rows(seq_ids(0, min(C::TM, R), nb), 0, min(C::TM, R), nb, 0);
+        seq_rows(seq_ids(0, min(C::TM, R), nb), min(C::TM, R), 0);
       if (T == 0) continue;
 
       // masked softmax + weighted sum of tile [t0, t0+n) held in S buffer `buf`.
@@ -1004,7 +1009,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       // 0 is issuing MMAs).
       auto softmax_tile = [&](int t0, int n, int tix, int buf, bool skip0) {
         const uint8_t* S = s_buf(buf);
-        const int ia = ms->row_samp[buf][0], ib = ms->row_samp[buf][n - 1];
+        const int slot = tix & 3;
+        const int ia = ms->row_samp[slot][0], ib = ms->row_samp[slot][n - 1];
         const int nseg = ib - ia + 1;
         const float* cin = ms->carry[tix & 1];
         float* cout = ms->carry[(tix + 1) & 1];
@@ -1016,8 +1022,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         const int t_lo = skip0 ? 32 : 0;
         if (p.logits) {
           for (int r = tid; r < n; r += kThreads) {
-            const int j = ms->row_j[buf][r];
-            if (j >= 0) p.logits[j] = z[r];
+            const int i = ms->row_samp[slot][r];
+            const long long j = (long long)ms->so[i] + (t0 + r - ms->rp[i]);
+            if (j < p.n_seq) p.logits[j] = z[r];
           }
           __syncthreads();
         }
@@ -1130,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               const int r = item >> 3, c = item & 7;
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               {
-                const long long b = bs + ms->row_samp[0][r];
+                const long long b = bs + ms->row_samp[tix & 3][r];
                 float qv[8], sv[8];
                 if (part != 1) {
                   const float* qp = qsrc + b * qstride + (pa ? p.q_feat[k] * D : k * D) + c * 8;
@@ -1243,26 +1250,28 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           if (tid < C::TM) ms->z[tid] = ((ms->red[0][tid] + ms->red[1][tid]) + (ms->red[2][tid] + ms->red[3][tid])) + b3;
           __syncthreads();
           softmax_tile(t0, n, tix, 0, false);
-          if (has_next) seq_rows(nxt, t1, min(C::TM, R - t1), nb, 0);
+          if (has_next) seq_rows(nxt, min(C::TM, R - t1), 0);
         }
       } else if constexpr (C::MODE == 0) {
         // ---------------------------------------------------------- pipelined tiles
         // Per tile k: wait layer 1 (k); epilogue 1 (h1 -> TMEM); issue layer 2 (k);
         // build x (k+1) while it runs; wait layer 2; epilogue 2 (z); issue layer 1
-        // (k+1); softmax (k) while it runs; copy the rows and query slices of tile
-        // k+2 into the freed buffers. Rows run two tiles ahead, their ids three.
+        // (k+1); softmax (k) while it runs; copy the rows of tile k+2 into the
+        // freed buffer. Rows run two tiles ahead (in L2 three), their ids three.
+        // The query slices of every sample of the batch sit in QS (pooling put
+        // them there).
         const uint32_t tbase = ms->tmem_base;
         const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-        const float* QS = reinterpret_cast<const float*>(sm + C::ACT_OFF);  // q tile [TM][Q]
+        const float* QS = reinterpret_cast<const float*>(sm + C::ACT_OFF);  // [kSB][QROW]
         // x tile -> tensor memory: warp w builds part w/4 of cat[q, s, q-s, q*s]
         // for rows 32*(w%4) .. +31, 8 dims (4 packed columns) at a time
-        auto build_x = [&](int n, int buf) {
+        auto build_x = [&](int n, int buf, int slot) {
           if ((warp & 3) * 32 >= n) return;  // rows past the tile end are never read back
           const uint8_t* S = s_buf(buf);
           const int part = warp >> 2;
           const int r = (warp & 3) * 32 + lane;
           const bool live = r < n;
-          const float* qrow = QS + r * C::QROW;
+          const float* qrow = QS + (live ? ms->row_samp[slot][r] : 0) * C::QROW;
           const uint8_t* srow = S + r * C::SROWB;
           const uint32_t xa = tbase + lane_base + C::TM_X + uint32_t(part * (Q / 2));
 #pragma unroll 2
@@ -1331,24 +1340,23 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           return true;
         };
 
-        // prologue: rows of tile 0 are in S0 (or on their way); its query slices
-        // and the rows of tile 1 go out now, then x (0) and layer 1 (0)
+        // prologue: rows of tile 0 are in S0 (or on their way); the rows of tile
+        // 1 go out now, then x (0) and layer 1 (0)
         auto tile_n = [&](int kt) { return min(C::TM, R - kt * C::TM); };
         long long id1 = -1, nxt = -1;
         if (prefetched && bs == sb0) {
           id1 = second_id;
         } else {
-          seq_rows(seq_ids(0, tile_n(0), nb), 0, tile_n(0), nb, 0);
+          seq_rows(seq_ids(0, tile_n(0), nb), tile_n(0), 0);
           if (T > 1) id1 = seq_ids(C::TM, tile_n(1), nb);
         }
-        q_rows(0, tile_n(0), nb, bs);
-        if (T > 1) seq_rows(id1, C::TM, tile_n(1), nb, 1);
+        if (T > 1) seq_rows(id1, tile_n(1), 1);
         if (T > 2) nxt = seq_ids(2 * C::TM, tile_n(2), nb);
-        // wait for the rows and query slices of tile 0; tile 1's rows may stay in flight
+        // wait for the rows of tile 0; tile 1's rows may stay in flight
         if (T > 1) cp_async_wait_group<1>();
         else cp_async_wait_all();
         __syncthreads();
-        build_x(min(C::TM, R), 0);
+        build_x(min(C::TM, R), 0, 0);
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
@@ -1358,7 +1366,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           if (ok) issue_l1();
           else ms->abort_ = 2;
         }
-        if (T > 1) q_rows(C::TM, tile_n(1), nb, bs);  // x (0) is done reading the q tile
         __syncthreads();
         if (ms->abort_ != 0) tc_fail = true;
 
@@ -1389,14 +1396,14 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           // rows of tile k+2 into L2 now: their copy into S (after the softmax
           // of tile k frees the buffer) then hits L2
           if (k + 2 < T) seq_prefetch(nxt);
-          // (the rows and query slices of tile k+1 have landed too)
+          // (the rows of tile k+1 have landed too)
           cp_async_wait_all();
           tc_fence_before();
           __syncthreads();
           if (tid == 0) issue_l2();
           // ---- x of tile k+1 while layer 2 (k) runs
           if (k + 1 < T) {
-            build_x(min(C::TM, R - t0 - C::TM), buf ^ 1);
+            build_x(min(C::TM, R - t0 - C::TM), buf ^ 1, (k + 1) & 3);
             tc_fence_before();
           }
           // ---- layer 2 (k) done: epilogue 2, z = w3 . ReLU(acc + b2) + b3
@@ -1421,10 +1428,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           // ---- layer 1 (k+1) runs during the softmax of tile k (warp 0 issues it)
           if (tid == 0 && k + 1 < T) issue_l1();
           softmax_tile(t0, n, k, buf, k + 1 < T);
-          // ---- rows and query slices of tile k+2 into the freed buffers
+          // ---- rows of tile k+2 into the freed buffer
           if (k + 2 < T) {
-            seq_rows(nxt, t0 + 2 * C::TM, tile_n(k + 2), nb, buf);
-            q_rows(t0 + 2 * C::TM, tile_n(k + 2), nb, bs);
+            seq_rows(nxt, tile_n(k + 2), buf);
             if (k + 3 < T) nxt = seq_ids(t0 + 3 * C::TM, tile_n(k + 3), nb);
           }
         }
@@ -1450,7 +1456,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               const int r = item / Q4, o = item - r * Q4;
               float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
               if (r < n) {
-                const long long b = bs + ms->row_samp[0][r];
+                const long long b = bs + ms->row_samp[tix & 3][r];
                 const int d0 = o * 4, k = d0 / D, dd = d0 - k * D;
                 v = ldcg4(qsrc + b * qstride + (pool_all ? p.q_feat[k] * D : k * D) + dd);
               }
@@ -1526,7 +1532,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 
           }
           softmax_tile(t0, n, tix, 0, false);
-          if (has_next) seq_rows(nxt, t1, min(C::TM, R - t1), nb, 0);
+          if (has_next) seq_rows(nxt, min(C::TM, R - t1), 0);
         }
       }
     }

@@ -16,6 +16,7 @@ int grid_for_device(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return 0;
   if (cache[dev] > 0) return cache[dev];
   constexpr int smem = smem_bytes<C>();
+  static_assert(smem <= 227 * 1024, "shared memory per block above the sm_100-family limit");
   int optin = 0, nsm = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
   if (optin < smem) return 0;
