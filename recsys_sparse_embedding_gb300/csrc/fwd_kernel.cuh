@@ -319,6 +319,18 @@ __device__ __forceinline__ float s_elem(const uint8_t* S, int srowb, int r, int 
   }
 }
 
+// Elements d .. d+3 of row r of a staged S tile (d a multiple of 4).
+template <bool BF16>
+__device__ __forceinline__ float4 s_quad(const uint8_t* S, int srowb, int r, int d) {
+  if constexpr (BF16) {
+    const uint2 h = *reinterpret_cast<const uint2*>(S + r * srowb + d * 2);
+    return make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xffff0000u),
+                       __uint_as_float(h.y << 16), __uint_as_float(h.y & 0xffff0000u));
+  } else {
+    return *reinterpret_cast<const float4*>(S + r * srowb + d * 4);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -1003,8 +1015,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       // (1) Per sample segment of the tile, a group of 8 lanes: the running max
       // m over its valid rows (merged with the state carried from the previous
       // tile), z[r] <- exp(z[r] - m) and l = sum of those. (2) One thread per
-      // (segment, d): sum_r exp(z_r - m) s[r][d] over the segment's rows with
-      // four interleaved partial sums. A segment that continues into the next
+      // (segment, 4 consecutive d): sum_r exp(z_r - m) s[r][d] over the
+      // segment's rows with two interleaved partial sums. A segment that continues into the next
       // tile hands (m, l, acc) on. With skip0, warp 0 takes no part (its thread
       // 0 is issuing MMAs).
       auto softmax_tile = [&](int t0, int n, int tix, int buf, bool skip0) {
@@ -1065,32 +1077,44 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         }
         __syncthreads();
         const int stride = kThreads - t_lo;
-        for (int item = tid - t_lo; item >= 0 && item < nseg * Q; item += stride) {
-          const int g = item / Q, d = item - g * Q;
+        constexpr int Q4 = Q / 4;
+        for (int item = tid - t_lo; item >= 0 && item < nseg * Q4; item += stride) {
+          const int g = item / Q4, d = (item - g * Q4) * 4;
           const int si = ia + g;
           const int ra = ms->rp[si], re = ms->rp[si + 1];
           const int r0 = max(ra, t0) - t0, r1 = min(re, t0 + n) - t0;
           if (r1 <= r0) continue;
           const bool has_in = ra < t0, has_out = re > t0 + n;
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          // two interleaved partial sums (even / odd rows of the segment)
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
           int r = r0;
-          for (; r + 4 <= r1; r += 4) {
-            a0 = fmaf(z[r], s_elem<C::BF16>(S, C::SROWB, r, d), a0);
-            a1 = fmaf(z[r + 1], s_elem<C::BF16>(S, C::SROWB, r + 1, d), a1);
-            a2 = fmaf(z[r + 2], s_elem<C::BF16>(S, C::SROWB, r + 2, d), a2);
-            a3 = fmaf(z[r + 3], s_elem<C::BF16>(S, C::SROWB, r + 3, d), a3);
+          for (; r + 2 <= r1; r += 2) {
+            const float e0 = z[r], e1 = z[r + 1];
+            const float4 s0 = s_quad<C::BF16>(S, C::SROWB, r, d), s1 = s_quad<C::BF16>(S, C::SROWB, r + 1, d);
+            a.x = fmaf(e0, s0.x, a.x); a.y = fmaf(e0, s0.y, a.y); a.z = fmaf(e0, s0.z, a.z); a.w = fmaf(e0, s0.w, a.w);
+            b.x = fmaf(e1, s1.x, b.x); b.y = fmaf(e1, s1.y, b.y); b.z = fmaf(e1, s1.z, b.z); b.w = fmaf(e1, s1.w, b.w);
           }
-          for (; r < r1; ++r) a0 = fmaf(z[r], s_elem<C::BF16>(S, C::SROWB, r, d), a0);
-          float acc = (a0 + a1) + (a2 + a3);
-          if (has_in) acc = fmaf(cin[4 + d], seg_sc[g], acc);
+          if (r < r1) {
+            const float e0 = z[r];
+            const float4 s0 = s_quad<C::BF16>(S, C::SROWB, r, d);
+            a.x = fmaf(e0, s0.x, a.x); a.y = fmaf(e0, s0.y, a.y); a.z = fmaf(e0, s0.z, a.z); a.w = fmaf(e0, s0.w, a.w);
+          }
+          float4 acc = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+          if (has_in) {
+            const float sc = seg_sc[g];
+            const float4 c = *reinterpret_cast<const float4*>(cin + 4 + d);
+            acc = make_float4(fmaf(c.x, sc, acc.x), fmaf(c.y, sc, acc.y), fmaf(c.z, sc, acc.z), fmaf(c.w, sc, acc.w));
+          }
           if (has_out) {
-            cout[4 + d] = acc;
+            *reinterpret_cast<float4*>(cout + 4 + d) = acc;
             if (d == 0) {
               cout[0] = seg_m[g];
               cout[1] = seg_l[g];
             }
           } else {
-            p.din[(long long)(bs + si) * Q + d] = acc * seg_inv[g];
+            const float inv = seg_inv[g];
+            *reinterpret_cast<float4*>(p.din + (long long)(bs + si) * Q + d) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
           }
         }
         __syncthreads();
@@ -1378,18 +1402,21 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             const int cg = warp >> 2;
             const uint32_t ta = tbase + lane_base + C::TM_ACC1 + uint32_t(cg * 64);
 #pragma unroll 1
-            for (int qq = 0; qq < 4; ++qq) {
-              float v[16];
-              tmem_ld16(ta + qq * 16, v);
+            for (int qp = 0; qp < 2; ++qp) {
+              float v[32];
+              tmem_ld16(ta + qp * 32, v);
+              tmem_ld16(ta + qp * 32 + 16, v + 16);
               tmem_ld_wait();
-              uint32_t h[8];
+              uint32_t h[16];
+              const float* bq = ms->b1 + cg * 64 + qp * 32;
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const int col = cg * 64 + qq * 16 + 2 * e;
-                h[e] = pack_bf16x2(fmaxf(v[2 * e] + ms->b1[col], 0.f), fmaxf(v[2 * e + 1] + ms->b1[col + 1], 0.f));
+                const float4 bb = *reinterpret_cast<const float4*>(bq + 4 * e);
+                h[2 * e] = pack_bf16x2(fmaxf(v[4 * e] + bb.x, 0.f), fmaxf(v[4 * e + 1] + bb.y, 0.f));
+                h[2 * e + 1] = pack_bf16x2(fmaxf(v[4 * e + 2] + bb.z, 0.f), fmaxf(v[4 * e + 3] + bb.w, 0.f));
               }
-              // columns [64cg + 8qq, +8) were read by this warp already
-              tmem_st8(ta + qq * 8, h);
+              // columns [64cg + 16qp, +16) were read by this warp already
+              tmem_st16(ta + qp * 16, h);
             }
             tmem_st_wait();
           }
@@ -1415,9 +1442,13 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             tmem_ld_wait();
             float part = 0.f;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int col = cg * 16 + e;
-              part += fmaxf(v[e] + ms->b2[col], 0.f) * ms->w3[col];
+            for (int e = 0; e < 16; e += 4) {
+              const float4 bb = *reinterpret_cast<const float4*>(ms->b2 + cg * 16 + e);
+              const float4 ww = *reinterpret_cast<const float4*>(ms->w3 + cg * 16 + e);
+              part += fmaxf(v[e] + bb.x, 0.f) * ww.x;
+              part += fmaxf(v[e + 1] + bb.y, 0.f) * ww.y;
+              part += fmaxf(v[e + 2] + bb.z, 0.f) * ww.z;
+              part += fmaxf(v[e + 3] + bb.w, 0.f) * ww.w;
             }
             ms->red[cg][(warp & 3) * 32 + lane] = part;
           }
