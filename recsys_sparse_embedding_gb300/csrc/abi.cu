@@ -113,7 +113,6 @@ void fill_common(FwdParams& p, const dsf_tables* t, const dsf_kjt* k, int32_t B,
   p.lengths = k->lengths_dev;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.magic = reinterpret_cast<const uint32_t*>(w + kWsMagicOff);
-  p.done = reinterpret_cast<unsigned long long*>(w + kWsDoneOff);
   p.epoch = reinterpret_cast<unsigned int*>(w + kWsEpochOff);
   p.partials = reinterpret_cast<unsigned long long*>(w + kWsPartOff);
   p.status = status;

@@ -46,7 +46,7 @@ constexpr int kShortBag = 16;       // batches whose bags all fit pool directly
 // Workspace layout (bytes). The header holds the prepared-weights tag, the
 // launch epoch and the exit counter that advances it.
 constexpr size_t kWsMagicOff = 0;
-constexpr size_t kWsDoneOff = 64;
+constexpr size_t kWsDoneOff = 64;   // unused (kept: the layout is shared with the host)
 constexpr size_t kWsEpochOff = 128;
 constexpr size_t kWsPartOff = 256;
 constexpr size_t kWsPartBytes = size_t(kMaxG) * kMaxF * 8;
@@ -73,7 +73,6 @@ struct FwdParams {
   const float* w1t;      // fp32 W1^T [K1][256]
   const float* w2t;      // fp32 W2^T [256][64]
   const uint32_t* magic;
-  unsigned long long* done;      // CTAs that finished this launch
   unsigned int* epoch;           // launch counter, tags the partials
   unsigned long long* partials;  // [G][kMaxF]: (epoch + 1) << 32 | length total
   int* status;
@@ -165,7 +164,7 @@ struct Misc {
   long long ft[kMaxF];
   long long fpre[kMaxF];
   long long scan64[2][kWarps + 2];
-  long long red3[3][kWarps];
+  long long cred[kWarps + 1];   // block_scan2_sum: per-warp sums, then the total
   uint64_t mbar_w;
   uint64_t mbar_mma;
   uint64_t mbar_full[3];       // W1 K-block landed in ring slot (stream mode)
@@ -238,26 +237,41 @@ __device__ __forceinline__ void block_scan2(long long a, long long b, long long 
   __syncthreads();
 }
 
-// Block-wide sums of three int64 values. Contains __syncthreads.
-__device__ __forceinline__ void block_sum3(long long& a, long long& b, long long& c,
-                                           long long (*scr)[kWarps]) {
+// block_scan2 of (a, b) plus the block-wide total of c (cscr: kWarps + 1 words).
+__device__ __forceinline__ void block_scan2_sum(long long a, long long b, long long c,
+                                                long long (*scr)[kWarps + 2], long long* cscr,
+                                                long long& ea, long long& eb, long long& ta,
+                                                long long& tb, long long& tc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
-  c = warp_sum(c);
-  if (lane == 0) {
-    scr[0][warp] = a;
-    scr[1][warp] = b;
-    scr[2][warp] = c;
+  long long ia = warp_incl_scan(a), ib = warp_incl_scan(b), sc = warp_sum(c);
+  if (lane == 31) {
+    scr[0][warp] = ia;
+    scr[1][warp] = ib;
+    cscr[warp] = sc;
   }
   __syncthreads();
-  a = b = c = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    a += scr[0][w];
-    b += scr[1][w];
-    c += scr[2][w];
+  if (warp == 0) {
+    long long wa = lane < kWarps ? scr[0][lane] : 0;
+    long long wb = lane < kWarps ? scr[1][lane] : 0;
+    long long wc = lane < kWarps ? cscr[lane] : 0;
+    long long xa = warp_incl_scan(wa), xb = warp_incl_scan(wb);
+    wc = warp_sum(wc);
+    if (lane < kWarps) {
+      scr[0][lane] = xa - wa;
+      scr[1][lane] = xb - wb;
+    }
+    if (lane == kWarps - 1) {
+      scr[0][kWarps] = xa;
+      scr[1][kWarps] = xb;
+      cscr[kWarps] = wc;
+    }
   }
+  __syncthreads();
+  ea = scr[0][warp] + ia - a;
+  eb = scr[1][warp] + ib - b;
+  ta = scr[0][kWarps];
+  tb = scr[1][kWarps];
+  tc = cscr[kWarps];
   __syncthreads();
 }
 
@@ -345,14 +359,47 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   constexpr int D = C::D, Q = C::Q;
   int local_flags = 0;
 
-  // ---------------------------------------------------------------- prologue
-  // Nothing here waits on global memory: the prepared tag is read into a
-  // register for later, the biases and the weights are copied asynchronously.
-  bool attn_ok = C::ATTN;
+  // ---------------------------------------------------------------- partition
+  // Equal sample counts per CTA: no cross-CTA work is needed to place them.
+  const int sb0 = int((long long)cta * B / G);
+  const int sb1 = int((long long)(cta + 1) * B / G);
+  const int ns = sb1 - sb0;
+  const int nb0 = min(kSB, ns);
+
+  // ---------------------------------------------------------------- early loads
+  // Every global read the first phases depend on goes out before the
+  // prologue, so that their latencies overlap: the launch epoch and prepared
+  // tag, the first batch's bag lengths (pooling scan), its sequence lengths
+  // (batch setup) and the first pass of sequence lengths before it (offset).
+  const unsigned int epoch = *p.epoch;
   const uint32_t magic = C::ATTN ? *p.magic : 0u;
+  int lenv[8];
+  auto pool_len_load = [&](int bs, int nb) {
+    const int per = (F * nb + kThreads - 1) / kThreads;  // <= 8
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lenv[k] = 0;
+      const int g = tid * per + k;
+      if (k < per && g < F * nb) {
+        const int f = g / nb, i = g - f * nb;
+        lenv[k] = p.lengths[(long long)f * B + bs + i];
+      }
+    }
+  };
+  if (ns > 0) pool_len_load(sb0, nb0);
+  const int seq_len0 = (C::ATTN && tid < nb0) ? p.seq_lengths[sb0 + tid] : 0;
+  int seq_pre[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int b = k * kThreads + tid;
+    seq_pre[k] = (C::ATTN && b < sb0) ? p.seq_lengths[b] : 0;
+  }
+
+  // ---------------------------------------------------------------- prologue
+  // The biases and the weights are copied asynchronously.
+  bool attn_ok = C::ATTN;
   if (tid == 0) {
     ms->abort_ = 0;
-    ms->epoch = *p.epoch;
     if constexpr (C::ATTN && C::MODE == 0) {
       mbar_init(&ms->mbar_w, 1);
       mbar_init(&ms->mbar_mma, 1);
@@ -393,14 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   if constexpr (C::ATTN && C::MODE == 0) tc_fence_after();
   const float b3 = C::ATTN ? __ldg(p.b3) : 0.f;
 
-  // ---------------------------------------------------------------- partition
-  // Equal sample counts per CTA: no cross-CTA work is needed to place them.
-  const int sb0 = int((long long)cta * B / G);
-  const int sb1 = int((long long)(cta + 1) * B / G);
   attn_ok = C::ATTN && magic == (kMagicBase | uint32_t(D));
   if (C::ATTN && tid == 0 && !attn_ok && cta == 0) flag(p.status, DSF_FLAG_NOT_PREPARED);
-  const int ns = sb1 - sb0;
-  const unsigned long long tag = (unsigned long long)(ms->epoch + 1u) << 32;
+  const unsigned long long tag = (unsigned long long)(epoch + 1u) << 32;
 
   // ---------------------------------------------------------------- pooling helpers
   // Bag offsets of a batch of nb samples live at the end of the pool region
@@ -423,21 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   // Exclusive scan of the batch's bag lengths (key-major bags g = f*nb + i)
   // into offs; returns the batch's value count and whether any bag holds more
   // than kShortBag values. Contains barriers.
-  auto pool_scan = [&](int bs, int nb, bool& longbag) -> long long {
+  // (the lengths come from pool_len_load)
+  auto pool_scan = [&](int nb, bool& longbag) -> long long {
     const int nbag = F * nb;
     uint32_t* offs = pool_offs(nb);
     const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
     const int g0 = tid * per;
-    int loc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      loc[k] = 0;
-      const int g = g0 + k;
-      if (k < per && g < nbag) {
-        const int f = g / nb, i = g - f * nb;
-        loc[k] = p.lengths[(long long)f * B + bs + i];
-      }
-    }
+    int* loc = lenv;
     long long sum = 0;
     bool lng = false;
 #pragma unroll
@@ -482,8 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   // straight from them.
   long long U0 = 0;
   bool long0 = false;
-  const int nb0 = min(kSB, ns);
-  if (ns > 0) U0 = pool_scan(sb0, nb0, long0);
+  if (ns > 0) U0 = pool_scan(nb0, long0);
   if (tid < kMaxF) {
     ms->ft[tid] = 0;
     ms->fpre[tid] = 0;
@@ -496,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         t = (long long)offs[(tid + 1) * ns] - (long long)offs[tid * ns];
       }
       if (t > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; t = 0x7fffffffll; }
+      // (each word carries its own tag: no fence needed behind it)
       st_relaxed_u64(&p.partials[(long long)cta * kMaxF + tid], tag | (unsigned long long)t);
-      __threadfence();
     }
   } else for (int f = warp; f < F; f += kWarps) {
     long long s = 0;
@@ -521,16 +554,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     if (s > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; s = 0x7fffffffll; }
     if (lane == 0) {
       st_relaxed_u64(&p.partials[(long long)cta * kMaxF + f], tag | (unsigned long long)s);
-      __threadfence();  // push the tagged total out to L2 now
     }
   }
   if (ns > 0 && long0) pool_map(nb0, 0, min(U0, (long long)pool_cap(nb0)));
 
   // ---------------------------------------------------------------- sequence offset
-  // First sequence value index of sample sb0: sum of the full lengths before it.
+  // First sequence value index of sample sb0: sum of the full lengths before
+  // it (this thread's part; the first batch setup adds the parts up).
+  long long seq_part = 0;
   if constexpr (C::ATTN) {
-    long long acc = 0;
-    for (int b0 = 0; b0 < sb0; b0 += 4 * kThreads) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) seq_part += max(seq_pre[k], 0);  // first pass, loaded early
+    for (int b0 = 4 * kThreads; b0 < sb0; b0 += 4 * kThreads) {
       int l[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -538,37 +573,37 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         l[k] = b < sb0 ? p.seq_lengths[b] : 0;
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc += max(l[k], 0);
+      for (int k = 0; k < 4; ++k) seq_part += max(l[k], 0);
     }
-    long long u0 = 0, u1 = 0;
-    block_sum3(acc, u0, u1, ms->red3);
-    if (tid == 0) ms->seq_cur = acc;
-    __syncthreads();
   }
 
   // ---------------------------------------------------------------- batch setup
   // Valid-row prefix rp[] and sequence value offsets so[] for samples [bs, be).
+  // The first batch takes its lengths from seq_len0 and starts at the sum of
+  // the seq_part of all threads; later batches continue from seq_cur.
   auto setup_batch = [&](int bs, int be) {
+    const bool first = bs == sb0;
     const int nb = be - bs;
     long long lv = 0, lf = 0;
     if (tid < nb) {
-      const int L = p.seq_lengths[bs + tid];
+      const int L = first ? seq_len0 : p.seq_lengths[bs + tid];
       if (L < 0) local_flags |= DSF_FLAG_NEG_LENGTH;
       if (L > p.max_len) local_flags |= DSF_FLAG_SEQ_TRUNC;
       lf = max(L, 0);
       lv = min(lf, (long long)p.max_len);
     }
-    long long ev, ef, tv, tf;
-    block_scan2(lv, lf, ms->scan64, ev, ef, tv, tf);
+    long long ev, ef, tv, tf, tc;
+    block_scan2_sum(lv, lf, first ? seq_part : 0ll, ms->scan64, ms->cred, ev, ef, tv, tf, tc);
+    const long long base = first ? tc : ms->seq_cur;
     if (tid < nb) {
       ms->rp[tid] = int(ev);
-      const long long so = ms->seq_cur + ef;
+      const long long so = base + ef;
       ms->so[tid] = so < p.n_seq ? int(so) : int(p.n_seq);
     }
     if (tid == 0) ms->rp[nb] = int(tv);
     __syncthreads();
-    if (tid == 0) ms->seq_cur += tf;
-    __syncthreads();
+    // read again only by the next batch's setup, many barriers later
+    if (tid == 0) ms->seq_cur = base + tf;
   };
 
   // Sequence rows of a tile [t0, t0+n): thread tid < 3n owns sub-row
@@ -725,6 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       }
     }
     if (!ok && tid == 0) ms->abort_ = 1;
+    // Every CTA read the epoch before it published its totals, and none reads
+    // it again: once CTA 0 has seen all totals it advances the epoch (which
+    // tags the next launch's totals). On a timeout it advances it too.
+    if (cta == 0 && tid == 0) atomicAdd(p.epoch, 1u);
   }
   // the first tile's row copies go out once the exchange no longer competes
   // with them for the load pipeline
@@ -734,15 +773,13 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   if (aborted) {
     if (tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
   } else {
-    if (tid < F) {
-      long long base = ms->fpre[tid];
-      for (int f = 0; f < tid; ++f) base += ms->ft[f];
-      ms->fcur[tid] = base;
-    }
-    if (tid == 0 && cta == 0) {
-      long long total = 0;
-      for (int f = 0; f < F; ++f) total += ms->ft[f];
-      if (total != p.n_values) local_flags |= DSF_FLAG_COUNT;
+    if (warp == 0) {
+      // feature f's values start after all values of features < f
+      const long long t = lane < F ? (long long)ms->ft[lane] : 0;
+      const long long incl = warp_incl_scan(t);
+      if (lane < F) ms->fcur[lane] = (long long)ms->fpre[lane] + (incl - t);
+      const long long total = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0 && cta == 0 && total != p.n_values) local_flags |= DSF_FLAG_COUNT;
     }
     __syncthreads();
   }
@@ -767,7 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       uint32_t* offs = pool_offs(nb);
       const int cap = pool_cap(nb);
       bool longbag = long0;
-      const long long tot = bs == sb0 ? U0 : pool_scan(bs, nb, longbag);
+      if (bs != sb0) pool_len_load(bs, nb);
+      const long long tot = bs == sb0 ? U0 : pool_scan(nb, longbag);
       const long long U = longbag ? tot : 0;  // staged windows only for long bags
       if (!longbag) {
         // Direct: one thread per (bag, 16*PPT-byte part), bags in sample-major
@@ -1592,17 +1630,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
   }
   if (tc_fail && tid == 0) local_flags |= DSF_FLAG_TIMEOUT;
-  // the last CTA to finish advances the epoch for the next launch
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned long long old = atomicAdd(p.done, 1ull);
-    if (old == (unsigned long long)(G - 1)) {
-      atomicExch(p.done, 0ull);
-      __threadfence();
-      atomicExch(p.epoch, ms->epoch + 1u);
-    }
-  }
   // one status write per warp
   local_flags = __reduce_or_sync(0xffffffffu, local_flags);
   if (lane == 0 && local_flags) flag(p.status, local_flags);
