@@ -146,6 +146,7 @@ struct Cfg {
   static constexpr uint32_t TM_ACC1 = 0, TM_ACC2 = kN1, TM_X = kN1 + kN2;
   static_assert(!TWO_S || TM_X + K1 / 2 <= 512, "tensor memory columns");
   static_assert(!TWO_S || kSB * QROW * 4 <= ACT_BYTES, "query slices of a batch");
+  static_assert(32 + 3 * TM <= kThreads, "sequence rows: one thread per (row, key) outside warp 0");
 };
 
 template <int D, int Q>
@@ -161,6 +162,7 @@ struct Misc {
   int rp[kSB + 4];             // valid-row prefix of the batch's samples
   int so[kSB];                 // first sequence value index of each sample
   long long fcur[kMaxF];       // next global value index of feature f for this CTA
+  long long ftb[kMaxF];        // value count of feature f in the current batch
   long long ft[kMaxF];
   long long fpre[kMaxF];
   long long scan64[2][kWarps + 2];
@@ -373,16 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   // (batch setup) and the first pass of sequence lengths before it (offset).
   const unsigned int epoch = *p.epoch;
   const uint32_t magic = C::ATTN ? *p.magic : 0u;
-  int lenv[8];
+  // Bag lengths of a batch, one feature per warp: warp w holds features
+  // w + kWarps*a (a < kLF), lane l the samples l + 32j (j < kLJ).
+  constexpr int kLF = (kMaxF + kWarps - 1) / kWarps, kLJ = kSB / 32;
+  int lenv[kLF][kLJ];
   auto pool_len_load = [&](int bs, int nb) {
-    const int per = (F * nb + kThreads - 1) / kThreads;  // <= 8
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      lenv[k] = 0;
-      const int g = tid * per + k;
-      if (k < per && g < F * nb) {
-        const int f = g / nb, i = g - f * nb;
-        lenv[k] = p.lengths[(long long)f * B + bs + i];
+    for (int a = 0; a < kLF; ++a) {
+      const int f = warp + a * kWarps;
+#pragma unroll
+      for (int j = 0; j < kLJ; ++j) {
+        const int i = lane + 32 * j;
+        lenv[a][j] = (f < F && i < nb) ? p.lengths[(long long)f * B + bs + i] : 0;
       }
     }
   };
@@ -462,38 +466,57 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   };
   // bag g -> feature g / nb as a multiply-shift, exact for g < 4097, nb <= 128
   auto nb_recip_of = [](int nb) -> unsigned { return ((1u << 20) + unsigned(nb) - 1u) / unsigned(nb); };
-  // Exclusive scan of the batch's bag lengths (key-major bags g = f*nb + i)
-  // into offs; returns the batch's value count and whether any bag holds more
-  // than kShortBag values. Contains barriers.
-  // (the lengths come from pool_len_load)
-  auto pool_scan = [&](int nb, bool& longbag) -> long long {
-    const int nbag = F * nb;
+  // Exclusive scan of the batch's bag lengths (key-major bags g = f*nb + i,
+  // from pool_len_load) into offs; returns the batch's value count and
+  // whether any bag holds more than kShortBag values. With publish, each
+  // feature's total is stored to this CTA's partials row as soon as its warp
+  // has summed it. Contains barriers.
+  auto pool_scan = [&](int nb, bool& longbag, bool publish) -> long long {
     uint32_t* offs = pool_offs(nb);
-    const int per = (nbag + kThreads - 1) / kThreads;  // <= 8
-    const int g0 = tid * per;
-    int* loc = lenv;
-    long long sum = 0;
     bool lng = false;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (loc[k] < 0) { local_flags |= DSF_FLAG_NEG_LENGTH; loc[k] = 0; }
-      if (loc[k] > kMaxBagLen) { local_flags |= DSF_FLAG_COUNT; loc[k] = kMaxBagLen; }
-      lng = lng || loc[k] > kShortBag;
-      sum += loc[k];
-    }
-    long long ex, d0, tot, d1;
-    block_scan2(sum, 0, ms->scan64, ex, d0, tot, d1);
-    long long run = ex;
+    for (int a = 0; a < kLF; ++a) {
+      long long sf = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int g = g0 + k;
-      if (k < per && g < nbag) {
-        offs[g] = uint32_t(run);
-        run += loc[k];
+      for (int j = 0; j < kLJ; ++j) {
+        int& v = lenv[a][j];
+        if (v < 0) { local_flags |= DSF_FLAG_NEG_LENGTH; v = 0; }
+        if (v > kMaxBagLen) { local_flags |= DSF_FLAG_COUNT; v = kMaxBagLen; }
+        lng = lng || v > kShortBag;
+        sf += v;
+      }
+      sf = warp_sum(sf);
+      const int f = warp + a * kWarps;
+      if (lane == 0 && f < F) {
+        ms->ftb[f] = sf;
+        if (publish) {
+          if (sf > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; sf = 0x7fffffffll; }
+          // (each word carries its own tag: no fence needed behind it)
+          st_relaxed_u64(&p.partials[(long long)cta * kMaxF + f], tag | (unsigned long long)sf);
+        }
       }
     }
-    if (tid == 0) offs[nbag] = uint32_t(tot);
     longbag = __syncthreads_or(lng) != 0;
+    // feature f starts after all bags of features < f
+    const long long tf = lane < F ? ms->ftb[lane] : 0;
+    const long long incl = warp_incl_scan(tf);
+    const long long tot = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+    for (int a = 0; a < kLF; ++a) {
+      const int f = warp + a * kWarps;
+      if (f >= F) continue;  // warp-uniform
+      long long base = __shfl_sync(0xffffffffu, incl - tf, f);
+#pragma unroll
+      for (int j = 0; j < kLJ; ++j) {
+        const long long v = lenv[a][j];
+        const long long in = warp_incl_scan(v);
+        const int i = lane + 32 * j;
+        if (i < nb) offs[f * nb + i] = uint32_t(base + in - v);
+        base += __shfl_sync(0xffffffffu, in, 31);
+      }
+    }
+    if (tid == 0) offs[F * nb] = uint32_t(tot);
+    __syncthreads();
     return tot;
   };
   // For the values [w0, w1) of a window: bag -> (feature, index within the
@@ -516,23 +539,14 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   // straight from them.
   long long U0 = 0;
   bool long0 = false;
-  if (ns > 0) U0 = pool_scan(nb0, long0);
   if (tid < kMaxF) {
     ms->ft[tid] = 0;
     ms->fpre[tid] = 0;
   }
-  if (ns <= kSB) {
-    if (tid < F) {
-      long long t = 0;
-      if (ns > 0) {
-        const uint32_t* offs = pool_offs(ns);
-        t = (long long)offs[(tid + 1) * ns] - (long long)offs[tid * ns];
-      }
-      if (t > 0x7fffffffll) { local_flags |= DSF_FLAG_COUNT; t = 0x7fffffffll; }
-      // (each word carries its own tag: no fence needed behind it)
-      st_relaxed_u64(&p.partials[(long long)cta * kMaxF + tid], tag | (unsigned long long)t);
-    }
-  } else for (int f = warp; f < F; f += kWarps) {
+  if (ns > 0) U0 = pool_scan(nb0, long0, ns <= kSB);
+  if (ns == 0) {
+    if (tid < F) st_relaxed_u64(&p.partials[(long long)cta * kMaxF + tid], tag);
+  } else if (ns > kSB) for (int f = warp; f < F; f += kWarps) {
     long long s = 0;
     const int* lp = p.lengths + (long long)f * B + sb0;
     for (int i0 = 0; i0 < ns; i0 += 128) {
@@ -606,16 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     if (tid == 0) ms->seq_cur = base + tf;
   };
 
-  // Sequence rows of a tile [t0, t0+n): thread tid < 3n owns sub-row
-  // (r = tid/3, key k = tid%3). seq_ids finds the row's sample (written once
+  // Sequence rows of a tile [t0, t0+n): thread tid = 32 + ri, ri < 3n, owns
+  // sub-row (r = ri/3, key k = ri%3); warp 0 has none, so that its thread 0
+  // can issue MMAs meanwhile. seq_ids finds the row's sample (written once
   // per tile to the ring slot (t0/TM) % 4 by the k = 0 thread) and value index
   // and loads the id; only the id stays in a register until the row copy.
   // kNoRow marks a thread without a row.
   constexpr long long kNoRow = (long long)(~0ull >> 1) * -1 - 1;
+  const int ri = tid - 32;
   auto seq_ids = [&](int t0, int n, int nb) -> long long {
     long long id = kNoRow;
-    if (tid < 3 * n) {
-      const int r = tid / 3, k = tid - 3 * r;
+    if (ri >= 0 && ri < 3 * n) {
+      const int r = ri / 3, k = ri - 3 * r;
       const int rr = t0 + r;
       const int i = upper_index(ms->rp, nb + 1, rr);
       const long long jj = (long long)ms->so[i] + (rr - ms->rp[i]);
@@ -630,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   // The row copy (L1-allocating cp.async) behind a prefetched id; a thread
   // whose row has no value (or an id out of range) zero-fills its piece.
   auto seq_rows = [&](long long id, int n, int buf) {
-    if (tid < 3 * n) {
-      const int r = tid / 3, k = tid - 3 * r;
+    if (ri >= 0 && ri < 3 * n) {
+      const int r = ri / 3, k = ri - 3 * r;
       const int tb = p.seq_table[k];
       const uint8_t* base = static_cast<const uint8_t*>(p.tables[tb]);
       const bool ok = id >= 0 && id < p.rows[tb];
@@ -643,11 +659,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
     cp_async_commit();
   };
-  // L2 prefetch of the rows behind a prefetched id (thread tid < 3n holds key
-  // tid % 3 of row tid / 3, or -1).
+  // L2 prefetch of the rows behind a prefetched id (key ri % 3 of row ri / 3).
   auto seq_prefetch = [&](long long id) {
     if (id < 0) return;
-    const int tb = p.seq_table[tid % 3];
+    const int tb = p.seq_table[ri % 3];
     if (id >= p.rows[tb]) return;
     const uint8_t* row = static_cast<const uint8_t*>(p.tables[tb]) + id * C::ROWB;
 #pragma unroll
@@ -688,6 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   };
   exch_issue(0);
 
+  // The first batch's sequence rows: the ids of its first (two) tiles are
+  // loaded while pooling waits for its own ids, and the rows of tile 0 are
+  // copied into S0 (those of tile 1 prefetched into L2) while pooling waits
+  // for its rows.
   bool prefetched = false;
   long long first_id = -1, second_id = -1;
   int first_n = 0, second_n = 0;
@@ -698,15 +717,25 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       const int R0 = ms->rp[be - sb0];
       if (attn_ok && R0 > 0) {
         first_n = min(C::TM, R0);
-        first_id = seq_ids(0, first_n, be - sb0);
-        if (C::TWO_S && R0 > C::TM) {
-          second_n = min(C::TM, R0 - C::TM);
-          second_id = seq_ids(C::TM, second_n, be - sb0);
-        }
+        if (C::TWO_S && R0 > C::TM) second_n = min(C::TM, R0 - C::TM);
         prefetched = true;
       }
     }
   }
+  bool first_ids_todo = prefetched, first_rows_todo = prefetched;
+  auto first_ids = [&]() {
+    if (!first_ids_todo) return;
+    first_ids_todo = false;
+    first_id = seq_ids(0, first_n, nb0);
+    if (second_n > 0) second_id = seq_ids(C::TM, second_n, nb0);
+  };
+  auto first_rows = [&]() {
+    first_ids();
+    if (!first_rows_todo) return;
+    first_rows_todo = false;
+    seq_rows(first_id, first_n, 0);
+    if (C::TWO_S) seq_prefetch(second_id);  // tile 1 lands in S1 after pooling
+  };
 
   // ---------------------------------------------------------------- exchange
   // Wait until every row read carries this launch's tag, then sum the totals
@@ -767,7 +796,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   }
   // the first tile's row copies go out once the exchange no longer competes
   // with them for the load pipeline
-  if (C::ATTN && prefetched) seq_rows(first_id, first_n, 0);
   __syncthreads();
   const bool aborted = ms->abort_ != 0;
   if (aborted) {
@@ -805,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       const int cap = pool_cap(nb);
       bool longbag = long0;
       if (bs != sb0) pool_len_load(bs, nb);
-      const long long tot = bs == sb0 ? U0 : pool_scan(nb, longbag);
+      const long long tot = bs == sb0 ? U0 : pool_scan(nb, longbag, false);
       const long long U = longbag ? tot : 0;  // staged windows only for long bags
       if (!longbag) {
         // Direct: one thread per (bag, 16*PPT-byte part), bags in sample-major
@@ -841,6 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               }
             }
           }
+          if constexpr (C::ATTN) first_ids();  // (their latency overlaps ours)
           // first value of both bags: all row loads in flight before the adds
           // (a bag without a usable first value reads row 0 and adds nothing)
           float acc[2][EPT];
@@ -859,6 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               for (int e = 0; e < C::EPL; ++e) acc[k][q * C::EPL + e] = 0.f + (ok ? x[e] : 0.f);
             }
           }
+          if constexpr (C::ATTN) first_rows();
           // the rest of each bag, in value order
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -899,6 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           }
         }
       }
+      if constexpr (C::ATTN) first_rows();  // (staged pooling: before its windows)
       int widx = 0;
       for (long long w0 = 0; w0 < U; w0 += cap, ++widx) {
         const long long w1 = min(U, w0 + (long long)cap);
@@ -1402,8 +1433,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           return true;
         };
 
-        // prologue: rows of tile 0 are in S0 (or on their way); the rows of tile
-        // 1 go out now, then x (0) and layer 1 (0)
+        // prologue: rows of tile 0 are in S0 (or on their way); x (0), then
+        // layer 1 (0) from thread 0 while warps 1.. send out the rows of tile 1
+        // (already in L2 for the first batch) and the ids of tile 2
         auto tile_n = [&](int kt) { return min(C::TM, R - kt * C::TM); };
         long long id1 = -1, nxt = -1;
         if (prefetched && bs == sb0) {
@@ -1412,11 +1444,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           seq_rows(seq_ids(0, tile_n(0), nb), tile_n(0), 0);
           if (T > 1) id1 = seq_ids(C::TM, tile_n(1), nb);
         }
-        if (T > 1) seq_rows(id1, tile_n(1), 1);
-        if (T > 2) nxt = seq_ids(2 * C::TM, tile_n(2), nb);
-        // wait for the rows of tile 0; tile 1's rows may stay in flight
-        if (T > 1) cp_async_wait_group<1>();
-        else cp_async_wait_all();
+        cp_async_wait_all();
         __syncthreads();
         build_x(min(C::TM, R), 0, 0);
         tc_fence_before();
@@ -1428,6 +1456,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           if (ok) issue_l1();
           else ms->abort_ = 2;
         }
+        if (T > 1) seq_rows(id1, tile_n(1), 1);
+        if (T > 2) nxt = seq_ids(2 * C::TM, tile_n(2), nb);
         __syncthreads();
         if (ms->abort_ != 0) tc_fail = true;
 
