@@ -642,6 +642,34 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     }
     return id;
   };
+  // seq_ids of two tiles at once, the two row -> sample searches interleaved
+  auto seq_ids2 = [&](int t0a, int na, int t0b, int nbt, int nb, long long& ida, long long& idb) {
+    ida = idb = kNoRow;
+    if (ri < 0 || ri >= 3 * na) return;
+    const int r = ri / 3, k = ri - 3 * r;
+    const bool vb = ri < 3 * nbt;
+    const int xa = t0a + r, xb = t0b + r;
+    int loa = 0, hia = nb, lob = 0, hib = vb ? nb : 0;
+    while (loa < hia || lob < hib) {
+      if (loa < hia) {
+        const int mid = (loa + hia + 1) >> 1;
+        if (ms->rp[mid] <= xa) loa = mid; else hia = mid - 1;
+      }
+      if (lob < hib) {
+        const int mid = (lob + hib + 1) >> 1;
+        if (ms->rp[mid] <= xb) lob = mid; else hib = mid - 1;
+      }
+    }
+    auto finish = [&](int t0, int xr, int i, long long& id) {
+      const long long jj = (long long)ms->so[i] + (xr - ms->rp[i]);
+      const int j = jj < p.n_seq ? int(jj) : -1;
+      if (k == 0) ms->row_samp[(t0 / C::TM) & 3][r] = uint8_t(i);
+      if (j >= 0) id = p.seq_values[(long long)k * p.n_seq + j];
+      else local_flags |= DSF_FLAG_COUNT;
+    };
+    finish(t0a, xa, loa, ida);
+    if (vb) finish(t0b, xb, lob, idb);
+  };
   auto s_buf = [&](int buf) -> uint8_t* { return sm + (buf ? C::S1_OFF : C::S_OFF); };
   // The row copy (L1-allocating cp.async) behind a prefetched id; a thread
   // whose row has no value (or an id out of range) zero-fills its piece.
@@ -726,8 +754,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
   auto first_ids = [&]() {
     if (!first_ids_todo) return;
     first_ids_todo = false;
-    first_id = seq_ids(0, first_n, nb0);
-    if (second_n > 0) second_id = seq_ids(C::TM, second_n, nb0);
+    if (second_n > 0) seq_ids2(0, first_n, C::TM, second_n, nb0, first_id, second_id);
+    else first_id = seq_ids(0, first_n, nb0);
   };
   auto first_rows = [&]() {
     first_ids();
@@ -888,7 +916,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               for (int e = 0; e < C::EPL; ++e) acc[k][q * C::EPL + e] = 0.f + (ok ? x[e] : 0.f);
             }
           }
-          if constexpr (C::ATTN) first_rows();
           // the rest of each bag, in value order
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -928,6 +955,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             }
           }
         }
+        // tile 0's rows into S0 (its ids have landed meanwhile)
+        if constexpr (C::ATTN) first_rows();
       }
       if constexpr (C::ATTN) first_rows();  // (staged pooling: before its windows)
       int widx = 0;
