@@ -52,6 +52,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, ws, device=None):
+    """The largest of every rank's x (a float), through torch.distributed's
+    MAX all-reduce on whatever backend the group uses; x itself when ws == 1."""
+    if ws == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_rate(units_per_rank, slowest_ms, ws):
+    """Whole-job throughput of ws replicas that each processed units_per_rank
+    units, over the slowest rank's time."""
+    return units_per_rank * ws / (slowest_ms / 1e3)
+
+
 def peaks():
     """Measured HBM GB/s and bf16 TFLOP/s (burst, sustained) or the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -301,12 +319,8 @@ def main():
             dist.barrier()
         times_ms = [a.elapsed_time(b) for a, b in ev]
         st = int(status.item())
-        total_ms = float(sum(times_ms))
-        if ws > 1:
-            t = torch.tensor([total_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
-        value = B * K * ws / (total_ms / 1e3)
+        total_ms = max_over_ranks(sum(times_ms), ws, dev)
+        value = weak_rate(B * K, total_ms, ws)
         ms_step = total_ms / K
 
         # end to end: pinned host inputs -> device, the C-ABI call, results -> host
@@ -337,8 +351,8 @@ def main():
             e2e_step()
             eev[i][1].record(stream)
         stream.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
-        e2e_value = B * E / (e2e_ms / 1e3)
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), ws, dev)
+        e2e_value = weak_rate(B * E, e2e_ms, ws)
 
     # roofline of the fused kernel (the only kernel of a step)
     nbytes, flops, P = algorithmic_work(batch)

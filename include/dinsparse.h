@@ -30,8 +30,8 @@
  *     launch errors only; data errors found on the device are OR-ed into
  *     *status_dev (DSF_FLAG_* bits), which the caller zeroes beforehand.
  *   - One workspace may serve one stream at a time: two calls that overlap on
- *     the GPU must not share a workspace (its grid-barrier counter and
- *     per-block partial sums would race).
+ *     the GPU must not share a workspace (its launch epoch and per-block
+ *     partial sums would race).
  *   - Device data errors never fault or trap: an id outside [0, rows) or a
  *     value index past the values array contributes a zero row; a negative
  *     length counts as zero; a sequence longer than max_len keeps its first
@@ -116,12 +116,14 @@ typedef struct {
 } dsf_mlp;
 
 /* Bytes of workspace needed for batch size B and embedding dim D (packed MLP
- * weights, per-block partial sums, grid-barrier counter, query buffer).
+ * weights, epoch-tagged per-block partial sums, launch epoch, query buffer).
  * Returns 0 for unsupported D. */
 size_t dsf_workspace_bytes(int32_t B, int32_t D);
 
-/* Zeroes the workspace's barrier state. Call once after allocating a
- * workspace (before any other call that uses it). Asynchronous on stream. */
+/* Zeroes the workspace's exchange state (launch epoch and tagged partial
+ * sums). Call once after allocating a workspace, before any other call that
+ * uses it, and again after a call reported DSF_FLAG_TIMEOUT. Asynchronous on
+ * stream. */
 int dsf_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
 
 /* Packs the MLP weights into the workspace: bf16 in the tensor-core operand
