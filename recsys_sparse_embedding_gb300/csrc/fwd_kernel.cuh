@@ -132,19 +132,26 @@ struct Cfg {
   static constexpr int ACT_OFF = STREAM ? W1_OFF : ((ATTN && MODE == 0) ? W2_OFF + W2B : 0);
   static constexpr int ACT_BYTES =
       !ATTN ? POOL_BYTES
-            : (STREAM ? W1_STAGES * W1KB + 2 * XKB : (MODE == 0 ? 36 * 1024 : cmax(H1FB, POOL_BYTES)));
+            : (STREAM ? W1_STAGES * W1KB + 2 * XKB
+                      : (MODE == 0 ? (kSB * QROW * 4 + 1023) / 1024 * 1024 : cmax(H1FB, POOL_BYTES)));
   static constexpr int QT_OFF = ACT_OFF + ACT_BYTES;  // fp32 mode only
   static constexpr int S_BYTES = ATTN ? TM * SROWB : 0;
   static constexpr int S1_OFF = QT_OFF + ((ATTN && MODE == 1) ? QTB : 0);
   static constexpr int S_OFF = S1_OFF + (TWO_S ? S_BYTES : 0);  // buffer 0
-  static constexpr int MISC_OFF = (S_OFF + S_BYTES + 127) / 128 * 128;
+  // pipelined tiles: the bias operands of the extra K-step of each layer
+  // (N rows of 16 bf16: b_hi, b_lo, zeros; 32-byte swizzled K-major)
+  static constexpr int BIAS1B = kN1 * 32, BIAS2B = kN2 * 32;
+  static constexpr int BIAS_OFF = S_OFF + S_BYTES;
+  static constexpr int MISC_OFF = (BIAS_OFF + (TWO_S ? BIAS1B + BIAS2B : 0) + 127) / 128 * 128;
   static constexpr int POOL_AVAIL = ACT_BYTES + (TWO_S ? S_BYTES : 0);
   // values a thread stages per pooling window
   static constexpr int VPT = (POOL_AVAIL / ROWB + kThreads - 1) / kThreads;
   // tensor-memory columns: layer-1 accumulator (h1 packed over its first half),
   // layer-2 accumulator, the bf16 x tile
   static constexpr uint32_t TM_ACC1 = 0, TM_ACC2 = kN1, TM_X = kN1 + kN2;
-  static_assert(!TWO_S || TM_X + K1 / 2 <= 512, "tensor memory columns");
+  // pipelined tiles: 8 constant columns, the A operand of the bias K-step (1, 1, 0 ...)
+  static constexpr uint32_t TM_ONE = TM_X + K1 / 2;
+  static_assert(!TWO_S || TM_ONE + 8 <= 512, "tensor memory columns");
   static_assert(!TWO_S || kSB * QROW * 4 <= ACT_BYTES, "query slices of a batch");
   static_assert(32 + 3 * TM <= kThreads, "sequence rows: one thread per (row, key) outside warp 0");
 };
@@ -842,6 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 
   // ---------------------------------------------------------------- batches
   uint32_t mma_phase = 0;
+  bool bias_ready = false;  // pipelined tiles: bias K-step operands built
   uint32_t gk = 0;  // W1 K-blocks consumed so far (stream mode)
   bool weights_ready = false;
   bool tc_fail = false;
@@ -1436,6 +1444,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             tc_mma_f16_ts(tbase + C::TM_ACC1, tbase + C::TM_X + uint32_t(kk * 8),
                           sw128_kmajor_desc(wa + kb * kN1 * 128 + ko), IDESC1, kk > 0);
           }
+          // + b1: one more K-step, (1, 1, 0 ...) against (b1_hi, b1_lo, 0 ...)
+          tc_mma_f16_ts(tbase + C::TM_ACC1, tbase + C::TM_ONE, sw32_kmajor_desc(smem_u32(sm + C::BIAS_OFF)),
+                        IDESC1, 1u);
           tc_commit(&ms->mbar_mma);
         };
         // h1 of hidden units [64g, 64g+64) sits packed in accumulator columns
@@ -1450,6 +1461,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             tc_mma_f16_ts(tbase + C::TM_ACC2, tbase + C::TM_ACC1 + kb * 64 + uint32_t((kk & 3) * 8),
                           sw128_kmajor_desc(wa + kb * kN2 * 128 + ko), IDESC2, kk > 0);
           }
+          // + b2, as for layer 1
+          tc_mma_f16_ts(tbase + C::TM_ACC2, tbase + C::TM_ONE,
+                        sw32_kmajor_desc(smem_u32(sm + C::BIAS_OFF + C::BIAS1B)), IDESC2, 1u);
           tc_commit(&ms->mbar_mma);
         };
         // one thread waits for the MMAs, the block learns the outcome together
@@ -1475,6 +1489,27 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
         }
         cp_async_wait_all();
         __syncthreads();
+        if (!bias_ready) {
+          // The bias K-step operands, once per launch (the biases are in smem by
+          // now): row n of B holds (b_hi, b_lo, 0 ...) in both 16-byte halves,
+          // b_hi = bf16(b), b_lo = bf16(b - b_hi), so that either half read
+          // against A's (1, 1, 0 ...) adds b_hi + b_lo (within 2^-17 |b| of b).
+          bias_ready = true;
+          for (int r = tid; r < kN1 + kN2; r += kThreads) {
+            const float b = r < kN1 ? ms->b1[r] : ms->b2[r - kN1];
+            const float hi = __bfloat162float(__float2bfloat16_rn(b));
+            const uint4 row = make_uint4(pack_bf16x2(hi, b - hi), 0u, 0u, 0u);
+            uint4* dst = reinterpret_cast<uint4*>(sm + C::BIAS_OFF + r * 32);
+            dst[0] = row;
+            dst[1] = row;
+          }
+          fence_proxy_async_smem();
+          if (warp < 4) {
+            uint32_t one[8] = {pack_bf16x2(1.f, 1.f), 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            tmem_st8(tbase + lane_base + C::TM_ONE, one);
+            tmem_st_wait();
+          }
+        }
         build_x(min(C::TM, R), 0, 0);
         tc_fence_before();
         __syncthreads();
@@ -1504,14 +1539,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
               tmem_ld16(ta + qp * 32, v);
               tmem_ld16(ta + qp * 32 + 16, v + 16);
               tmem_ld_wait();
+              // (b1 is in the accumulator already: ReLU and round to bf16)
               uint32_t h[16];
-              const float* bq = ms->b1 + cg * 64 + qp * 32;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float4 bb = *reinterpret_cast<const float4*>(bq + 4 * e);
-                h[2 * e] = pack_bf16x2(fmaxf(v[4 * e] + bb.x, 0.f), fmaxf(v[4 * e + 1] + bb.y, 0.f));
-                h[2 * e + 1] = pack_bf16x2(fmaxf(v[4 * e + 2] + bb.z, 0.f), fmaxf(v[4 * e + 3] + bb.w, 0.f));
-              }
+              for (int e = 0; e < 16; ++e) h[e] = pack_bf16x2_relu(v[2 * e], v[2 * e + 1]);
               // columns [64cg + 16qp, +16) were read by this warp already
               tmem_st16(ta + qp * 16, h);
             }
@@ -1530,7 +1561,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             build_x(min(C::TM, R - t0 - C::TM), buf ^ 1, (k + 1) & 3);
             tc_fence_before();
           }
-          // ---- layer 2 (k) done: epilogue 2, z = w3 . ReLU(acc + b2) + b3
+          // ---- layer 2 (k) done: epilogue 2, z = w3 . ReLU(acc) + b3 (b2 is in acc)
           if (!wait_mma()) { tc_fail = true; break; }
           if ((warp & 3) * 32 < n) {
             const int cg = warp >> 2;
@@ -1540,12 +1571,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             float part = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; e += 4) {
-              const float4 bb = *reinterpret_cast<const float4*>(ms->b2 + cg * 16 + e);
               const float4 ww = *reinterpret_cast<const float4*>(ms->w3 + cg * 16 + e);
-              part += fmaxf(v[e] + bb.x, 0.f) * ww.x;
-              part += fmaxf(v[e + 1] + bb.y, 0.f) * ww.y;
-              part += fmaxf(v[e + 2] + bb.z, 0.f) * ww.z;
-              part += fmaxf(v[e + 3] + bb.w, 0.f) * ww.w;
+              part += fmaxf(v[e], 0.f) * ww.x;
+              part += fmaxf(v[e + 1], 0.f) * ww.y;
+              part += fmaxf(v[e + 2], 0.f) * ww.z;
+              part += fmaxf(v[e + 3], 0.f) * ww.w;
             }
             ms->red[cg][(warp & 3) * 32 + lane] = part;
           }

@@ -222,6 +222,19 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of a K-major bf16 operand with 32-byte
+// swizzling whose rows hold one K-step (16 elements, 32 bytes): 8-row atoms of
+// 256 bytes (SBO), layout type 6 (32-byte swizzle) at bits [61,64).
+__device__ __forceinline__ uint64_t sw32_kmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(6u) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator [4,6)=1, A bf16 [7,10)=1,
 // B bf16 [10,13)=1, both K-major (bits 15, 16 = 0), N >> 3 at [17,23), M >> 4 at [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
@@ -239,6 +252,13 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+// max(x, 0) of two floats, each rounded to bf16 (nearest even), packed with lo
+// in the low half (the conversion's relu form: its first source goes high).
+__device__ __forceinline__ uint32_t pack_bf16x2_relu(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
