@@ -74,15 +74,24 @@ enum {
 #define DSF_FLAG_TIMEOUT       0x10 /* a device wait ran out (about 1 s); outputs invalid */
 #define DSF_FLAG_NOT_PREPARED  0x20 /* dsf_prepare_mlp was not run on this workspace */
 
+/* Pooling of a table's bags (EmbeddingBag modes: the pages' tables pool by
+ * sum, section 3; mean divides the fp32 sum by the bag's length, an empty bag
+ * staying 0). */
+#define DSF_POOL_SUM  0
+#define DSF_POOL_MEAN 1
+
 /* F embedding tables, one per KJT key, all with the same D and element type.
  * table_ptrs[f]: device pointer to a row-major [table_rows[f], D] table,
- * 16-byte aligned. Host arrays of length F. */
+ * 16-byte aligned. Host arrays of length F. pooling: host array [F] of
+ * DSF_POOL_SUM / DSF_POOL_MEAN, or NULL for all sum. A mean-pooled query
+ * table feeds the attention its mean too. */
 typedef struct {
   const void* const* table_ptrs;
   const int64_t* table_rows;
   int32_t F;      /* 1 .. DSF_MAX_TABLES */
   int32_t D;      /* 16 or 64 */
   int32_t dtype;  /* DSF_F32 or DSF_BF16 */
+  const int32_t* pooling;
 } dsf_tables;
 
 /* KeyedJaggedTensor of the deep group (section 2: values + lengths).

@@ -61,11 +61,11 @@ def lib() -> ctypes.CDLL:
         i32, i64 = ctypes.c_int32, ctypes.c_int64
         L.oracle_offsets.argtypes = [P, i64, P]
         L.oracle_offsets.restype = ctypes.c_int
-        L.oracle_emb_bag_pool.argtypes = [i32, i32, i32, P, P, i32, P, i64, P, P, i32, P]
+        L.oracle_emb_bag_pool.argtypes = [i32, i32, i32, P, P, P, i32, P, i64, P, P, i32, P]
         L.oracle_emb_bag_pool.restype = ctypes.c_int
         L.oracle_attn_mlp.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P, i32, P]
         L.oracle_attn_mlp.restype = ctypes.c_int
-        L.oracle_din.argtypes = ([i32, i32, i32, i32, i32, P, P, i32, P, i64, P, P, P,
+        L.oracle_din.argtypes = ([i32, i32, i32, i32, i32, P, P, P, i32, P, i64, P, P, P,
                                   P, i64, P, i32, P, P, P, P, P, P, i32, i32, P, i32,
                                   P, P, P])
         L.oracle_din.restype = ctypes.c_int
@@ -99,15 +99,29 @@ def offsets(lengths: np.ndarray):
     return out, flags
 
 
-def emb_bag_pool(tables, values, lengths, B: int, samples: Optional[Sequence[int]] = None):
-    """pooled [n_samples, F*D] float32 (fp32 left-to-right bag sums), flags."""
+def _pooling(pooling, F):
+    """int32 [F] pooling modes (0 sum, 1 mean), or None."""
+    if pooling is None:
+        return None
+    a = _c(pooling, np.int32)
+    if a.size != F:
+        raise ValueError("pooling needs one mode per table")
+    return a
+
+
+def emb_bag_pool(tables, values, lengths, B: int, samples: Optional[Sequence[int]] = None,
+                 pooling=None):
+    """pooled [n_samples, F*D] float32 (fp32 left-to-right bag sums, or those
+    sums over the bag length for mean-pooled tables), flags."""
     T = _Tables(tables)
     F = len(T.arrs)
+    pl = _pooling(pooling, F)
     values = _c(values, np.int64)
     lengths = _c(lengths, np.int32)
     samples = _c(np.arange(B) if samples is None else samples, np.int32)
     out = np.zeros((samples.size, F * T.D), dtype=np.float32)
-    flags = lib().oracle_emb_bag_pool(F, T.D, T.dtype, _ptr(T.ptrs), _ptr(T.rows), B,
+    flags = lib().oracle_emb_bag_pool(F, T.D, T.dtype, _ptr(T.ptrs), _ptr(T.rows),
+                                      _ptr(pl) if pl is not None else None, B,
                                       _ptr(values), values.size, _ptr(lengths),
                                       _ptr(samples), samples.size, _ptr(out))
     if flags < 0:
@@ -131,10 +145,11 @@ def attn_mlp(x, W1, b1, W2, b2, w3, b3, bf16_mlp: bool = False) -> np.ndarray:
 
 def din(tables, values, lengths, B: int, q_feat, seq_table, seq_values, seq_lengths,
         max_len: int, W1, b1, W2, b2, w3, b3, samples=None, padded: bool = False,
-        bf16_mlp: bool = False, want_logits: bool = False):
+        bf16_mlp: bool = False, want_logits: bool = False, pooling=None):
     """din [n_samples, 3D] float64, flags, (logits, weights) if want_logits."""
     T = _Tables(tables)
     F = len(T.arrs)
+    pl = _pooling(pooling, F)
     values = _c(values, np.int64)
     lengths = _c(lengths, np.int32)
     seq_values = _c(seq_values, np.int64).reshape(3, -1)
@@ -150,7 +165,8 @@ def din(tables, values, lengths, B: int, q_feat, seq_table, seq_values, seq_leng
     lg = np.zeros((samples.size, max_len), dtype=np.float64) if want_logits else None
     wt = np.zeros((samples.size, max_len), dtype=np.float64) if want_logits else None
     flags = lib().oracle_din(int(padded), int(bf16_mlp), F, T.D, T.dtype, _ptr(T.ptrs),
-                             _ptr(T.rows), B, _ptr(values), values.size, _ptr(lengths),
+                             _ptr(T.rows), _ptr(pl) if pl is not None else None, B,
+                             _ptr(values), values.size, _ptr(lengths),
                              _ptr(qf), _ptr(st), _ptr(seq_values), n_seq, _ptr(seq_lengths),
                              max_len, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(w3),
                              _ptr(b3), W1.shape[0], W2.shape[0], _ptr(samples), samples.size,
@@ -163,13 +179,18 @@ def din(tables, values, lengths, B: int, q_feat, seq_table, seq_values, seq_leng
     return out, flags
 
 
-def din_batch(batch, samples=None, padded=False, bf16_mlp=False, want_logits=False):
-    """oracle_din on a synth.Batch."""
+def din_batch(batch, samples=None, padded=False, bf16_mlp=False, want_logits=False, pooling=None):
+    """oracle_din on a synth.Batch (pooling: the batch's own modes by default)."""
+    if pooling is None:
+        pooling = getattr(batch, "pooling", None)
     return din(batch.tables, batch.values, batch.lengths, batch.B, batch.q_feat,
                batch.seq_table, batch.seq_values, batch.seq_lengths, batch.max_len,
                batch.W1, batch.b1, batch.W2, batch.b2, batch.w3, batch.b3,
-               samples=samples, padded=padded, bf16_mlp=bf16_mlp, want_logits=want_logits)
+               samples=samples, padded=padded, bf16_mlp=bf16_mlp, want_logits=want_logits,
+               pooling=pooling)
 
 
-def pool_batch(batch, samples=None):
-    return emb_bag_pool(batch.tables, batch.values, batch.lengths, batch.B, samples)
+def pool_batch(batch, samples=None, pooling=None):
+    if pooling is None:
+        pooling = getattr(batch, "pooling", None)
+    return emb_bag_pool(batch.tables, batch.values, batch.lengths, batch.B, samples, pooling)

@@ -94,10 +94,12 @@ int oracle_offsets(const int32_t *lengths, int64_t n, int64_t *offsets)
     return flags;
 }
 
-/* Sum-pool one bag into out[0..D): fp32, left to right. */
+/* Pool one bag into out[0..D): the fp32 sum, left to right; with mean, that
+ * sum divided (fp32) by the bag's length, which counts every id of the bag
+ * (EmbeddingBag mean mode). An empty bag gives 0 either way. */
 static int pool_bag(const void *table, int64_t rows, int32_t dtype, int32_t D,
                     const int64_t *values, int64_t n_values, int64_t begin, int64_t end,
-                    float *out)
+                    int mean, float *out)
 {
     int flags = 0;
     for (int32_t d = 0; d < D; d++) out[d] = 0.0f;
@@ -107,16 +109,20 @@ static int pool_bag(const void *table, int64_t rows, int32_t dtype, int32_t D,
         if (id < 0 || id >= rows) { flags |= OR_ID_RANGE; continue; }
         for (int32_t d = 0; d < D; d++) out[d] += table_at(table, dtype, D, id, d);
     }
+    if (mean && end > begin)
+        for (int32_t d = 0; d < D; d++) out[d] = out[d] / (float)(end - begin);
     return flags;
 }
 
 /*
- * EmbeddingBag sum pooling over a key-major KJT.
- * tables[f]: [rows[f], D]; lengths: [F*B]; samples: which samples to produce;
+ * EmbeddingBag pooling over a key-major KJT.
+ * tables[f]: [rows[f], D]; lengths: [F*B]; pooling: [F], 0 = sum, 1 = mean
+ * (NULL: all sum); samples: which samples to produce;
  * pooled: [n_samples, F*D] float, row i is sample samples[i].
  */
 int oracle_emb_bag_pool(int32_t F, int32_t D, int32_t dtype,
                         const void *const *tables, const int64_t *rows,
+                        const int32_t *pooling,
                         int32_t B, const int64_t *values, int64_t n_values,
                         const int32_t *lengths,
                         const int32_t *samples, int32_t n_samples, float *pooled)
@@ -131,7 +137,8 @@ int oracle_emb_bag_pool(int32_t F, int32_t D, int32_t dtype,
         for (int32_t f = 0; f < F; f++) {
             int64_t g = (int64_t)f * B + b;
             flags |= pool_bag(tables[f], rows[f], dtype, D, values, n_values,
-                              off[g], off[g + 1], pooled + ((int64_t)i * F + f) * D);
+                              off[g], off[g + 1], pooling && pooling[f] == 1,
+                              pooled + ((int64_t)i * F + f) * D);
         }
     }
     free(off);
@@ -201,7 +208,7 @@ int oracle_attn_mlp(const double *x, int64_t n, int32_t K1, int32_t N1, int32_t 
  */
 int oracle_din(int32_t padded, int32_t bf16_mlp,
                int32_t F, int32_t D, int32_t dtype,
-               const void *const *tables, const int64_t *rows,
+               const void *const *tables, const int64_t *rows, const int32_t *pooling,
                int32_t B, const int64_t *values, int64_t n_values, const int32_t *lengths,
                const int32_t *q_feat, const int32_t *seq_table,
                const int64_t *seq_values, int64_t n_seq, const int32_t *seq_lengths,
@@ -235,7 +242,7 @@ int oracle_din(int32_t padded, int32_t bf16_mlp,
             int32_t f = q_feat[k];
             int64_t g = (int64_t)f * B + b;
             flags |= pool_bag(tables[f], rows[f], dtype, D, values, n_values,
-                              off[g], off[g + 1], qf + k * D);
+                              off[g], off[g + 1], pooling && pooling[f] == 1, qf + k * D);
         }
         int32_t L = seq_lengths[b];
         if (L < 0) L = 0;

@@ -33,7 +33,8 @@ _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c
 
 
 class CTables(ctypes.Structure):
-    _fields_ = [("table_ptrs", _vp), ("table_rows", _vp), ("F", _i32), ("D", _i32), ("dtype", _i32)]
+    _fields_ = [("table_ptrs", _vp), ("table_rows", _vp), ("F", _i32), ("D", _i32), ("dtype", _i32),
+                ("pooling", _vp)]
 
 
 class CKjt(ctypes.Structure):
@@ -113,9 +114,10 @@ def _dptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 
 class EmbeddingTables:
-    """F device tables [rows_f, D], all fp32 or all bf16."""
+    """F device tables [rows_f, D], all fp32 or all bf16. pooling: per table
+    DSF_POOL_SUM or DSF_POOL_MEAN (None: all sum)."""
 
-    def __init__(self, tables: Sequence[torch.Tensor]):
+    def __init__(self, tables: Sequence[torch.Tensor], pooling: Optional[Sequence[int]] = None):
         self.tables = list(tables)
         F = len(self.tables)
         D = int(self.tables[0].shape[1])
@@ -127,7 +129,12 @@ class EmbeddingTables:
         self.dtype = DSF_BF16 if dt == torch.bfloat16 else DSF_F32
         self._ptrs = (ctypes.c_void_p * F)(*[t.data_ptr() for t in self.tables])
         self._rows = (ctypes.c_int64 * F)(*[int(t.shape[0]) for t in self.tables])
-        self.c = CTables(ctypes.cast(self._ptrs, _vp), ctypes.cast(self._rows, _vp), F, D, self.dtype)
+        self.pooling = None if pooling is None else [int(x) for x in pooling]
+        if self.pooling is not None and len(self.pooling) != F:
+            raise ValueError("pooling needs one mode per table")
+        self._pool = None if self.pooling is None else (ctypes.c_int32 * F)(*self.pooling)
+        self.c = CTables(ctypes.cast(self._ptrs, _vp), ctypes.cast(self._rows, _vp), F, D, self.dtype,
+                         None if self._pool is None else ctypes.cast(self._pool, _vp))
 
     @property
     def rows(self):

@@ -63,6 +63,7 @@ int check_tables(const dsf_tables* t) {
   for (int f = 0; f < t->F; ++f) {
     if (!t->table_ptrs[f] || !aligned(t->table_ptrs[f], 16)) return DSF_EINVAL;
     if (t->table_rows[f] < 0) return DSF_EINVAL;
+    if (t->pooling && t->pooling[f] != DSF_POOL_SUM && t->pooling[f] != DSF_POOL_MEAN) return DSF_EINVAL;
   }
   return DSF_OK;
 }
@@ -105,6 +106,7 @@ void fill_common(FwdParams& p, const dsf_tables* t, const dsf_kjt* k, int32_t B,
   for (int f = 0; f < t->F; ++f) {
     p.tables[f] = t->table_ptrs[f];
     p.rows[f] = t->table_rows[f];
+    if (t->pooling && t->pooling[f] == DSF_POOL_MEAN) p.mean_mask |= 1u << f;
   }
   p.F = t->F;
   p.B = B;

@@ -57,6 +57,7 @@ struct FwdParams {
   const void* tables[kMaxF];
   long long rows[kMaxF];
   int F, B, max_len;
+  unsigned int mean_mask;  // bit f: table f pools by mean
   const long long* values;
   long long n_values;
   const int* lengths;
@@ -944,6 +945,15 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           for (int k = 0; k < 2; ++k) {
             if (!live[k]) continue;
             const long long b = bs + ik[k];
+            if ((p.mean_mask >> fk[k]) & 1u) {
+              // mean pooling: the fp32 sum over the bag's length (empty stays 0)
+              const int g = fk[k] * nb + ik[k];
+              const uint32_t L = offs[g + 1] - offs[g];
+              if (L > 0) {
+#pragma unroll
+                for (int q = 0; q < EPT; ++q) acc[k][q] = acc[k][q] / float(L);
+              }
+            }
             auto put = [&](float* o) {
 #pragma unroll
               for (int q = 0; q < EPT; q += 4)
@@ -1043,6 +1053,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             for (int q = 0; q < C::EPL; ++q) acc[q] += v[q];
           }
           if (e <= w1) {
+            if ((p.mean_mask >> f) & 1u) {
+              // mean pooling: the fp32 sum over the bag's length (e > a here)
+#pragma unroll
+              for (int q = 0; q < C::EPL; ++q) acc[q] = acc[q] / float(e - a);
+            }
             const int i = g - f * nb;
             const long long b = bs + i;
             if (pool_all) {

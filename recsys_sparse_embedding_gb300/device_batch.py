@@ -45,7 +45,8 @@ def to_device(batch, device="cuda") -> DeviceBatch:
              for a in (batch.W1, batch.b1, batch.W2, batch.b2, batch.w3, batch.b3)]
     return DeviceBatch(
         B=batch.B, D=batch.D, max_len=batch.max_len, q_feat=tuple(batch.q_feat),
-        seq_table=tuple(batch.seq_table), tables=binding.EmbeddingTables(tabs),
+        seq_table=tuple(batch.seq_table),
+        tables=binding.EmbeddingTables(tabs, getattr(batch, "pooling", None)),
         values=torch.from_numpy(np.ascontiguousarray(batch.values, np.int64)).to(device),
         lengths=torch.from_numpy(np.ascontiguousarray(batch.lengths, np.int32)).to(device),
         seq_values=torch.from_numpy(np.ascontiguousarray(batch.seq_values, np.int64)).to(device),

@@ -116,6 +116,7 @@ class Batch:
     b2: np.ndarray
     w3: np.ndarray
     b3: np.ndarray
+    pooling: Optional[tuple] = None  # per table 0 (sum) / 1 (mean); None: all sum
 
     @property
     def F(self) -> int:

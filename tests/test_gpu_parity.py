@@ -190,3 +190,18 @@ def test_edge_out_of_range_ids_flagged_not_faulting():
     b.values[5] = -7
     b.seq_values[1, 2] = 50           # == rows: out of range
     check_batch(b, expect_status=binding.FLAG_ID_RANGE)
+
+
+def test_mean_pooling_deep_and_query_tables():
+    """Mean-pooled tables, three of them query tables (1, 5, 2), so the
+    attention's query is the bag mean too: the direct pooling path (bags of at
+    most 16 values) on long_multihot, and the staged path on bags of up to 30."""
+    pooling = tuple(1 if f in (0, 1, 2, 5, 9) else 0 for f in range(16))
+    b = synth.generate("long_multihot", seed=0, B=1000)
+    b.pooling = pooling
+    check_batch(b, samples=sample_ids(b.B, 300))
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 31, size=(16, 120)).astype(np.int32)
+    c = _custom_batch(list(rng.integers(0, 40, size=120)), bags_len=lens)
+    c.pooling = pooling
+    check_batch(c)

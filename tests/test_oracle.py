@@ -356,3 +356,41 @@ def test_generator_is_seeded_and_shaped():
     assert a.lengths.size == 16 * 64 and a.values.size == a.lengths.sum()
     assert a.seq_values.shape == (3, a.seq_lengths.sum())
     assert a.seq_lengths.min() >= 0 and a.seq_lengths.max() <= 10
+
+
+def test_mean_pooling_is_the_exact_mean_rounded_once():
+    """EmbeddingBag mean mode (the pooling variant next to sum): each pooled
+    element equals the exact rational mean of the bag's rows, rounded to the
+    nearest float32. Integer-valued rows keep the fp32 sums exact, so the only
+    rounding is the final division; the check compares against the exact mean
+    with Fractions and the float32 neighbours of the result. Empty bags give 0;
+    sum-pooled tables are untouched by the mode of the others."""
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    F, D, B, rows = 4, 16, 40, 30
+    tables = [rng.integers(-64, 65, size=(rows, D)).astype(np.float32) for _ in range(F)]
+    lengths = rng.integers(0, 9, size=(F, B)).astype(np.int32)
+    values = np.concatenate([rng.integers(0, rows, size=int(lengths[f].sum())) for f in range(F)])
+    pooling = np.array([1, 0, 1, 1], np.int32)
+    got, flags = oracle.emb_bag_pool(tables, values, lengths.reshape(-1), B, pooling=pooling)
+    summed, _ = oracle.emb_bag_pool(tables, values, lengths.reshape(-1), B)
+    assert flags == 0
+    off = np.concatenate([[0], np.cumsum(lengths.reshape(-1))])
+    for f in range(F):
+        for b in range(B):
+            g = f * B + b
+            ids = values[off[g]:off[g + 1]]
+            cell = got[b, f * D:(f + 1) * D]
+            if pooling[f] == 0:
+                assert np.array_equal(cell, summed[b, f * D:(f + 1) * D])
+                continue
+            if ids.size == 0:
+                assert np.all(cell == 0)
+                continue
+            for d in range(D):
+                exact = Fraction(int(sum(int(tables[f][i, d]) for i in ids)), int(ids.size))
+                r = np.float32(cell[d])
+                lo = np.nextafter(r, np.float32(-np.inf))
+                hi = np.nextafter(r, np.float32(np.inf))
+                e = abs(Fraction(float(r)) - exact)
+                assert e <= abs(Fraction(float(lo)) - exact) and e <= abs(Fraction(float(hi)) - exact), (f, b, d)
