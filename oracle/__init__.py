@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
                                   P, i64, P, i32, P, P, P, P, P, P, i32, i32, P, i32,
                                   P, P, P])
         L.oracle_din.restype = ctypes.c_int
+        L.oracle_towers.argtypes = [P, P, i64] + [P] * 10 + [i32, P]
+        L.oracle_towers.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -194,3 +196,22 @@ def pool_batch(batch, samples=None, pooling=None):
     if pooling is None:
         pooling = getattr(batch, "pooling", None)
     return emb_bag_pool(batch.tables, batch.values, batch.lengths, batch.B, samples, pooling)
+
+
+def towers(pooled, din, Wd1, bd1, Wd2, bd2, Wd3, bd3, Wf1, bf1, wo, bo, bf16_mlp: bool = False):
+    """The dense towers: pooled [n, 256] (float32), din [n, 48] -> logit [n]
+    float64 (see oracle_towers)."""
+    pooled = _c(pooled, np.float32).reshape(-1, 256)
+    din = _c(din, np.float64).reshape(-1, 48)
+    n = pooled.shape[0]
+    ws = [_c(a, np.float32).reshape(-1) for a in (Wd1, bd1, Wd2, bd2, Wd3, bd3, Wf1, bf1, wo, bo)]
+    sizes = (512 * 256, 512, 256 * 512, 256, 128 * 256, 128, 64 * 176, 64, 64, 1)
+    for a, sz in zip(ws, sizes):
+        if a.size != sz:
+            raise ValueError("tower weight of %d elements, expected %d" % (a.size, sz))
+    out = np.zeros(n, dtype=np.float64)
+    rc = lib().oracle_towers(_ptr(pooled), _ptr(din), n, *[_ptr(a) for a in ws],
+                             int(bf16_mlp), _ptr(out))
+    if rc != 0:
+        raise MemoryError("oracle_towers")
+    return out

@@ -313,3 +313,61 @@ done:
     free(off); free(soff); free(qf); free(S); free(X); free(Z); free(A);
     return flags;
 }
+
+/*
+ * The dense towers after the sparse path (MultiTowerDIN: current state
+ * analysis, section 4.4 and the model config of section 7):
+ *   deep tower  h = ReLU(W_d3 ReLU(W_d2 ReLU(W_d1 p + b_d1) + b_d2) + b_d3)
+ *               with p the pooled deep group [256] and widths 512, 256, 128;
+ *   final tower y = w_o . ReLU(W_f1 cat[h, din] + b_f1) + b_o
+ *               with cat[h, din] of width 128 + 48 = 176 and W_f1 [64, 176];
+ * y is the logit (the loss, binary cross entropy, applies the sigmoid).
+ * Weights in Linear [out, in] layout.  pooled: [n, 256] float; din: [n, 48]
+ * double; logit: [n] double.  Accumulation in double.  bf16_mlp: every
+ * GEMM operand is taken as bf16 -- the inputs p, h1, h2 and cat[h, din] are
+ * produced in fp32 (bias added, ReLU) and rounded to nearest-even bf16, the
+ * weights W_d1, W_d2, W_d3, W_f1 rounded too; the output dot stays fp32/double.
+ */
+int oracle_towers(const float *pooled, const double *din, int64_t n,
+                  const float *Wd1, const float *bd1, const float *Wd2, const float *bd2,
+                  const float *Wd3, const float *bd3, const float *Wf1, const float *bf1,
+                  const float *wo, const float *bo, int32_t bf16_mlp, double *logit)
+{
+    enum { P = 256, H1 = 512, H2 = 256, H3 = 128, DQ = 48, KF = H3 + DQ, HF = 64 };
+    double x[H1], h1[H1], h2[H2], c[KF], hf[HF];
+    for (int64_t r = 0; r < n; r++) {
+        const float *pr = pooled + r * P;
+        for (int32_t k = 0; k < P; k++)
+            x[k] = bf16_mlp ? (double)round_bf16(pr[k]) : (double)pr[k];
+        /* one Linear + ReLU layer: out[j] = ReLU(W[j,:] . in + b[j]) */
+#define DENSE(W, b, in, K, out, N)                                                   \
+        for (int32_t j = 0; j < (N); j++) {                                          \
+            double acc = 0.0;                                                        \
+            for (int32_t k = 0; k < (K); k++) {                                      \
+                double w = bf16_mlp ? (double)round_bf16((W)[(int64_t)j * (K) + k])  \
+                                    : (double)(W)[(int64_t)j * (K) + k];             \
+                acc += w * (in)[k];                                                  \
+            }                                                                        \
+            if (bf16_mlp) {                                                          \
+                float v = (float)acc + (b)[j];                                       \
+                (out)[j] = v > 0.0f ? (double)v : 0.0;                               \
+            } else {                                                                 \
+                double v = acc + (double)(b)[j];                                     \
+                (out)[j] = v > 0.0 ? v : 0.0;                                        \
+            }                                                                        \
+        }
+        DENSE(Wd1, bd1, x, P, h1, H1)
+        if (bf16_mlp) for (int32_t k = 0; k < H1; k++) h1[k] = (double)round_bf16((float)h1[k]);
+        DENSE(Wd2, bd2, h1, H1, h2, H2)
+        if (bf16_mlp) for (int32_t k = 0; k < H2; k++) h2[k] = (double)round_bf16((float)h2[k]);
+        DENSE(Wd3, bd3, h2, H2, c, H3)
+        for (int32_t k = 0; k < DQ; k++) c[H3 + k] = din[r * DQ + k];
+        if (bf16_mlp) for (int32_t k = 0; k < KF; k++) c[k] = (double)round_bf16((float)c[k]);
+        DENSE(Wf1, bf1, c, KF, hf, HF)
+#undef DENSE
+        double y = (double)bo[0];
+        for (int32_t j = 0; j < HF; j++) y += (double)wo[j] * hf[j];
+        logit[r] = y;
+    }
+    return 0;
+}

@@ -394,3 +394,88 @@ def test_mean_pooling_is_the_exact_mean_rounded_once():
                 hi = np.nextafter(r, np.float32(np.inf))
                 e = abs(Fraction(float(r)) - exact)
                 assert e <= abs(Fraction(float(lo)) - exact) and e <= abs(Fraction(float(hi)) - exact), (f, b, d)
+
+
+def _tower_zero():
+    return dict(Wd1=np.zeros((512, 256), np.float32), bd1=np.zeros(512, np.float32),
+                Wd2=np.zeros((256, 512), np.float32), bd2=np.zeros(256, np.float32),
+                Wd3=np.zeros((128, 256), np.float32), bd3=np.zeros(128, np.float32),
+                Wf1=np.zeros((64, 176), np.float32), bf1=np.zeros(64, np.float32),
+                wo=np.zeros(64, np.float32), bo=np.zeros(1, np.float32))
+
+
+def _towers(w, pooled, din, bf16=False):
+    return oracle.towers(pooled, din, w["Wd1"], w["bd1"], w["Wd2"], w["bd2"], w["Wd3"], w["bd3"],
+                         w["Wf1"], w["bf1"], w["wo"], w["bo"], bf16_mlp=bf16)
+
+
+def test_towers_zero_weights_give_the_bias_path():
+    """All weight matrices zero: y = b_o + w_o . ReLU(b_f1), whatever the inputs
+    (the deep tower then feeds ReLU(b_d3) forward, which W_f1 = 0 ignores)."""
+    rng = np.random.default_rng(21)
+    w = _tower_zero()
+    w["bf1"][:] = rng.uniform(-1, 1, 64)
+    w["wo"][:] = rng.uniform(-1, 1, 64)
+    w["bo"][:] = 0.25
+    pooled = rng.standard_normal((7, 256)).astype(np.float32)
+    din = rng.standard_normal((7, 48))
+    want = 0.25 + float(np.dot(w["wo"].astype(np.float64), np.maximum(w["bf1"].astype(np.float64), 0)))
+    for bf16 in (False, True):
+        y = _towers(w, pooled, din, bf16)
+        assert np.allclose(y, want, rtol=0, atol=1e-12)
+
+
+def test_towers_identity_chain_is_the_mean_of_the_final_input():
+    """Non-negative inputs through identity blocks (Linear [out, in]: W_d1 = [I; 0],
+    W_d2 = [I 0], W_d3 = [I 0], zero biases) reach the final tower as
+    cat[p[:128], din]; one row of W_f1 = 1/176 then gives its mean: y equals
+    (sum p[:128] + sum din) / 176 exactly up to rounding. A transposed weight,
+    a shifted slice or a swapped cat order changes the value."""
+    rng = np.random.default_rng(22)
+    w = _tower_zero()
+    w["Wd1"][:256, :] = np.eye(256, dtype=np.float32)
+    w["Wd2"][:, :256] = np.eye(256, dtype=np.float32)
+    w["Wd3"][:, :128] = np.eye(128, dtype=np.float32)
+    w["Wf1"][0, :] = 1.0 / 176
+    w["wo"][0] = 1.0
+    pooled = rng.uniform(0, 1, (9, 256)).astype(np.float32)
+    din = rng.uniform(0, 1, (9, 48))
+    want = (pooled[:, :128].astype(np.float64).sum(1) + din.sum(1)) / 176
+    y = _towers(w, pooled, din)
+    assert np.allclose(y, want, rtol=1e-6, atol=0)
+    # a single din slot: W_f1 row 0 picks position 128 + 5 of cat[h, din]
+    w["Wf1"][0, :] = 0.0
+    w["Wf1"][0, 128 + 5] = 1.0
+    assert np.allclose(_towers(w, pooled, din), din[:, 5], rtol=0, atol=1e-15)
+
+
+def test_towers_relu_after_every_hidden_layer():
+    """W_d1 = -[I; 0]: the first layer's pre-activations are -p <= 0 for p >= 0,
+    so ReLU zeroes them and the rest sees h1 = 0: y = b_o + w_o . ReLU(W_f1
+    cat[ReLU(b_d3), din] + b_f1) with b_d2 = 0, here with W_f1 picking b_d3's
+    first slot (kept by ReLU) and a negative b_f1 entry (cut by ReLU)."""
+    w = _tower_zero()
+    w["Wd1"][:256, :] = -np.eye(256, dtype=np.float32)
+    w["bd3"][0] = 0.5
+    w["Wf1"][0, 0] = 2.0
+    w["bf1"][1] = -3.0
+    w["wo"][:2] = (1.0, 1.0)
+    pooled = np.abs(np.random.default_rng(23).standard_normal((4, 256))).astype(np.float32)
+    y = _towers(w, pooled, np.zeros((4, 48)))
+    assert np.allclose(y, 1.0, rtol=0, atol=1e-15)   # 2 * 0.5 + ReLU(-3) = 1
+
+
+def test_towers_bf16_mode_is_exact_on_bf16_representable_data():
+    """Inputs, weights and every intermediate exactly representable in bf16
+    (small multiples of 1/8 through identity-like layers): the bf16-operand
+    mode and the double mode agree to the last bit."""
+    rng = np.random.default_rng(24)
+    w = _tower_zero()
+    w["Wd1"][:256, :] = np.eye(256, dtype=np.float32)
+    w["Wd2"][:, :256] = np.eye(256, dtype=np.float32)
+    w["Wd3"][:, :128] = np.eye(128, dtype=np.float32)
+    w["Wf1"][np.arange(64), np.arange(64) * 2] = 1.0
+    w["wo"][:] = 0.5
+    pooled = (rng.integers(0, 16, (6, 256)) / 8).astype(np.float32)
+    din = rng.integers(0, 16, (6, 48)) / 8.0
+    assert np.array_equal(_towers(w, pooled, din), _towers(w, pooled, din, True))
