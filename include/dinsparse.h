@@ -193,6 +193,41 @@ const char* dsf_status_string(int code);
  * call shape; 0 if unsupported. For diagnostics and benchmarks. */
 int32_t dsf_grid_size(int32_t D, int32_t dtype, int32_t mode, int32_t with_attention);
 
+/* ------------------------------------------------------------------------
+ * The dense towers after the sparse path (MultiTowerDIN: current state
+ * analysis, section 4.4; the model config, section 7): the deep tower
+ * h = ReLU(Wd3 ReLU(Wd2 ReLU(Wd1 p + bd1) + bd2) + bd3) on the pooled deep
+ * group p [256] (widths 512, 256, 128) and the final tower
+ * logit = wo . ReLU(Wf1 cat[h, din] + bf1) + bo on cat[h, din] [176]. The
+ * GEMMs take bf16 operands (inputs rounded to nearest-even bf16 after bias
+ * and ReLU in fp32) and accumulate in fp32 on the tensor cores.
+ *
+ * Device fp32 weights in Linear [out, in] layout: Wd1 [512, 256], bd1 [512],
+ * Wd2 [256, 512], bd2 [256], Wd3 [128, 256], bd3 [128], Wf1 [64, 176],
+ * bf1 [64], wo [64], bo [1]. The biases, wo and bo are read at each call;
+ * the four matrices are packed into the towers workspace by
+ * dsf_prepare_towers (call again when they change). */
+typedef struct {
+  const float *Wd1, *bd1, *Wd2, *bd2, *Wd3, *bd3;
+  const float *Wf1, *bf1, *wo, *bo;
+} dsf_towers;
+
+/* Bytes of the towers workspace (packed bf16 weights and a prepared tag);
+ * the caller allocates it, 256-byte aligned. */
+size_t dsf_towers_workspace_bytes(void);
+
+/* Packs the tower matrices into the workspace (asynchronous on stream). */
+int dsf_prepare_towers(const dsf_towers* towers, void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* The towers on the outputs of din_sparse_fwd (D = 16): pooled_dev [B, 256]
+ * and din_dev [B, 48] fp32, 16-byte aligned; writes logit_dev [B] fp32. One
+ * 512-thread CTA per 128 samples. Returns DSF_EWORKSPACE for a missing or
+ * small workspace; DSF_FLAG_NOT_PREPARED when dsf_prepare_towers has not run
+ * on it; DSF_FLAG_TIMEOUT if a device wait ran out. */
+int ctr_towers_fwd(const float* pooled_dev, const float* din_dev, int32_t B, const dsf_towers* towers,
+                   float* logit_dev, const void* workspace_dev, size_t ws_bytes, int32_t* status_dev,
+                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

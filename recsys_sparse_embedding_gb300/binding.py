@@ -27,7 +27,7 @@ FLAG_NOT_PREPARED = 0x20
 
 EXPORTS = ["dsf_workspace_bytes", "dsf_workspace_init", "dsf_prepare_mlp", "emb_bag_pool",
            "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size",
-           "emb_bag_pool_noalloc"]
+           "emb_bag_pool_noalloc", "dsf_towers_workspace_bytes", "dsf_prepare_towers", "ctr_towers_fwd"]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
@@ -88,6 +88,12 @@ def lib() -> ctypes.CDLL:
         L.emb_bag_pool_noalloc.restype = ctypes.c_int
         L.dsf_grid_size.argtypes = [_i32, _i32, _i32, _i32]
         L.dsf_grid_size.restype = _i32
+        L.dsf_towers_workspace_bytes.argtypes = []
+        L.dsf_towers_workspace_bytes.restype = _sz
+        L.dsf_prepare_towers.argtypes = [P(CTowers), _vp, _sz, _vp]
+        L.dsf_prepare_towers.restype = ctypes.c_int
+        L.ctr_towers_fwd.argtypes = [_vp, _vp, _i32, P(CTowers), _vp, _vp, _sz, _vp, _vp]
+        L.ctr_towers_fwd.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -245,3 +251,35 @@ def din_sparse_fwd(tables: EmbeddingTables, values: torch.Tensor, lengths: torch
 
 def grid_size(D: int, dtype: int, mode: int, with_attention: bool) -> int:
     return int(lib().dsf_grid_size(int(D), int(dtype), int(mode), int(bool(with_attention))))
+
+
+class CTowers(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("Wd1", "bd1", "Wd2", "bd2", "Wd3", "bd3", "Wf1", "bf1", "wo", "bo")]
+
+
+class Towers:
+    """The dense towers' device fp32 weights ([out, in]) and their packed
+    workspace. Wd1 [512, 256], bd1 [512], Wd2 [256, 512], bd2 [256],
+    Wd3 [128, 256], bd3 [128], Wf1 [64, 176], bf1 [64], wo [64], bo [1]."""
+
+    NAMES = ("Wd1", "bd1", "Wd2", "bd2", "Wd3", "bd3", "Wf1", "bf1", "wo", "bo")
+
+    def __init__(self, weights: Sequence[torch.Tensor], device="cuda"):
+        self.w = [torch.as_tensor(t, dtype=torch.float32, device=device).contiguous() for t in weights]
+        if len(self.w) != len(self.NAMES):
+            raise ValueError("towers need %d weight tensors" % len(self.NAMES))
+        self.c = CTowers(*[t.data_ptr() for t in self.w])
+        self.nbytes = int(lib().dsf_towers_workspace_bytes())
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+
+    def prepare(self, stream=None):
+        _check(lib().dsf_prepare_towers(ctypes.byref(self.c), self.buf.data_ptr(), self.nbytes,
+                                        _stream_ptr(stream)), "dsf_prepare_towers")
+
+
+def ctr_towers_fwd(pooled: torch.Tensor, din: torch.Tensor, B: int, towers: Towers,
+                   logit: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().ctr_towers_fwd(pooled.data_ptr(), din.data_ptr(), int(B), ctypes.byref(towers.c),
+                                logit.data_ptr(), towers.buf.data_ptr(), towers.nbytes,
+                                _dptr(status), _stream_ptr(stream)), "ctr_towers_fwd")
+    return logit

@@ -262,3 +262,24 @@ def generate(wl_name: str, seed: int = 0, B: Optional[int] = None,
 
 def table_bytes(b: Batch) -> int:
     return sum(int(t.nbytes) for t in b.tables)
+
+
+TOWER_SHAPES = (("Wd1", (512, 256)), ("bd1", (512,)), ("Wd2", (256, 512)), ("bd2", (256,)),
+                ("Wd3", (128, 256)), ("bd3", (128,)), ("Wf1", (64, 176)), ("bf1", (64,)),
+                ("wo", (64,)), ("bo", (1,)))
+
+
+def tower_weights(seed: int = 0, bias: float = 0.1) -> list:
+    """Random-init dense-tower weights in [out, in] layout, in TOWER_SHAPES
+    order: Xavier-uniform matrices (wo as a [1, 64] matrix) and biases drawn
+    U(-bias, bias), all float32."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x70A3])))
+    out = []
+    for name, shape in TOWER_SHAPES:
+        if name == "wo":
+            out.append(xavier_uniform(rng, 1, shape[0]).reshape(shape))
+        elif len(shape) == 2:
+            out.append(xavier_uniform(rng, shape[0], shape[1]))
+        else:
+            out.append(rng.uniform(-bias, bias, shape).astype(np.float32))
+    return out

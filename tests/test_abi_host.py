@@ -99,6 +99,28 @@ def test_attention_rejects_bad_arguments(L):
                             1 << 30, None, None) == binding.DSF_EINVAL
 
 
+def test_towers_reject_bad_arguments(L):
+    w = binding.CTowers(*([4096] * 10))
+    P = ctypes.byref
+    n = L.dsf_towers_workspace_bytes()
+    assert n >= (512 * 256 + 256 * 512 + 128 * 256 + 64 * 192) * 2
+
+    def call(pooled=4096, din=4096, B=4, tw=P(w), logit=4096, ws=4096, nb=n):
+        return L.ctr_towers_fwd(pooled, din, B, tw, logit, ws, nb, None, None)
+    assert call(B=-1) == binding.DSF_EINVAL
+    assert call(tw=None) == binding.DSF_EINVAL
+    assert call(pooled=None) == binding.DSF_EINVAL
+    assert call(din=4100) == binding.DSF_EINVAL
+    assert call(logit=None) == binding.DSF_EINVAL
+    assert call(tw=P(binding.CTowers(*([4096] * 9 + [0])))) == binding.DSF_EINVAL
+    assert call(ws=None) == binding.DSF_EWORKSPACE
+    assert call(ws=4096 + 16) == binding.DSF_EWORKSPACE
+    assert call(nb=n - 1) == binding.DSF_EWORKSPACE
+    assert call(B=0) == binding.DSF_OK
+    assert L.dsf_prepare_towers(None, 4096, n, None) == binding.DSF_EINVAL
+    assert L.dsf_prepare_towers(P(w), 4096, n - 1, None) == binding.DSF_EWORKSPACE
+
+
 def test_status_strings(L):
     for code in range(5):
         assert binding.status_string(code)
