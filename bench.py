@@ -190,6 +190,47 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+TOWER_FLOPS_PER_SAMPLE = 2 * (256 * 512 + 512 * 256 + 256 * 128 + 176 * 64)
+
+
+def time_towers(binding, synth, pooled, din, B, dev, flush, steps):
+    """The dense towers (deep 256-512-256-128, final cat[deep, din] 176-64-1)
+    on the timed step's own outputs: one ctr_towers_fwd launch per step, L2
+    flushed between steps, CUDA events on the launching stream. Reported beside
+    the sparse forward, not inside its timed step."""
+    import torch
+    tw = binding.Towers([torch.from_numpy(w) for w in synth.tower_weights(0)], device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    logit = torch.empty(B, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        tw.prepare(stream)
+        for _ in range(5):
+            binding.ctr_towers_fwd(pooled, din, B, tw, logit, status=st, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        stream.synchronize()
+        for i in range(steps):
+            flush.fill_(float(i & 7))
+            ev[i][0].record(stream)
+            binding.ctr_towers_fwd(pooled, din, B, tw, logit, status=st, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if int(st.item()):
+        raise RuntimeError("towers status 0x%x" % int(st.item()))
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+    mean_us = sum(us) / len(us)
+    flops = TOWER_FLOPS_PER_SAMPLE * B
+    _, tfs, _, src = peaks()
+    ach = flops / (mean_us * 1e-6) / 1e12
+    return {"what": "ctr_towers_fwd on this step's pooled [B,256] and din [B,48] -> logit [B]",
+            "B": B, "launches": steps, "us_per_launch": mean_us, "us_median": us[len(us) // 2],
+            "samples_per_s": B / (mean_us * 1e-6),
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": tfs, "unit": "TFLOP/s",
+                         "frac": ach / tfs, "flops_per_launch": flops, "peak_source": src,
+                         "peak_kind": "burst (kernel timed alone)"}}
+
+
 def cpu_oracle_rate(batch, samples_per_pass, passes, threads):
     """The oracle as it stands, split over host threads by sample chunks."""
     import concurrent.futures as cf
@@ -247,6 +288,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=8192)
     ap.add_argument("--cpu-passes", type=int, default=8)
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-towers", action="store_true")
+    ap.add_argument("--towers-steps", type=int, default=300)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -403,6 +446,10 @@ def main():
                 torch.equal(h_out[(E - 1) & 1][0], pooled.cpu())):
             raise RuntimeError("end-to-end outputs differ from the device-timed run")
 
+    towers = None
+    if rank == 0 and not args.skip_towers:
+        towers = time_towers(binding, synth, pooled, din, B, dev, flush, args.towers_steps)
+
     # roofline of the fused kernel (the only kernel of a step)
     nbytes, flops, P = algorithmic_work(batch)
     hbm, tfs, tfs_s, src = peaks()
@@ -453,6 +500,7 @@ def main():
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "status": st,
+            "towers": towers,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -21,6 +21,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "dinsparse.h"
 #include "ptx.cuh"
@@ -117,16 +118,31 @@ __global__ void __launch_bounds__(kThreads, 1) towers_kernel(const __grid_consta
     ms->bf1[tid] = p.bf1[tid];
     ms->wo[tid] = p.wo[tid];
   }
-  // layer-1 A: the pooled rows as bf16, 8 elements (one 16-byte chunk) at a time
-  for (int c = tid; c < kTM * (kP / 8); c += kThreads) {
-    const int r = c / (kP / 8), k = (c - r * (kP / 8)) * 8;
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (r < n) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(p.pooled + (long long)(s0 + r) * kP + k));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(p.pooled + (long long)(s0 + r) * kP + k + 4));
-      w = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  // layer-1 A: the pooled rows as bf16, 8 elements (one 16-byte chunk) per
+  // item; a thread's items are loaded in batches of kPB before any is stored,
+  // so each thread keeps kPB * 32 bytes in flight instead of one round trip
+  // per item
+  {
+    constexpr int kItems = kTM * (kP / 8) / kThreads, kPB = 8;
+    static_assert(kItems % kPB == 0, "towers: pooled batches");
+#pragma unroll 1
+    for (int i0 = 0; i0 < kItems; i0 += kPB) {
+      float4 a[kPB], b[kPB];
+#pragma unroll
+      for (int j = 0; j < kPB; ++j) {
+        const int c = tid + (i0 + j) * kThreads, r = c / (kP / 8), k = (c - r * (kP / 8)) * 8;
+        const float4* src = reinterpret_cast<const float4*>(p.pooled + (long long)(s0 + r) * kP + k);
+        a[j] = r < n ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        b[j] = r < n ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kPB; ++j) {
+        const int c = tid + (i0 + j) * kThreads, r = c / (kP / 8), k = (c - r * (kP / 8)) * 8;
+        *reinterpret_cast<uint4*>(sm + kX0 + xoff(r, k, kTM)) =
+            make_uint4(pack_bf16x2(a[j].x, a[j].y), pack_bf16x2(a[j].z, a[j].w), pack_bf16x2(b[j].x, b[j].y),
+                       pack_bf16x2(b[j].z, b[j].w));
+      }
     }
-    *reinterpret_cast<uint4*>(sm + kX0 + xoff(r, k, kTM)) = w;
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -181,18 +197,26 @@ __global__ void __launch_bounds__(kThreads, 1) towers_kernel(const __grid_consta
     if (!mbar_wait(&ms->mma, mma_phase & 1u)) fail();
     ++mma_phase;
   };
-  // epilogue: accumulator columns [c0, c0 + 16) of this thread's row -> ReLU(acc
-  // + bias) as bf16 into the next layer's A operand at K offset c0 (`rows` rows)
-  auto epi_store = [&](int c0, const float* bias, uint8_t* dst) {
-    float v[16];
-    tmem_ld16(tbase + lane_base + uint32_t(c0), v);
-    tmem_ld_wait();
-    uint32_t h[8];
+  // epilogue: accumulator columns [c0, c0 + 16 NB) of this thread's row ->
+  // ReLU(acc + bias) as bf16 into the next layer's A operand at K offset c0.
+  // The NB loads are issued before one wait: the wait covers every load in
+  // flight, so batching pays its latency once per 16 NB columns.
+  auto epi_store = [&](auto nb_tag, int c0, const float* bias, uint8_t* dst) {
+    constexpr int NB = decltype(nb_tag)::value;
+    float v[16 * NB];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      h[e] = pack_bf16x2_relu(v[2 * e] + bias[c0 + 2 * e], v[2 * e + 1] + bias[c0 + 2 * e + 1]);
-    *reinterpret_cast<uint4*>(dst + xoff(row, c0, kTM)) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(dst + xoff(row, c0 + 8, kTM)) = make_uint4(h[4], h[5], h[6], h[7]);
+    for (int b = 0; b < NB; ++b) tmem_ld16(tbase + lane_base + uint32_t(c0 + 16 * b), v + 16 * b);
+    tmem_ld_wait();
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int c = c0 + 16 * b;
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        h[e] = pack_bf16x2_relu(v[16 * b + 2 * e] + bias[c + 2 * e], v[16 * b + 2 * e + 1] + bias[c + 2 * e + 1]);
+      *reinterpret_cast<uint4*>(dst + xoff(row, c, kTM)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(dst + xoff(row, c + 8, kTM)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
   };
   // all warps: wait for the layer's MMAs (thread 0 waited already), then read
   auto sync_after_mma = [&]() {
@@ -219,7 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1) towers_kernel(const __grid_consta
   sync_after_mma();
   if (ms->abort_ == 0) {
     // h1 [128 x 512] -> X0 X1 (8 K-blocks); warp w: columns 128 (w / 4) .. + 128
-    for (int c = (warp >> 2) * 128; c < (warp >> 2) * 128 + 128; c += 16) epi_store(c, ms->bd1, sm + kX0);
+#pragma unroll 1
+    for (int c = (warp >> 2) * 128; c < (warp >> 2) * 128 + 128; c += 64)
+      epi_store(std::integral_constant<int, 4>{}, c, ms->bd1, sm + kX0);
   }
   sync_before_mma();
 
@@ -236,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) towers_kernel(const __grid_consta
   sync_after_mma();
   if (ms->abort_ == 0) {
     // h2 [128 x 256] -> X1 (4 K-blocks); warp w: columns 64 (w / 4) .. + 64
-    for (int c = (warp >> 2) * 64; c < (warp >> 2) * 64 + 64; c += 16) epi_store(c, ms->bd2, sm + kX1);
+    epi_store(std::integral_constant<int, 4>{}, (warp >> 2) * 64, ms->bd2, sm + kX1);
   }
   sync_before_mma();
 
@@ -254,19 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1) towers_kernel(const __grid_consta
   if (ms->abort_ == 0) {
     // cat[h3, din, 0] [128 x 192] -> X1 (3 K-blocks): h3 in K 0..127, warp w:
     // columns 32 (w / 4) .. + 32 ...
-    for (int c = (warp >> 2) * 32; c < (warp >> 2) * 32 + 32; c += 16) epi_store(c, ms->bd3, sm + kX1);
+    epi_store(std::integral_constant<int, 2>{}, (warp >> 2) * 32, ms->bd3, sm + kX1);
   }
   // ... and din (fp32 -> bf16) in K 128..175, zeros in K 176..191
-  for (int c = tid; c < kTM * (kKFP - kH3) / 8; c += kThreads) {
-    const int r = c / ((kKFP - kH3) / 8), k = kH3 + (c - r * ((kKFP - kH3) / 8)) * 8;
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (r < n && k < kKF) {
-      const float* src = p.din + (long long)(s0 + r) * kDQ + (k - kH3);
-      const float4 a = __ldg(reinterpret_cast<const float4*>(src));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(src + 4));
-      w = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  {
+    constexpr int kItems = kTM * (kKFP - kH3) / 8 / kThreads;
+    float4 a[kItems], b[kItems];
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      const int c = tid + j * kThreads, r = c / ((kKFP - kH3) / 8), k = kH3 + (c - r * ((kKFP - kH3) / 8)) * 8;
+      const float4* src = reinterpret_cast<const float4*>(p.din + (long long)(s0 + r) * kDQ + (k - kH3));
+      const bool in = r < n && k < kKF;
+      a[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      b[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *reinterpret_cast<uint4*>(sm + kX1 + xoff(r, k, kTM)) = w;
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      const int c = tid + j * kThreads, r = c / ((kKFP - kH3) / 8), k = kH3 + (c - r * ((kKFP - kH3) / 8)) * 8;
+      *reinterpret_cast<uint4*>(sm + kX1 + xoff(r, k, kTM)) =
+          make_uint4(pack_bf16x2(a[j].x, a[j].y), pack_bf16x2(a[j].z, a[j].w), pack_bf16x2(b[j].x, b[j].y),
+                     pack_bf16x2(b[j].z, b[j].w));
+    }
   }
   sync_before_mma();
 
