@@ -15,6 +15,10 @@ Parity status of each oracle function (what pins it, in tests/test_oracle.py):
   oracle_din           pinned: L=1 -> s0, uniform weights -> mean, padded ==
                        jagged, two-position closed-form softmax (sigmoid), the
                        cat order [q, s, q-s, q*s] via selection MLPs, L=0 -> 0
+  oracle_towers        pinned: zero weights -> bias path, identity chain, ReLU
+                       after every layer, bf16 mode on representable data
+  hash_translate       pinned: a brute-force dict on random keys, unseen -> the
+                       zero row, key spaces of different tables kept apart
 """
 from __future__ import annotations
 
@@ -181,12 +185,61 @@ def din(tables, values, lengths, B: int, q_feat, seq_table, seq_values, seq_leng
     return out, flags
 
 
+KEY_LIMIT = 1 << 56  # raw keys of hash-table features lie in [0, 2^56)
+
+
+def hash_translate(keys, raw):
+    """The hash-table lookup by its definition (MultiTowerDIN: integrating
+    DynamicEmb, sections 1 and 3.2): a raw key admitted to the table reads its
+    own row, an unseen key reads the constant zero vector. keys: int64 [n],
+    key i owning row i; raw: int64 ids. Returns row indices into the table
+    with one zero row appended at index n; a raw id outside [0, 2^56) maps to
+    -1, an invalid id (flagged, contributes zero)."""
+    keys = np.asarray(keys, dtype=np.int64)
+    raw = np.asarray(raw, dtype=np.int64)
+    order = np.argsort(keys, kind="stable")
+    sk = keys[order]
+    pos = np.searchsorted(sk, raw)
+    pos_c = np.minimum(pos, max(sk.size - 1, 0))
+    hit = (pos < sk.size) & (sk[pos_c] == raw) if sk.size else np.zeros(raw.shape, bool)
+    out = np.where(hit, order[pos_c] if sk.size else 0, keys.size).astype(np.int64)
+    out[(raw < 0) | (raw >= KEY_LIMIT)] = -1
+    return out
+
+
+def resolve_hashed(batch):
+    """(tables, values, seq_values) of a batch with its hash-table features
+    turned into plain tables: each such table gains the zero row, and its
+    ids become row indices by hash_translate. Batches without hash tables
+    come back unchanged."""
+    hk = getattr(batch, "hash_keys", None)
+    if not hk:
+        return batch.tables, batch.values, batch.seq_values
+    F, B = len(batch.tables), batch.B
+    lengths = np.asarray(batch.lengths, np.int64).reshape(F, B)
+    starts = np.concatenate([[0], np.cumsum(np.maximum(lengths, 0).sum(axis=1))])
+    tables = list(batch.tables)
+    values = np.array(batch.values, dtype=np.int64, copy=True)
+    seq_values = np.array(batch.seq_values, dtype=np.int64, copy=True).reshape(3, -1)
+    for f, keys in hk.items():
+        t = tables[f]
+        tables[f] = np.concatenate([t, np.zeros((1, t.shape[1]), t.dtype)])
+        a, b = int(starts[f]), min(int(starts[f + 1]), values.size)
+        values[a:b] = hash_translate(keys, values[a:b])
+        for k, tb in enumerate(batch.seq_table):
+            if tb == f:
+                seq_values[k] = hash_translate(keys, seq_values[k])
+    return tables, values, seq_values
+
+
 def din_batch(batch, samples=None, padded=False, bf16_mlp=False, want_logits=False, pooling=None):
-    """oracle_din on a synth.Batch (pooling: the batch's own modes by default)."""
+    """oracle_din on a synth.Batch (pooling: the batch's own modes by default;
+    hash-table features resolved by resolve_hashed)."""
     if pooling is None:
         pooling = getattr(batch, "pooling", None)
-    return din(batch.tables, batch.values, batch.lengths, batch.B, batch.q_feat,
-               batch.seq_table, batch.seq_values, batch.seq_lengths, batch.max_len,
+    tables, values, seq_values = resolve_hashed(batch)
+    return din(tables, values, batch.lengths, batch.B, batch.q_feat,
+               batch.seq_table, seq_values, batch.seq_lengths, batch.max_len,
                batch.W1, batch.b1, batch.W2, batch.b2, batch.w3, batch.b3,
                samples=samples, padded=padded, bf16_mlp=bf16_mlp, want_logits=want_logits,
                pooling=pooling)
@@ -195,7 +248,8 @@ def din_batch(batch, samples=None, padded=False, bf16_mlp=False, want_logits=Fal
 def pool_batch(batch, samples=None, pooling=None):
     if pooling is None:
         pooling = getattr(batch, "pooling", None)
-    return emb_bag_pool(batch.tables, batch.values, batch.lengths, batch.B, samples, pooling)
+    tables, values, _ = resolve_hashed(batch)
+    return emb_bag_pool(tables, values, batch.lengths, batch.B, samples, pooling)
 
 
 def towers(pooled, din, Wd1, bd1, Wd2, bd2, Wd3, bd3, Wf1, bf1, wo, bo, bf16_mlp: bool = False):

@@ -117,6 +117,10 @@ class Batch:
     w3: np.ndarray
     b3: np.ndarray
     pooling: Optional[tuple] = None  # per table 0 (sum) / 1 (mean); None: all sum
+    # hash-table (DynamicEmb-style) features: f -> int64 keys of the admitted
+    # rows, key i owning row i of tables[f]; those features' values (and the
+    # sequence values of their sub-features) are raw keys, not row indices
+    hash_keys: Optional[dict] = None
 
     @property
     def F(self) -> int:
@@ -283,3 +287,47 @@ def tower_weights(seed: int = 0, bias: float = 0.1) -> list:
         else:
             out.append(rng.uniform(-bias, bias, shape).astype(np.float32))
     return out
+
+
+# The five tables above 100K rows that the DynamicEmb migration moves to hash
+# tables (user_id, adgroup_id, campaign_id, brand, customer), and its
+# per-GPU capacity of 300K rows.
+DYNEMB_FEATURES = (0, 1, 2, 3, 4)
+DYNEMB_CAPACITY = 300_000
+KEY_BITS = 56  # raw keys are drawn from [0, 2^56)
+
+
+def dynamic_emb(batch: Batch, features: Sequence[int] = DYNEMB_FEATURES,
+                capacity: int = DYNEMB_CAPACITY, seed: int = 0) -> Batch:
+    """The same batch with `features` served from hash tables.
+
+    Every row r of such a feature's vocabulary gets a distinct random raw key
+    in [0, 2^56); the ids become those keys. The table holds the rows whose
+    rank is below `capacity` -- the Zipf-hot ids, as a frequency-admitted table
+    would -- so the ids of the colder rows are unseen keys. Draws come from
+    their own stream, so everything else equals the plain batch.
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xD1E7])))
+    F, B = batch.F, batch.B
+    tables = list(batch.tables)
+    values = batch.values.copy()
+    seq_values = batch.seq_values.copy()
+    lengths = batch.lengths.reshape(F, B)
+    starts = np.concatenate([[0], np.cumsum(lengths.sum(axis=1))])
+    hash_keys = {}
+    for f in features:
+        n = tables[f].shape[0]
+        keys = np.unique(rng.integers(0, 1 << KEY_BITS, size=n + n // 8 + 16, dtype=np.int64))
+        keys = rng.permutation(keys)[:n]
+        if keys.size < n:
+            raise RuntimeError("not enough distinct keys")
+        cap = min(capacity, n)
+        hash_keys[f] = np.ascontiguousarray(keys[:cap])
+        tables[f] = np.ascontiguousarray(tables[f][:cap])
+        seg = slice(int(starts[f]), int(starts[f + 1]))
+        values[seg] = keys[values[seg]]
+        for k, t in enumerate(batch.seq_table):
+            if t == f:
+                seq_values[k] = keys[seq_values[k]]
+    return dataclasses.replace(batch, tables=tables, values=values, seq_values=seq_values,
+                               hash_keys=hash_keys)

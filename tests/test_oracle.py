@@ -1,6 +1,7 @@
 """Pins for the CPU oracle: each test checks it against something other than
 itself -- closed forms, exact integer sums, library routines, invariants and the
 figures the pages print. No GPU needed."""
+import dataclasses
 import json
 import math
 import os
@@ -479,3 +480,68 @@ def test_towers_bf16_mode_is_exact_on_bf16_representable_data():
     pooled = (rng.integers(0, 16, (6, 256)) / 8).astype(np.float32)
     din = rng.integers(0, 16, (6, 48)) / 8.0
     assert np.array_equal(_towers(w, pooled, din), _towers(w, pooled, din, True))
+
+
+# ---------------------------------------------------------------- hash tables
+def test_hash_translate_matches_a_dict():
+    """The lookup against a brute-force dict: admitted keys read their own
+    row, unseen keys the appended zero row, keys outside [0, 2^56) are -1."""
+    rng = np.random.default_rng(7)
+    keys = np.unique(rng.integers(0, 1 << 56, size=3000))[:2000]
+    keys = rng.permutation(keys)
+    row_of = {int(k): i for i, k in enumerate(keys)}
+    q = np.concatenate([rng.choice(keys, 500), rng.integers(0, 1 << 56, size=500),
+                        np.array([-1, -(1 << 40), 1 << 56, (1 << 63) - 1, 0])])
+    want = [(-1 if (x < 0 or x >= 1 << 56) else row_of.get(int(x), keys.size)) for x in q]
+    assert oracle.hash_translate(keys, q).tolist() == want
+    assert oracle.hash_translate(np.zeros(0, np.int64), np.array([5])).tolist() == [0]
+
+
+def _zero_cold_rows(plain, cap, feats):
+    """The plain batch with every row at or above `cap` of `feats` zeroed:
+    what a table that admitted only the first `cap` rows returns."""
+    tables = [t.copy() for t in plain.tables]
+    for f in feats:
+        tables[f][cap:] = 0
+    return dataclasses.replace(plain, tables=tables)
+
+
+@pytest.mark.parametrize("cap", [1000, 600, 1])
+def test_hashed_batch_equals_plain_batch_with_cold_rows_zeroed(cap):
+    """Hash-table features give exactly the plain path's pooled rows and DIN
+    output once the rows the table did not admit read as zero."""
+    plain = synth.generate("tiny", seed=3, nonzero_bias=True)
+    hashed = synth.dynamic_emb(plain, capacity=cap, seed=3)
+    ref = _zero_cold_rows(plain, cap, synth.DYNEMB_FEATURES)
+    p_h, fl_h = oracle.pool_batch(hashed)
+    p_r, fl_r = oracle.pool_batch(ref)
+    assert fl_h == fl_r == 0
+    assert np.array_equal(p_h, p_r)
+    d_h, _ = oracle.din_batch(hashed)
+    d_r, _ = oracle.din_batch(ref)
+    assert np.array_equal(d_h, d_r)
+    if cap < 1000:  # some ids are unseen, so the cold rows mattered
+        assert not np.array_equal(p_r, oracle.pool_batch(plain)[0])
+
+
+def test_hash_key_spaces_of_different_tables_are_independent():
+    """One raw key admitted by two tables reads each table's own row; a key
+    admitted only by table 0 is unseen (zero) in table 1."""
+    plain = synth.generate("tiny", seed=4, B=8)
+    hashed = synth.dynamic_emb(plain, features=(0, 1), capacity=1000, seed=4)
+    k0, k1 = hashed.hash_keys[0].copy(), hashed.hash_keys[1].copy()
+    k1[7] = k0[3]          # the same raw key, rows 3 of table 0 and 7 of table 1
+    shared, only0 = k0[3], k0[5]
+    assert only0 not in set(k1.tolist())
+    hk = {0: k0, 1: k1}
+    B = hashed.B
+    vals = hashed.values.copy()
+    vals[0] = shared       # sample 0 of feature 0
+    vals[B] = shared       # sample 0 of feature 1
+    vals[B + 1] = only0    # sample 1 of feature 1
+    b = dataclasses.replace(hashed, hash_keys=hk, values=vals)
+    pooled, _ = oracle.pool_batch(b)
+    D = b.D
+    assert np.array_equal(pooled[0, 0:D], b.tables[0][3])
+    assert np.array_equal(pooled[0, D:2 * D], b.tables[1][7])
+    assert not pooled[1, D:2 * D].any()
