@@ -73,6 +73,8 @@ enum {
 #define DSF_FLAG_COUNT         0x08 /* lengths sum differs from the values array size */
 #define DSF_FLAG_TIMEOUT       0x10 /* a device wait ran out (about 1 s); outputs invalid */
 #define DSF_FLAG_NOT_PREPARED  0x20 /* dsf_prepare_mlp was not run on this workspace */
+#define DSF_FLAG_HASH          0x40 /* the hash workspace was not initialised for this capacity */
+#define DSF_FLAG_HASH_FULL     0x80 /* dsf_hash_insert found no free slot for a key (left out) */
 
 /* Pooling of a table's bags (EmbeddingBag modes: the pages' tables pool by
  * sum, section 3; mean divides the fp32 sum by the bag's length, an empty bag
@@ -80,11 +82,64 @@ enum {
 #define DSF_POOL_SUM  0
 #define DSF_POOL_MEAN 1
 
+/* ------------------------------------------------------------------------
+ * Hash-table storage for large tables (MultiTowerDIN: integrating DynamicEmb,
+ * sections 1 and 3.2: open-addressing hash lookup; the large tables of a
+ * feature group fused into one storage with independent key spaces; an unseen
+ * id reads the constant 0). Admission and eviction are not part of this
+ * library: keys and their rows are inserted by the caller.
+ *
+ * A table served this way takes raw ids in [0, 2^56) as keys in its own key
+ * space (0 .. 254), so equal raw ids of two tables never collide. Several
+ * tables share one workspace: one key array (buckets of 8 slots, one 64-byte
+ * line each, probed linearly from a 64-bit hash of the key) and one row pool
+ * [slots + 1, D] whose last row is zero.
+ *
+ * workspace: device, 256-byte aligned, dsf_hash_workspace_bytes(capacity, D,
+ * dtype) bytes, caller-owned. capacity: the minimum slot count (rounded up to
+ * 8 times a power of two); keep the keys at most ~3/4 of it. key_space: host
+ * array [F] for dsf_tables (-1: table f is a plain table; k: table f's ids are
+ * raw keys of key space k), unused by the calls below. */
+typedef struct {
+  void* workspace;
+  size_t ws_bytes;
+  int64_t capacity;
+  int32_t D;      /* 16 or 64, as the tables it serves */
+  int32_t dtype;  /* DSF_F32 or DSF_BF16 */
+  const int32_t* key_space;
+} dsf_hash;
+
+/* Bytes of a hash workspace (0 for invalid arguments). */
+size_t dsf_hash_workspace_bytes(int64_t capacity, int32_t D, int32_t dtype);
+
+/* Empties the table: every slot free, the zero row zeroed, the header written.
+ * Asynchronous on stream. */
+int dsf_hash_init(const dsf_hash* hash, void* stream);
+
+/* Inserts n keys (device int64 [n], raw ids in [0, 2^56)) of one key space
+ * with their rows (device [n, D] of the table dtype, 16-byte aligned). A key
+ * already present has its row overwritten; a key given twice in one call keeps
+ * one of its rows. A raw id out of range sets DSF_FLAG_ID_RANGE, a key with no
+ * free slot DSF_FLAG_HASH_FULL, an uninitialised workspace DSF_FLAG_HASH (in
+ * *status_dev, nullable); those keys are left out. Asynchronous on stream. */
+int dsf_hash_insert(const dsf_hash* hash, int32_t key_space, const int64_t* keys_dev, const void* rows_dev,
+                    int64_t n, int32_t* status_dev, void* stream);
+
+/* The lookup alone: slots_dev[i] = the slot of keys_dev[i] in key_space, the
+ * zero row's index (the slot count) for an unseen key, or -2 (with
+ * DSF_FLAG_ID_RANGE) for a raw id outside [0, 2^56). Device int64 arrays [n]. */
+int dsf_hash_find(const dsf_hash* hash, int32_t key_space, const int64_t* keys_dev, int64_t n, int64_t* slots_dev,
+                  int32_t* status_dev, void* stream);
+
 /* F embedding tables, one per KJT key, all with the same D and element type.
  * table_ptrs[f]: device pointer to a row-major [table_rows[f], D] table,
  * 16-byte aligned. Host arrays of length F. pooling: host array [F] of
  * DSF_POOL_SUM / DSF_POOL_MEAN, or NULL for all sum. A mean-pooled query
- * table feeds the attention its mean too. */
+ * table feeds the attention its mean too. hash: NULL, or the hash-table
+ * storage serving the tables whose hash->key_space[f] >= 0 (their table_ptrs
+ * and table_rows entries are then ignored; an unseen key adds a zero row and
+ * counts in a mean's length; a raw id outside [0, 2^56) sets
+ * DSF_FLAG_ID_RANGE and adds nothing). Its D and dtype match the tables'. */
 typedef struct {
   const void* const* table_ptrs;
   const int64_t* table_rows;
@@ -92,6 +147,7 @@ typedef struct {
   int32_t D;      /* 16 or 64 */
   int32_t dtype;  /* DSF_F32 or DSF_BF16 */
   const int32_t* pooling;
+  const dsf_hash* hash;
 } dsf_tables;
 
 /* KeyedJaggedTensor of the deep group (section 2: values + lengths).

@@ -24,17 +24,25 @@ FLAG_SEQ_TRUNC = 0x04
 FLAG_COUNT = 0x08
 FLAG_TIMEOUT = 0x10
 FLAG_NOT_PREPARED = 0x20
+FLAG_HASH = 0x40
+FLAG_HASH_FULL = 0x80
 
 EXPORTS = ["dsf_workspace_bytes", "dsf_workspace_init", "dsf_prepare_mlp", "emb_bag_pool",
            "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size",
-           "emb_bag_pool_noalloc", "dsf_towers_workspace_bytes", "dsf_prepare_towers", "ctr_towers_fwd"]
+           "emb_bag_pool_noalloc", "dsf_towers_workspace_bytes", "dsf_prepare_towers", "ctr_towers_fwd",
+           "dsf_hash_workspace_bytes", "dsf_hash_init", "dsf_hash_insert", "dsf_hash_find"]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
 
+class CHash(ctypes.Structure):
+    _fields_ = [("workspace", _vp), ("ws_bytes", _sz), ("capacity", _i64), ("D", _i32), ("dtype", _i32),
+                ("key_space", _vp)]
+
+
 class CTables(ctypes.Structure):
     _fields_ = [("table_ptrs", _vp), ("table_rows", _vp), ("F", _i32), ("D", _i32), ("dtype", _i32),
-                ("pooling", _vp)]
+                ("pooling", _vp), ("hash", _vp)]
 
 
 class CKjt(ctypes.Structure):
@@ -94,6 +102,14 @@ def lib() -> ctypes.CDLL:
         L.dsf_prepare_towers.restype = ctypes.c_int
         L.ctr_towers_fwd.argtypes = [_vp, _vp, _i32, P(CTowers), _vp, _vp, _sz, _vp, _vp]
         L.ctr_towers_fwd.restype = ctypes.c_int
+        L.dsf_hash_workspace_bytes.argtypes = [_i64, _i32, _i32]
+        L.dsf_hash_workspace_bytes.restype = _sz
+        L.dsf_hash_init.argtypes = [P(CHash), _vp]
+        L.dsf_hash_init.restype = ctypes.c_int
+        L.dsf_hash_insert.argtypes = [P(CHash), _i32, _vp, _vp, _i64, _vp, _vp]
+        L.dsf_hash_insert.restype = ctypes.c_int
+        L.dsf_hash_find.argtypes = [P(CHash), _i32, _vp, _i64, _vp, _vp, _vp]
+        L.dsf_hash_find.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -123,8 +139,10 @@ class EmbeddingTables:
     """F device tables [rows_f, D], all fp32 or all bf16. pooling: per table
     DSF_POOL_SUM or DSF_POOL_MEAN (None: all sum)."""
 
-    def __init__(self, tables: Sequence[torch.Tensor], pooling: Optional[Sequence[int]] = None):
+    def __init__(self, tables: Sequence[torch.Tensor], pooling: Optional[Sequence[int]] = None,
+                 hash_table: Optional["HashTable"] = None):
         self.tables = list(tables)
+        self.hash = hash_table
         F = len(self.tables)
         D = int(self.tables[0].shape[1])
         dt = self.tables[0].dtype
@@ -140,7 +158,10 @@ class EmbeddingTables:
             raise ValueError("pooling needs one mode per table")
         self._pool = None if self.pooling is None else (ctypes.c_int32 * F)(*self.pooling)
         self.c = CTables(ctypes.cast(self._ptrs, _vp), ctypes.cast(self._rows, _vp), F, D, self.dtype,
-                         None if self._pool is None else ctypes.cast(self._pool, _vp))
+                         None if self._pool is None else ctypes.cast(self._pool, _vp),
+                         None if hash_table is None else ctypes.cast(ctypes.pointer(hash_table.c), _vp))
+        if hash_table is not None and len(hash_table.key_space) != F:
+            raise ValueError("the hash table needs one key space entry per table")
 
     @property
     def rows(self):
@@ -283,3 +304,37 @@ def ctr_towers_fwd(pooled: torch.Tensor, din: torch.Tensor, B: int, towers: Towe
                                 logit.data_ptr(), towers.buf.data_ptr(), towers.nbytes,
                                 _dptr(status), _stream_ptr(stream)), "ctr_towers_fwd")
     return logit
+
+
+class HashTable:
+    """Hash-table storage (one device workspace) for the tables whose
+    key_space[f] >= 0: raw int64 keys in [0, 2^56) map to rows of one fused
+    pool; an unseen key reads zero. capacity: the minimum slot count."""
+
+    def __init__(self, capacity: int, D: int, dtype: int, key_space: Sequence[int], device="cuda",
+                 stream=None):
+        self.key_space = [int(k) for k in key_space]
+        self._ks = (ctypes.c_int32 * len(self.key_space))(*self.key_space)
+        self.nbytes = int(lib().dsf_hash_workspace_bytes(int(capacity), int(D), int(dtype)))
+        if self.nbytes == 0:
+            raise DsfError(DSF_EINVAL, "dsf_hash_workspace_bytes")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.c = CHash(self.buf.data_ptr(), self.nbytes, int(capacity), int(D), int(dtype),
+                       ctypes.cast(self._ks, _vp))
+        _check(lib().dsf_hash_init(ctypes.byref(self.c), _stream_ptr(stream)), "dsf_hash_init")
+
+    def insert(self, key_space: int, keys: torch.Tensor, rows: torch.Tensor,
+               status: Optional[torch.Tensor] = None, stream=None):
+        keys = keys.contiguous()
+        rows = rows.contiguous()
+        _check(lib().dsf_hash_insert(ctypes.byref(self.c), int(key_space), keys.data_ptr(), rows.data_ptr(),
+                                     int(keys.numel()), _dptr(status), _stream_ptr(stream)),
+               "dsf_hash_insert")
+
+    def find(self, key_space: int, keys: torch.Tensor, status: Optional[torch.Tensor] = None,
+             stream=None) -> torch.Tensor:
+        keys = keys.contiguous()
+        out = torch.empty_like(keys)
+        _check(lib().dsf_hash_find(ctypes.byref(self.c), int(key_space), keys.data_ptr(), int(keys.numel()),
+                                   out.data_ptr(), _dptr(status), _stream_ptr(stream)), "dsf_hash_find")
+        return out

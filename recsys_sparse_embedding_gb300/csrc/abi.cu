@@ -55,15 +55,26 @@ __global__ void prepare_kernel(const float* __restrict__ W1, const float* __rest
 
 __global__ void tag_kernel(uint32_t* magic, uint32_t tag) { *magic = tag; }
 
+bool hashed(const dsf_tables* t, int f) { return t->hash && t->hash->key_space[f] >= 0; }
+
 int check_tables(const dsf_tables* t) {
   if (!t || !t->table_ptrs || !t->table_rows) return DSF_EINVAL;
   if (t->F < 1 || t->F > DSF_MAX_TABLES) return DSF_EINVAL;
   if (t->D != 16 && t->D != 64) return DSF_EUNSUPPORTED;
   if (t->dtype != DSF_F32 && t->dtype != DSF_BF16) return DSF_EUNSUPPORTED;
+  if (const dsf_hash* h = t->hash) {
+    if (!h->key_space || h->D != t->D || h->dtype != t->dtype) return DSF_EINVAL;
+    if (h->capacity < 1 || h->capacity > (1ll << 40)) return DSF_EINVAL;
+    const hash::Layout L = hash::layout(h->capacity, h->D, t->dtype == DSF_BF16 ? 2 : 4);
+    if (!h->workspace || !aligned(h->workspace, 256) || h->ws_bytes < L.total) return DSF_EWORKSPACE;
+    for (int f = 0; f < t->F; ++f)
+      if (h->key_space[f] < -1 || h->key_space[f] > hash::kMaxKeySpace) return DSF_EINVAL;
+  }
   for (int f = 0; f < t->F; ++f) {
+    if (t->pooling && t->pooling[f] != DSF_POOL_SUM && t->pooling[f] != DSF_POOL_MEAN) return DSF_EINVAL;
+    if (hashed(t, f)) continue;
     if (!t->table_ptrs[f] || !aligned(t->table_ptrs[f], 16)) return DSF_EINVAL;
     if (t->table_rows[f] < 0) return DSF_EINVAL;
-    if (t->pooling && t->pooling[f] != DSF_POOL_SUM && t->pooling[f] != DSF_POOL_MEAN) return DSF_EINVAL;
   }
   return DSF_OK;
 }
@@ -103,9 +114,26 @@ int check_ws(void* ws, size_t bytes, int32_t B, int32_t D) {
 void fill_common(FwdParams& p, const dsf_tables* t, const dsf_kjt* k, int32_t B, void* ws,
                  int32_t* status) {
   std::memset(&p, 0, sizeof(p));
+  hash::Layout L{};
+  uint8_t* hw = nullptr;
+  if (t->hash) {
+    L = hash::layout(t->hash->capacity, t->hash->D, t->dtype == DSF_BF16 ? 2 : 4);
+    hw = static_cast<uint8_t*>(t->hash->workspace);
+    p.hkeys = reinterpret_cast<const unsigned long long*>(hw + L.keys_off);
+    p.hhdr = reinterpret_cast<const hash::Header*>(hw);
+    p.hbmask = L.n_buckets - 1;
+    p.hslots = L.n_slots;
+  }
   for (int f = 0; f < t->F; ++f) {
-    p.tables[f] = t->table_ptrs[f];
-    p.rows[f] = t->table_rows[f];
+    if (hashed(t, f)) {  // the fused row pool; the zero row is the last
+      p.tables[f] = hw + L.pool_off;
+      p.rows[f] = static_cast<long long>(L.n_slots) + 1;
+      p.hash_mask |= 1u << f;
+      p.kspace[f] = static_cast<unsigned char>(t->hash->key_space[f]);
+    } else {
+      p.tables[f] = t->table_ptrs[f];
+      p.rows[f] = t->table_rows[f];
+    }
     if (t->pooling && t->pooling[f] == DSF_POOL_MEAN) p.mean_mask |= 1u << f;
   }
   p.F = t->F;

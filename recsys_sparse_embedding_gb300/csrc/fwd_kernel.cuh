@@ -30,6 +30,7 @@
 #include <type_traits>
 
 #include "dinsparse.h"
+#include "hash.cuh"
 #include "ptx.cuh"
 
 namespace dsf {
@@ -74,6 +75,14 @@ struct FwdParams {
   const float* w1t;      // fp32 W1^T [K1][256]
   const float* w2t;      // fp32 W2^T [256][64]
   const uint32_t* magic;
+  // hash-table storage (null hkeys: none): tables in hash_mask read the fused
+  // row pool at the slot of their raw key in key space kspace[f]
+  const unsigned long long* hkeys;
+  const hash::Header* hhdr;
+  unsigned long long hbmask;  // buckets - 1
+  unsigned long long hslots;  // slots (the zero row's index)
+  unsigned int hash_mask;
+  unsigned char kspace[kMaxF];
   unsigned int* epoch;           // launch counter, tags the partials
   unsigned long long* partials;  // [G][kMaxF]: (epoch + 1) << 32 | length total
   int* status;
@@ -454,6 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 
   attn_ok = C::ATTN && magic == (kMagicBase | uint32_t(D));
   if (C::ATTN && tid == 0 && !attn_ok && cta == 0) flag(p.status, DSF_FLAG_NOT_PREPARED);
+  // the hash workspace's header, checked once (off the critical threads)
+  if (p.hkeys && cta == 0 && tid == kThreads - 1 &&
+      (p.hhdr->tag != hash::kHashTag || p.hhdr->n_slots != p.hslots || p.hhdr->D != uint32_t(D)))
+    flag(p.status, DSF_FLAG_HASH);
   const unsigned long long tag = (unsigned long long)(epoch + 1u) << 32;
 
   // ---------------------------------------------------------------- pooling helpers
@@ -628,6 +641,12 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
     if (tid == 0) ms->seq_cur = base + tf;
   };
 
+  // The row of an id of table f: the id itself, or, for a table served by the
+  // hash table, the pool slot of its raw key (the zero row when unseen,
+  // hash::kBadKey -- flagged as out of range below -- for an invalid key).
+  auto rid = [&](int f, long long id) -> long long {
+    return ((p.hash_mask >> f) & 1u) ? hash::find(p.hkeys, p.hbmask, p.kspace[f], id) : id;
+  };
   // Sequence rows of a tile [t0, t0+n): thread tid = 32 + ri, ri < 3n, owns
   // sub-row (r = ri/3, key k = ri%3); warp 0 has none, so that its thread 0
   // can issue MMAs meanwhile. seq_ids finds the row's sample (written once
@@ -645,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       const long long jj = (long long)ms->so[i] + (rr - ms->rp[i]);
       const int j = jj < p.n_seq ? int(jj) : -1;
       if (k == 0) ms->row_samp[(t0 / C::TM) & 3][r] = uint8_t(i);
-      if (j >= 0) id = p.seq_values[(long long)k * p.n_seq + j];
+      if (j >= 0) id = rid(p.seq_table[k], p.seq_values[(long long)k * p.n_seq + j]);
       else local_flags |= DSF_FLAG_COUNT;
     }
     return id;
@@ -672,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
       const long long jj = (long long)ms->so[i] + (xr - ms->rp[i]);
       const int j = jj < p.n_seq ? int(jj) : -1;
       if (k == 0) ms->row_samp[(t0 / C::TM) & 3][r] = uint8_t(i);
-      if (j >= 0) id = p.seq_values[(long long)k * p.n_seq + j];
+      if (j >= 0) id = rid(p.seq_table[k], p.seq_values[(long long)k * p.n_seq + j]);
       else local_flags |= DSF_FLAG_COUNT;
     };
     finish(t0a, xa, loa, ida);
@@ -907,6 +926,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
             }
           }
           if constexpr (C::ATTN) first_ids();  // (their latency overlaps ours)
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            if (va[k] < ve[k]) id[k] = rid(fk[k], id[k]);
           // first value of both bags: all row loads in flight before the adds
           // (a bag without a usable first value reads row 0 and adds nothing)
           float acc[2][EPT];
@@ -929,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             for (long long u = va[k] + 1; u < ve[k]; ++u) {
-              const long long v = __ldg(p.values + u);
+              const long long v = rid(fk[k], __ldg(p.values + u));
               if (v < 0 || v >= p.rows[fk[k]]) { local_flags |= DSF_FLAG_ID_RANGE; continue; }
               const uint8_t* src = static_cast<const uint8_t*>(p.tables[fk[k]]) + v * C::ROWB + pk[k] * PPT * 16;
 #pragma unroll
@@ -1014,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsf_fwd_kernel(const __grid_const
           const long long u = w0 + tid + (long long)k * kThreads;
           const int f = fv[k];
           const uint8_t* tbase = static_cast<const uint8_t*>(p.tables[f]);
-          const long long id = idv[k];
+          const long long id = rid(f, idv[k]);
           const bool ok = id >= 0 && id < p.rows[f];
           if (!ok) local_flags |= DSF_FLAG_ID_RANGE;
           uint8_t* dst = stage + (u - w0) * C::ROWB;

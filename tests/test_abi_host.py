@@ -121,6 +121,50 @@ def test_towers_reject_bad_arguments(L):
     assert L.dsf_prepare_towers(P(w), 4096, n - 1, None) == binding.DSF_EWORKSPACE
 
 
+def test_hash_entry_points_reject_bad_arguments(L):
+    P = ctypes.byref
+    n = L.dsf_hash_workspace_bytes(1000, 16, 0)
+    # 1000 slots round up to 1024 = 128 buckets of 8: keys, then 1025 rows
+    assert n == 256 + 1024 * 8 + ((1025 * 64 + 255) // 256) * 256
+    assert L.dsf_hash_workspace_bytes(0, 16, 0) == 0
+    assert L.dsf_hash_workspace_bytes(8, 32, 0) == 0
+    assert L.dsf_hash_workspace_bytes(8, 16, 2) == 0
+    ks = (ctypes.c_int32 * 16)(*([-1] * 16))
+    ok = binding.CHash(4096, n, 1000, 16, 0, ctypes.cast(ks, ctypes.c_void_p))
+    assert L.dsf_hash_init(None, None) == binding.DSF_EINVAL
+    assert L.dsf_hash_init(P(binding.CHash(4096, n - 1, 1000, 16, 0, None)), None) == binding.DSF_EWORKSPACE
+    assert L.dsf_hash_init(P(binding.CHash(4100, n, 1000, 16, 0, None)), None) == binding.DSF_EWORKSPACE
+    assert L.dsf_hash_init(P(binding.CHash(4096, n, 1000, 24, 0, None)), None) == binding.DSF_EUNSUPPORTED
+    assert L.dsf_hash_insert(P(ok), 255, 4096, 4096, 4, None, None) == binding.DSF_EINVAL
+    assert L.dsf_hash_insert(P(ok), -1, 4096, 4096, 4, None, None) == binding.DSF_EINVAL
+    assert L.dsf_hash_insert(P(ok), 0, 4096, 4100, 4, None, None) == binding.DSF_EINVAL
+    assert L.dsf_hash_insert(P(ok), 0, 4096, 4096, 0, None, None) == binding.DSF_OK
+    assert L.dsf_hash_find(P(ok), 0, 4096, 4, None, None, None) == binding.DSF_EINVAL
+    assert L.dsf_hash_find(P(ok), 0, 4096, 0, None, None, None) == binding.DSF_OK
+    # the tables' view of the hash storage: key spaces, D and the workspace
+    t, keep = _tables()
+    k = binding.CKjt(4096, 16, 4096)
+
+    def pool_with(h):
+        t.hash = ctypes.cast(ctypes.pointer(h), ctypes.c_void_p)
+        return L.emb_bag_pool(P(t), P(k), 1, 4096, 4096, 1 << 30, None, None)
+    bad_ks = (ctypes.c_int32 * 16)(*([255] + [-1] * 15))
+    assert pool_with(binding.CHash(4096, n, 1000, 16, 0, ctypes.cast(bad_ks, ctypes.c_void_p))) == binding.DSF_EINVAL
+    assert pool_with(binding.CHash(4096, n, 1000, 64, 0, ctypes.cast(ks, ctypes.c_void_p))) == binding.DSF_EINVAL
+    assert pool_with(binding.CHash(4096, n, 1000, 16, 0, None)) == binding.DSF_EINVAL
+    assert pool_with(binding.CHash(4096, n - 256, 1000, 16, 0, ctypes.cast(ks, ctypes.c_void_p))) == \
+        binding.DSF_EWORKSPACE
+    # a hashed table's own pointer is ignored (null is fine)
+    ptrs = (ctypes.c_void_p * 16)(*([None] + [4096] * 15))
+    t.table_ptrs = ctypes.cast(ptrs, ctypes.c_void_p)
+    one = (ctypes.c_int32 * 16)(*([0] + [-1] * 15))
+    t.hash = ctypes.cast(ctypes.pointer(binding.CHash(4096, n, 1000, 16, 0, ctypes.cast(one, ctypes.c_void_p))),
+                         ctypes.c_void_p)
+    assert L.emb_bag_pool(P(t), P(k), 0, 4096, 4096, 1 << 30, None, None) == binding.DSF_OK
+    t.hash = None
+    assert L.emb_bag_pool(P(t), P(k), 1, 4096, 4096, 1 << 30, None, None) == binding.DSF_EINVAL
+
+
 def test_status_strings(L):
     for code in range(5):
         assert binding.status_string(code)
