@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 D2H_STREAMS = 1   # output copies of a step, split over this many streams (4 measured slower)
-KERNEL_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "launch.cuh", "fwd_attn_tc.cu"]
+KERNEL_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "hash.cuh", "launch.cuh", "fwd_attn_tc.cu"]
 
 
 def workload_desc(B):
@@ -116,6 +116,18 @@ def algorithmic_work(batch):
     return deep + din, flops, P
 
 
+def hashed_lookups(batch):
+    """Lookups served by the hash table in one batch: the deep ids of the
+    hashed features and the sequence ids of hashed sub-features."""
+    hk = getattr(batch, "hash_keys", None) or {}
+    F, B = batch.F, batch.B
+    lengths = np.maximum(np.asarray(batch.lengths).reshape(F, B), 0)
+    L = np.minimum(np.maximum(batch.seq_lengths, 0), batch.max_len).astype(np.int64)
+    n = int(sum(int(lengths[f].sum()) for f in hk))
+    n += int(L.sum()) * sum(1 for t in batch.seq_table if t in hk)
+    return n
+
+
 def traffic_record():
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None)."""
@@ -188,6 +200,63 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def time_dynamic_emb(binding, synth, batch, dev, mode, flush, steps, ws):
+    """The same step with the five large tables served by one hash table
+    (300K admitted keys each, the Zipf-hot ids; colder ids unseen): graph
+    replays, L2 flushed between steps, CUDA events on the launching stream,
+    max over ranks. Algorithmic bytes add one 64-byte bucket per hashed
+    lookup to the plain step's."""
+    import torch
+    from recsys_sparse_embedding_gb300.device_batch import to_device
+    hb = synth.dynamic_emb(batch, seed=0)
+    db = to_device(hb, dev)
+    B, D, F = db.B, db.D, db.F
+    mlp = db.mlp(mode)
+    wsp = binding.Workspace(B, D, device=dev)
+    wsp.prepare(mlp)
+    pooled = torch.empty(B, F * D, device=dev)
+    din = torch.empty(B, 3 * D, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        binding.din_sparse_fwd(db.tables, db.values, db.lengths, db.seq_values, db.seq_lengths,
+                               db.max_len, db.q_feat, db.seq_table, B, mlp, pooled, din, wsp,
+                               status=status, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            step()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        stream.synchronize()
+        for i in range(steps):
+            flush.fill_(float(i & 7))
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()):
+        raise RuntimeError("hashed step status 0x%x" % int(status.item()))
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), ws, dev)
+    us = total_ms * 1e3 / steps
+    nbytes, flops, _ = algorithmic_work(hb)
+    nh = hashed_lookups(hb)
+    nbytes += 64 * nh
+    hbm, _, _, src = peaks()
+    ht = db.tables.hash
+    return {"what": "din_sparse_fwd with user_id, adgroup_id, campaign_id, brand, customer in one "
+                    "hash table (raw 56-bit keys, 300K admitted per table, unseen keys read zero)",
+            "us_per_step": us, "samples_per_s": weak_rate(B * steps, total_ms, ws),
+            "hashed_lookups_per_step": nh, "hash_workspace_bytes": ht.nbytes,
+            "hash_capacity": int(ht.c.capacity),
+            "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e-6) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": nbytes / (us * 1e-6) / 1e9 / hbm,
+                         "algorithmic_bytes_per_launch": nbytes, "peak_source": src}}
 
 
 TOWER_FLOPS_PER_SAMPLE = 2 * (256 * 512 + 512 * 256 + 256 * 128 + 176 * 64)
@@ -289,6 +358,8 @@ def main():
     ap.add_argument("--cpu-passes", type=int, default=8)
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-towers", action="store_true")
+    ap.add_argument("--skip-dynemb", action="store_true")
+    ap.add_argument("--dynemb-steps", type=int, default=500)
     ap.add_argument("--towers-steps", type=int, default=300)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -446,6 +517,10 @@ def main():
                 torch.equal(h_out[(E - 1) & 1][0], pooled.cpu())):
             raise RuntimeError("end-to-end outputs differ from the device-timed run")
 
+    dynemb = None
+    if not args.skip_dynemb:
+        dynemb = time_dynamic_emb(binding, synth, batch, dev, mode, flush, args.dynemb_steps, ws)
+
     towers = None
     if rank == 0 and not args.skip_towers:
         towers = time_towers(binding, synth, pooled, din, B, dev, flush, args.towers_steps)
@@ -501,6 +576,7 @@ def main():
             "clocks": clk.summary(),
             "status": st,
             "towers": towers,
+            "dynamic_emb": dynemb,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
