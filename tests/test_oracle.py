@@ -545,3 +545,134 @@ def test_hash_key_spaces_of_different_tables_are_independent():
     assert np.array_equal(pooled[0, 0:D], b.tables[0][3])
     assert np.array_equal(pooled[0, D:2 * D], b.tables[1][7])
     assert not pooled[1, D:2 * D].any()
+
+
+# ---------------------------------------------------------------- backward
+from oracle import backward as obw  # noqa: E402
+
+
+def _small_batch(seed=0, B=6, rows=12, f64=False, wl="long_multihot"):
+    """A small batch with few rows per table, so rows repeat across bags,
+    features and positions; bags of 1..8 values on features 0-4; nonzero
+    biases."""
+    g = synth.generate(wl, seed=seed, B=B, rows=[rows] * 16, nonzero_bias=True)
+    if f64:
+        g = dataclasses.replace(g, tables=[t.astype(np.float64) for t in g.tables])
+    return g
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_backward_forward_equals_oracle_din(bf16):
+    """The backward oracle's own forward reproduces oracle_din (fp64 and the
+    bf16-operand mode) on a workload batch."""
+    b = synth.generate("tiny", seed=2, nonzero_bias=True)
+    ref, _ = oracle.din_batch(b, bf16_mlp=bf16)
+    fw = obw.forward(b, bf16)
+    assert np.abs(fw["din"] - ref).max() <= 1e-12
+
+
+def test_backward_matches_finite_differences():
+    """Every gradient against central differences of the fp64 forward on
+    loss = sum(dpooled * pooled) + sum(ddin * din): table rows reached through
+    deep bags, the query and the sequence, and entries of every MLP tensor."""
+    b = _small_batch(seed=1, f64=True)
+    b.pooling = tuple(1 if f in (1, 3) else 0 for f in range(16))  # multi-hot query and plain tables by mean
+    rng = np.random.default_rng(0)
+    B, F, D = b.B, b.F, b.D
+    dpooled = rng.standard_normal((B, F * D))
+    ddin = rng.standard_normal((B, 3 * D))
+
+    def loss(bb):
+        fw = obw.forward(bb)
+        return float((dpooled * obw.pooled64(bb)).sum() + (ddin * fw["din"]).sum())
+    g = obw.backward(b, dpooled, ddin)
+    h = 1e-6
+
+    def fd(mutate):
+        return (loss(mutate(+h)) - loss(mutate(-h))) / (2 * h)
+
+    def check(an, num):
+        assert abs(an - num) <= 1e-6 * max(1.0, abs(num)), (an, num)
+    # table rows: one of a query table (1), of a plain deep table (7), of a
+    # sequence-only lookup through table 2
+    for f in (1, 2, 3, 7):
+        rows, grads = g["rows"][f]
+        for ri in (0, len(rows) - 1):
+            r, d = int(rows[ri]), 3
+
+            def mut(e, f=f, r=r, d=d):
+                tabs = [t.copy() for t in b.tables]
+                tabs[f][r, d] += e
+                return dataclasses.replace(b, tables=tabs)
+            check(grads[ri, d], fd(mut))
+    for name, idx in (("W1", (5, 17)), ("W1", (200, 150)), ("b1", (3,)), ("W2", (7, 100)),
+                      ("b2", (11,)), ("w3", (9,)), ("b3", (0,))):
+        def mut(e, name=name, idx=idx):
+            a = getattr(b, name).astype(np.float64).copy()
+            a[idx] += e
+            return dataclasses.replace(b, **{name: a})
+        an = g["d" + name][idx] if name != "b3" else g["db3"][0]
+        check(an, fd(mut))
+
+
+def test_backward_bf16_operands_stay_within_bf16_error():
+    """The bf16-operand mode differs from fp64 only through the roundings of
+    the GEMM operands (2^-9 relative each), measured against the sum of each
+    gradient entry's term magnitudes. (Relative to the entry itself the
+    difference can be large: per sample the dz_t sum to zero, so the
+    gradients are small residuals of larger terms.)"""
+    b = synth.generate("tiny", seed=3, nonzero_bias=True)
+    rng = np.random.default_rng(1)
+    ddin = rng.standard_normal((b.B, 3 * b.D))
+    g64 = obw.backward(b, None, ddin)
+    g16 = obw.backward(b, None, ddin, bf16=True)
+    fw = obw.forward(b)
+    a, s = fw["a"], fw["s32"].astype(np.float64)
+    samp = fw["samp"]
+    da = np.einsum("pd,pd->p", ddin[samp], s)
+    c = np.zeros(b.B)
+    np.add.at(c, samp, a * da)
+    dz = a * (da - c[samp])
+    dh2 = np.abs(dz)[:, None] * np.abs(b.w3)[None, :]
+    dh1 = dh2 @ np.abs(b.W2.astype(np.float64))
+    bound = {"dW2": dh2.T @ np.abs(fw["h1"]), "dW1": dh1.T @ np.abs(fw["x"]),
+             "db2": dh2.sum(axis=0), "db1": dh1.sum(axis=0), "dw3": np.abs(dz) @ np.abs(fw["h2"])}
+    for k, m in bound.items():
+        # typical entries sit at the operand roundings' size; a ReLU whose
+        # input the roundings move across zero changes whole terms, in a few
+        # entries only
+        r = (np.abs(g16[k] - g64[k]) / np.maximum(m, 1e-300))[m > 0]
+        assert np.median(r) <= 2.0 ** -9 and np.percentile(r, 95) <= 2.0 ** -6, k
+        assert not np.array_equal(g16[k], g64[k]), k  # the roundings did apply
+
+
+def test_adagrad_step_closed_form():
+    """w = 1, G = 5, g = 2, lr = 0.5, eps = 0: G -> 9, w -> 1 - 0.5 * 2 / 3."""
+    w, G = obw.adagrad(np.ones((3, 2)), np.full((3, 2), 5.0), np.array([1]), np.array([[2.0, -4.0]]),
+                       lr=0.5, eps=0.0)
+    assert np.array_equal(G, [[5, 5], [9, 21], [5, 5]])
+    assert np.allclose(w, [[1, 1], [1 - 1 / 3, 1 + 2 / np.sqrt(21)], [1, 1]], rtol=0, atol=1e-15)
+
+
+def test_backward_hash_rows_skip_unseen_keys():
+    """Hash-table features: gradients reach admitted keys only (the zero row an
+    unseen key reads is not a parameter), and equal the plain batch's
+    gradients of the same rows once the unadmitted rows read zero."""
+    plain = synth.generate("tiny", seed=5, B=32, nonzero_bias=True)
+    hb = synth.dynamic_emb(plain, capacity=500, seed=5)
+    ref = _zero_cold_rows(plain, 500, synth.DYNEMB_FEATURES)
+    rng = np.random.default_rng(2)
+    dp = rng.standard_normal((hb.B, hb.F * hb.D))
+    dd = rng.standard_normal((hb.B, 3 * hb.D))
+    g = obw.backward(hb, dp, dd)
+    gr = obw.backward(ref, dp, dd)
+    for k in ("dW1", "db1", "dW2", "db2", "dw3", "db3", "dq"):
+        assert np.array_equal(g[k], gr[k]), k
+    for f in range(hb.F):
+        rows, grads = g["rows"][f]
+        rr, gg = gr["rows"][f]
+        if f in synth.DYNEMB_FEATURES:
+            assert rows.max() < 500
+            keep = rr < 500
+            rr, gg = rr[keep], gg[keep]
+        assert np.array_equal(rows, rr) and np.array_equal(grads, gg), f
