@@ -75,6 +75,7 @@ enum {
 #define DSF_FLAG_NOT_PREPARED  0x20 /* dsf_prepare_mlp was not run on this workspace */
 #define DSF_FLAG_HASH          0x40 /* the hash workspace was not initialised for this capacity */
 #define DSF_FLAG_HASH_FULL     0x80 /* dsf_hash_insert found no free slot for a key (left out) */
+#define DSF_FLAG_GRAD_LIST     0x100 /* more touched rows than the row-gradient list holds */
 
 /* Pooling of a table's bags (EmbeddingBag modes: the pages' tables pool by
  * sum, section 3; mean divides the fp32 sum by the bag's length, an empty bag
@@ -283,6 +284,69 @@ int dsf_prepare_towers(const dsf_towers* towers, void* workspace_dev, size_t ws_
 int ctr_towers_fwd(const float* pooled_dev, const float* din_dev, int32_t B, const dsf_towers* towers,
                    float* logit_dev, const void* workspace_dev, size_t ws_bytes, int32_t* status_dev,
                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * Backward of the sparse path and the sparse optimizer step (MultiTowerDIN:
+ * current state analysis, section 1: training with sparse AdaGrad, lr 1e-3;
+ * the forward of sections 4.2 and 4.4 differentiated).
+ *
+ * din_sparse_bwd takes the forward's inputs, its pooled output and the
+ * upstream gradients dpooled [B, F*D] (nullable: zero) and ddin [B, 3D]
+ * (fp32, device, 16-byte aligned), recomputes the attention forward, and
+ * produces
+ *   - the attention MLP's gradients (dsf_mlp_grads, device fp32, overwritten:
+ *     dW1 [256, 12D], db1 [256], dW2 [64, 256], db2 [64], dw3 [64], db3 [1]);
+ *   - every touched row's summed gradient, accumulated into dsf_row_grads.
+ * The MLP runs as in the forward's mode (mlp->mode): bf16 GEMM operands with
+ * fp32 accumulation, or fp32 throughout. Its six GEMMs are library GEMMs
+ * (cuBLAS) over the valid positions only; the rest are this library's
+ * kernels. Row gradients are summed with fp32 atomics, so their rounding
+ * order varies between runs. Gradients of unseen hash keys and of invalid ids
+ * are dropped. emb_adagrad_update then applies AdaGrad to the touched rows
+ * and leaves the row-gradient state zero for the next step.
+ *
+ * Row-gradient state, caller-owned: host arrays [F] of device pointers, per
+ * table f: grad[f] fp32 [rows_f, D] and touched[f] int32 [rows_f], zero
+ * before the first step; for the tables served by a hash table, the pool's
+ * [slots + 1, D] and [slots + 1] arrays, the same pointers for all of them.
+ * list: device int64 [list_cap], the touched rows (table << 40 | row); count:
+ * device int32 [1], zero before the first step. list_cap bounds the distinct
+ * rows of one step (at most n_values + 3 * n_per_key); more set
+ * DSF_FLAG_GRAD_LIST. */
+typedef struct {
+  float *dW1, *db1, *dW2, *db2, *dw3, *db3;
+} dsf_mlp_grads;
+
+typedef struct {
+  float* const* grad;
+  int32_t* const* touched;
+  int64_t* list;
+  int32_t* count;
+  int64_t list_cap;
+} dsf_row_grads;
+
+/* Workspace bytes of din_sparse_bwd for B samples and n_per_key sequence
+ * values (0 for invalid arguments); caller-owned, 256-byte aligned. */
+size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_per_key, int32_t D);
+
+/* Returns DSF_EINVAL / DSF_EUNSUPPORTED / DSF_EWORKSPACE for bad arguments
+ * (as din_sparse_fwd), DSF_ECUDA when a launch or a library call fails.
+ * Device data errors set bits in *status_dev (nullable). Asynchronous on
+ * stream; the GEMMs run on the same stream with this workspace as theirs. */
+int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
+                   const int32_t* q_feat, const int32_t* seq_table, int32_t B, const dsf_mlp* mlp,
+                   const float* pooled_dev, const float* dpooled_dev, const float* ddin_dev,
+                   const dsf_mlp_grads* mlp_grads, const dsf_row_grads* row_grads, void* workspace_dev,
+                   size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/* Sparse AdaGrad on the touched rows: per element G += g * g and
+ * w -= lr * g / (sqrt(G) + eps), in fp32 (bf16 tables round the new weight to
+ * nearest even); then the rows' gradients, touched flags and the count are
+ * zeroed. The tables (their table_ptrs, or the hash pool) are updated in
+ * place. accum: host array [F] of device fp32 [rows_f, D] AdaGrad
+ * accumulators (the pool's for hash-table tables, as for the gradients). */
+int emb_adagrad_update(const dsf_tables* tables, float* const* accum, const dsf_row_grads* row_grads, float lr,
+                       float eps, int32_t* status_dev, void* stream);
 
 #ifdef __cplusplus
 }

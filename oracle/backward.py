@@ -148,7 +148,10 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
     dq [B, 3D], ds [P, 3D], and rows: {f: (row indices, grads [n, D])} per
     table -- the summed gradient of every row the batch touched (rows of
     hash-table features index their admitted keys; unseen keys, whose zero
-    row is not a parameter, and invalid ids get none)."""
+    row is not a parameter, and invalid ids get none); rows_abs and bounds:
+    each row gradient's and weight gradient's sum of absolute terms, carried
+    through the whole chain (|da| = |ddin|.|s|, |dz| = a (|da| + sum a |da|),
+    ...), which bounds the rounding errors of any evaluation order."""
     fw = forward(batch, bf16, pooled)
     D, B, F = batch.D, batch.B, batch.F
     Q = 3 * D
@@ -180,6 +183,19 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
     dq = np.zeros((B, Q))
     np.add.at(dq, samp, dxq + dxd + dxp * s)
     ds = ds + dxs - dxd + dxp * qp
+    # first-order magnitudes: each quantity's sum of absolute terms, through
+    # the same chain (rounding errors are bounded by multiples of these)
+    da_m = np.einsum("pd,pd->p", np.abs(ddin[samp]), np.abs(s))
+    c_m = np.zeros(B)
+    np.add.at(c_m, samp, a * da_m)
+    dz_m = a * (da_m + c_m[samp])
+    dh2_m = dz_m[:, None] * np.abs(fw["w3"])[None, :] * (fw["pre2"] > 0)
+    dh1_m = (dh2_m @ np.abs(fw["W2"])) * (fw["pre1"] > 0)
+    dx_m = dh1_m @ np.abs(fw["W1"])
+    aq = np.abs(qp)
+    dq_m = np.zeros((B, Q))
+    np.add.at(dq_m, samp, dx_m[:, :Q] + dx_m[:, 2 * Q:3 * Q] + dx_m[:, 3 * Q:] * np.abs(s))
+    ds_m = a[:, None] * np.abs(ddin[samp]) + dx_m[:, Q:2 * Q] + dx_m[:, 2 * Q:3 * Q] + dx_m[:, 3 * Q:] * aq
     # row gradients
     tables, values, seq_values = resolve_hashed(batch)
     hk = getattr(batch, "hash_keys", None) or {}
@@ -187,9 +203,11 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
     bag_off = np.concatenate([[0], np.cumsum(lengths.reshape(-1))])
     pooling = getattr(batch, "pooling", None)
     g_bag = dpooled.reshape(B, F, D).copy()
+    g_bag_m = np.abs(g_bag)
     for k, f in enumerate(batch.q_feat):
         g_bag[:, f, :] += dq[:, k * D:(k + 1) * D]
-    contrib_f, contrib_r, contrib_g = [], [], []
+        g_bag_m[:, f, :] += dq_m[:, k * D:(k + 1) * D]
+    contrib_f, contrib_r, contrib_g, contrib_m = [], [], [], []
 
     def valid(f, ids):
         n = tables[f].shape[0] - (1 if f in hk else 0)   # the zero row is not a parameter
@@ -203,27 +221,37 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
         ids = values[start:start + n]
         bag = np.repeat(np.arange(B), lf)
         g = g_bag[bag, f, :]
+        gm = g_bag_m[bag, f, :]
         if pooling is not None and pooling[f] == 1:
             g = g / lf[bag][:, None]
+            gm = gm / lf[bag][:, None]
         ok = valid(f, ids)
         contrib_f.append(np.full(int(ok.sum()), f)); contrib_r.append(ids[ok]); contrib_g.append(g[ok])
+        contrib_m.append(gm[ok])
     for k, tb in enumerate(batch.seq_table):
         ids = seq_values[k, fw["j"]] if P else np.zeros(0, np.int64)
         ok = valid(tb, ids)
         contrib_f.append(np.full(int(ok.sum()), tb)); contrib_r.append(ids[ok])
         contrib_g.append(ds[ok, k * D:(k + 1) * D])
+        contrib_m.append(ds_m[ok, k * D:(k + 1) * D])
     cf = np.concatenate(contrib_f) if contrib_f else np.zeros(0, np.int64)
     cr = np.concatenate(contrib_r) if contrib_r else np.zeros(0, np.int64)
     cg = np.concatenate(contrib_g) if contrib_g else np.zeros((0, D))
-    rows = {}
+    cm = np.concatenate(contrib_m) if contrib_m else np.zeros((0, D))
+    rows, rows_abs = {}, {}
     for f in np.unique(cf):
         m = cf == f
         u, inv = np.unique(cr[m], return_inverse=True)
         acc = np.zeros((u.size, D))
         np.add.at(acc, inv, cg[m])
+        mag = np.zeros((u.size, D))
+        np.add.at(mag, inv, cm[m])
         rows[int(f)] = (u, acc)
+        rows_abs[int(f)] = mag
+    bounds = dict(dW2=dh2_m.T @ np.abs(fw["h1"]), dW1=dh1_m.T @ np.abs(fw["x"]), db2=dh2_m.sum(axis=0),
+                  db1=dh1_m.sum(axis=0), dw3=dz_m @ np.abs(fw["h2"]), db3=np.array([dz_m.sum()]))
     return dict(dW1=dW1, db1=db1, dW2=dW2, db2=db2, dw3=dw3, db3=db3, dq=dq, ds=ds, rows=rows,
-                din=fw["din"])
+                rows_abs=rows_abs, bounds=bounds, din=fw["din"])
 
 
 def adagrad(table, accum, rows, grads, lr=1e-3, eps=1e-10):

@@ -26,11 +26,13 @@ FLAG_TIMEOUT = 0x10
 FLAG_NOT_PREPARED = 0x20
 FLAG_HASH = 0x40
 FLAG_HASH_FULL = 0x80
+FLAG_GRAD_LIST = 0x100
 
 EXPORTS = ["dsf_workspace_bytes", "dsf_workspace_init", "dsf_prepare_mlp", "emb_bag_pool",
            "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size",
            "emb_bag_pool_noalloc", "dsf_towers_workspace_bytes", "dsf_prepare_towers", "ctr_towers_fwd",
-           "dsf_hash_workspace_bytes", "dsf_hash_init", "dsf_hash_insert", "dsf_hash_find"]
+           "dsf_hash_workspace_bytes", "dsf_hash_init", "dsf_hash_insert", "dsf_hash_find",
+           "dsf_bwd_workspace_bytes", "din_sparse_bwd", "emb_adagrad_update"]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
@@ -38,6 +40,14 @@ _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c
 class CHash(ctypes.Structure):
     _fields_ = [("workspace", _vp), ("ws_bytes", _sz), ("capacity", _i64), ("D", _i32), ("dtype", _i32),
                 ("key_space", _vp)]
+
+
+class CMlpGrads(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("dW1", "db1", "dW2", "db2", "dw3", "db3")]
+
+
+class CRowGrads(ctypes.Structure):
+    _fields_ = [("grad", _vp), ("touched", _vp), ("list", _vp), ("count", _vp), ("list_cap", _i64)]
 
 
 class CTables(ctypes.Structure):
@@ -110,6 +120,13 @@ def lib() -> ctypes.CDLL:
         L.dsf_hash_insert.restype = ctypes.c_int
         L.dsf_hash_find.argtypes = [P(CHash), _i32, _vp, _i64, _vp, _vp, _vp]
         L.dsf_hash_find.restype = ctypes.c_int
+        L.dsf_bwd_workspace_bytes.argtypes = [_i32, _i64, _i32]
+        L.dsf_bwd_workspace_bytes.restype = _sz
+        L.din_sparse_bwd.argtypes = [P(CTables), P(CKjt), P(CSeq), _vp, _vp, _i32, P(CMlp), _vp, _vp, _vp,
+                                     P(CMlpGrads), P(CRowGrads), _vp, _sz, _vp, _vp]
+        L.din_sparse_bwd.restype = ctypes.c_int
+        L.emb_adagrad_update.argtypes = [P(CTables), _vp, P(CRowGrads), ctypes.c_float, ctypes.c_float, _vp, _vp]
+        L.emb_adagrad_update.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -338,3 +355,91 @@ class HashTable:
         _check(lib().dsf_hash_find(ctypes.byref(self.c), int(key_space), keys.data_ptr(), int(keys.numel()),
                                    out.data_ptr(), _dptr(status), _stream_ptr(stream)), "dsf_hash_find")
         return out
+
+
+class MlpGrads:
+    """Device fp32 gradients of the attention MLP (overwritten by a backward
+    call): dW1 [256, 12D], db1 [256], dW2 [64, 256], db2 [64], dw3 [64], db3 [1]."""
+
+    def __init__(self, D: int, device="cuda"):
+        K1 = 12 * D
+        self.t = dict(dW1=torch.zeros(256, K1, device=device), db1=torch.zeros(256, device=device),
+                      dW2=torch.zeros(64, 256, device=device), db2=torch.zeros(64, device=device),
+                      dw3=torch.zeros(64, device=device), db3=torch.zeros(1, device=device))
+        self.c = CMlpGrads(*[self.t[n].data_ptr() for n in ("dW1", "db1", "dW2", "db2", "dw3", "db3")])
+
+    def __getitem__(self, k):
+        return self.t[k]
+
+
+class SparseState:
+    """Per-storage row-gradient buffers, touched flags and AdaGrad
+    accumulators for a set of tables: one [rows, D] / [rows] set per plain
+    table, and one for the hash pool shared by the hash-table tables; the
+    touched-row list holds list_cap entries."""
+
+    def __init__(self, tables: EmbeddingTables, list_cap: int, device="cuda", accum_init: float = 0.0):
+        F, D = tables.F, tables.D
+        ks = tables.hash.key_space if tables.hash is not None else [-1] * F
+        pool_rows = None
+        if tables.hash is not None:
+            pool_rows = (self._pool_rows(tables.hash))
+        first = next((f for f in range(F) if ks[f] >= 0), None)
+        self.grad, self.touched, self.accum = [], [], []
+        for f in range(F):
+            if ks[f] >= 0 and f != first:
+                self.grad.append(self.grad[first])
+                self.touched.append(self.touched[first])
+                self.accum.append(self.accum[first])
+                continue
+            n = pool_rows if ks[f] >= 0 else int(tables.tables[f].shape[0])
+            self.grad.append(torch.zeros(n, D, device=device))
+            self.touched.append(torch.zeros(n, dtype=torch.int32, device=device))
+            self.accum.append(torch.full((n, D), float(accum_init), device=device))
+        self.list = torch.zeros(max(1, int(list_cap)), dtype=torch.int64, device=device)
+        self.count = torch.zeros(1, dtype=torch.int32, device=device)
+        self._g = (_vp * F)(*[t.data_ptr() for t in self.grad])
+        self._t = (_vp * F)(*[t.data_ptr() for t in self.touched])
+        self._a = (_vp * F)(*[t.data_ptr() for t in self.accum])
+        self.c = CRowGrads(ctypes.cast(self._g, _vp), ctypes.cast(self._t, _vp), self.list.data_ptr(),
+                           self.count.data_ptr(), int(list_cap))
+
+    @staticmethod
+    def _pool_rows(ht: "HashTable") -> int:
+        slots = 8
+        while slots < ht.c.capacity:
+            slots *= 2
+        return slots + 1
+
+    @property
+    def accum_ptrs(self):
+        return ctypes.cast(self._a, _vp)
+
+
+class BwdWorkspace:
+    def __init__(self, B: int, n_per_key: int, D: int, device="cuda"):
+        self.nbytes = int(lib().dsf_bwd_workspace_bytes(int(B), int(n_per_key), int(D)))
+        if self.nbytes == 0:
+            raise DsfError(DSF_EINVAL, "dsf_bwd_workspace_bytes")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+
+
+def din_sparse_bwd(tables: EmbeddingTables, values, lengths, seq_values, seq_lengths, max_len: int, q_feat,
+                   seq_table, B: int, mlp: AttnMLP, pooled, dpooled, ddin, grads: MlpGrads,
+                   state: SparseState, ws: BwdWorkspace, status=None, stream=None):
+    kjt = _kjt(values, lengths)
+    seq = _seq(seq_values, seq_lengths, max_len)
+    qf = (ctypes.c_int32 * 3)(*q_feat)
+    st = (ctypes.c_int32 * 3)(*seq_table)
+    _check(lib().din_sparse_bwd(ctypes.byref(tables.c), ctypes.byref(kjt), ctypes.byref(seq),
+                                ctypes.cast(qf, _vp), ctypes.cast(st, _vp), int(B), ctypes.byref(mlp.c),
+                                pooled.data_ptr(), _dptr(dpooled), ddin.data_ptr(), ctypes.byref(grads.c),
+                                ctypes.byref(state.c), ws.buf.data_ptr(), ws.nbytes, _dptr(status),
+                                _stream_ptr(stream)), "din_sparse_bwd")
+
+
+def emb_adagrad_update(tables: EmbeddingTables, state: SparseState, lr: float = 1e-3, eps: float = 1e-10,
+                       status=None, stream=None):
+    _check(lib().emb_adagrad_update(ctypes.byref(tables.c), state.accum_ptrs, ctypes.byref(state.c),
+                                    float(lr), float(eps), _dptr(status), _stream_ptr(stream)),
+           "emb_adagrad_update")

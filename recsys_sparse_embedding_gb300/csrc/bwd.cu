@@ -1,0 +1,788 @@
+// Backward of the sparse path and the sparse AdaGrad step (MultiTowerDIN:
+// current state analysis, section 1 -- training with sparse AdaGrad -- and the
+// forward of sections 4.2 and 4.4, differentiated).
+//
+// One call, in stream order:
+//   scans      bag offsets of the KJT; raw and clamped sequence offsets
+//   gather     per valid position: s (the three rows), x = [q, s, q-s, q*s]
+//   GEMM 1, 2  recompute h1 = ReLU(x W1^T + b1), h2 pre-activation = h1 W2^T
+//   softmax    per sample: z, a, da = ddin.s, dz = a (da - sum a da),
+//              dh2 = dz w3 [h2 > 0], ds = a ddin; dw3, db2, db3
+//   GEMM 3     dh1 pre-mask = dh2 W2;  mask [h1 > 0], db1
+//   GEMM 4..6  dx = dh1 W1;  dW1 = dh1^T x;  dW2 = dh2^T h1
+//   scatter    per sample: dq = sum_t (dx_q + dx_d + dx_p s_t), ds_t += dx_s -
+//              dx_d + dx_p q; row gradients: ds_t slices into the sequence
+//              rows, dpooled + dq slices into every value of the bags
+// The six GEMMs are plain library GEMMs (cuBLAS) over the valid positions,
+// sized by the sequence values' length (rows past the valid count are zero).
+// Row gradients are summed with vector fp32 atomics into caller-owned
+// per-table buffers; the first contribution to a row appends it to a list,
+// which the AdaGrad step walks.
+#include <cublas_v2.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "abi_checks.cuh"
+#include "dinsparse.h"
+#include "hash.cuh"
+
+namespace dsf {
+namespace bwd {
+namespace {
+
+constexpr size_t kCublasWs = size_t(32) << 20;
+constexpr int kRowBits = 40;
+constexpr int kWarpsPerBlock = 8;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t boff, soff, roff, samp, zb, dab, w1b, w2b, X, S, G1, H1, H2, dH2, dH1, dX, dS, cublas, total;
+};
+
+// Every buffer is sized for fp32 elements, so the layout does not depend on
+// the MLP mode.
+Layout layout(long long B, long long Pc, int F, int D) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  const size_t Q = 3 * size_t(D), K1 = 12 * size_t(D), P = size_t(Pc);
+  L.boff = take((size_t(F) * B + 1) * 8);
+  L.soff = take((size_t(B) + 1) * 8);
+  L.roff = take((size_t(B) + 1) * 8);
+  L.samp = take(P * 4);
+  L.zb = take(P * 4);
+  L.dab = take(P * 4);
+  L.w1b = take(size_t(kN1) * K1 * 2);
+  L.w2b = take(size_t(kN2) * kN1 * 2);
+  L.X = take(P * K1 * 4);
+  L.S = take(P * Q * 4);
+  L.G1 = take(P * kN1 * 4);
+  L.H1 = take(P * kN1 * 4);
+  L.H2 = take(P * kN2 * 4);
+  L.dH2 = take(P * kN2 * 4);
+  L.dH1 = take(P * kN1 * 4);
+  L.dX = take(P * K1 * 4);
+  L.dS = take(P * Q * 4);
+  L.cublas = take(kCublasWs);
+  L.total = o;
+  return L;
+}
+
+struct Params {
+  const void* tables[kMaxF];
+  long long rows[kMaxF];    // row count of the table's storage
+  long long glimit[kMaxF];  // rows that are parameters (the hash pool's zero row is not)
+  int sid[kMaxF];           // storage of table f (hash-table tables share one)
+  float* grad[kMaxF];       // by storage
+  int* touched[kMaxF];      // by storage
+  unsigned int hash_mask;
+  unsigned char kspace[kMaxF];
+  const unsigned long long* hkeys;
+  unsigned long long hbmask;
+  int F, B, D, max_len;
+  bool bf16_tables, bf16_mlp;
+  unsigned int mean_mask;
+  const long long* values;
+  long long n_values;
+  const long long* seq_values;
+  long long n_seq;
+  int q_feat[3], seq_table[3];
+  long long* list;
+  int* count;
+  long long list_cap;
+  int* status;
+};
+
+__device__ __forceinline__ long long rid(const Params& p, int f, long long id) {
+  return ((p.hash_mask >> f) & 1u) ? hash::find(p.hkeys, p.hbmask, p.kspace[f], id) : id;
+}
+
+__device__ __forceinline__ void flag(int* status, int bits) {
+  if (status && bits) atomicOr(status, bits);
+}
+
+// 16 table elements starting at element e of `row` (fp32 or bf16) as fp32
+__device__ __forceinline__ void load16(const Params& p, const void* base, long long row, int e, float* v) {
+  if (p.bf16_tables) {
+    const uint4* q = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + row * p.D + e);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 w = __ldg(q + h);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[h * 8 + 2 * i] = __uint_as_float(u[i] << 16);
+        v[h * 8 + 2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+      }
+    }
+  } else {
+    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * p.D + e);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float4 w = __ldg(q + h);
+      v[4 * h] = w.x;
+      v[4 * h + 1] = w.y;
+      v[4 * h + 2] = w.z;
+      v[4 * h + 3] = w.w;
+    }
+  }
+}
+
+// Adds a 4-element gradient piece (elements e..e+3) to row `row` of table f's
+// storage; the piece holding element 0 also records the row as touched.
+__device__ __forceinline__ int add_grad(const Params& p, int f, long long row, int e, float4 g) {
+  const int s = p.sid[f];
+  atomicAdd(reinterpret_cast<float4*>(p.grad[s] + row * p.D + e), g);
+  if (e != 0) return 0;
+  int* t = p.touched[s] + row;
+  if (*reinterpret_cast<volatile int*>(t) != 0 || atomicExch(t, 1) != 0) return 0;
+  const int i = atomicAdd(p.count, 1);
+  if (i < p.list_cap) {
+    p.list[i] = (static_cast<long long>(s) << kRowBits) | row;
+    return 0;
+  }
+  return DSF_FLAG_GRAD_LIST;
+}
+
+// ---------------------------------------------------------------- kernels
+// Exclusive scans of max(len, 0) (raw) and of min(max(len, 0), clamp)
+// (clamped, optional) over n entries; one block of 1024 threads, each owning
+// a contiguous run.
+__global__ void __launch_bounds__(1024) scan_kernel(const int* __restrict__ len, int n, int clamp, long long* raw,
+                                                    long long* clp) {
+  __shared__ long long ws[32], ws2[32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int per = (n + 1023) / 1024;
+  const int a = min(n, t * per), e = min(n, a + per);
+  long long s = 0, s2 = 0;
+  for (int i = a; i < e; ++i) {
+    const int v = max(len[i], 0);
+    s += v;
+    s2 += min(v, clamp);
+  }
+  long long x = s, x2 = s2;  // inclusive warp scans
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o), y2 = __shfl_up_sync(0xffffffffu, x2, o);
+    if (lane >= o) x += y, x2 += y2;
+  }
+  if (lane == 31) ws[w] = x, ws2[w] = x2;
+  __syncthreads();
+  if (w == 0) {
+    long long u = ws[lane], u2 = ws2[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, u, o), y2 = __shfl_up_sync(0xffffffffu, u2, o);
+      if (lane >= o) u += y, u2 += y2;
+    }
+    ws[lane] = u;
+    ws2[lane] = u2;
+  }
+  __syncthreads();
+  long long run = x - s + (w ? ws[w - 1] : 0), run2 = x2 - s2 + (w ? ws2[w - 1] : 0);
+  for (int i = a; i < e; ++i) {
+    raw[i] = run;
+    if (clp) clp[i] = run2;
+    const int v = max(len[i], 0);
+    run += v;
+    run2 += min(v, clamp);
+  }
+  if (t == 1023) {
+    raw[n] = ws[31];
+    if (clp) clp[n] = ws2[31];
+  }
+}
+
+__global__ void pack_kernel(const float* __restrict__ W1, const float* __restrict__ W2, int n1, int n2,
+                            __nv_bfloat16* w1b, __nv_bfloat16* w2b) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n1 + n2; i += gridDim.x * blockDim.x) {
+    if (i < n1) w1b[i] = __float2bfloat16_rn(W1[i]);
+    else w2b[i - n1] = __float2bfloat16_rn(W2[i - n1]);
+  }
+}
+
+template <class T>
+__device__ __forceinline__ void store4(T* dst, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b, float c, float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// One thread per position (rows past the valid count are zeroed): its
+// sample, s (fp32) and x = [q, s, q - s, q * s] (the MLP operand type).
+template <class T>
+__global__ void gather_kernel(const Params p, const float* __restrict__ pooled, const long long* __restrict__ soff,
+                              const long long* __restrict__ roff, int* samp, T* X, float* S, long long Pc) {
+  const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D;
+  const long long P = min(soff[p.B], Pc);
+  if (soff[p.B] > Pc && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, DSF_FLAG_COUNT);
+  int flags = 0;
+  for (long long pos = blockIdx.x * (long long)blockDim.x + threadIdx.x; pos < Pc;
+       pos += (long long)gridDim.x * blockDim.x) {
+    T* x = X + pos * K1;
+    if (pos >= P) {
+      for (int d = 0; d < K1; d += 4) store4<T>(x + d, 0.f, 0.f, 0.f, 0.f);
+      continue;
+    }
+    int lo = 0, hi = p.B - 1;  // the sample: the last b with soff[b] <= pos
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (soff[mid] <= pos) lo = mid;
+      else hi = mid - 1;
+    }
+    const int b = lo;
+    samp[pos] = b;
+    const long long j = roff[b] + (pos - soff[b]);
+    long long row[3];
+    bool ok[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int tb = p.seq_table[k];
+      long long id = -1;
+      if (j < p.n_seq) id = rid(p, tb, p.seq_values[k * p.n_seq + j]);
+      else flags |= DSF_FLAG_COUNT;
+      ok[k] = id >= 0 && id < p.rows[tb];
+      if (!ok[k] && j < p.n_seq) flags |= DSF_FLAG_ID_RANGE;
+      row[k] = ok[k] ? id : 0;
+    }
+    for (int c = 0; c < Q / 16; ++c) {
+      const int k = (c * 16) / D, e = (c * 16) % D;
+      float s[16], q[16];
+      if (ok[k]) load16(p, p.tables[p.seq_table[k]], row[k], e, s);
+      else
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[i] = 0.f;
+      const float4* qp = reinterpret_cast<const float4*>(pooled + (long long)b * FD + p.q_feat[k] * D + e);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float4 v = __ldg(qp + h);
+        q[4 * h] = v.x, q[4 * h + 1] = v.y, q[4 * h + 2] = v.z, q[4 * h + 3] = v.w;
+      }
+      float* sd = S + pos * Q + c * 16;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int i = 4 * h;
+        *reinterpret_cast<float4*>(sd + i) = make_float4(s[i], s[i + 1], s[i + 2], s[i + 3]);
+        store4<T>(x + c * 16 + i, q[i], q[i + 1], q[i + 2], q[i + 3]);
+        store4<T>(x + Q + c * 16 + i, s[i], s[i + 1], s[i + 2], s[i + 3]);
+        store4<T>(x + 2 * Q + c * 16 + i, q[i] - s[i], q[i + 1] - s[i + 1], q[i + 2] - s[i + 2], q[i + 3] - s[i + 3]);
+        store4<T>(x + 3 * Q + c * 16 + i, q[i] * s[i], q[i + 1] * s[i + 1], q[i + 2] * s[i + 2], q[i + 3] * s[i + 3]);
+      }
+    }
+  }
+  flag(p.status, flags);
+}
+
+// h1 = ReLU(G1 + b1) in the MLP operand type, over [Pc, 256].
+template <class T>
+__global__ void relu1_kernel(const float* __restrict__ G1, const float* __restrict__ b1, T* H1, long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const float4 g = reinterpret_cast<const float4*>(G1)[i];
+    const int c = int((i * 4) % kN1);
+    store4<T>(H1 + i * 4, fmaxf(g.x + b1[c], 0.f), fmaxf(g.y + b1[c + 1], 0.f), fmaxf(g.z + b1[c + 2], 0.f),
+              fmaxf(g.w + b1[c + 3], 0.f));
+  }
+}
+
+template <class T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <class T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp per sample: softmax and score backward over its positions.
+// Accumulates dw3, db2, db3; writes dH2 (zero past the valid rows) and dS.
+template <class T>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
+    const Params p, const long long* __restrict__ soff, const float* __restrict__ H2, const float* __restrict__ S,
+    const float* __restrict__ ddin, const float* __restrict__ b2, const float* __restrict__ w3,
+    const float* __restrict__ b3, float* zb, float* dab, T* dH2, float* dS, float* dw3, float* db2, float* db3,
+    long long Pc) {
+  __shared__ float red[kWarpsPerBlock][2 * kN2 + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Q = 3 * p.D;
+  const int b = blockIdx.x * kWarpsPerBlock + warp;
+  float acc_w3[2] = {0.f, 0.f}, acc_b2[2] = {0.f, 0.f}, acc_b3 = 0.f;
+  if (b < p.B) {
+    const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
+    const float w3a = w3[lane], w3b = w3[lane + 32], b2a = b2[lane], b2b = b2[lane + 32], bb3 = __ldg(b3);
+    const float* dd = ddin + (long long)b * Q;
+    float m = -INFINITY;
+    for (long long q = p0; q < p1; ++q) {
+      const float ha = fmaxf(H2[(long long)q * kN2 + lane] + b2a, 0.f),
+                  hb = fmaxf(H2[(long long)q * kN2 + lane + 32] + b2b, 0.f);
+      const float z = warp_sum(ha * w3a + hb * w3b) + bb3;
+      if (lane == 0) zb[q] = z;
+      m = fmaxf(m, z);
+    }
+    __syncwarp();
+    float l = 0.f, sda = 0.f;
+    for (long long q = p0; q < p1; ++q) {
+      float part = 0.f;
+      for (int d = lane; d < Q; d += 32) part += dd[d] * S[(long long)q * Q + d];
+      const float da = warp_sum(part);
+      const float e = expf(zb[q] - m);
+      l += e;
+      sda += e * da;
+      __syncwarp();
+      if (lane == 0) zb[q] = e, dab[q] = da;
+    }
+    __syncwarp();
+    const float c = p1 > p0 ? sda / l : 0.f;
+    for (long long q = p0; q < p1; ++q) {
+      const float a = zb[q] / l, dz = a * (dab[q] - c);
+      const float pa = H2[(long long)q * kN2 + lane] + b2a, pb = H2[(long long)q * kN2 + lane + 32] + b2b;
+      const float ga = pa > 0.f ? dz * w3a : 0.f, gb = pb > 0.f ? dz * w3b : 0.f;
+      dH2[(long long)q * kN2 + lane] = from_f<T>(ga);
+      dH2[(long long)q * kN2 + lane + 32] = from_f<T>(gb);
+      acc_w3[0] += dz * fmaxf(pa, 0.f);
+      acc_w3[1] += dz * fmaxf(pb, 0.f);
+      acc_b2[0] += ga;
+      acc_b2[1] += gb;
+      acc_b3 += dz;
+      for (int d = lane; d < Q; d += 32) dS[(long long)q * Q + d] = a * dd[d];
+    }
+  }
+  red[warp][lane] = acc_w3[0];
+  red[warp][lane + 32] = acc_w3[1];
+  red[warp][lane + 64] = acc_b2[0];
+  red[warp][lane + 96] = acc_b2[1];
+  if (lane == 0) red[warp][2 * kN2] = acc_b3;
+  __syncthreads();
+  for (int i = threadIdx.x; i <= 2 * kN2; i += blockDim.x) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerBlock; ++w) v += red[w][i];
+    if (i < kN2) atomicAdd(dw3 + i, v);
+    else if (i < 2 * kN2) atomicAdd(db2 + i - kN2, v);
+    else atomicAdd(db3, v);
+  }
+  // rows past the valid count: zero gradient
+  const long long P = min(soff[p.B], Pc);
+  for (long long i = P * kN2 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < Pc * kN2;
+       i += (long long)gridDim.x * blockDim.x)
+    dH2[i] = from_f<T>(0.f);
+}
+
+// dh1 = G (dh2 W2) * [h1 > 0], over [Pc, 256] with one column per thread;
+// db1 sums the masked values.
+template <class T>
+__global__ void __launch_bounds__(kN1) relu1_bwd_kernel(const float* __restrict__ G, const T* __restrict__ H1,
+                                                       T* dH1, float* db1, long long Pc) {
+  const int c = threadIdx.x;
+  float acc = 0.f;
+  for (long long r = blockIdx.x; r < Pc; r += gridDim.x) {
+    const long long i = r * kN1 + c;
+    const float v = to_f<T>(H1[i]) > 0.f ? G[i] : 0.f;
+    dH1[i] = from_f<T>(v);
+    acc += v;
+  }
+  atomicAdd(db1 + c, acc);
+}
+
+__device__ __forceinline__ float4 f4(const float* q) { return *reinterpret_cast<const float4*>(q); }
+__device__ __forceinline__ float4 operator+(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 operator-(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+__device__ __forceinline__ float4 operator*(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+__device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
+
+// One warp per sample: dq and the final ds of each position, then every row
+// gradient of the sample (sequence rows, then the values of its bags).
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
+    const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
+    const long long* __restrict__ roff, long long Pc,
+    const float* __restrict__ pooled, const float* __restrict__ dpooled, const float* __restrict__ dX,
+    const float* __restrict__ S, const float* __restrict__ dS) {
+  __shared__ float dqs[kWarpsPerBlock][3 * 64];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
+  const int b = blockIdx.x * kWarpsPerBlock + warp;
+  int flags = 0;
+  if (b < p.B) {
+    float4 dq[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
+    for (long long q = p0; q < p1; ++q) {
+      const long long j = roff[b] + (q - p0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c4 = lane + 32 * h;
+        if (c4 >= nc) continue;
+        const int d = 4 * c4, k = d / D, e = d % D;
+        const float* dx = dX + (long long)q * K1;
+        const float4 xq = f4(dx + d), xs = f4(dx + Q + d), xd = f4(dx + 2 * Q + d), xp = f4(dx + 3 * Q + d);
+        const float4 s4 = f4(S + (long long)q * Q + d);
+        const float4 q4 = f4(pooled + (long long)b * FD + p.q_feat[k] * D + e);
+        dq[h] = dq[h] + xq + xd + xp * s4;
+        const float4 ds = f4(dS + (long long)q * Q + d) + xs - xd + xp * q4;
+        const int tb = p.seq_table[k];
+        if (j < p.n_seq) {
+          const long long id = rid(p, tb, p.seq_values[k * p.n_seq + j]);
+          if (id >= 0 && id < p.glimit[tb]) flags |= add_grad(p, tb, id, e, ds);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c4 = lane + 32 * h;
+      if (c4 < nc) *reinterpret_cast<float4*>(&dqs[warp][4 * c4]) = dq[h];
+    }
+    __syncwarp();
+    // bags: one (feature, 4-element piece) per lane step
+    const int npieces = p.F * (D / 4);
+    for (int c = lane; c < npieces; c += 32) {
+      const int f = c / (D / 4), e = (c % (D / 4)) * 4;
+      float4 g = dpooled ? f4(dpooled + (long long)b * FD + f * D + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        if (p.q_feat[k] == f) g = g + *reinterpret_cast<const float4*>(&dqs[warp][k * D + e]);
+      const long long v0 = boff[(long long)f * p.B + b], v1 = boff[(long long)f * p.B + b + 1];
+      if (v1 <= v0) continue;
+      if ((p.mean_mask >> f) & 1u) g = scale4(g, 1.f / float(v1 - v0));
+      for (long long v = v0; v < v1; ++v) {
+        if (v >= p.n_values) {
+          flags |= DSF_FLAG_COUNT;
+          break;
+        }
+        const long long id = rid(p, f, p.values[v]);
+        if (id >= 0 && id < p.glimit[f]) flags |= add_grad(p, f, id, e, g);
+      }
+    }
+  }
+  flag(p.status, flags);
+}
+
+struct Upd {
+  void* table[kMaxF];
+  float* accum[kMaxF];
+  float* grad[kMaxF];
+  int* touched[kMaxF];
+  const long long* list;
+  const int* count;
+  long long cap;
+  int D;
+  float lr, eps;
+};
+
+// AdaGrad over the touched rows (4 elements per thread), then the row's
+// gradient and touched flag are cleared.
+template <bool BF16>
+__global__ void update_kernel(const Upd u) {
+  const long long n = min((long long)*u.count, u.cap);
+  const int pieces = u.D / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n * pieces;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long ent = u.list[i / pieces];
+    const int s = int(ent >> kRowBits), e = int(i % pieces) * 4;
+    const long long row = ent & ((1ll << kRowBits) - 1);
+    float* gp = u.grad[s] + row * u.D + e;
+    float* Gp = u.accum[s] + row * u.D + e;
+    const float4 g = *reinterpret_cast<float4*>(gp);
+    float4 G = *reinterpret_cast<float4*>(Gp);
+    G.x += g.x * g.x, G.y += g.y * g.y, G.z += g.z * g.z, G.w += g.w * g.w;
+    *reinterpret_cast<float4*>(Gp) = G;
+    const float dw[4] = {u.lr * g.x / (sqrtf(G.x) + u.eps), u.lr * g.y / (sqrtf(G.y) + u.eps),
+                         u.lr * g.z / (sqrtf(G.z) + u.eps), u.lr * g.w / (sqrtf(G.w) + u.eps)};
+    if (BF16) {
+      __nv_bfloat16* w = static_cast<__nv_bfloat16*>(u.table[s]) + row * u.D + e;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[k] = __float2bfloat16_rn(__bfloat162float(w[k]) - dw[k]);
+    } else {
+      float4* w = reinterpret_cast<float4*>(static_cast<float*>(u.table[s]) + row * u.D + e);
+      float4 v = *w;
+      v.x -= dw[0], v.y -= dw[1], v.z -= dw[2], v.w -= dw[3];
+      *w = v;
+    }
+    *reinterpret_cast<float4*>(gp) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e == 0) u.touched[s][row] = 0;
+  }
+}
+
+__global__ void reset_count_kernel(int* count) { *count = 0; }
+
+// ---------------------------------------------------------------- host
+cublasHandle_t handle_for(int dev) {
+  static std::mutex mu;
+  static cublasHandle_t h[64] = {};
+  std::lock_guard<std::mutex> g(mu);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!h[dev] && cublasCreate(&h[dev]) != CUBLAS_STATUS_SUCCESS) h[dev] = nullptr;
+  return h[dev];
+}
+std::mutex& call_mutex() {
+  static std::mutex m;
+  return m;
+}
+
+// Row-major C[M, N] = op(A) op(B) (fp32 output), A, B row-major with leading
+// dimensions lda, ldb: the column-major product C^T = op(B)^T op(A)^T.
+bool gemm_rm(cublasHandle_t h, bool ta, bool tb, long long M, long long N, long long K, const void* A, long long lda,
+             const void* B, long long ldb, float* C, long long ldc, bool bf16) {
+  const float alpha = 1.f, beta = 0.f;
+  const cudaDataType_t it = bf16 ? CUDA_R_16BF : CUDA_R_32F;
+  return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, int(N), int(M), int(K),
+                      &alpha, B, it, int(ldb), A, it, int(lda), &beta, C, CUDA_R_32F, int(ldc), CUBLAS_COMPUTE_32F,
+                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+}
+
+int grid_for(long long n, int threads, int cap = 152 * 16) {
+  long long g = (n + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return int(g);
+}
+
+// Storage of table f: hash-table tables share the first such table's index.
+int storage_of(const dsf_tables* t, int f) {
+  if (!hashed(t, f)) return f;
+  for (int g = 0; g < t->F; ++g)
+    if (hashed(t, g)) return g;
+  return f;
+}
+
+int check_row_state(const dsf_tables* t, float* const* grad, int32_t* const* touched) {
+  for (int f = 0; f < t->F; ++f) {
+    const int s = storage_of(t, f);
+    if (!grad[f] || !aligned(grad[f], 16) || (touched && !touched[f])) return DSF_EINVAL;
+    if (s != f && (grad[f] != grad[s] || (touched && touched[f] != touched[s]))) return DSF_EINVAL;
+  }
+  return DSF_OK;
+}
+
+void fill_tables(Params& p, const dsf_tables* t) {
+  hash::Layout L{};
+  uint8_t* hw = nullptr;
+  if (t->hash) {
+    L = hash::layout(t->hash->capacity, t->hash->D, t->dtype == DSF_BF16 ? 2 : 4);
+    hw = static_cast<uint8_t*>(t->hash->workspace);
+    p.hkeys = reinterpret_cast<const unsigned long long*>(hw + L.keys_off);
+    p.hbmask = L.n_buckets - 1;
+  }
+  for (int f = 0; f < t->F; ++f) {
+    if (hashed(t, f)) {
+      p.tables[f] = hw + L.pool_off;
+      p.rows[f] = static_cast<long long>(L.n_slots) + 1;
+      p.glimit[f] = static_cast<long long>(L.n_slots);
+      p.hash_mask |= 1u << f;
+      p.kspace[f] = static_cast<unsigned char>(t->hash->key_space[f]);
+    } else {
+      p.tables[f] = t->table_ptrs[f];
+      p.rows[f] = p.glimit[f] = t->table_rows[f];
+    }
+    p.sid[f] = storage_of(t, f);
+    if (t->pooling && t->pooling[f] == DSF_POOL_MEAN) p.mean_mask |= 1u << f;
+  }
+  p.F = t->F;
+  p.D = t->D;
+  p.bf16_tables = t->dtype == DSF_BF16;
+}
+
+}  // namespace
+}  // namespace bwd
+}  // namespace dsf
+
+using namespace dsf;
+using namespace dsf::bwd;
+
+extern "C" size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_per_key, int32_t D) {
+  if (B < 0 || n_per_key < 0 || n_per_key > INT32_MAX || (D != 16 && D != 64)) return 0;
+  return bwd::layout(B, n_per_key, kMaxF, D).total;
+}
+
+extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq, const int32_t* q_feat,
+                              const int32_t* seq_table, int32_t B, const dsf_mlp* mlp, const float* pooled_dev,
+                              const float* dpooled_dev, const float* ddin_dev, const dsf_mlp_grads* mg,
+                              const dsf_row_grads* rg, void* workspace_dev, size_t ws_bytes, int32_t* status_dev,
+                              void* stream) {
+  int rc;
+  if ((rc = check_tables(tables)) != DSF_OK) return rc;
+  if (B < 0 || B > (1 << 24)) return DSF_EINVAL;
+  if ((rc = check_kjt(kjt, B, tables->F)) != DSF_OK) return rc;
+  if ((rc = check_seq(seq, B)) != DSF_OK) return rc;
+  if ((rc = check_mlp(mlp, tables->D)) != DSF_OK) return rc;
+  if (!q_feat || !seq_table) return DSF_EINVAL;
+  for (int k = 0; k < 3; ++k)
+    if (q_feat[k] < 0 || q_feat[k] >= tables->F || seq_table[k] < 0 || seq_table[k] >= tables->F) return DSF_EINVAL;
+  if (!pooled_dev || !ddin_dev || !aligned(pooled_dev, 16) || !aligned(ddin_dev, 16)) return DSF_EINVAL;
+  if (dpooled_dev && !aligned(dpooled_dev, 16)) return DSF_EINVAL;
+  if (!mg || !mg->dW1 || !mg->db1 || !mg->dW2 || !mg->db2 || !mg->dw3 || !mg->db3) return DSF_EINVAL;
+  if (!rg || !rg->grad || !rg->touched || !rg->list || !rg->count || rg->list_cap < 0) return DSF_EINVAL;
+  if ((rc = check_row_state(tables, rg->grad, rg->touched)) != DSF_OK) return rc;
+  const long long Pc = seq->n_per_key;
+  const bwd::Layout L = bwd::layout(B, Pc, kMaxF, tables->D);
+  if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < L.total) return DSF_EWORKSPACE;
+  if (B == 0) return DSF_OK;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSF_ECUDA;
+  cublasHandle_t h = handle_for(dev);
+  if (!h) return DSF_ECUDA;
+  std::lock_guard<std::mutex> lock(call_mutex());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace_dev);
+  const int D = tables->D, F = tables->F, K1 = 12 * D;
+  const bool bf = mlp->mode == DSF_MODE_BF16_TC;
+
+  Params p{};
+  fill_tables(p, tables);
+  p.B = B;
+  p.max_len = seq->max_len;
+  p.values = reinterpret_cast<const long long*>(kjt->values_dev);
+  p.n_values = kjt->n_values;
+  p.seq_values = reinterpret_cast<const long long*>(seq->values_dev);
+  p.n_seq = seq->n_per_key;
+  for (int k = 0; k < 3; ++k) p.q_feat[k] = q_feat[k], p.seq_table[k] = seq_table[k];
+  p.bf16_mlp = bf;
+  for (int f = 0; f < F; ++f) {
+    p.grad[f] = rg->grad[f];
+    p.touched[f] = rg->touched[f];
+  }
+  p.list = reinterpret_cast<long long*>(rg->list);
+  p.count = rg->count;
+  p.list_cap = rg->list_cap;
+  p.status = status_dev;
+
+  long long* boff = reinterpret_cast<long long*>(w + L.boff);
+  long long* soff = reinterpret_cast<long long*>(w + L.soff);
+  long long* roff = reinterpret_cast<long long*>(w + L.roff);
+  int* samp = reinterpret_cast<int*>(w + L.samp);
+  float* zb = reinterpret_cast<float*>(w + L.zb);
+  float* dab = reinterpret_cast<float*>(w + L.dab);
+  float* S = reinterpret_cast<float*>(w + L.S);
+  float* G1 = reinterpret_cast<float*>(w + L.G1);
+  float* H2 = reinterpret_cast<float*>(w + L.H2);
+  float* dX = reinterpret_cast<float*>(w + L.dX);
+  float* dS = reinterpret_cast<float*>(w + L.dS);
+  void* X = w + L.X;
+  void* H1 = w + L.H1;
+  void* dH2 = w + L.dH2;
+  void* dH1 = w + L.dH1;
+  const void* W1 = mlp->W1;
+  const void* W2 = mlp->W2;
+
+  if (cudaMemsetAsync(mg->db1, 0, kN1 * 4, s) != cudaSuccess || cudaMemsetAsync(mg->db2, 0, kN2 * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(mg->dw3, 0, kN2 * 4, s) != cudaSuccess || cudaMemsetAsync(mg->db3, 0, 4, s) != cudaSuccess)
+    return DSF_ECUDA;
+  scan_kernel<<<1, 1024, 0, s>>>(kjt->lengths_dev, F * B, INT_MAX, boff, nullptr);
+  scan_kernel<<<1, 1024, 0, s>>>(seq->lengths_dev, B, seq->max_len, roff, soff);
+  if (bf) {
+    pack_kernel<<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
+        mlp->W1, mlp->W2, kN1 * K1, kN2 * kN1, reinterpret_cast<__nv_bfloat16*>(w + L.w1b),
+        reinterpret_cast<__nv_bfloat16*>(w + L.w2b));
+    W1 = w + L.w1b;
+    W2 = w + L.w2b;
+  }
+  if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
+  if (Pc > 0) {
+    if (bf)
+      gather_kernel<__nv_bfloat16><<<grid_for(Pc, 256), 256, 0, s>>>(p, pooled_dev, soff, roff, samp,
+                                                                     static_cast<__nv_bfloat16*>(X), S, Pc);
+    else
+      gather_kernel<float><<<grid_for(Pc, 256), 256, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
+                                                             S, Pc);
+    if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
+    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
+        cublasSetWorkspace(h, w + L.cublas, kCublasWs) != CUBLAS_STATUS_SUCCESS)
+      return DSF_ECUDA;
+    // recompute: h1 = ReLU(x W1^T + b1), then the layer-2 pre-activation
+    if (!gemm_rm(h, false, true, Pc, kN1, K1, X, K1, W1, K1, G1, kN1, bf)) return DSF_ECUDA;
+    if (bf)
+      relu1_kernel<__nv_bfloat16><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1,
+                                                                               static_cast<__nv_bfloat16*>(H1), Pc * kN1 / 4);
+    else
+      relu1_kernel<float><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1, static_cast<float*>(H1), Pc * kN1 / 4);
+    if (!gemm_rm(h, false, true, Pc, kN2, kN1, H1, kN1, W2, kN1, H2, kN2, bf)) return DSF_ECUDA;
+  }
+  const int sb = (B + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  if (bf)
+    softmax_bwd_kernel<__nv_bfloat16><<<sb, kWarpsPerBlock * 32, 0, s>>>(
+        p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3, zb, dab, static_cast<__nv_bfloat16*>(dH2), dS, mg->dw3,
+        mg->db2, mg->db3, Pc);
+  else
+    softmax_bwd_kernel<float><<<sb, kWarpsPerBlock * 32, 0, s>>>(p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3,
+                                                                 zb, dab, static_cast<float*>(dH2), dS, mg->dw3,
+                                                                 mg->db2, mg->db3, Pc);
+  if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
+  if (Pc > 0) {
+    if (!gemm_rm(h, false, false, Pc, kN1, kN2, dH2, kN2, W2, kN1, G1, kN1, bf)) return DSF_ECUDA;
+    const int rb = grid_for(Pc, 1, 152 * 8);
+    if (bf)
+      relu1_bwd_kernel<__nv_bfloat16><<<rb, kN1, 0, s>>>(G1, static_cast<const __nv_bfloat16*>(H1),
+                                                          static_cast<__nv_bfloat16*>(dH1), mg->db1, Pc);
+    else
+      relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), mg->db1,
+                                                 Pc);
+    if (!gemm_rm(h, false, false, Pc, K1, kN1, dH1, kN1, W1, K1, dX, K1, bf)) return DSF_ECUDA;
+    if (!gemm_rm(h, true, false, kN1, K1, Pc, dH1, kN1, X, K1, mg->dW1, K1, bf)) return DSF_ECUDA;
+    if (!gemm_rm(h, true, false, kN2, kN1, Pc, dH2, kN2, H1, kN1, mg->dW2, kN1, bf)) return DSF_ECUDA;
+  } else {
+    if (cudaMemsetAsync(mg->dW1, 0, size_t(kN1) * K1 * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess)
+      return DSF_ECUDA;
+  }
+  scatter_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS);
+  return cudaGetLastError() == cudaSuccess ? DSF_OK : DSF_ECUDA;
+}
+
+extern "C" int emb_adagrad_update(const dsf_tables* tables, float* const* accum, const dsf_row_grads* rg, float lr,
+                                  float eps, int32_t* status_dev, void* stream) {
+  int rc;
+  if ((rc = check_tables(tables)) != DSF_OK) return rc;
+  if (!accum || !rg || !rg->grad || !rg->touched || !rg->list || !rg->count || rg->list_cap < 0) return DSF_EINVAL;
+  if (!(lr >= 0.f) || !(eps >= 0.f)) return DSF_EINVAL;
+  if ((rc = check_row_state(tables, rg->grad, rg->touched)) != DSF_OK) return rc;
+  if ((rc = check_row_state(tables, accum, nullptr)) != DSF_OK) return rc;
+  Params p{};
+  fill_tables(p, tables);
+  Upd u{};
+  for (int f = 0; f < tables->F; ++f) {
+    u.table[f] = const_cast<void*>(p.tables[f]);
+    u.accum[f] = accum[f];
+    u.grad[f] = rg->grad[f];
+    u.touched[f] = rg->touched[f];
+  }
+  u.list = reinterpret_cast<const long long*>(rg->list);
+  u.count = rg->count;
+  u.cap = rg->list_cap;
+  u.D = tables->D;
+  u.lr = lr;
+  u.eps = eps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the grid covers the largest possible list; threads past the count exit
+  const int g = grid_for(rg->list_cap * (tables->D / 4), 256, 152 * 8);
+  if (tables->dtype == DSF_BF16) update_kernel<true><<<g, 256, 0, s>>>(u);
+  else update_kernel<false><<<g, 256, 0, s>>>(u);
+  reset_count_kernel<<<1, 1, 0, s>>>(rg->count);
+  (void)status_dev;
+  return cudaGetLastError() == cudaSuccess ? DSF_OK : DSF_ECUDA;
+}

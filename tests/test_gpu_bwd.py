@@ -1,0 +1,227 @@
+"""The backward of the sparse path and the sparse AdaGrad step on the GPU,
+through the C ABI, against the backward oracle.
+
+Weight gradients are sums over positions of terms that largely cancel (per
+sample the dz_t sum to zero), so each entry is held to a multiple of the sum
+of its terms' magnitudes (the oracle returns those sums): fp32 mode against
+the fp64 oracle; the bf16 mode against the oracle with the same bf16 operand
+roundings. Row gradients are summed by fp32 atomics in varying order and are
+held to a multiple of the sum of their contributions' magnitudes. The set of
+touched rows is compared exactly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import backward as obw
+from recsys_sparse_embedding_gb300 import binding, synth
+
+from helpers import GpuRun
+from test_gpu_parity import F32, TC, _custom_batch
+
+pytestmark = pytest.mark.gpu
+
+# entrywise factors of the magnitude sums. fp32: every entry. bf16 against
+# the oracle with the same operand roundings: the median and the 99th
+# percentile sit at accumulation-order size; the maximum allows a ReLU whose
+# input fp32-vs-fp64 accumulation moved across zero (one term of the entry).
+TOL_F32 = 2.0 ** -13
+TOL_BF16_MEDIAN = 2.0 ** -12
+TOL_BF16_P99 = 2.0 ** -8
+TOL_BF16_MAX = 2.0 ** -2
+
+
+class Bwd:
+    """One forward + backward of a batch on the device."""
+
+    def __init__(self, batch, mode, seed=0, list_cap=None, with_dpooled=True):
+        self.batch, self.mode = batch, mode
+        run = GpuRun(batch)
+        pooled, _, _, st = run.fwd(mode, logits=False)
+        assert st & ~binding.FLAG_SEQ_TRUNC == 0
+        self.run, self.db = run, run.db
+        db = run.db
+        rng = np.random.default_rng(seed)
+        B, F, D = batch.B, batch.F, batch.D
+        self.dpooled = rng.standard_normal((B, F * D)).astype(np.float32) if with_dpooled else None
+        self.ddin = rng.standard_normal((B, 3 * D)).astype(np.float32)
+        self.pooled = pooled
+        n_seq = int(db.seq_values.shape[-1])
+        cap = list_cap if list_cap is not None else int(db.values.numel()) + 3 * n_seq
+        self.grads = binding.MlpGrads(D)
+        self.state = binding.SparseState(db.tables, cap)
+        self.ws = binding.BwdWorkspace(B, n_seq, D)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.pooled_t = torch.from_numpy(pooled).cuda()
+        self.dp_t = None if self.dpooled is None else torch.from_numpy(self.dpooled).cuda()
+        self.dd_t = torch.from_numpy(self.ddin).cuda()
+
+    def backward(self):
+        db = self.db
+        self.status.zero_()
+        binding.din_sparse_bwd(db.tables, db.values, db.lengths, db.seq_values, db.seq_lengths, db.max_len,
+                               db.q_feat, db.seq_table, self.batch.B, db.mlp(self.mode), self.pooled_t, self.dp_t,
+                               self.dd_t, self.grads, self.state, self.ws, status=self.status)
+        torch.cuda.synchronize()
+        return int(self.status.item())
+
+    def oracle(self, bf16):
+        return obw.backward(self.batch, self.dpooled, self.ddin, bf16=bf16, pooled=self.pooled)
+
+    def storage_rows(self, f, rows):
+        """Storage rows of table f's oracle rows (hash-table tables: the slots
+        of their admitted keys)."""
+        hk = getattr(self.batch, "hash_keys", None) or {}
+        if f not in hk:
+            return rows
+        ht = self.db.tables.hash
+        keys = torch.from_numpy(np.ascontiguousarray(hk[f][rows], np.int64)).cuda()
+        return ht.find(f, keys).cpu().numpy()
+
+
+def check_ratios(err, m, bf16, what):
+    """err within the tolerance's multiple of the magnitude sums m; returns the
+    largest ratio."""
+    assert (err[m == 0] == 0).all(), what + ": an entry with no terms is not zero"
+    r = (err / np.maximum(m, 1e-300))[m > 0]
+    if r.size == 0:
+        return 0.0
+    if not bf16:
+        assert r.max() <= TOL_F32, "%s: max ratio %.3e" % (what, r.max())
+    else:
+        assert np.median(r) <= TOL_BF16_MEDIAN and np.percentile(r, 99) <= TOL_BF16_P99 and \
+            r.max() <= TOL_BF16_MAX, "%s: ratios median %.3e p99 %.3e max %.3e" % (
+                what, np.median(r), np.percentile(r, 99), r.max())
+    return float(r.max())
+
+
+def check_dense(g, ref, bf16):
+    out = {}
+    for k in ("dW1", "db1", "dW2", "db2", "dw3", "db3"):
+        got = g[k].cpu().numpy().astype(np.float64).reshape(ref[k].shape)
+        out[k] = check_ratios(np.abs(got - ref[k]), ref["bounds"][k], bf16, k)
+    return out
+
+
+def check_rows(bw, ref, bf16):
+    """Row gradients against the oracle's; returns the expected touched set."""
+    st = bw.state
+    F = bw.batch.F
+    expect = set()
+    worst = 0.0
+    for f, (rows, grads) in ref["rows"].items():
+        srow = bw.storage_rows(f, rows)
+        sid = next(g for g in range(F) if st.grad[g].data_ptr() == st.grad[f].data_ptr())
+        got = st.grad[f][torch.from_numpy(srow).cuda()].cpu().numpy().astype(np.float64)
+        worst = max(worst, check_ratios(np.abs(got - grads), ref["rows_abs"][f], bf16, "table %d rows" % f))
+        expect |= {(sid << 40) | int(r) for r in srow}
+    n = int(st.count.item())
+    listed = set(st.list[:n].cpu().numpy().tolist())
+    assert n == len(expect) and listed == expect
+    return worst
+
+
+def run_case(batch, modes=(F32, TC), seed=0):
+    for mode in modes:
+        bw = Bwd(batch, mode, seed)
+        assert bw.backward() == 0
+        bf16 = mode == TC
+        ref = bw.oracle(bf16)
+        d = check_dense(bw.grads, ref, bf16)
+        r = check_rows(bw, ref, bf16)
+        print("%s: dense max ratios %s; rows max ratio %.3e" % ("bf16" if bf16 else "fp32",
+                                                                  {k: "%.1e" % v for k, v in d.items()}, r))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tiny_backward(seed):
+    run_case(synth.generate("tiny", seed=seed, nonzero_bias=True), seed=seed)
+
+
+def test_backward_small_batches_of_full_workloads():
+    run_case(synth.generate("taobao", seed=1, B=1000, nonzero_bias=True), seed=1)
+    run_case(synth.generate("long_multihot", seed=1, B=600, nonzero_bias=True), seed=2)
+
+
+def test_backward_taobao_full_size():
+    run_case(synth.generate("taobao", seed=0), modes=(TC,), seed=3)
+
+
+def test_backward_mean_pooling_and_long_bags():
+    rng = np.random.default_rng(4)
+    lens = rng.integers(0, 12, size=(16, 200)).astype(np.int32)
+    c = _custom_batch(list(rng.integers(0, 120, size=200)), bags_len=lens, seed=4)
+    c.pooling = tuple(1 if f in (1, 3, 5) else 0 for f in range(16))
+    run_case(c, seed=4)
+
+
+def test_backward_edges():
+    run_case(_custom_batch([0, 0, 0]), seed=5)            # no positions at all
+    run_case(_custom_batch([7]), seed=6)                  # one sample
+    run_case(_custom_batch([250, 3, 130, 0], max_len=100), seed=7)   # truncated sequences
+
+
+def test_backward_hashed_tables():
+    b = synth.dynamic_emb(synth.generate("taobao", seed=2, B=800, nonzero_bias=True), seed=2)
+    run_case(b, seed=8)
+    t = synth.dynamic_emb(synth.generate("tiny", seed=3, nonzero_bias=True), capacity=600, seed=3)
+    run_case(t, seed=9)
+
+
+def test_backward_without_dpooled():
+    b = synth.generate("tiny", seed=7, nonzero_bias=True)
+    bw = Bwd(b, F32, seed=10, with_dpooled=False)
+    assert bw.backward() == 0
+    ref = bw.oracle(False)
+    check_dense(bw.grads, ref, False)
+    check_rows(bw, ref, False)
+
+
+def test_list_overflow_is_flagged():
+    b = synth.generate("tiny", seed=8, nonzero_bias=True)
+    bw = Bwd(b, F32, seed=11, list_cap=10)
+    assert bw.backward() & binding.FLAG_GRAD_LIST
+
+
+def test_adagrad_step_and_state_reset():
+    """Two training steps: each backward's row gradients, AdaGrad applied to
+    exactly the touched rows (checked against the update formula on the
+    kernel's own gradients), and the gradient state zero again afterwards."""
+    b = synth.generate("tiny", seed=9, nonzero_bias=True)
+    bw = Bwd(b, TC, seed=12)
+    st = bw.state
+    tabs = bw.db.tables.tables
+    lr, eps = 0.05, 1e-10
+    for step in range(2):
+        assert bw.backward() == 0
+        n = int(st.count.item())
+        ent = st.list[:n].cpu().numpy()
+        sid, rows = ent >> 40, ent & ((1 << 40) - 1)
+        before = {}
+        for s in np.unique(sid):
+            r = rows[sid == s]
+            rt = torch.from_numpy(r).cuda()
+            before[int(s)] = (r, st.grad[s][rt].cpu().numpy().astype(np.float64),
+                              tabs[s][rt].cpu().numpy().astype(np.float64), st.accum[s][rt].cpu().numpy())
+        w_all = [t.clone() for t in tabs]
+        binding.emb_adagrad_update(bw.db.tables, st, lr=lr, eps=eps)
+        torch.cuda.synchronize()
+        for s, (r, g, w, G) in before.items():
+            w_ref, G_ref = obw.adagrad(w, G, np.arange(r.size), g, lr=lr, eps=eps)
+            rt = torch.from_numpy(r).cuda()
+            w_new = tabs[s][rt].cpu().numpy().astype(np.float64)
+            G_new = st.accum[s][rt].cpu().numpy().astype(np.float64)
+            # fp32 against fp64: a few units of the last place of G, and of
+            # the weight and its step (about lr on the first step, G starting at 0)
+            assert (np.abs(G_new - G_ref) <= 2.0 ** -21 * G_ref).all()
+            assert (np.abs(w_new - w_ref) <= 2.0 ** -20 * (np.abs(w) + lr)).all()
+            untouched = torch.ones(tabs[s].shape[0], dtype=torch.bool, device="cuda")
+            untouched[rt] = False
+            assert torch.equal(tabs[s][untouched], w_all[s][untouched])
+        assert int(st.count.item()) == 0
+        for s in range(len(st.grad)):
+            assert not st.grad[s].any() and not st.touched[s].any()
+        # the next step's forward reads the updated tables
+        pooled, _, _, _ = bw.run.fwd(TC, logits=False)
+        bw.pooled = pooled
+        bw.pooled_t = torch.from_numpy(pooled).cuda()
