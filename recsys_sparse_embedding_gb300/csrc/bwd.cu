@@ -37,11 +37,16 @@ namespace {
 constexpr size_t kCublasWs = size_t(32) << 20;
 constexpr int kRowBits = 40;
 constexpr int kWarpsPerBlock = 8;
+constexpr int kScanThreads = 256, kScanRounds = 8, kScanTile = kScanThreads * kScanRounds;
+constexpr int kMaxBlocks = 152 * 8;  // grid cap of the grid-stride kernels (their partial sums)
+constexpr int kRedCols = 2 * 64 + 1;  // dw3 | db2 | db3 partials of the softmax kernel
+
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t boff, soff, roff, samp, zb, dab, w1b, w2b, X, S, G1, H1, H2, dH2, dH1, dX, dS, cublas, total;
+  size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, w1b, w2b, X, S, G1, H1, H2, dH2, dH1, dX, dS, cublas,
+      total;
 };
 
 // Every buffer is sized for fp32 elements, so the layout does not depend on
@@ -58,9 +63,12 @@ Layout layout(long long B, long long Pc, int F, int D) {
   L.boff = take((size_t(F) * B + 1) * 8);
   L.soff = take((size_t(B) + 1) * 8);
   L.roff = take((size_t(B) + 1) * 8);
+  L.tsum = take(4 * ((size_t(F) * B) / kScanTile + 2) * 8);
   L.samp = take(P * 4);
   L.zb = take(P * 4);
   L.dab = take(P * 4);
+  L.part1 = take(size_t(kMaxBlocks) * kRedCols * 4);
+  L.part2 = take(size_t(kMaxBlocks) * kN1 * 4);
   L.w1b = take(size_t(kN1) * K1 * 2);
   L.w2b = take(size_t(kN2) * kN1 * 2);
   L.X = take(P * K1 * 4);
@@ -139,13 +147,33 @@ __device__ __forceinline__ void load16(const Params& p, const void* base, long l
 
 // Adds a 4-element gradient piece (elements e..e+3) to row `row` of table f's
 // storage; the piece holding element 0 also records the row as touched.
-__device__ __forceinline__ int add_grad(const Params& p, int f, long long row, int e, float4 g) {
+// Adds a 4-element gradient piece (elements e..e+3) to row `row` of table f's
+// storage (a vector reduction: no value comes back).
+__device__ __forceinline__ void add_grad(const Params& p, int f, long long row, int e, float4 g) {
+  float* dst = p.grad[p.sid[f]] + row * p.D + e;
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(g.x), "f"(g.y), "f"(g.z), "f"(g.w)
+               : "memory");
+}
+
+// Records row `row` of table f's storage as touched (valid: the row is a
+// parameter). The lanes that are first to touch a row reserve their list
+// entries with one atomic per warp.
+__device__ __forceinline__ int mark_row(const Params& p, int f, long long row, bool valid) {
   const int s = p.sid[f];
-  atomicAdd(reinterpret_cast<float4*>(p.grad[s] + row * p.D + e), g);
-  if (e != 0) return 0;
-  int* t = p.touched[s] + row;
-  if (*reinterpret_cast<volatile int*>(t) != 0 || atomicExch(t, 1) != 0) return 0;
-  const int i = atomicAdd(p.count, 1);
+  bool first = false;
+  if (valid) {
+    int* t = p.touched[s] + row;
+    first = *reinterpret_cast<volatile int*>(t) == 0 && atomicExch(t, 1) == 0;
+  }
+  const unsigned act = __activemask();
+  const unsigned want = __ballot_sync(act, first);
+  if (!want) return 0;
+  const int lane = threadIdx.x & 31, leader = __ffs(want) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(p.count, __popc(want));
+  base = __shfl_sync(act, base, leader);
+  if (!first) return 0;
+  const int i = base + __popc(want & ((1u << lane) - 1u));
   if (i < p.list_cap) {
     p.list[i] = (static_cast<long long>(s) << kRowBits) | row;
     return 0;
@@ -154,51 +182,95 @@ __device__ __forceinline__ int add_grad(const Params& p, int f, long long row, i
 }
 
 // ---------------------------------------------------------------- kernels
-// Exclusive scans of max(len, 0) (raw) and of min(max(len, 0), clamp)
-// (clamped, optional) over n entries; one block of 1024 threads, each owning
-// a contiguous run.
-__global__ void __launch_bounds__(1024) scan_kernel(const int* __restrict__ len, int n, int clamp, long long* raw,
-                                                    long long* clp) {
-  __shared__ long long ws[32], ws2[32];
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int per = (n + 1023) / 1024;
-  const int a = min(n, t * per), e = min(n, a + per);
-  long long s = 0, s2 = 0;
-  for (int i = a; i < e; ++i) {
-    const int v = max(len[i], 0);
-    s += v;
-    s2 += min(v, clamp);
-  }
-  long long x = s, x2 = s2;  // inclusive warp scans
+// Block-wide inclusive scan of two 64-bit values (256 threads); returns the
+// block totals through the references.
+__device__ __forceinline__ void block_scan2(long long& a, long long& b, long long& ta, long long& tb) {
+  __shared__ long long wa[kScanThreads / 32], wb[kScanThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, o), y2 = __shfl_up_sync(0xffffffffu, x2, o);
-    if (lane >= o) x += y, x2 += y2;
+    const long long ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+    if (lane >= o) a += ya, b += yb;
   }
-  if (lane == 31) ws[w] = x, ws2[w] = x2;
+  if (lane == 31) wa[w] = a, wb[w] = b;
   __syncthreads();
-  if (w == 0) {
-    long long u = ws[lane], u2 = ws2[lane];
+  long long pa = 0, pb = 0;
+  ta = tb = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, u, o), y2 = __shfl_up_sync(0xffffffffu, u2, o);
-      if (lane >= o) u += y, u2 += y2;
-    }
-    ws[lane] = u;
-    ws2[lane] = u2;
+  for (int i = 0; i < kScanThreads / 32; ++i) {
+    if (i < w) pa += wa[i], pb += wb[i];
+    ta += wa[i], tb += wb[i];
   }
+  a += pa;
+  b += pb;
   __syncthreads();
-  long long run = x - s + (w ? ws[w - 1] : 0), run2 = x2 - s2 + (w ? ws2[w - 1] : 0);
-  for (int i = a; i < e; ++i) {
-    raw[i] = run;
-    if (clp) clp[i] = run2;
-    const int v = max(len[i], 0);
-    run += v;
-    run2 += min(v, clamp);
+}
+
+// Pass 1 of the exclusive scans of max(len, 0) (raw) and min(max(len, 0),
+// clamp): the sums of each 2048-entry tile (coalesced loads).
+__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(const int* __restrict__ len, int n, int clamp,
+                                                                 long long* tsum) {
+  long long a = 0, b = 0;
+  for (int r = 0; r < kScanRounds; ++r) {
+    const long long k = (long long)blockIdx.x * kScanTile + r * kScanThreads + threadIdx.x;
+    if (k < n) {
+      const int v = max(len[k], 0);
+      a += v;
+      b += min(v, clamp);
+    }
   }
-  if (t == 1023) {
-    raw[n] = ws[31];
-    if (clp) clp[n] = ws2[31];
+  long long ta, tb;
+  block_scan2(a, b, ta, tb);
+  if (threadIdx.x == 0) tsum[2 * blockIdx.x] = ta, tsum[2 * blockIdx.x + 1] = tb;
+}
+
+// Pass 2: each tile adds the sums of the tiles before it and scans its own
+// entries; the last tile writes the totals at index n.
+__global__ void __launch_bounds__(kScanThreads) scan_apply_kernel(const int* __restrict__ len, int n, int clamp,
+                                                                 const long long* __restrict__ tsum, long long* raw,
+                                                                 long long* clp) {
+  long long ca = 0, cb = 0;
+  for (int i = threadIdx.x; i < (int)blockIdx.x; i += kScanThreads) ca += tsum[2 * i], cb += tsum[2 * i + 1];
+  {
+    long long ta, tb;
+    block_scan2(ca, cb, ta, tb);
+    ca = ta, cb = tb;
+  }
+  for (int r = 0; r < kScanRounds; ++r) {
+    const long long k = (long long)blockIdx.x * kScanTile + r * kScanThreads + threadIdx.x;
+    const int v = k < n ? max(len[k], 0) : 0;
+    long long a = v, b = min(v, clamp), ta, tb;
+    block_scan2(a, b, ta, tb);
+    if (k < n) {
+      raw[k] = ca + a - v;
+      if (clp) clp[k] = cb + b - min(v, clamp);
+    }
+    ca += ta, cb += tb;
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    raw[n] = ca;
+    if (clp) clp[n] = cb;
+  }
+}
+
+// Column sums over rows of a [rows, cols] fp32 array, in a fixed order: one
+// block per column.
+__global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restrict__ part, int rows, int cols,
+                                                         float* out0, int n0, float* out1, int n1, float* out2) {
+  __shared__ float sh[256];
+  const int c = blockIdx.x;
+  float v = 0.f;
+  for (int r = threadIdx.x; r < rows; r += 256) v += part[(long long)r * cols + c];
+  sh[threadIdx.x] = v;
+  __syncthreads();
+  for (int o = 128; o; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (c < n0) out0[c] = sh[0];
+    else if (c < n0 + n1) out1[c - n0] = sh[0];
+    else out2[c - n0 - n1] = sh[0];
   }
 }
 
@@ -225,68 +297,67 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// One thread per position (rows past the valid count are zeroed): its
-// sample, s (fp32) and x = [q, s, q - s, q * s] (the MLP operand type).
+// One warp per sample, one lane per position: its sample, s (fp32) and
+// x = [q, s, q - s, q * s] (the MLP operand type). Rows past the valid count
+// are zeroed.
 template <class T>
-__global__ void gather_kernel(const Params p, const float* __restrict__ pooled, const long long* __restrict__ soff,
-                              const long long* __restrict__ roff, int* samp, T* X, float* S, long long Pc) {
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
+    const Params p, const float* __restrict__ pooled, const long long* __restrict__ soff,
+    const long long* __restrict__ roff, int* samp, T* X, float* S, long long Pc) {
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D;
+  const int lane = threadIdx.x & 31;
   const long long P = min(soff[p.B], Pc);
-  if (soff[p.B] > Pc && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, DSF_FLAG_COUNT);
-  int flags = 0;
-  for (long long pos = blockIdx.x * (long long)blockDim.x + threadIdx.x; pos < Pc;
-       pos += (long long)gridDim.x * blockDim.x) {
-    T* x = X + pos * K1;
-    if (pos >= P) {
-      for (int d = 0; d < K1; d += 4) store4<T>(x + d, 0.f, 0.f, 0.f, 0.f);
-      continue;
-    }
-    int lo = 0, hi = p.B - 1;  // the sample: the last b with soff[b] <= pos
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (soff[mid] <= pos) lo = mid;
-      else hi = mid - 1;
-    }
-    const int b = lo;
-    samp[pos] = b;
-    const long long j = roff[b] + (pos - soff[b]);
-    long long row[3];
-    bool ok[3];
+  int flags = (soff[p.B] > Pc && blockIdx.x == 0 && threadIdx.x == 0) ? DSF_FLAG_COUNT : 0;
+  const int nwarps = gridDim.x * kWarpsPerBlock;
+  for (int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); b < p.B; b += nwarps) {
+    const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
+    for (long long pos = p0 + lane; pos < p1; pos += 32) {
+      T* x = X + pos * K1;
+      samp[pos] = b;
+      const long long j = roff[b] + (pos - soff[b]);
+      long long row[3];
+      bool ok[3];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const int tb = p.seq_table[k];
-      long long id = -1;
-      if (j < p.n_seq) id = rid(p, tb, p.seq_values[k * p.n_seq + j]);
-      else flags |= DSF_FLAG_COUNT;
-      ok[k] = id >= 0 && id < p.rows[tb];
-      if (!ok[k] && j < p.n_seq) flags |= DSF_FLAG_ID_RANGE;
-      row[k] = ok[k] ? id : 0;
-    }
-    for (int c = 0; c < Q / 16; ++c) {
-      const int k = (c * 16) / D, e = (c * 16) % D;
-      float s[16], q[16];
-      if (ok[k]) load16(p, p.tables[p.seq_table[k]], row[k], e, s);
-      else
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = 0.f;
-      const float4* qp = reinterpret_cast<const float4*>(pooled + (long long)b * FD + p.q_feat[k] * D + e);
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float4 v = __ldg(qp + h);
-        q[4 * h] = v.x, q[4 * h + 1] = v.y, q[4 * h + 2] = v.z, q[4 * h + 3] = v.w;
+      for (int k = 0; k < 3; ++k) {
+        const int tb = p.seq_table[k];
+        long long id = -1;
+        if (j < p.n_seq) id = rid(p, tb, p.seq_values[k * p.n_seq + j]);
+        else flags |= DSF_FLAG_COUNT;
+        ok[k] = id >= 0 && id < p.rows[tb];
+        if (!ok[k] && j < p.n_seq) flags |= DSF_FLAG_ID_RANGE;
+        row[k] = ok[k] ? id : 0;
       }
-      float* sd = S + pos * Q + c * 16;
+      for (int c = 0; c < Q / 16; ++c) {
+        const int k = (c * 16) / D, e = (c * 16) % D;
+        float sv[16], q[16];
+        if (ok[k]) load16(p, p.tables[p.seq_table[k]], row[k], e, sv);
+        else
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int i = 4 * h;
-        *reinterpret_cast<float4*>(sd + i) = make_float4(s[i], s[i + 1], s[i + 2], s[i + 3]);
-        store4<T>(x + c * 16 + i, q[i], q[i + 1], q[i + 2], q[i + 3]);
-        store4<T>(x + Q + c * 16 + i, s[i], s[i + 1], s[i + 2], s[i + 3]);
-        store4<T>(x + 2 * Q + c * 16 + i, q[i] - s[i], q[i + 1] - s[i + 1], q[i + 2] - s[i + 2], q[i + 3] - s[i + 3]);
-        store4<T>(x + 3 * Q + c * 16 + i, q[i] * s[i], q[i + 1] * s[i + 1], q[i + 2] * s[i + 2], q[i + 3] * s[i + 3]);
+          for (int i = 0; i < 16; ++i) sv[i] = 0.f;
+        const float4* qp = reinterpret_cast<const float4*>(pooled + (long long)b * FD + p.q_feat[k] * D + e);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float4 v = __ldg(qp + h);
+          q[4 * h] = v.x, q[4 * h + 1] = v.y, q[4 * h + 2] = v.z, q[4 * h + 3] = v.w;
+        }
+        float* sd = S + pos * Q + c * 16;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int i = 4 * h;
+          *reinterpret_cast<float4*>(sd + i) = make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
+          store4<T>(x + c * 16 + i, q[i], q[i + 1], q[i + 2], q[i + 3]);
+          store4<T>(x + Q + c * 16 + i, sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
+          store4<T>(x + 2 * Q + c * 16 + i, q[i] - sv[i], q[i + 1] - sv[i + 1], q[i + 2] - sv[i + 2],
+                    q[i + 3] - sv[i + 3]);
+          store4<T>(x + 3 * Q + c * 16 + i, q[i] * sv[i], q[i + 1] * sv[i + 1], q[i + 2] * sv[i + 2],
+                    q[i + 3] * sv[i + 3]);
+        }
       }
     }
   }
+  for (long long i = P * K1 / 4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < Pc * K1 / 4;
+       i += (long long)gridDim.x * blockDim.x)
+    store4<T>(X + 4 * i, 0.f, 0.f, 0.f, 0.f);
   flag(p.status, flags);
 }
 
@@ -321,57 +392,85 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One warp per sample: softmax and score backward over its positions.
-// Accumulates dw3, db2, db3; writes dH2 (zero past the valid rows) and dS.
+// One warp per sample: softmax and score backward over its positions. z and
+// da = ddin.s take one lane per position; dH2, dS and the sums of dw3, db2,
+// db3 take one position per step with the lanes over dimensions (steps are
+// independent). Writes each block's partial sums (dw3 | db2 | db3); rows
+// of dH2 past the valid count are zeroed.
 template <class T>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
     const Params p, const long long* __restrict__ soff, const float* __restrict__ H2, const float* __restrict__ S,
     const float* __restrict__ ddin, const float* __restrict__ b2, const float* __restrict__ w3,
-    const float* __restrict__ b3, float* zb, float* dab, T* dH2, float* dS, float* dw3, float* db2, float* db3,
-    long long Pc) {
-  __shared__ float red[kWarpsPerBlock][2 * kN2 + 1];
+    const float* __restrict__ b3, float* zb, float* dab, T* dH2, float* dS, float* part, long long Pc) {
+  __shared__ float red[kWarpsPerBlock][kRedCols];
+  __shared__ float sw3[kN2], sb2[kN2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Q = 3 * p.D;
-  const int b = blockIdx.x * kWarpsPerBlock + warp;
+  for (int i = threadIdx.x; i < kN2; i += blockDim.x) sw3[i] = w3[i], sb2[i] = b2[i];
+  __syncthreads();
+  const float bb3 = __ldg(b3);
   float acc_w3[2] = {0.f, 0.f}, acc_b2[2] = {0.f, 0.f}, acc_b3 = 0.f;
-  if (b < p.B) {
+  for (int b = blockIdx.x * kWarpsPerBlock + warp; b < p.B; b += gridDim.x * kWarpsPerBlock) {
     const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
-    const float w3a = w3[lane], w3b = w3[lane + 32], b2a = b2[lane], b2b = b2[lane + 32], bb3 = __ldg(b3);
+    if (p1 <= p0) continue;
     const float* dd = ddin + (long long)b * Q;
+    // z and da per position (a lane each), the running max
     float m = -INFINITY;
-    for (long long q = p0; q < p1; ++q) {
-      const float ha = fmaxf(H2[(long long)q * kN2 + lane] + b2a, 0.f),
-                  hb = fmaxf(H2[(long long)q * kN2 + lane + 32] + b2b, 0.f);
-      const float z = warp_sum(ha * w3a + hb * w3b) + bb3;
-      if (lane == 0) zb[q] = z;
+    for (long long q = p0 + lane; q < p1; q += 32) {
+      const float4* h = reinterpret_cast<const float4*>(H2 + q * kN2);
+      float z = bb3;
+#pragma unroll 4
+      for (int i = 0; i < kN2 / 4; ++i) {
+        const float4 v = h[i];
+        z += sw3[4 * i] * fmaxf(v.x + sb2[4 * i], 0.f) + sw3[4 * i + 1] * fmaxf(v.y + sb2[4 * i + 1], 0.f) +
+             sw3[4 * i + 2] * fmaxf(v.z + sb2[4 * i + 2], 0.f) + sw3[4 * i + 3] * fmaxf(v.w + sb2[4 * i + 3], 0.f);
+      }
+      const float4* sr = reinterpret_cast<const float4*>(S + q * Q);
+      const float4* dr = reinterpret_cast<const float4*>(dd);
+      float da = 0.f;
+      for (int i = 0; i < Q / 4; ++i) {
+        const float4 x = sr[i], y = __ldg(dr + i);
+        da += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+      }
+      zb[q] = z;
+      dab[q] = da;
       m = fmaxf(m, z);
     }
-    __syncwarp();
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f, sda = 0.f;
-    for (long long q = p0; q < p1; ++q) {
-      float part = 0.f;
-      for (int d = lane; d < Q; d += 32) part += dd[d] * S[(long long)q * Q + d];
-      const float da = warp_sum(part);
+    for (long long q = p0 + lane; q < p1; q += 32) {
       const float e = expf(zb[q] - m);
       l += e;
-      sda += e * da;
-      __syncwarp();
-      if (lane == 0) zb[q] = e, dab[q] = da;
+      sda += e * dab[q];
+      zb[q] = e;
     }
-    __syncwarp();
-    const float c = p1 > p0 ? sda / l : 0.f;
-    for (long long q = p0; q < p1; ++q) {
-      const float a = zb[q] / l, dz = a * (dab[q] - c);
-      const float pa = H2[(long long)q * kN2 + lane] + b2a, pb = H2[(long long)q * kN2 + lane + 32] + b2b;
-      const float ga = pa > 0.f ? dz * w3a : 0.f, gb = pb > 0.f ? dz * w3b : 0.f;
-      dH2[(long long)q * kN2 + lane] = from_f<T>(ga);
-      dH2[(long long)q * kN2 + lane + 32] = from_f<T>(gb);
-      acc_w3[0] += dz * fmaxf(pa, 0.f);
-      acc_w3[1] += dz * fmaxf(pb, 0.f);
-      acc_b2[0] += ga;
-      acc_b2[1] += gb;
-      acc_b3 += dz;
-      for (int d = lane; d < Q; d += 32) dS[(long long)q * Q + d] = a * dd[d];
+    l = warp_sum(l);
+    sda = warp_sum(sda);
+    const float c = sda / l, il = 1.f / l;
+    // each lane's a and dz for its positions, handed out one position per step
+    for (long long q0 = p0; q0 < p1; q0 += 32) {
+      const long long qm = q0 + lane;
+      float a_l = 0.f, dz_l = 0.f;
+      if (qm < p1) {
+        a_l = zb[qm] * il;
+        dz_l = a_l * (dab[qm] - c);
+      }
+      const int n = int(min((long long)32, p1 - q0));
+      for (int t = 0; t < n; ++t) {
+        const long long q = q0 + t;
+        const float a = __shfl_sync(0xffffffffu, a_l, t), dz = __shfl_sync(0xffffffffu, dz_l, t);
+        const float pa = H2[q * kN2 + lane] + sb2[lane], pb = H2[q * kN2 + lane + 32] + sb2[lane + 32];
+        const float ga = pa > 0.f ? dz * sw3[lane] : 0.f, gb = pb > 0.f ? dz * sw3[lane + 32] : 0.f;
+        dH2[q * kN2 + lane] = from_f<T>(ga);
+        dH2[q * kN2 + lane + 32] = from_f<T>(gb);
+        acc_w3[0] += dz * fmaxf(pa, 0.f);
+        acc_w3[1] += dz * fmaxf(pb, 0.f);
+        acc_b2[0] += ga;
+        acc_b2[1] += gb;
+        if (lane == 0) acc_b3 += dz;
+        for (int d = lane; d < Q; d += 32) dS[q * Q + d] = a * dd[d];
+      }
     }
   }
   red[warp][lane] = acc_w3[0];
@@ -380,13 +479,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
   red[warp][lane + 96] = acc_b2[1];
   if (lane == 0) red[warp][2 * kN2] = acc_b3;
   __syncthreads();
-  for (int i = threadIdx.x; i <= 2 * kN2; i += blockDim.x) {
+  for (int i = threadIdx.x; i < kRedCols; i += blockDim.x) {
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarpsPerBlock; ++w) v += red[w][i];
-    if (i < kN2) atomicAdd(dw3 + i, v);
-    else if (i < 2 * kN2) atomicAdd(db2 + i - kN2, v);
-    else atomicAdd(db3, v);
+    part[(long long)blockIdx.x * kRedCols + i] = v;
   }
   // rows past the valid count: zero gradient
   const long long P = min(soff[p.B], Pc);
@@ -399,7 +496,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
 // db1 sums the masked values.
 template <class T>
 __global__ void __launch_bounds__(kN1) relu1_bwd_kernel(const float* __restrict__ G, const T* __restrict__ H1,
-                                                       T* dH1, float* db1, long long Pc) {
+                                                       T* dH1, float* part, long long Pc) {
   const int c = threadIdx.x;
   float acc = 0.f;
   for (long long r = blockIdx.x; r < Pc; r += gridDim.x) {
@@ -408,7 +505,7 @@ __global__ void __launch_bounds__(kN1) relu1_bwd_kernel(const float* __restrict_
     dH1[i] = from_f<T>(v);
     acc += v;
   }
-  atomicAdd(db1 + c, acc);
+  part[(long long)blockIdx.x * kN1 + c] = acc;
 }
 
 __device__ __forceinline__ float4 f4(const float* q) { return *reinterpret_cast<const float4*>(q); }
@@ -417,48 +514,97 @@ __device__ __forceinline__ float4 operator-(float4 a, float4 b) { return make_fl
 __device__ __forceinline__ float4 operator*(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
 __device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
 
-// One warp per sample: dq and the final ds of each position, then every row
-// gradient of the sample (sequence rows, then the values of its bags).
+// Touched rows, one thread per id occurrence: every value of the KJT's bags
+// (its table: the feature whose value range holds it) and every valid
+// position's three sequence ids.
+__global__ void mark_kernel(const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
+                            const long long* __restrict__ roff, const int* __restrict__ samp, long long Pc) {
+  const long long nv = min(boff[(long long)p.F * p.B], p.n_values);
+  const long long P = min(soff[p.B], Pc);
+  int flags = 0;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv + 3 * P;
+       i += (long long)gridDim.x * blockDim.x) {
+    int f;
+    long long id;
+    if (i < nv) {
+      int lo = 0, hi = p.F - 1;  // the last feature whose first value index is <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (boff[(long long)mid * p.B] <= i) lo = mid;
+        else hi = mid - 1;
+      }
+      f = lo;
+      id = rid(p, f, p.values[i]);
+    } else {
+      const long long r = i - nv, pos = r / 3;
+      const int k = int(r - 3 * pos), b = samp[pos];
+      const long long j = roff[b] + (pos - soff[b]);
+      f = p.seq_table[k];
+      id = j < p.n_seq ? rid(p, f, p.seq_values[k * p.n_seq + j]) : -1;
+    }
+    flags |= mark_row(p, f, id, id >= 0 && id < p.glimit[f]);
+  }
+  flag(p.status, flags);
+}
+
+// One warp per sample. Positions, a lane each: ds = dS + dx_s - dx_d + dx_p q
+// into the three sequence rows, and the lane's share of dq = sum_t (dx_q +
+// dx_d + dx_p s_t), reduced over the lanes afterwards. Then the bags: one
+// (feature, 4-element piece) per lane step, dpooled + dq into every value.
+// Pieces of x are handled kPG at a time so the dq shares stay in registers.
+constexpr int kPG = 12;
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
     const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
-    const long long* __restrict__ roff, long long Pc,
-    const float* __restrict__ pooled, const float* __restrict__ dpooled, const float* __restrict__ dX,
-    const float* __restrict__ S, const float* __restrict__ dS) {
+    const long long* __restrict__ roff, long long Pc, const float* __restrict__ pooled,
+    const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S,
+    const float* __restrict__ dS) {
   __shared__ float dqs[kWarpsPerBlock][3 * 64];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
-  const int b = blockIdx.x * kWarpsPerBlock + warp;
   int flags = 0;
-  if (b < p.B) {
-    float4 dq[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (int b = blockIdx.x * kWarpsPerBlock + warp; b < p.B; b += gridDim.x * kWarpsPerBlock) {
     const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
-    for (long long q = p0; q < p1; ++q) {
-      const long long j = roff[b] + (q - p0);
+    const float* qrow = pooled + (long long)b * FD;
+    for (int g0 = 0; g0 < nc; g0 += kPG) {
+      float4 dq[kPG];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c4 = lane + 32 * h;
-        if (c4 >= nc) continue;
-        const int d = 4 * c4, k = d / D, e = d % D;
-        const float* dx = dX + (long long)q * K1;
-        const float4 xq = f4(dx + d), xs = f4(dx + Q + d), xd = f4(dx + 2 * Q + d), xp = f4(dx + 3 * Q + d);
-        const float4 s4 = f4(S + (long long)q * Q + d);
-        const float4 q4 = f4(pooled + (long long)b * FD + p.q_feat[k] * D + e);
-        dq[h] = dq[h] + xq + xd + xp * s4;
-        const float4 ds = f4(dS + (long long)q * Q + d) + xs - xd + xp * q4;
-        const int tb = p.seq_table[k];
-        if (j < p.n_seq) {
-          const long long id = rid(p, tb, p.seq_values[k * p.n_seq + j]);
-          if (id >= 0 && id < p.glimit[tb]) flags |= add_grad(p, tb, id, e, ds);
+      for (int i = 0; i < kPG; ++i) dq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (long long q = p0 + lane; q < p1; q += 32) {
+        const long long j = roff[b] + (q - soff[b]);
+        long long id[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int tb = p.seq_table[k];
+          id[k] = j < p.n_seq ? rid(p, tb, p.seq_values[k * p.n_seq + j]) : -1;
+          if (!(id[k] >= 0 && id[k] < p.glimit[tb])) id[k] = -1;
+        }
+        const float* dx = dX + q * K1;
+#pragma unroll
+        for (int i = 0; i < kPG; ++i) {
+          const int c4 = g0 + i;
+          if (c4 >= nc) break;
+          const int d = 4 * c4, k = d / D, e = d % D;
+          const float4 xq = f4(dx + d), xs = f4(dx + Q + d), xd = f4(dx + 2 * Q + d), xp = f4(dx + 3 * Q + d);
+          const float4 s4 = f4(S + q * Q + d);
+          const float4 q4 = f4(qrow + p.q_feat[k] * D + e);
+          dq[i] = dq[i] + xq + xd + xp * s4;
+          if (id[k] >= 0) add_grad(p, p.seq_table[k], id[k], e, f4(dS + q * Q + d) + xs - xd + xp * q4);
         }
       }
-    }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c4 = lane + 32 * h;
-      if (c4 < nc) *reinterpret_cast<float4*>(&dqs[warp][4 * c4]) = dq[h];
+      for (int i = 0; i < kPG; ++i) {
+        float4 v = dq[i];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+          v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+          v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+        }
+        if (lane == 0 && g0 + i < nc) *reinterpret_cast<float4*>(&dqs[warp][4 * (g0 + i)]) = v;
+      }
     }
     __syncwarp();
-    // bags: one (feature, 4-element piece) per lane step
     const int npieces = p.F * (D / 4);
     for (int c = lane; c < npieces; c += 32) {
       const int f = c / (D / 4), e = (c % (D / 4)) * 4;
@@ -475,9 +621,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
           break;
         }
         const long long id = rid(p, f, p.values[v]);
-        if (id >= 0 && id < p.glimit[f]) flags |= add_grad(p, f, id, e, g);
+        if (id >= 0 && id < p.glimit[f]) add_grad(p, f, id, e, g);
       }
     }
+    __syncwarp();
   }
   flag(p.status, flags);
 }
@@ -602,6 +749,7 @@ void fill_tables(Params& p, const dsf_tables* t) {
     p.sid[f] = storage_of(t, f);
     if (t->pooling && t->pooling[f] == DSF_POOL_MEAN) p.mean_mask |= 1u << f;
   }
+
   p.F = t->F;
   p.D = t->D;
   p.bf16_tables = t->dtype == DSF_BF16;
@@ -690,11 +838,17 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   const void* W1 = mlp->W1;
   const void* W2 = mlp->W2;
 
-  if (cudaMemsetAsync(mg->db1, 0, kN1 * 4, s) != cudaSuccess || cudaMemsetAsync(mg->db2, 0, kN2 * 4, s) != cudaSuccess ||
-      cudaMemsetAsync(mg->dw3, 0, kN2 * 4, s) != cudaSuccess || cudaMemsetAsync(mg->db3, 0, 4, s) != cudaSuccess)
-    return DSF_ECUDA;
-  scan_kernel<<<1, 1024, 0, s>>>(kjt->lengths_dev, F * B, INT_MAX, boff, nullptr);
-  scan_kernel<<<1, 1024, 0, s>>>(seq->lengths_dev, B, seq->max_len, roff, soff);
+  long long* tsum = reinterpret_cast<long long*>(w + L.tsum);
+  float* part1 = reinterpret_cast<float*>(w + L.part1);
+  float* part2 = reinterpret_cast<float*>(w + L.part2);
+  {  // bag offsets of the KJT; raw and clamped sequence offsets
+    const int nk = F * B, tk = (nk + kScanTile - 1) / kScanTile, ts = (B + kScanTile - 1) / kScanTile;
+    scan_tiles_kernel<<<tk, kScanThreads, 0, s>>>(kjt->lengths_dev, nk, INT_MAX, tsum);
+    scan_apply_kernel<<<tk, kScanThreads, 0, s>>>(kjt->lengths_dev, nk, INT_MAX, tsum, boff, nullptr);
+    long long* tsum2 = tsum + 2 * (tk + 1);
+    scan_tiles_kernel<<<ts, kScanThreads, 0, s>>>(seq->lengths_dev, B, seq->max_len, tsum2);
+    scan_apply_kernel<<<ts, kScanThreads, 0, s>>>(seq->lengths_dev, B, seq->max_len, tsum2, roff, soff);
+  }
   if (bf) {
     pack_kernel<<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
         mlp->W1, mlp->W2, kN1 * K1, kN2 * kN1, reinterpret_cast<__nv_bfloat16*>(w + L.w1b),
@@ -704,12 +858,13 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   }
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   if (Pc > 0) {
+    const int gb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
     if (bf)
-      gather_kernel<__nv_bfloat16><<<grid_for(Pc, 256), 256, 0, s>>>(p, pooled_dev, soff, roff, samp,
-                                                                     static_cast<__nv_bfloat16*>(X), S, Pc);
+      gather_kernel<__nv_bfloat16><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp,
+                                                                      static_cast<__nv_bfloat16*>(X), S, Pc);
     else
-      gather_kernel<float><<<grid_for(Pc, 256), 256, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
-                                                             S, Pc);
+      gather_kernel<float><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
+                                                              S, Pc);
     if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
     if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
         cublasSetWorkspace(h, w + L.cublas, kCublasWs) != CUBLAS_STATUS_SUCCESS)
@@ -723,33 +878,35 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       relu1_kernel<float><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1, static_cast<float*>(H1), Pc * kN1 / 4);
     if (!gemm_rm(h, false, true, Pc, kN2, kN1, H1, kN1, W2, kN1, H2, kN2, bf)) return DSF_ECUDA;
   }
-  const int sb = (B + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int sb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
   if (bf)
     softmax_bwd_kernel<__nv_bfloat16><<<sb, kWarpsPerBlock * 32, 0, s>>>(
-        p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3, zb, dab, static_cast<__nv_bfloat16*>(dH2), dS, mg->dw3,
-        mg->db2, mg->db3, Pc);
+        p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3, zb, dab, static_cast<__nv_bfloat16*>(dH2), dS, part1, Pc);
   else
     softmax_bwd_kernel<float><<<sb, kWarpsPerBlock * 32, 0, s>>>(p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3,
-                                                                 zb, dab, static_cast<float*>(dH2), dS, mg->dw3,
-                                                                 mg->db2, mg->db3, Pc);
+                                                                 zb, dab, static_cast<float*>(dH2), dS, part1, Pc);
+  reduce_cols_kernel<<<kRedCols, 256, 0, s>>>(part1, sb, kRedCols, mg->dw3, kN2, mg->db2, kN2, mg->db3);
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   if (Pc > 0) {
     if (!gemm_rm(h, false, false, Pc, kN1, kN2, dH2, kN2, W2, kN1, G1, kN1, bf)) return DSF_ECUDA;
-    const int rb = grid_for(Pc, 1, 152 * 8);
+    const int rb = grid_for(Pc, 1, kMaxBlocks);
     if (bf)
       relu1_bwd_kernel<__nv_bfloat16><<<rb, kN1, 0, s>>>(G1, static_cast<const __nv_bfloat16*>(H1),
-                                                          static_cast<__nv_bfloat16*>(dH1), mg->db1, Pc);
+                                                          static_cast<__nv_bfloat16*>(dH1), part2, Pc);
     else
-      relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), mg->db1,
+      relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
                                                  Pc);
+    reduce_cols_kernel<<<kN1, 256, 0, s>>>(part2, rb, kN1, mg->db1, kN1, nullptr, 0, nullptr);
     if (!gemm_rm(h, false, false, Pc, K1, kN1, dH1, kN1, W1, K1, dX, K1, bf)) return DSF_ECUDA;
     if (!gemm_rm(h, true, false, kN1, K1, Pc, dH1, kN1, X, K1, mg->dW1, K1, bf)) return DSF_ECUDA;
     if (!gemm_rm(h, true, false, kN2, kN1, Pc, dH2, kN2, H1, kN1, mg->dW2, kN1, bf)) return DSF_ECUDA;
   } else {
     if (cudaMemsetAsync(mg->dW1, 0, size_t(kN1) * K1 * 4, s) != cudaSuccess ||
-        cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess)
+        cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(mg->db1, 0, size_t(kN1) * 4, s) != cudaSuccess)
       return DSF_ECUDA;
   }
+  mark_kernel<<<grid_for(kjt->n_values + 3 * Pc, 256), 256, 0, s>>>(p, boff, soff, roff, samp, Pc);
   scatter_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS);
   return cudaGetLastError() == cudaSuccess ? DSF_OK : DSF_ECUDA;
 }
