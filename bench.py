@@ -259,6 +259,70 @@ def time_dynamic_emb(binding, synth, batch, dev, mode, flush, steps, ws):
                          "algorithmic_bytes_per_launch": nbytes, "peak_source": src}}
 
 
+BWD_FLOPS_PER_POSITION_D16 = 2 * (192 * 256 + 256 * 64 + 64 * 256 + 256 * 192 + 256 * 192 + 64 * 256)
+
+
+def time_train_step(binding, db, mlp, wsp, pooled, din, status, flush, steps, batch):
+    """One training step of the sparse path per iteration: din_sparse_fwd,
+    din_sparse_bwd on fixed synthetic upstream gradients, and sparse AdaGrad
+    (lr 1e-3) on the touched rows; L2 flushed between steps, CUDA events on
+    the launching stream around each part. The tables are updated in place
+    (a copy of the batch's tables, so the forward leg above is unaffected)."""
+    import torch
+    dev = pooled.device
+    B, F, D = db.B, db.F, db.D
+    tabs = binding.EmbeddingTables([t.clone() for t in db.tables.tables], db.tables.pooling, db.tables.hash)
+    n_seq = int(db.seq_values.shape[-1])
+    grads = binding.MlpGrads(D, device=dev)
+    state = binding.SparseState(tabs, int(db.values.numel()) + 3 * n_seq, device=dev)
+    bws = binding.BwdWorkspace(B, n_seq, D, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    dpooled = torch.randn(B, F * D, device=dev, generator=gen)
+    ddin = torch.randn(B, 3 * D, device=dev, generator=gen)
+    stream = torch.cuda.Stream(device=dev)
+
+    def fwd():
+        binding.din_sparse_fwd(tabs, db.values, db.lengths, db.seq_values, db.seq_lengths, db.max_len, db.q_feat,
+                               db.seq_table, B, mlp, pooled, din, wsp, status=status, stream=stream)
+
+    def bwd():
+        binding.din_sparse_bwd(tabs, db.values, db.lengths, db.seq_values, db.seq_lengths, db.max_len, db.q_feat,
+                               db.seq_table, B, mlp, pooled, dpooled, ddin, grads, state, bws, status=status,
+                               stream=stream)
+
+    def upd():
+        binding.emb_adagrad_update(tabs, state, 1e-3, 1e-10, status=status, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fwd(); bwd(); upd()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        stream.synchronize()
+        for i in range(steps):
+            flush.fill_(float(i & 7))
+            e = ev[i]
+            e[0].record(stream); fwd(); e[1].record(stream); bwd(); e[2].record(stream); upd(); e[3].record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()):
+        raise RuntimeError("train step status 0x%x" % int(status.item()))
+    f_us = sum(e[0].elapsed_time(e[1]) for e in ev) * 1e3 / steps
+    b_us = sum(e[1].elapsed_time(e[2]) for e in ev) * 1e3 / steps
+    u_us = sum(e[2].elapsed_time(e[3]) for e in ev) * 1e3 / steps
+    step_us = f_us + b_us + u_us
+    _, _, P = algorithmic_work(batch)
+    flops = BWD_FLOPS_PER_POSITION_D16 * P if D == 16 else None
+    _, tfs, _, src = peaks()
+    out = {"what": "din_sparse_fwd + din_sparse_bwd (upstream gradients dpooled, ddin) + emb_adagrad_update",
+           "us_per_step": step_us, "fwd_us": f_us, "bwd_us": b_us, "adagrad_us": u_us,
+           "samples_per_s": B / (step_us * 1e-6)}
+    if flops:
+        ach = flops / (b_us * 1e-6) / 1e12
+        out["bwd_roofline"] = {"bound": "tensor", "achieved": ach, "peak": tfs, "unit": "TFLOP/s",
+                               "frac": ach / tfs, "flops_per_launch": flops, "peak_source": src,
+                               "note": "the six MLP GEMMs of the backward over the valid positions"}
+    return out
+
+
 TOWER_FLOPS_PER_SAMPLE = 2 * (256 * 512 + 512 * 256 + 256 * 128 + 176 * 64)
 
 
@@ -359,6 +423,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-towers", action="store_true")
     ap.add_argument("--skip-dynemb", action="store_true")
+    ap.add_argument("--skip-train", action="store_true")
+    ap.add_argument("--train-steps", type=int, default=100)
     ap.add_argument("--dynemb-steps", type=int, default=500)
     ap.add_argument("--towers-steps", type=int, default=300)
     args = ap.parse_args()
@@ -521,6 +587,10 @@ def main():
     if not args.skip_dynemb:
         dynemb = time_dynamic_emb(binding, synth, batch, dev, mode, flush, args.dynemb_steps, ws)
 
+    train = None
+    if rank == 0 and not args.skip_train:
+        train = time_train_step(binding, db, mlp, wsp, pooled, din, status, flush, args.train_steps, batch)
+
     towers = None
     if rank == 0 and not args.skip_towers:
         towers = time_towers(binding, synth, pooled, din, B, dev, flush, args.towers_steps)
@@ -577,6 +647,7 @@ def main():
             "status": st,
             "towers": towers,
             "dynamic_emb": dynemb,
+            "train_step": train,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
