@@ -275,7 +275,7 @@ def time_train_step(binding, db, mlp, wsp, pooled, din, status, flush, steps, ba
     n_seq = int(db.seq_values.shape[-1])
     grads = binding.MlpGrads(D, device=dev)
     state = binding.SparseState(tabs, int(db.values.numel()) + 3 * n_seq, device=dev)
-    bws = binding.BwdWorkspace(B, n_seq, D, device=dev)
+    bws = binding.BwdWorkspace(B, int(db.values.numel()), n_seq, D, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     dpooled = torch.randn(B, F * D, device=dev, generator=gen)

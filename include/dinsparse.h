@@ -325,9 +325,10 @@ typedef struct {
   int64_t list_cap;
 } dsf_row_grads;
 
-/* Workspace bytes of din_sparse_bwd for B samples and n_per_key sequence
- * values (0 for invalid arguments); caller-owned, 256-byte aligned. */
-size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_per_key, int32_t D);
+/* Workspace bytes of din_sparse_bwd for B samples, n_values KJT values and
+ * n_per_key sequence values (0 for invalid arguments); caller-owned,
+ * 256-byte aligned. */
+size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_values, int64_t n_per_key, int32_t D);
 
 /* Returns DSF_EINVAL / DSF_EUNSUPPORTED / DSF_EWORKSPACE for bad arguments
  * (as din_sparse_fwd), DSF_ECUDA when a launch or a library call fails.

@@ -120,7 +120,7 @@ def lib() -> ctypes.CDLL:
         L.dsf_hash_insert.restype = ctypes.c_int
         L.dsf_hash_find.argtypes = [P(CHash), _i32, _vp, _i64, _vp, _vp, _vp]
         L.dsf_hash_find.restype = ctypes.c_int
-        L.dsf_bwd_workspace_bytes.argtypes = [_i32, _i64, _i32]
+        L.dsf_bwd_workspace_bytes.argtypes = [_i32, _i64, _i64, _i32]
         L.dsf_bwd_workspace_bytes.restype = _sz
         L.din_sparse_bwd.argtypes = [P(CTables), P(CKjt), P(CSeq), _vp, _vp, _i32, P(CMlp), _vp, _vp, _vp,
                                      P(CMlpGrads), P(CRowGrads), _vp, _sz, _vp, _vp]
@@ -417,8 +417,8 @@ class SparseState:
 
 
 class BwdWorkspace:
-    def __init__(self, B: int, n_per_key: int, D: int, device="cuda"):
-        self.nbytes = int(lib().dsf_bwd_workspace_bytes(int(B), int(n_per_key), int(D)))
+    def __init__(self, B: int, n_values: int, n_per_key: int, D: int, device="cuda"):
+        self.nbytes = int(lib().dsf_bwd_workspace_bytes(int(B), int(n_values), int(n_per_key), int(D)))
         if self.nbytes == 0:
             raise DsfError(DSF_EINVAL, "dsf_bwd_workspace_bytes")
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)

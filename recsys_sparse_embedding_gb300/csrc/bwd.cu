@@ -40,18 +40,20 @@ constexpr int kWarpsPerBlock = 8;
 constexpr int kScanThreads = 256, kScanRounds = 8, kScanTile = kScanThreads * kScanRounds;
 constexpr int kMaxBlocks = 152 * 8;  // grid cap of the grid-stride kernels (their partial sums)
 constexpr int kRedCols = 2 * 64 + 1;  // dw3 | db2 | db3 partials of the softmax kernel
+constexpr int kTile = 1024, kRowThreads = 512;  // row-gradient tiles (id occurrences) and their blocks
+constexpr unsigned long long kNoKey = ~0ull;
 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, w1b, w2b, X, S, G1, H1, H2, dH2, dH1, dX, dS, cublas,
+  size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, gbag, okey, osrc, w1b, w2b, X, S, G1, H1, H2, dH2, dH1, dX, dS, cublas,
       total;
 };
 
 // Every buffer is sized for fp32 elements, so the layout does not depend on
 // the MLP mode.
-Layout layout(long long B, long long Pc, int F, int D) {
+Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   Layout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -69,6 +71,9 @@ Layout layout(long long B, long long Pc, int F, int D) {
   L.dab = take(P * 4);
   L.part1 = take(size_t(kMaxBlocks) * kRedCols * 4);
   L.part2 = take(size_t(kMaxBlocks) * kN1 * 4);
+  L.gbag = take(size_t(B) * F * D * 4);
+  L.okey = take((size_t(NV) + 3 * P) * 8);
+  L.osrc = take((size_t(NV) + 3 * P) * 8);
   L.w1b = take(size_t(kN1) * K1 * 2);
   L.w2b = take(size_t(kN2) * kN1 * 2);
   L.X = take(P * K1 * 4);
@@ -145,21 +150,10 @@ __device__ __forceinline__ void load16(const Params& p, const void* base, long l
   }
 }
 
-// Adds a 4-element gradient piece (elements e..e+3) to row `row` of table f's
-// storage; the piece holding element 0 also records the row as touched.
-// Adds a 4-element gradient piece (elements e..e+3) to row `row` of table f's
-// storage (a vector reduction: no value comes back).
-__device__ __forceinline__ void add_grad(const Params& p, int f, long long row, int e, float4 g) {
-  float* dst = p.grad[p.sid[f]] + row * p.D + e;
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(g.x), "f"(g.y), "f"(g.z), "f"(g.w)
-               : "memory");
-}
-
-// Records row `row` of table f's storage as touched (valid: the row is a
-// parameter). The lanes that are first to touch a row reserve their list
-// entries with one atomic per warp.
-__device__ __forceinline__ int mark_row(const Params& p, int f, long long row, bool valid) {
-  const int s = p.sid[f];
+// Records row `row` of storage s as touched (valid: the row is a parameter).
+// The lanes that are first to touch a row reserve their list entries with
+// one atomic per warp.
+__device__ __forceinline__ int mark_row(const Params& p, int s, long long row, bool valid) {
   bool first = false;
   if (valid) {
     int* t = p.touched[s] + row;
@@ -514,50 +508,20 @@ __device__ __forceinline__ float4 operator-(float4 a, float4 b) { return make_fl
 __device__ __forceinline__ float4 operator*(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
 __device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
 
-// Touched rows, one thread per id occurrence: every value of the KJT's bags
-// (its table: the feature whose value range holds it) and every valid
-// position's three sequence ids.
-__global__ void mark_kernel(const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
-                            const long long* __restrict__ roff, const int* __restrict__ samp, long long Pc) {
-  const long long nv = min(boff[(long long)p.F * p.B], p.n_values);
-  const long long P = min(soff[p.B], Pc);
-  int flags = 0;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv + 3 * P;
-       i += (long long)gridDim.x * blockDim.x) {
-    int f;
-    long long id;
-    if (i < nv) {
-      int lo = 0, hi = p.F - 1;  // the last feature whose first value index is <= i
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (boff[(long long)mid * p.B] <= i) lo = mid;
-        else hi = mid - 1;
-      }
-      f = lo;
-      id = rid(p, f, p.values[i]);
-    } else {
-      const long long r = i - nv, pos = r / 3;
-      const int k = int(r - 3 * pos), b = samp[pos];
-      const long long j = roff[b] + (pos - soff[b]);
-      f = p.seq_table[k];
-      id = j < p.n_seq ? rid(p, f, p.seq_values[k * p.n_seq + j]) : -1;
-    }
-    flags |= mark_row(p, f, id, id >= 0 && id < p.glimit[f]);
-  }
-  flag(p.status, flags);
-}
-
-// One warp per sample. Positions, a lane each: ds = dS + dx_s - dx_d + dx_p q
-// into the three sequence rows, and the lane's share of dq = sum_t (dx_q +
-// dx_d + dx_p s_t), reduced over the lanes afterwards. Then the bags: one
-// (feature, 4-element piece) per lane step, dpooled + dq into every value.
-// Pieces of x are handled kPG at a time so the dq shares stay in registers.
-constexpr int kPG = 12;
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
+// One warp per sample, no atomics. Positions, a lane each: the final ds =
+// dS + dx_s - dx_d + dx_p q (in place) and the lane's share of dq = sum_t
+// (dx_q + dx_d + dx_p s_t), reduced over the lanes afterwards; the position's
+// three sequence ids become occurrences (storage << 40 | row, and where their
+// gradient is). Then the bags, one (feature, 4-element piece) per lane step:
+// g = dpooled + dq (over L for mean pooling) into the bag-gradient rows, and
+// every value of the bag becomes an occurrence. Pieces of x are handled kPG
+// at a time so the dq shares stay in registers.
+constexpr int kPG = 4;
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
     const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
     const long long* __restrict__ roff, long long Pc, const float* __restrict__ pooled,
-    const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S,
-    const float* __restrict__ dS) {
+    const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S, float* dS,
+    float* gbag, unsigned long long* okey, long long* osrc) {
   __shared__ float dqs[kWarpsPerBlock][3 * 64];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
@@ -571,12 +535,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
       for (int i = 0; i < kPG; ++i) dq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (long long q = p0 + lane; q < p1; q += 32) {
         const long long j = roff[b] + (q - soff[b]);
-        long long id[3];
+        if (g0 == 0) {
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int tb = p.seq_table[k];
-          id[k] = j < p.n_seq ? rid(p, tb, p.seq_values[k * p.n_seq + j]) : -1;
-          if (!(id[k] >= 0 && id[k] < p.glimit[tb])) id[k] = -1;
+          for (int k = 0; k < 3; ++k) {
+            const int tb = p.seq_table[k];
+            const long long id = j < p.n_seq ? rid(p, tb, p.seq_values[k * p.n_seq + j]) : -1;
+            const long long o = p.n_values + 3 * q + k;
+            okey[o] = (id >= 0 && id < p.glimit[tb]) ? (static_cast<unsigned long long>(p.sid[tb]) << kRowBits) |
+                                                           static_cast<unsigned long long>(id)
+                                                     : kNoKey;
+            osrc[o] = -(3 * q + k) - 1;
+          }
         }
         const float* dx = dX + q * K1;
 #pragma unroll
@@ -588,7 +557,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
           const float4 s4 = f4(S + q * Q + d);
           const float4 q4 = f4(qrow + p.q_feat[k] * D + e);
           dq[i] = dq[i] + xq + xd + xp * s4;
-          if (id[k] >= 0) add_grad(p, p.seq_table[k], id[k], e, f4(dS + q * Q + d) + xs - xd + xp * q4);
+          float* dsp = dS + q * Q + d;
+          *reinterpret_cast<float4*>(dsp) = f4(dsp) + xs - xd + xp * q4;
         }
       }
 #pragma unroll
@@ -613,18 +583,132 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) scatter_kernel(
       for (int k = 0; k < 3; ++k)
         if (p.q_feat[k] == f) g = g + *reinterpret_cast<const float4*>(&dqs[warp][k * D + e]);
       const long long v0 = boff[(long long)f * p.B + b], v1 = boff[(long long)f * p.B + b + 1];
-      if (v1 <= v0) continue;
-      if ((p.mean_mask >> f) & 1u) g = scale4(g, 1.f / float(v1 - v0));
+      if (v1 > v0 && ((p.mean_mask >> f) & 1u)) g = scale4(g, 1.f / float(v1 - v0));
+      *reinterpret_cast<float4*>(gbag + (long long)b * FD + f * D + e) = g;
+      if (e != 0) continue;
       for (long long v = v0; v < v1; ++v) {
         if (v >= p.n_values) {
           flags |= DSF_FLAG_COUNT;
           break;
         }
         const long long id = rid(p, f, p.values[v]);
-        if (id >= 0 && id < p.glimit[f]) add_grad(p, f, id, e, g);
+        okey[v] = (id >= 0 && id < p.glimit[f])
+                      ? (static_cast<unsigned long long>(p.sid[f]) << kRowBits) | static_cast<unsigned long long>(id)
+                      : kNoKey;
+        osrc[v] = (long long)b * p.F + f;
       }
     }
     __syncwarp();
+  }
+  flag(p.status, flags);
+}
+
+__device__ __forceinline__ float4 shfl_up4(float4 v, int o) {
+  return make_float4(__shfl_up_sync(0xffffffffu, v.x, o), __shfl_up_sync(0xffffffffu, v.y, o),
+                     __shfl_up_sync(0xffffffffu, v.z, o), __shfl_up_sync(0xffffffffu, v.w, o));
+}
+
+// Row gradients of a tile of kTile id occurrences (the KJT's values at
+// [0, n_values), the sequence ids at n_values + 3 * position + k): the tile's
+// (key, source) pairs sorted by key in shared memory (bitonic network), then
+// per 4-element piece a segmented inclusive scan over the sorted order (two
+// elements per thread, shuffles within warps, a carry across warps) gives each
+// run's sum at its last element, which issues one vector reduction into the
+// row's gradient (the first piece also marks the row touched). Occurrences
+// past the valid counts or with no parameter row sort last and are skipped.
+__global__ void __launch_bounds__(kRowThreads) rowgrad_kernel(
+    const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff, long long Pc,
+    const unsigned long long* __restrict__ okey, const long long* __restrict__ osrc, const float* __restrict__ gbag,
+    const float* __restrict__ dS) {
+  constexpr int NW = kRowThreads / 32;
+  __shared__ unsigned long long key[kTile];
+  __shared__ long long src[kTile];
+  __shared__ float4 wagg[NW];
+  __shared__ int whead[NW];
+  const int D = p.D, Q = 3 * D, pieces = D / 4, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const long long nv = min(boff[(long long)p.F * p.B], p.n_values), P = min(soff[p.B], Pc);
+  const long long o0 = (long long)blockIdx.x * kTile;
+  for (int i = tid; i < kTile; i += kRowThreads) {
+    const long long o = o0 + i;
+    const bool ok = o < p.n_values ? o < nv : (o - p.n_values) < 3 * P;
+    key[i] = ok ? okey[o] : kNoKey;
+    src[i] = ok ? osrc[o] : 0;
+  }
+  __syncthreads();
+  for (int k = 2; k <= kTile; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < kTile; i += kRowThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool up = (i & k) == 0;
+          const unsigned long long a = key[i], b = key[l];
+          if ((a > b) == up) {
+            key[i] = b, key[l] = a;
+            const long long t = src[i];
+            src[i] = src[l], src[l] = t;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  const int ia = 2 * tid, ib = ia + 1;
+  const unsigned long long ka = key[ia], kb = key[ib];
+  const unsigned long long kn = ib + 1 < kTile ? key[ib + 1] : kNoKey;
+  const bool va = ka != kNoKey, vb = kb != kNoKey;
+  const bool sa = va && (ia == 0 || key[ia - 1] != ka), sb = vb && ka != kb;
+  const bool ea = va && ka != kb, eb = vb && kn != kb;  // last element of a run
+  auto piece = [&](long long sj, int c) {
+    const float* v = sj >= 0 ? gbag + sj * D : dS + ((-sj - 1) / 3) * Q + ((-sj - 1) % 3) * D;
+    return f4(v + 4 * c);
+  };
+  int flags = 0;
+  for (int c = 0; c < pieces; ++c) {
+    const float4 xa = va ? piece(src[ia], c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 xb = vb ? piece(src[ib], c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // this thread's trailing segment (from its last run start, or all of it)
+    float4 agg = sb ? xb : xa + xb;
+    bool head = sa || sb;
+    // segmented inclusive scan over the warp's lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float4 y = shfl_up4(agg, o);
+      const bool hy = __shfl_up_sync(0xffffffffu, head, o);
+      if (lane >= o) {
+        if (!head) agg = agg + y;
+        head = head || hy;
+      }
+    }
+    if (lane == 31) wagg[w] = agg, whead[w] = head;
+    __syncthreads();
+    // the carry into this warp: the trailing segments of the warps before it
+    float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = w - 1; u >= 0; --u) {
+      cw = cw + wagg[u];
+      if (whead[u]) break;
+    }
+    // the carry into this thread's first element
+    const float4 prev = shfl_up4(agg, 1);
+    const bool hprev = __shfl_up_sync(0xffffffffu, head, 1);
+    float4 carry = lane == 0 ? cw : (hprev ? prev : prev + cw);
+    const float4 ta = sa ? xa : carry + xa;  // run sums through element a and b
+    const float4 tb = sb ? xb : ta + xb;
+    const float4 tot[2] = {ta, tb};
+    const bool end[2] = {ea, eb};
+    const unsigned long long kk[2] = {ka, kb};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s = int(kk[h] >> kRowBits);
+      const long long row = end[h] ? (long long)(kk[h] & ((1ull << kRowBits) - 1)) : 0;
+      if (end[h]) {
+        float* dst = p.grad[s] + row * D + 4 * c;
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(tot[h].x), "f"(tot[h].y),
+                     "f"(tot[h].z), "f"(tot[h].w)
+                     : "memory");
+      }
+      if (c == 0) flags |= mark_row(p, end[h] ? s : 0, row, end[h]);
+    }
+    __syncthreads();
   }
   flag(p.status, flags);
 }
@@ -762,9 +846,11 @@ void fill_tables(Params& p, const dsf_tables* t) {
 using namespace dsf;
 using namespace dsf::bwd;
 
-extern "C" size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_per_key, int32_t D) {
-  if (B < 0 || n_per_key < 0 || n_per_key > INT32_MAX || (D != 16 && D != 64)) return 0;
-  return bwd::layout(B, n_per_key, kMaxF, D).total;
+extern "C" size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_values, int64_t n_per_key, int32_t D) {
+  if (B < 0 || n_values < 0 || n_values > INT32_MAX || n_per_key < 0 || n_per_key > INT32_MAX ||
+      (D != 16 && D != 64))
+    return 0;
+  return bwd::layout(B, n_values, n_per_key, kMaxF, D).total;
 }
 
 extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq, const int32_t* q_feat,
@@ -787,7 +873,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   if (!rg || !rg->grad || !rg->touched || !rg->list || !rg->count || rg->list_cap < 0) return DSF_EINVAL;
   if ((rc = check_row_state(tables, rg->grad, rg->touched)) != DSF_OK) return rc;
   const long long Pc = seq->n_per_key;
-  const bwd::Layout L = bwd::layout(B, Pc, kMaxF, tables->D);
+  const bwd::Layout L = bwd::layout(B, kjt->n_values, Pc, kMaxF, tables->D);
   if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < L.total) return DSF_EWORKSPACE;
   if (B == 0) return DSF_OK;
 
@@ -906,8 +992,16 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
         cudaMemsetAsync(mg->db1, 0, size_t(kN1) * 4, s) != cudaSuccess)
       return DSF_ECUDA;
   }
-  mark_kernel<<<grid_for(kjt->n_values + 3 * Pc, 256), 256, 0, s>>>(p, boff, soff, roff, samp, Pc);
-  scatter_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS);
+  {
+    float* gbag = reinterpret_cast<float*>(w + L.gbag);
+    unsigned long long* okey = reinterpret_cast<unsigned long long*>(w + L.okey);
+    long long* osrc = reinterpret_cast<long long*>(w + L.osrc);
+    dsdq_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS, gbag,
+                                                   okey, osrc);
+    const long long nocc = kjt->n_values + 3 * Pc;
+    if (nocc > 0)
+      rowgrad_kernel<<<int((nocc + kTile - 1) / kTile), kRowThreads, 0, s>>>(p, boff, soff, Pc, okey, osrc, gbag, dS);
+  }
   return cudaGetLastError() == cudaSuccess ? DSF_OK : DSF_ECUDA;
 }
 

@@ -50,7 +50,7 @@ class Bwd:
         cap = list_cap if list_cap is not None else int(db.values.numel()) + 3 * n_seq
         self.grads = binding.MlpGrads(D)
         self.state = binding.SparseState(db.tables, cap)
-        self.ws = binding.BwdWorkspace(B, n_seq, D)
+        self.ws = binding.BwdWorkspace(B, int(db.values.numel()), n_seq, D)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.pooled_t = torch.from_numpy(pooled).cuda()
         self.dp_t = None if self.dpooled is None else torch.from_numpy(self.dpooled).cuda()
