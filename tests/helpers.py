@@ -1,5 +1,5 @@
 """Shared test plumbing: run the CUDA path on a synthetic batch and compare
-with the oracle. Tolerances follow the benchmark spec of the path:
+with the oracle. Tolerances follow the path's stated accuracy targets:
 pooled sums within 1e-6 relative (here: bit-exact, since both sides sum fp32
 rows in bag order), attention output within 1e-5 in the fp32 check mode and
 within 2e-2 absolute or 1e-2 relative with the bf16 tensor-core MLP."""
