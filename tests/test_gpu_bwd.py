@@ -225,3 +225,36 @@ def test_adagrad_step_and_state_reset():
         pooled, _, _, _ = bw.run.fwd(TC, logits=False)
         bw.pooled = pooled
         bw.pooled_t = torch.from_numpy(pooled).cuda()
+
+
+def test_backward_wide_bf16_tables():
+    """D = 64 with bf16 tables: Q = 192, x of 768, the tensor-core and fp32 modes."""
+    run_case(synth.generate("wide_bf16", seed=1, B=256, nonzero_bias=True), seed=13)
+
+
+def test_adagrad_on_bf16_tables():
+    """The update of bf16 tables: fp32 arithmetic, the new weight rounded to
+    nearest-even bf16 (within one bf16 unit of the fp64 update)."""
+    b = synth.generate("wide_bf16", seed=2, B=128, nonzero_bias=True)
+    bw = Bwd(b, TC, seed=14)
+    st = bw.state
+    tabs = bw.db.tables.tables
+    assert bw.backward() == 0
+    n = int(st.count.item())
+    ent = st.list[:n].cpu().numpy()
+    sid, rows = ent >> 40, ent & ((1 << 40) - 1)
+    before = {}
+    for s in np.unique(sid):
+        rt = torch.from_numpy(rows[sid == s]).cuda()
+        before[int(s)] = (rt, st.grad[s][rt].cpu().numpy().astype(np.float64),
+                          tabs[s][rt].float().cpu().numpy().astype(np.float64), st.accum[s][rt].cpu().numpy())
+    lr = 0.05
+    binding.emb_adagrad_update(bw.db.tables, st, lr=lr, eps=1e-10)
+    torch.cuda.synchronize()
+    for s, (rt, g, w, G) in before.items():
+        w_ref, _ = obw.adagrad(w, G, np.arange(rt.numel()), g, lr=lr, eps=1e-10)
+        w_new = tabs[s][rt].float().cpu().numpy().astype(np.float64)
+        # one bf16 unit (2^-7 relative) of the result, plus fp32 rounding of the step
+        assert (np.abs(w_new - w_ref) <= 2.0 ** -8 * np.abs(w_ref) + 2.0 ** -20 * (np.abs(w) + lr) + 1e-30).all()
+        assert (w_new != w).any()
+    assert int(st.count.item()) == 0
