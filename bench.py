@@ -36,7 +36,7 @@ UNIT = "samples/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
-D2H_STREAMS = 1   # output copies of a step, split over this many streams (4 measured slower)
+E2E_GRAPH = 20    # pipelined end-to-end steps per captured graph
 KERNEL_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "hash.cuh", "launch.cuh", "fwd_attn_tc.cu"]
 
 
@@ -508,7 +508,9 @@ def main():
         # device, calls the C ABI, and copies both outputs back to pinned host
         # memory. Steps are pipelined over two buffer slots: the copies of one
         # step run on their own streams (copy engines) while the kernel of the
-        # next runs; events keep each slot's buffers from being reused early.
+        # next runs; events order each slot's reuse. E2E_GRAPH steps are
+        # captured into one CUDA graph (host enqueue of ~15 calls per step would
+        # otherwise bound the rate) and the graph is replayed.
         h_in = [x.cpu().pin_memory() for x in (db.values, db.lengths, db.seq_values, db.seq_lengths)]
         d_in = [[torch.empty_like(x, device=dev) for x in h_in] for _ in range(2)]
         d_out = [(torch.empty_like(pooled), torch.empty_like(din)) for _ in range(2)]
@@ -516,71 +518,57 @@ def main():
         h2d = sum(x.numel() * x.element_size() for x in h_in)
         d2h = sum(t.numel() * t.element_size() for t in d_out[0])
         s_h2d = torch.cuda.Stream(device=dev)
-        s_d2h = [torch.cuda.Stream(device=dev) for _ in range(D2H_STREAMS)]
-        # the outputs of a slot, cut into D2H_STREAMS pieces of about equal size
-        def out_pieces(j):
-            flat = [(d.view(-1), h.view(-1)) for d, h in zip(d_out[j], h_out[j])]
-            total = sum(d.numel() for d, _ in flat)
-            per = -(-total // D2H_STREAMS)
-            out, k, used = [[] for _ in range(D2H_STREAMS)], 0, 0
-            for d, h in flat:
-                off = 0
-                while off < d.numel():
-                    n = min(d.numel() - off, per - used)
-                    out[k].append((d[off:off + n], h[off:off + n]))
-                    off += n
-                    used += n
-                    if used == per:
-                        k, used = min(k + 1, D2H_STREAMS - 1), 0
-            return out
-        slot_pieces = [out_pieces(j) for j in range(2)]
-        ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of slot j landed
-        ev_run = [torch.cuda.Event() for _ in range(2)]   # kernel of slot j done
-        ev_out = [[torch.cuda.Event() for _ in range(D2H_STREAMS)] for _ in range(2)]
-        for j in range(2):
-            ev_run[j].record(stream)
-            for e in ev_out[j]:
-                e.record(stream)
+        s_d2h = torch.cuda.Stream(device=dev)
 
-        def e2e_step(i):
-            j = i & 1
-            s_h2d.wait_event(ev_run[j])          # the kernel that read slot j is done
-            with torch.cuda.stream(s_h2d):
-                for h, d in zip(h_in, d_in[j]):
-                    d.copy_(h, non_blocking=True)
-            ev_in[j].record(s_h2d)
-            stream.wait_event(ev_in[j])
-            for e in ev_out[j]:                  # slot j's previous outputs are on the host
-                stream.wait_event(e)
-            binding.din_sparse_fwd(db.tables, d_in[j][0], d_in[j][1], d_in[j][2], d_in[j][3],
-                                   db.max_len, db.q_feat, db.seq_table, B, mlp, d_out[j][0],
-                                   d_out[j][1], wsp, status=status, stream=stream)
-            ev_run[j].record(stream)
-            for k, sk in enumerate(s_d2h):
-                sk.wait_event(ev_run[j])
-                with torch.cuda.stream(sk):
-                    for d, h in slot_pieces[j][k]:
+        def e2e_steps(n):
+            ev_run, ev_out = [None, None], [None, None]
+            for i in range(n):
+                j = i & 1
+                if ev_run[j] is not None:
+                    s_h2d.wait_event(ev_run[j])      # the kernel that read slot j is done
+                with torch.cuda.stream(s_h2d):
+                    for h, d in zip(h_in, d_in[j]):
+                        d.copy_(h, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_h2d)
+                stream.wait_event(ev_in)
+                if ev_out[j] is not None:
+                    stream.wait_event(ev_out[j])     # slot j's previous outputs are on the host
+                binding.din_sparse_fwd(db.tables, d_in[j][0], d_in[j][1], d_in[j][2], d_in[j][3],
+                                       db.max_len, db.q_feat, db.seq_table, B, mlp, d_out[j][0],
+                                       d_out[j][1], wsp, status=status, stream=stream)
+                ev_run[j] = torch.cuda.Event()
+                ev_run[j].record(stream)
+                s_d2h.wait_event(ev_run[j])
+                with torch.cuda.stream(s_d2h):
+                    for d, h in zip(d_out[j], h_out[j]):
                         h.copy_(d, non_blocking=True)
-                ev_out[j][k].record(sk)
+                ev_out[j] = torch.cuda.Event()
+                ev_out[j].record(s_d2h)
 
-        for i in range(4):
-            e2e_step(i)
+        G = E2E_GRAPH
+        E = max(G, (args.e2e_steps // G) * G)
+        graph_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_e2e, stream=stream):
+            s_h2d.wait_stream(stream)
+            s_d2h.wait_stream(stream)
+            e2e_steps(G)
+            stream.wait_stream(s_h2d)
+            stream.wait_stream(s_d2h)
+        for _ in range(2):
+            graph_e2e.replay()
         torch.cuda.synchronize()
-        E = args.e2e_steps
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(E):
-            e2e_step(i)
-        stream.wait_stream(s_h2d)
-        for sk in s_d2h:
-            stream.wait_stream(sk)
+        for _ in range(E // G):
+            graph_e2e.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
         e2e_value = weak_rate(B * E, e2e_ms, ws)
         # the last step's results, read back, match the device-timed outputs
-        if not (torch.equal(h_out[(E - 1) & 1][1], din.cpu()) and
-                torch.equal(h_out[(E - 1) & 1][0], pooled.cpu())):
+        if not (torch.equal(h_out[(G - 1) & 1][1], din.cpu()) and
+                torch.equal(h_out[(G - 1) & 1][0], pooled.cpu())):
             raise RuntimeError("end-to-end outputs differ from the device-timed run")
 
     dynemb = None
@@ -640,8 +628,9 @@ def main():
                     "d2h_bytes_per_step": d2h,
                     "method": "pinned host inputs -> device, din_sparse_fwd, both outputs -> "
                               "pinned host, every step; two buffer slots, copies on their own "
-                              "streams (outputs split over %d) overlap the next step's kernel; no L2 "
-                              "flush (tables 201 MB > 129 MB L2)" % D2H_STREAMS},
+                              "streams overlap the next step's kernel; %d steps per captured CUDA "
+                              "graph, %d steps timed; no L2 flush (tables 201 MB > 129 MB L2)"
+                              % (E2E_GRAPH, E)},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "status": st,
