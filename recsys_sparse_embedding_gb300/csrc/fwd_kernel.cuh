@@ -47,7 +47,6 @@ constexpr int kShortBag = 16;       // batches whose bags all fit pool directly
 // Workspace layout (bytes). The header holds the prepared-weights tag, the
 // launch epoch and the exit counter that advances it.
 constexpr size_t kWsMagicOff = 0;
-constexpr size_t kWsDoneOff = 64;   // unused (kept: the layout is shared with the host)
 constexpr size_t kWsEpochOff = 128;
 constexpr size_t kWsPartOff = 256;
 constexpr size_t kWsPartBytes = size_t(kMaxG) * kMaxF * 8;

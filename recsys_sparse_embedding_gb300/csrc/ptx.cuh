@@ -61,13 +61,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- cp.async (16 B)
-// src_bytes = 0 writes 16 zero bytes without reading global memory.
-__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
-               "l"(gmem_src), "r"(src_bytes)
-               : "memory");
-}
-// L1-allocating variant: repeated rows (hot ids, small tables) hit in L1.
+// L1-allocating 16-byte copy: repeated rows (hot ids, small tables) hit in
+// L1. src_bytes = 0 writes 16 zero bytes without reading global memory.
 __device__ __forceinline__ void cp_async_16_ca(void* smem_dst, const void* gmem_src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
                "l"(gmem_src), "r"(src_bytes)
@@ -78,19 +73,10 @@ __device__ __forceinline__ void cp_async_16_ca(void* smem_dst, const void* gmem_
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
-// 4-byte copy (no alignment beyond 4 bytes needed).
-__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-// Wait until at most N of this thread's most recent cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// Wait until all of this thread's cp.async groups have landed.
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -273,14 +259,6 @@ __device__ __forceinline__ ulonglong2 ld_relaxed_u64x2(const unsigned long long*
   return v;
 }
 
-// Weak 16-byte load from L2 (not cached in L1), re-issued on every call: the
-// polling loads of the tagged exchange (each 8-byte word carries its own tag,
-// so a stale word is simply read again).
-__device__ __forceinline__ ulonglong2 ld_cg_u64x2(const unsigned long long* p) {
-  ulonglong2 v;
-  asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
-  return v;
-}
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
