@@ -97,6 +97,52 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def pool_bytes(batch):
+    """Algorithmic bytes of the pooling stage alone (rows a1-a2): 8 B per id +
+    4 B per bag length + one table row per id + the pooled output row."""
+    es = 2 if batch.wl.dtype == "bf16" else 4
+    n_ids = int(batch.values.size)
+    return 8 * n_ids + 4 * batch.F * batch.B + batch.D * es * n_ids + 4 * batch.F * batch.D * batch.B
+
+
+def time_pool_only(binding, db, wsp, flush, steps, batch, ws):
+    """emb_bag_pool alone (the KJT offsets scan and the pooled gather), graph
+    replays with L2 flushed between steps, against the HBM peak."""
+    import torch
+    B, F, D = db.B, db.F, db.D
+    pooled = torch.empty(B, F * D, device=flush.device)
+    status = torch.zeros(1, dtype=torch.int32, device=flush.device)
+    stream = torch.cuda.Stream(device=flush.device)
+
+    def step():
+        binding.emb_bag_pool(db.tables, db.values, db.lengths, B, pooled, wsp, status=status, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            step()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        stream.synchronize()
+        for i in range(steps):
+            flush.fill_(float(i & 7))
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()):
+        raise RuntimeError("pool-only status 0x%x" % int(status.item()))
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), ws, flush.device)
+    us = total_ms * 1e3 / steps
+    nbytes = pool_bytes(batch)
+    hbm, _, _, src = peaks()
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"what": "emb_bag_pool: KJT offsets and the pooled gather of all 16 tables (rows a1-a2)",
+            "us_per_step": us, "samples_per_s": weak_rate(B * steps, total_ms, ws),
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "algorithmic_bytes_per_launch": nbytes, "peak_source": src}}
+
+
 def algorithmic_work(batch):
     """Bytes and FLOPs the method must move / do for one batch (fp32 D=16):
     deep: 8 B per id + 4 B per bag length + 64 B per row + 1024 B output row;
@@ -423,6 +469,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-towers", action="store_true")
     ap.add_argument("--skip-dynemb", action="store_true")
+    ap.add_argument("--skip-pool", action="store_true")
+    ap.add_argument("--pool-steps", type=int, default=500)
     ap.add_argument("--skip-train", action="store_true")
     ap.add_argument("--train-steps", type=int, default=100)
     ap.add_argument("--dynemb-steps", type=int, default=500)
@@ -571,6 +619,10 @@ def main():
                 torch.equal(h_out[(G - 1) & 1][0], pooled.cpu())):
             raise RuntimeError("end-to-end outputs differ from the device-timed run")
 
+    pool_only = None
+    if not args.skip_pool:
+        pool_only = time_pool_only(binding, db, wsp, flush, args.pool_steps, batch, ws)
+
     dynemb = None
     if not args.skip_dynemb:
         dynemb = time_dynamic_emb(binding, synth, batch, dev, mode, flush, args.dynemb_steps, ws)
@@ -635,6 +687,7 @@ def main():
             "clocks": clk.summary(),
             "status": st,
             "towers": towers,
+            "pool_only": pool_only,
             "dynamic_emb": dynemb,
             "train_step": train,
         }

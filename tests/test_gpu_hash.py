@@ -145,3 +145,9 @@ def test_uninitialised_workspace_flagged():
     run.db.tables.hash.buf.zero_()      # header and keys gone: every probe sees full buckets
     _, _, _, st = run.fwd(TC)
     assert st & binding.FLAG_HASH
+
+
+def test_wide_bf16_tables_hashed():
+    """D = 64 bf16 rows in the hash pool (128-byte rows), both MLP modes."""
+    b = synth.dynamic_emb(synth.generate("wide_bf16", seed=3, B=384, nonzero_bias=True), seed=3)
+    check_batch(b)
