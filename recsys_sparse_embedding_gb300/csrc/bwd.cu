@@ -200,61 +200,89 @@ __device__ __forceinline__ void block_scan2(long long& a, long long& b, long lon
   __syncthreads();
 }
 
-// Pass 1 of the exclusive scans of max(len, 0) (raw) and min(max(len, 0),
-// clamp): the sums of each 2048-entry tile (coalesced loads).
-__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(const int* __restrict__ len, int n, int clamp,
-                                                                 long long* tsum) {
+// One scan: the exclusive scans of max(len, 0) (raw) and, when clp is given,
+// of min(max(len, 0), clamp) over n entries, in tiles of kScanTile.
+struct ScanJob {
+  const int* len;
+  int n, clamp, tiles;
+  long long *tsum, *raw, *clp;
+};
+// Both scans of a call run in the same two launches: blocks [0, tiles of job
+// 0) take job 0, the rest job 1.
+struct ScanJobs {
+  ScanJob j[2];
+};
+__device__ __forceinline__ const ScanJob& job_of(const ScanJobs& J, int& tile) {
+  const int which = int(blockIdx.x) < J.j[0].tiles ? 0 : 1;
+  tile = int(blockIdx.x) - (which ? J.j[0].tiles : 0);
+  return J.j[which];
+}
+
+// Pass 1: the sums of each tile (coalesced loads).
+__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(const ScanJobs jobs) {
+  int tile;
+  const ScanJob& J = job_of(jobs, tile);
   long long a = 0, b = 0;
   for (int r = 0; r < kScanRounds; ++r) {
-    const long long k = (long long)blockIdx.x * kScanTile + r * kScanThreads + threadIdx.x;
-    if (k < n) {
-      const int v = max(len[k], 0);
+    const long long k = (long long)tile * kScanTile + r * kScanThreads + threadIdx.x;
+    if (k < J.n) {
+      const int v = max(J.len[k], 0);
       a += v;
-      b += min(v, clamp);
+      b += min(v, J.clamp);
     }
   }
   long long ta, tb;
   block_scan2(a, b, ta, tb);
-  if (threadIdx.x == 0) tsum[2 * blockIdx.x] = ta, tsum[2 * blockIdx.x + 1] = tb;
+  if (threadIdx.x == 0) J.tsum[2 * tile] = ta, J.tsum[2 * tile + 1] = tb;
 }
 
 // Pass 2: each tile adds the sums of the tiles before it and scans its own
 // entries; the last tile writes the totals at index n.
-__global__ void __launch_bounds__(kScanThreads) scan_apply_kernel(const int* __restrict__ len, int n, int clamp,
-                                                                 const long long* __restrict__ tsum, long long* raw,
-                                                                 long long* clp) {
+__global__ void __launch_bounds__(kScanThreads) scan_apply_kernel(const ScanJobs jobs) {
+  int tile;
+  const ScanJob& J = job_of(jobs, tile);
   long long ca = 0, cb = 0;
-  for (int i = threadIdx.x; i < (int)blockIdx.x; i += kScanThreads) ca += tsum[2 * i], cb += tsum[2 * i + 1];
+  for (int i = threadIdx.x; i < tile; i += kScanThreads) ca += J.tsum[2 * i], cb += J.tsum[2 * i + 1];
   {
     long long ta, tb;
     block_scan2(ca, cb, ta, tb);
     ca = ta, cb = tb;
   }
   for (int r = 0; r < kScanRounds; ++r) {
-    const long long k = (long long)blockIdx.x * kScanTile + r * kScanThreads + threadIdx.x;
-    const int v = k < n ? max(len[k], 0) : 0;
-    long long a = v, b = min(v, clamp), ta, tb;
+    const long long k = (long long)tile * kScanTile + r * kScanThreads + threadIdx.x;
+    const int v = k < J.n ? max(J.len[k], 0) : 0;
+    long long a = v, b = min(v, J.clamp), ta, tb;
     block_scan2(a, b, ta, tb);
-    if (k < n) {
-      raw[k] = ca + a - v;
-      if (clp) clp[k] = cb + b - min(v, clamp);
+    if (k < J.n) {
+      J.raw[k] = ca + a - v;
+      if (J.clp) J.clp[k] = cb + b - min(v, J.clamp);
     }
     ca += ta, cb += tb;
   }
-  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
-    raw[n] = ca;
-    if (clp) clp[n] = cb;
+  if (tile == J.tiles - 1 && threadIdx.x == 0) {
+    J.raw[J.n] = ca;
+    if (J.clp) J.clp[J.n] = cb;
   }
 }
 
-// Column sums over rows of a [rows, cols] fp32 array, in a fixed order: one
-// block per column.
-__global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restrict__ part, int rows, int cols,
-                                                         float* out0, int n0, float* out1, int n1, float* out2) {
+// Column sums over the rows of [rows, cols] fp32 partial-sum arrays, in a
+// fixed order, one block per column: blocks [0, c0) sum part0 into dw3 | db2
+// | db3, the blocks after them (when part1 is given) part1 into db1.
+struct RedJobs {
+  const float* part0;
+  int rows0;
+  const float* part1;
+  int rows1;
+  float *dw3, *db2, *db3, *db1;
+};
+__global__ void __launch_bounds__(256) reduce_cols_kernel(const RedJobs r) {
   __shared__ float sh[256];
-  const int c = blockIdx.x;
+  const bool first = int(blockIdx.x) < kRedCols;
+  const int c = first ? int(blockIdx.x) : int(blockIdx.x) - kRedCols;
+  const float* part = first ? r.part0 : r.part1;
+  const int rows = first ? r.rows0 : r.rows1, cols = first ? kRedCols : kN1;
   float v = 0.f;
-  for (int r = threadIdx.x; r < rows; r += 256) v += part[(long long)r * cols + c];
+  for (int i = threadIdx.x; i < rows; i += 256) v += part[(long long)i * cols + c];
   sh[threadIdx.x] = v;
   __syncthreads();
   for (int o = 128; o; o >>= 1) {
@@ -262,9 +290,10 @@ __global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restric
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    if (c < n0) out0[c] = sh[0];
-    else if (c < n0 + n1) out1[c - n0] = sh[0];
-    else out2[c - n0 - n1] = sh[0];
+    if (!first) r.db1[c] = sh[0];
+    else if (c < kN2) r.dw3[c] = sh[0];
+    else if (c < 2 * kN2) r.db2[c - kN2] = sh[0];
+    else r.db3[0] = sh[0];
   }
 }
 
@@ -929,11 +958,11 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   float* part2 = reinterpret_cast<float*>(w + L.part2);
   {  // bag offsets of the KJT; raw and clamped sequence offsets
     const int nk = F * B, tk = (nk + kScanTile - 1) / kScanTile, ts = (B + kScanTile - 1) / kScanTile;
-    scan_tiles_kernel<<<tk, kScanThreads, 0, s>>>(kjt->lengths_dev, nk, INT_MAX, tsum);
-    scan_apply_kernel<<<tk, kScanThreads, 0, s>>>(kjt->lengths_dev, nk, INT_MAX, tsum, boff, nullptr);
-    long long* tsum2 = tsum + 2 * (tk + 1);
-    scan_tiles_kernel<<<ts, kScanThreads, 0, s>>>(seq->lengths_dev, B, seq->max_len, tsum2);
-    scan_apply_kernel<<<ts, kScanThreads, 0, s>>>(seq->lengths_dev, B, seq->max_len, tsum2, roff, soff);
+    ScanJobs jobs;
+    jobs.j[0] = ScanJob{kjt->lengths_dev, nk, INT_MAX, tk, tsum, boff, nullptr};
+    jobs.j[1] = ScanJob{seq->lengths_dev, B, seq->max_len, ts, tsum + 2 * (tk + 1), roff, soff};
+    scan_tiles_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
+    scan_apply_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
   }
   if (bf) {
     pack_kernel<<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
@@ -971,7 +1000,6 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   else
     softmax_bwd_kernel<float><<<sb, kWarpsPerBlock * 32, 0, s>>>(p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3,
                                                                  zb, dab, static_cast<float*>(dH2), dS, part1, Pc);
-  reduce_cols_kernel<<<kRedCols, 256, 0, s>>>(part1, sb, kRedCols, mg->dw3, kN2, mg->db2, kN2, mg->db3);
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   if (Pc > 0) {
     if (!gemm_rm(h, false, false, Pc, kN1, kN2, dH2, kN2, W2, kN1, G1, kN1, bf)) return DSF_ECUDA;
@@ -982,7 +1010,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     else
       relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
                                                  Pc);
-    reduce_cols_kernel<<<kN1, 256, 0, s>>>(part2, rb, kN1, mg->db1, kN1, nullptr, 0, nullptr);
+    reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s>>>(
+        RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
     if (!gemm_rm(h, false, false, Pc, K1, kN1, dH1, kN1, W1, K1, dX, K1, bf)) return DSF_ECUDA;
     if (!gemm_rm(h, true, false, kN1, K1, Pc, dH1, kN1, X, K1, mg->dW1, K1, bf)) return DSF_ECUDA;
     if (!gemm_rm(h, true, false, kN2, kN1, Pc, dH2, kN2, H1, kN1, mg->dW2, kN1, bf)) return DSF_ECUDA;
@@ -991,6 +1020,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
         cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess ||
         cudaMemsetAsync(mg->db1, 0, size_t(kN1) * 4, s) != cudaSuccess)
       return DSF_ECUDA;
+    reduce_cols_kernel<<<kRedCols, 256, 0, s>>>(RedJobs{part1, sb, nullptr, 0, mg->dw3, mg->db2, mg->db3, nullptr});
   }
   {
     float* gbag = reinterpret_cast<float*>(w + L.gbag);
