@@ -17,7 +17,7 @@ TOL_BF16 = (2e-2, 1e-2)         # abs OR rel
 TOL_BF16_EMUL = 2e-3            # vs the oracle with bf16-rounded MLP operands
 
 
-class GpuRun:
+class DeviceRun:
     def __init__(self, batch, device="cuda"):
         self.batch = batch
         self.db = to_device(batch, device)

@@ -16,7 +16,7 @@ import oracle
 from oracle import backward as obw
 from recsys_sparse_embedding_gb300 import binding, synth
 
-from helpers import GpuRun
+from helpers import DeviceRun
 from test_gpu_parity import F32, TC, _custom_batch
 
 pytestmark = pytest.mark.gpu
@@ -36,7 +36,7 @@ class Bwd:
 
     def __init__(self, batch, mode, seed=0, list_cap=None, with_dpooled=True):
         self.batch, self.mode = batch, mode
-        run = GpuRun(batch)
+        run = DeviceRun(batch)
         pooled, _, _, st = run.fwd(mode, logits=False)
         assert st & ~binding.FLAG_SEQ_TRUNC == 0
         self.run, self.db = run, run.db

@@ -12,7 +12,7 @@ import torch
 import oracle
 from recsys_sparse_embedding_gb300 import binding, synth
 
-from helpers import GpuRun, sample_ids
+from helpers import DeviceRun, sample_ids
 from test_gpu_parity import F32, TC, _custom_batch, check_batch
 
 pytestmark = pytest.mark.gpu
@@ -59,7 +59,7 @@ def test_hashed_staged_pooling_and_mean():
 
 def test_hashed_entry_points_agree():
     b = synth.dynamic_emb(synth.generate("taobao", seed=2, B=3000, nonzero_bias=True), seed=2)
-    run = GpuRun(b)
+    run = DeviceRun(b)
     for mode in (TC, F32):
         p_f, d_f, _, s1 = run.fwd(mode, "fused")
         p_p, _, _, s2 = run.fwd(mode, "pool")
@@ -141,7 +141,7 @@ def test_full_table_flags_and_keeps_what_fits():
 
 def test_uninitialised_workspace_flagged():
     b = synth.dynamic_emb(synth.generate("tiny", seed=8, B=16), capacity=1000, seed=8)
-    run = GpuRun(b)
+    run = DeviceRun(b)
     run.db.tables.hash.buf.zero_()      # header and keys gone: every probe sees full buckets
     _, _, _, st = run.fwd(TC)
     assert st & binding.FLAG_HASH

@@ -6,7 +6,7 @@ import torch
 import oracle
 from recsys_sparse_embedding_gb300 import binding, synth
 
-from helpers import (TOL_BF16_EMUL, GpuRun, assert_bf16_close, assert_f32_close, logits_of,
+from helpers import (TOL_BF16_EMUL, DeviceRun, assert_bf16_close, assert_f32_close, logits_of,
                      sample_ids)
 
 pytestmark = pytest.mark.gpu
@@ -19,7 +19,7 @@ def check_batch(batch, samples=None, modes=(TC, F32), expect_status=0, check_log
     """peaked=True: logits are large, so bf16 rounding of the MLP operands moves
     the softmax far more than 2e-2 from the fp64 result; the bf16 path is then
     held to the oracle at the same operand precision only."""
-    run = GpuRun(batch)
+    run = DeviceRun(batch)
     samples = np.arange(batch.B, dtype=np.int32) if samples is None else samples
     ref_pool, pflags = oracle.pool_batch(batch, samples)
     ref64, f64, lg64, _ = oracle.din_batch(batch, samples, want_logits=True)
@@ -119,7 +119,7 @@ def test_wide_bf16_full_size_sampled():
 
 def test_entry_points_agree():
     b = synth.generate("taobao", seed=2, B=3000, nonzero_bias=True)
-    run = GpuRun(b)
+    run = DeviceRun(b)
     for mode in (TC, F32):
         p_f, d_f, _, s1 = run.fwd(mode, "fused")
         p_p, _, _, s2 = run.fwd(mode, "pool")
@@ -132,7 +132,7 @@ def test_entry_points_agree():
 def test_repeated_calls_share_workspace():
     # the grid barrier resets itself between calls of different grid sizes
     b = synth.generate("tiny", seed=5, nonzero_bias=True)
-    run = GpuRun(b)
+    run = DeviceRun(b)
     first = run.fwd(TC)
     for i in range(20):
         which = ["fused", "pool", "attn"][i % 3]

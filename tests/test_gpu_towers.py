@@ -17,7 +17,7 @@ import torch
 import oracle
 from recsys_sparse_embedding_gb300 import binding, synth
 
-from helpers import GpuRun
+from helpers import DeviceRun
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +58,7 @@ def check(pooled, din, weights, name):
 def test_towers_on_sparse_path_outputs(wl, B, seed):
     """The CTR forward: din_sparse_fwd, then the towers on its device outputs."""
     batch = synth.generate(wl, seed=seed, B=B, nonzero_bias=True)
-    pooled, din, _, st = GpuRun(batch).fwd(binding.DSF_MODE_BF16_TC, logits=False)
+    pooled, din, _, st = DeviceRun(batch).fwd(binding.DSF_MODE_BF16_TC, logits=False)
     assert st == 0
     check(pooled, din, synth.tower_weights(seed, bias=0.1), wl)
 
