@@ -13,6 +13,10 @@ N>1 runs independent replicas, one per rank (launched by torch.distributed.run);
 the path has no cross-sample exchange, so there is no collective in a step.
 The reference arm (--impl reference) is the CPU oracle, timed on the host
 cores on a bounded sample of the same workload.
+
+Side legs, reported under their own keys of the same JSON line: the pooling
+stage alone (taobao, and the B=65536 gather-stress workload), the forward over
+hashed tables, the dense towers and one training step.
 """
 from __future__ import annotations
 
@@ -105,7 +109,7 @@ def pool_bytes(batch):
     return 8 * n_ids + 4 * batch.F * batch.B + batch.D * es * n_ids + 4 * batch.F * batch.D * batch.B
 
 
-def time_pool_only(binding, db, wsp, flush, steps, batch, ws):
+def time_pool_only(binding, db, wsp, flush, steps, batch, ws, workload="taobao B=8192"):
     """emb_bag_pool alone (the KJT offsets scan and the pooled gather), graph
     replays with L2 flushed between steps, against the HBM peak."""
     import torch
@@ -138,7 +142,7 @@ def time_pool_only(binding, db, wsp, flush, steps, batch, ws):
     hbm, _, _, src = peaks()
     ach = nbytes / (us * 1e-6) / 1e9
     return {"what": "emb_bag_pool: KJT offsets and the pooled gather of all 16 tables (rows a1-a2)",
-            "us_per_step": us, "samples_per_s": weak_rate(B * steps, total_ms, ws),
+            "workload": workload, "us_per_step": us, "samples_per_s": weak_rate(B * steps, total_ms, ws),
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "algorithmic_bytes_per_launch": nbytes, "peak_source": src}}
 
@@ -471,6 +475,8 @@ def main():
     ap.add_argument("--skip-dynemb", action="store_true")
     ap.add_argument("--skip-pool", action="store_true")
     ap.add_argument("--pool-steps", type=int, default=500)
+    ap.add_argument("--skip-pool-stress", action="store_true")
+    ap.add_argument("--pool-stress-steps", type=int, default=200)
     ap.add_argument("--skip-train", action="store_true")
     ap.add_argument("--train-steps", type=int, default=100)
     ap.add_argument("--dynemb-steps", type=int, default=500)
@@ -623,6 +629,17 @@ def main():
     if not args.skip_pool:
         pool_only = time_pool_only(binding, db, wsp, flush, args.pool_steps, batch, ws)
 
+    # the pooling stage where bandwidth, not the launch, dominates: B=65536,
+    # 1.92 GB of tables (five of 2M-10M rows), uniform ids
+    pool_stress = None
+    if not args.skip_pool_stress:
+        sb = synth.generate("gather_stress", seed=0)
+        sdb = to_device(sb, dev)
+        swsp = binding.Workspace(sb.B, sb.D, device=dev)
+        pool_stress = time_pool_only(binding, sdb, swsp, flush, args.pool_stress_steps, sb, ws,
+                                     workload="gather_stress B=65536, 1.92 GB fp32 tables, uniform ids")
+        del sdb, swsp, sb
+
     dynemb = None
     if not args.skip_dynemb:
         dynemb = time_dynamic_emb(binding, synth, batch, dev, mode, flush, args.dynemb_steps, ws)
@@ -688,6 +705,7 @@ def main():
             "status": st,
             "towers": towers,
             "pool_only": pool_only,
+            "pool_only_gather_stress": pool_stress,
             "dynamic_emb": dynemb,
             "train_step": train,
         }
