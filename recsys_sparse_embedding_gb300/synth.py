@@ -211,13 +211,16 @@ def xavier_uniform(rng: np.random.Generator, out_f: int, in_f: int,
 def generate(wl_name: str, seed: int = 0, B: Optional[int] = None,
              rows: Optional[Sequence[int]] = None, peaked: bool = False,
              nonzero_bias: bool = False,
-             seq_table: Optional[Sequence[int]] = None) -> Batch:
+             seq_table: Optional[Sequence[int]] = None,
+             ids_only: bool = False) -> Batch:
     """Draw one batch of the named workload.
 
     B / rows override the batch size and table sizes (for small parity cases
     that keep the workload's distributions). peaked=True draws tables N(0, 1)
     and scales the MLP weights by 4 so the softmax is far from uniform.
     nonzero_bias=True draws all biases U(-0.1, 0.1) instead of zeros.
+    ids_only=True skips drawing the tables (tables = []); every other field is
+    what a full draw with the same arguments gives (separate random streams).
     """
     wl = WORKLOADS[wl_name]
     B = wl.B if B is None else int(B)
@@ -228,7 +231,7 @@ def generate(wl_name: str, seed: int = 0, B: Optional[int] = None,
                                          for s in ss.spawn(5)]
     F, D = len(rows), wl.D
     std = 1.0 if peaked else 0.05
-    tables = [draw_table(r_tab, n, D, wl.dtype, std) for n in rows]
+    tables = [] if ids_only else [draw_table(r_tab, n, D, wl.dtype, std) for n in rows]
 
     # deep KJT: key-major lengths, then ids per feature
     lengths = np.ones((F, B), dtype=np.int32)
