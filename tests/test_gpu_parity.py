@@ -129,6 +129,19 @@ def test_entry_points_agree():
         assert np.array_equal(d_f, d_a)
 
 
+@pytest.mark.parametrize("wl,B,n", [("taobao", 20000, 512), ("long_multihot", 16384, 384),
+                                     ("gather_stress", None, 256)])
+def test_pool_only_large_batches(wl, B, n):
+    # more than 64 samples per CTA batch: pooling alone takes four bags per thread
+    b = synth.generate(wl, seed=1, B=B)
+    run = DeviceRun(b)
+    pooled, _, _, st = run.fwd(TC, "pool")
+    assert st == 0, "status 0x%x" % st
+    samples = sample_ids(b.B, n)
+    ref_pool, _ = oracle.pool_batch(b, samples)
+    assert np.array_equal(pooled[samples], ref_pool), "pooled differs from the oracle"
+
+
 def test_repeated_calls_share_workspace():
     # the grid barrier resets itself between calls of different grid sizes
     b = synth.generate("tiny", seed=5, nonzero_bias=True)
