@@ -470,12 +470,13 @@ def cpu_oracle_rate(batch, samples_per_pass, passes, threads):
         if ch.size:
             oracle.pool_batch(batch, ch)
             oracle.din_batch(batch, ch)
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         for _ in range(passes):
             list(ex.map(work, chunks))
     dt = time.perf_counter() - t0
-    return samples_per_pass * passes / dt, dt
+    cpu_s = time.process_time() - c0  # all threads of this process
+    return samples_per_pass * passes / dt, dt, cpu_s
 
 
 def run_reference(args):
@@ -488,7 +489,7 @@ def run_reference(args):
     per_step = 1024
     for _ in range(args.warmup):
         cpu_oracle_rate(batch, 64, 1, threads)
-    rate, dt = cpu_oracle_rate(batch, per_step, args.steps, threads)
+    rate, dt, cpu_s = cpu_oracle_rate(batch, per_step, args.steps, threads)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
@@ -497,7 +498,8 @@ def run_reference(args):
         "config": {"workload": workload_desc(batch.B), "B": batch.B,
                    "reference": "CPU oracle (plain C, fp64 attention), %d host threads" % threads},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "%d samples of the B=%d batch per step" % (per_step, batch.B)},
+                         "sample": "%d samples of the B=%d batch per step; %d steps took %.1f s wall, "
+                                   "%.1f s of CPU time" % (per_step, batch.B, args.steps, dt, cpu_s)},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -729,10 +731,10 @@ def main():
     cpu = None
     if rank == 0 and ws == 1 and not args.skip_cpu:
         threads = os.cpu_count() or 1
-        rate, dt = cpu_oracle_rate(batch, args.cpu_sample, args.cpu_passes, threads)
+        rate, dt, cpu_s = cpu_oracle_rate(batch, args.cpu_sample, args.cpu_passes, threads)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d passes over %d samples of the B=%d batch (%.1f s wall)"
-               % (args.cpu_passes, args.cpu_sample, B, dt)}
+               "sample": "%d passes over %d samples of the B=%d batch (%.1f s wall, %.1f s of CPU time)"
+               % (args.cpu_passes, args.cpu_sample, B, dt, cpu_s)}
 
     if rank == 0:
         line = {
