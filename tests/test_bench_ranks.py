@@ -1,5 +1,6 @@
-"""Host logic of bench.py's multi-GPU mode, run as two gloo ranks on the CPU:
-the max-over-ranks reduction and the whole-job (weak-scaling) rate."""
+"""Host logic of bench.py: the multi-GPU mode, run as two gloo ranks on the
+CPU (the max-over-ranks reduction and the whole-job, weak-scaling rate), and
+the JSON line of the reference arm."""
 import os
 import socket
 import sys
@@ -58,3 +59,22 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.weak_rate(100, 1000.0, 1) == pytest.approx(100.0)
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm is the CPU oracle: it runs without a GPU
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "samples/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
