@@ -424,7 +424,8 @@ template <class T>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
     const Params p, const long long* __restrict__ soff, const float* __restrict__ H2, const float* __restrict__ S,
     const float* __restrict__ ddin, const float* __restrict__ b2, const float* __restrict__ w3,
-    const float* __restrict__ b3, float* zb, float* dab, T* dH2, float* dS, float* part, long long Pc) {
+    const float* __restrict__ b3, float* __restrict__ zb, float* __restrict__ dab, T* __restrict__ dH2,
+    float* __restrict__ dS, float* __restrict__ part, long long Pc) {
   __shared__ float red[kWarpsPerBlock][kRedCols];
   __shared__ float sw3[kN2], sb2[kN2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
         dz_l = a_l * (dab[qm] - c);
       }
       const int n = int(min((long long)32, p1 - q0));
+#pragma unroll 4
       for (int t = 0; t < n; ++t) {
         const long long q = q0 + t;
         const float a = __shfl_sync(0xffffffffu, a_l, t), dz = __shfl_sync(0xffffffffu, dz_l, t);
@@ -549,8 +551,9 @@ constexpr int kPG = 4;
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
     const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
     const long long* __restrict__ roff, long long Pc, const float* __restrict__ pooled,
-    const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S, float* dS,
-    float* gbag, unsigned long long* okey, long long* osrc) {
+    const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S,
+    float* __restrict__ dS, float* __restrict__ gbag, unsigned long long* __restrict__ okey,
+    long long* __restrict__ osrc) {
   __shared__ float dqs[kWarpsPerBlock][3 * 64];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
