@@ -32,6 +32,10 @@
  *   - One workspace may serve one stream at a time: two calls that overlap on
  *     the GPU must not share a workspace (its launch epoch and per-block
  *     partial sums would race).
+ *   - The library keeps per-device state from its first call on a device
+ *     (grid sizes, the address of emb_bag_pool_noalloc's array, library
+ *     handles). It does not survive cudaDeviceReset of that device: after a
+ *     reset, start a new process before calling it again.
  *   - Device data errors never fault or trap: an id outside [0, rows) or a
  *     value index past the values array contributes a zero row; a negative
  *     length counts as zero; a sequence longer than max_len keeps its first
@@ -232,19 +236,34 @@ int din_sparse_fwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* 
  * It takes no workspace: the cross-CTA exchange state (a header and one partial
  * sum per CTA and table) lives in a fixed 262,400-byte array compiled into the
  * library, which every GPU that loads the library holds until the process
- * exits. Limits: F <= DSF_MAX_TABLES (32) and a kernel grid of at most 1024
- * CTAs (larger devices get DSF_EUNSUPPORTED); B is not limited by the array.
+ * exits. Limits: F <= DSF_MAX_TABLES (32); the kernel grid is capped at 1024
+ * CTAs (the array's rows), so a device with room for more resident CTAs runs
+ * 1024 of them; B is not limited by the array.
  * The first call on a device, made with that device current, looks up the
  * array's device address and clears it on `stream`; make that first call
- * before any stream capture. Every call shares the one array and leaves it
- * ready for the next call, so calls that overlap on the GPU (for instance on
- * two streams) race: serialise them. Allocates nothing (no cudaMalloc or
- * cudaFree, no allocating library call). */
+ * before any stream capture (later calls may be captured into a graph and
+ * replayed). Every call shares the one array and leaves it ready for the next
+ * call, so calls that overlap on the GPU (for instance on two streams) race:
+ * serialise them. After a call that set DSF_FLAG_TIMEOUT, that call's pooled
+ * rows are invalid; the array needs no reset, since the kernel advances its
+ * launch epoch on a timeout as well and the next call's exchange starts from
+ * it. Allocates nothing (no cudaMalloc or cudaFree, no allocating library
+ * call). */
 int emb_bag_pool_noalloc(const dsf_tables* tables, const dsf_kjt* kjt, int32_t B,
                          float* pooled_dev, int32_t* status_dev, void* stream);
 
 /* Human-readable name of a return code. */
 const char* dsf_status_string(int code);
+
+/* Copies the status word *status_dev (the DSF_FLAG_* bits the calls on
+ * `stream` OR-ed into it) to *status_host once the work queued on `stream`
+ * before this call has finished: an asynchronous device-to-host copy on
+ * `stream`, then a wait for that stream (blocks the host thread). The pages
+ * define no such call; it is the host side of the status convention above.
+ * Returns DSF_EINVAL for a null pointer (nothing copied), DSF_ECUDA if the
+ * copy or the wait fails (*status_host unchanged); must not be called while
+ * `stream` is being captured into a graph. */
+int dsf_read_status(const int32_t* status_dev, int32_t* status_host, void* stream);
 
 /* Grid size (CTAs) the forward kernels use on the current device for this
  * call shape; 0 if unsupported. For diagnostics and benchmarks. */
@@ -329,6 +348,24 @@ typedef struct {
  * n_per_key sequence values (0 for invalid arguments); caller-owned,
  * 256-byte aligned. */
 size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_values, int64_t n_per_key, int32_t D);
+
+/* Where din_sparse_bwd leaves its per-position intermediates inside a
+ * workspace sized by dsf_bwd_workspace_bytes with the same arguments: byte
+ * offsets from the workspace's start, written to offsets[6] in this order
+ *   x   [P, 12D] MLP operand type    [q, s, q - s, q * s] per position
+ *   h1  [P, 256] MLP operand type    ReLU(x W1^T + b1)
+ *   h2  [P, 64]  fp32                h1 W2^T (b2 not added)
+ *   dh2 [P, 64]  MLP operand type    dz w3 [h1 W2^T + b2 > 0]
+ *   g   [P, 256] fp32                dh2 W2 (before the layer-1 mask)
+ *   dh1 [P, 256] MLP operand type    g [h1 > 0]
+ * (operand type: bf16 in DSF_MODE_BF16_TC, else fp32; rows: the valid
+ * sequence positions in sample order, then zero rows up to n_per_key). The
+ * values stay there from the end of a din_sparse_bwd call on that workspace
+ * until the workspace's next use. An inspection aid (for tests of the
+ * intermediate values): the pages define no such call. Host only, no CUDA
+ * call; DSF_EINVAL for a null pointer or arguments that
+ * dsf_bwd_workspace_bytes rejects. */
+int dsf_bwd_workspace_offsets(int32_t B, int64_t n_values, int64_t n_per_key, int32_t D, int64_t* offsets);
 
 /* Returns DSF_EINVAL / DSF_EUNSUPPORTED / DSF_EWORKSPACE for bad arguments
  * (as din_sparse_fwd), DSF_ECUDA when a launch or a library call fails.

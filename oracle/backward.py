@@ -138,7 +138,54 @@ def forward(batch, bf16=False, pooled=None):
         a[sl] = e / e.sum()
         din[b] = a[sl] @ s32[sl].astype(np.float64)
     return dict(q32=q32, s32=s32, samp=samp, j=j, Lc=Lc, starts=starts, x=x, W1=W1, W2=W2,
-                pre1=pre1, h1=h1, pre2=pre2, h2=h2, z=z, a=a, din=din, w3=w3)
+                b1=b1, b2=b2, b3=b3, pre1=pre1, h1=h1, pre2=pre2, h2=h2, z=z, a=a, din=din, w3=w3)
+
+
+# Per-term relative error allowed for an fp32 sum evaluated in another order:
+# twice the unit roundoff of round-to-nearest fp32, so that adders which
+# truncate (tensor-core accumulation) are covered as well.
+ACC_UNIT = 2.0 ** -22
+
+
+def bf16_spread(v, e):
+    """Largest |bf16(w) - bf16(v)| over |w - v| <= e: rounding to bf16 is
+    monotone, so the extremes sit at the two ends of the interval (w is an
+    fp32 value, and rounding the ends to fp32 only widens the bound)."""
+    r = round_bf16(v)
+    return np.maximum(np.abs(round_bf16(v + e) - r), np.abs(round_bf16(v - e) - r))
+
+
+def error_bounds(fw, bf16, ddin, dh2_op):
+    """Where another evaluation of this backward may differ from this one.
+
+    Two evaluations with the same inputs and the same operand roundings
+    differ continuously (fp32 sums in another order) except where a step
+    function lies on the path: a ReLU whose input is within the accumulated
+    rounding error of zero may be taken either way, and a bf16 rounding whose
+    input is within that error of a rounding boundary may go to the other
+    neighbour. Returns, per quantity, the bound on the rounding error of the
+    step that forms it from its inputs (ACC_UNIT per term of its sums):
+    C1 and amb1 (|pre1| <= C1: the layer-1 ReLU may go either way), h1 (the
+    largest change of bf16(ReLU(pre1)) when pre1 moves by C1), acc2 (of
+    h1 W2^T + b2), accz (of w3 . h2 + b3), acc_da (of ddin . s), accG (of
+    dh2 W2), Lb (each position's sample length, for the softmax sums)."""
+    U = ACC_UNIT
+    x, W1, W2, w3 = fw["x"], fw["W1"], fw["W2"], fw["w3"]
+    pre1, h1, samp = fw["pre1"], fw["h1"], fw["samp"]
+    C1 = (x.shape[1] + 2) * U * (np.abs(x) @ np.abs(W1).T + np.abs(fw["b1"]))
+    if bf16:   # h1 = bf16(ReLU(pre1)) is monotone in pre1: its extremes at the ends
+        h1b = np.maximum(np.abs(round_bf16(np.maximum(pre1 + C1, 0)) - h1),
+                         np.abs(round_bf16(np.maximum(pre1 - C1, 0)) - h1))
+    else:
+        h1b = C1 * (pre1 > -C1)
+    s = fw["s32"].astype(np.float64)
+    B = ddin.shape[0]
+    Lb = np.bincount(samp, minlength=B)[samp] if samp.size else np.zeros(0)
+    return dict(C1=C1, amb1=np.abs(pre1) <= C1, h1=h1b, Lb=Lb,
+                acc2=(h1.shape[1] + 2) * U * (np.abs(h1) @ np.abs(W2).T + np.abs(fw["b2"])),
+                accz=(w3.size + 2) * U * (np.abs(fw["h2"]) @ np.abs(w3) + abs(fw["b3"])),
+                acc_da=(s.shape[1] + 1) * U * np.einsum("pd,pd->p", np.abs(ddin[samp]), np.abs(s)),
+                accG=(W2.shape[0] + 1) * U * (np.abs(dh2_op) @ np.abs(W2)))
 
 
 def backward(batch, dpooled, ddin, bf16=False, pooled=None):
@@ -151,7 +198,10 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
     row is not a parameter, and invalid ids get none); rows_abs and bounds:
     each row gradient's and weight gradient's sum of absolute terms, carried
     through the whole chain (|da| = |ddin|.|s|, |dz| = a (|da| + sum a |da|),
-    ...), which bounds the rounding errors of any evaluation order."""
+    ...), which bounds the rounding errors of any evaluation order; cand: the
+    error bounds of error_bounds; inter: the forward and backward
+    intermediates (per position: x, pre1, h1, pre2, h2, a, dz, dh2 and its
+    operand dh2_op, G = dh2_op W2, dh1 and dh1_op)."""
     fw = forward(batch, bf16, pooled)
     D, B, F = batch.D, batch.B, batch.F
     Q = 3 * D
@@ -172,7 +222,8 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
     db2 = dh2.sum(axis=0)
     dh2_op = round_bf16(dh2) if bf16 else dh2
     dW2 = dh2_op.T @ fw["h1"]
-    dh1 = (dh2_op @ fw["W2"]) * (fw["pre1"] > 0)
+    G = dh2_op @ fw["W2"]
+    dh1 = G * (fw["pre1"] > 0)
     db1 = dh1.sum(axis=0)
     dh1_op = round_bf16(dh1) if bf16 else dh1
     dW1 = dh1_op.T @ fw["x"]
@@ -196,22 +247,39 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
     dq_m = np.zeros((B, Q))
     np.add.at(dq_m, samp, dx_m[:, :Q] + dx_m[:, 2 * Q:3 * Q] + dx_m[:, 3 * Q:] * np.abs(s))
     ds_m = a[:, None] * np.abs(ddin[samp]) + dx_m[:, Q:2 * Q] + dx_m[:, 2 * Q:3 * Q] + dx_m[:, 3 * Q:] * aq
-    # row gradients
-    tables, values, seq_values = resolve_hashed(batch)
-    hk = getattr(batch, "hash_keys", None) or {}
-    lengths = np.maximum(np.asarray(batch.lengths, np.int64).reshape(F, B), 0)
-    bag_off = np.concatenate([[0], np.cumsum(lengths.reshape(-1))])
-    pooling = getattr(batch, "pooling", None)
+    # row gradients and their magnitude sums
     g_bag = dpooled.reshape(B, F, D).copy()
     g_bag_m = np.abs(g_bag)
     for k, f in enumerate(batch.q_feat):
         g_bag[:, f, :] += dq[:, k * D:(k + 1) * D]
         g_bag_m[:, f, :] += dq_m[:, k * D:(k + 1) * D]
-    contrib_f, contrib_r, contrib_g, contrib_m = [], [], [], []
+    rows = row_sums(batch, g_bag, ds, fw["j"])
+    rows_abs = {f: v for f, (_, v) in row_sums(batch, g_bag_m, ds_m, fw["j"]).items()}
+    bounds = dict(dW2=dh2_m.T @ np.abs(fw["h1"]), dW1=dh1_m.T @ np.abs(fw["x"]), db2=dh2_m.sum(axis=0),
+                  db1=dh1_m.sum(axis=0), dw3=dz_m @ np.abs(fw["h2"]), db3=np.array([dz_m.sum()]))
+    inter = dict(fw, dz=dz, da=da, c=c, dh2=dh2, dh2_op=dh2_op, G=G, dh1=dh1, dh1_op=dh1_op, ddin=ddin)
+    return dict(dW1=dW1, db1=db1, dW2=dW2, db2=db2, dw3=dw3, db3=db3, dq=dq, ds=ds, rows=rows,
+                rows_abs=rows_abs, bounds=bounds, cand=error_bounds(fw, bf16, ddin, dh2_op), inter=inter,
+                din=fw["din"])
+
+
+def row_sums(batch, g_bag, g_pos, j):
+    """Sums per touched row, as the row gradients are formed: every value of
+    bag (f, b) receives g_bag[b, f] (divided by the bag length when f pools by
+    mean), and row seq_values[k][j_t] of table seq_table[k] receives the k-th
+    D-slice of g_pos[t]; ids outside the table, unseen hash keys (the zero
+    row) and nothing else are left out. Returns {f: (rows, sums [n, D])}."""
+    F, B, D = batch.F, batch.B, batch.D
+    tables, values, seq_values = resolve_hashed(batch)
+    hk = getattr(batch, "hash_keys", None) or {}
+    lengths = np.maximum(np.asarray(batch.lengths, np.int64).reshape(F, B), 0)
+    bag_off = np.concatenate([[0], np.cumsum(lengths.reshape(-1))])
+    pooling = getattr(batch, "pooling", None)
 
     def valid(f, ids):
         n = tables[f].shape[0] - (1 if f in hk else 0)   # the zero row is not a parameter
         return (ids >= 0) & (ids < n)
+    cf, cr, cg = [], [], []
     for f in range(F):
         lf = lengths[f]
         n = int(lf.sum())
@@ -221,37 +289,25 @@ def backward(batch, dpooled, ddin, bf16=False, pooled=None):
         ids = values[start:start + n]
         bag = np.repeat(np.arange(B), lf)
         g = g_bag[bag, f, :]
-        gm = g_bag_m[bag, f, :]
         if pooling is not None and pooling[f] == 1:
             g = g / lf[bag][:, None]
-            gm = gm / lf[bag][:, None]
         ok = valid(f, ids)
-        contrib_f.append(np.full(int(ok.sum()), f)); contrib_r.append(ids[ok]); contrib_g.append(g[ok])
-        contrib_m.append(gm[ok])
+        cf.append(np.full(int(ok.sum()), f)); cr.append(ids[ok]); cg.append(g[ok])
     for k, tb in enumerate(batch.seq_table):
-        ids = seq_values[k, fw["j"]] if P else np.zeros(0, np.int64)
+        ids = seq_values[k, j] if j.size else np.zeros(0, np.int64)
         ok = valid(tb, ids)
-        contrib_f.append(np.full(int(ok.sum()), tb)); contrib_r.append(ids[ok])
-        contrib_g.append(ds[ok, k * D:(k + 1) * D])
-        contrib_m.append(ds_m[ok, k * D:(k + 1) * D])
-    cf = np.concatenate(contrib_f) if contrib_f else np.zeros(0, np.int64)
-    cr = np.concatenate(contrib_r) if contrib_r else np.zeros(0, np.int64)
-    cg = np.concatenate(contrib_g) if contrib_g else np.zeros((0, D))
-    cm = np.concatenate(contrib_m) if contrib_m else np.zeros((0, D))
-    rows, rows_abs = {}, {}
+        cf.append(np.full(int(ok.sum()), tb)); cr.append(ids[ok]); cg.append(g_pos[ok, k * D:(k + 1) * D])
+    cf = np.concatenate(cf) if cf else np.zeros(0, np.int64)
+    cr = np.concatenate(cr) if cr else np.zeros(0, np.int64)
+    cg = np.concatenate(cg) if cg else np.zeros((0, D))
+    out = {}
     for f in np.unique(cf):
         m = cf == f
         u, inv = np.unique(cr[m], return_inverse=True)
         acc = np.zeros((u.size, D))
         np.add.at(acc, inv, cg[m])
-        mag = np.zeros((u.size, D))
-        np.add.at(mag, inv, cm[m])
-        rows[int(f)] = (u, acc)
-        rows_abs[int(f)] = mag
-    bounds = dict(dW2=dh2_m.T @ np.abs(fw["h1"]), dW1=dh1_m.T @ np.abs(fw["x"]), db2=dh2_m.sum(axis=0),
-                  db1=dh1_m.sum(axis=0), dw3=dz_m @ np.abs(fw["h2"]), db3=np.array([dz_m.sum()]))
-    return dict(dW1=dW1, db1=db1, dW2=dW2, db2=db2, dw3=dw3, db3=db3, dq=dq, ds=ds, rows=rows,
-                rows_abs=rows_abs, bounds=bounds, din=fw["din"])
+        out[int(f)] = (u, acc)
+    return out
 
 
 def adagrad(table, accum, rows, grads, lr=1e-3, eps=1e-10):

@@ -32,7 +32,8 @@ EXPORTS = ["dsf_workspace_bytes", "dsf_workspace_init", "dsf_prepare_mlp", "emb_
            "din_jagged_attn", "din_sparse_fwd", "dsf_status_string", "dsf_grid_size",
            "emb_bag_pool_noalloc", "dsf_towers_workspace_bytes", "dsf_prepare_towers", "ctr_towers_fwd",
            "dsf_hash_workspace_bytes", "dsf_hash_init", "dsf_hash_insert", "dsf_hash_find",
-           "dsf_bwd_workspace_bytes", "din_sparse_bwd", "emb_adagrad_update"]
+           "dsf_bwd_workspace_bytes", "din_sparse_bwd", "emb_adagrad_update", "dsf_read_status",
+           "dsf_bwd_workspace_offsets"]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
@@ -127,12 +128,24 @@ def lib() -> ctypes.CDLL:
         L.din_sparse_bwd.restype = ctypes.c_int
         L.emb_adagrad_update.argtypes = [P(CTables), _vp, P(CRowGrads), ctypes.c_float, ctypes.c_float, _vp, _vp]
         L.emb_adagrad_update.restype = ctypes.c_int
+        L.dsf_read_status.argtypes = [_vp, _vp, _vp]
+        L.dsf_read_status.restype = ctypes.c_int
+        L.dsf_bwd_workspace_offsets.argtypes = [_i32, _i64, _i64, _i32, _vp]
+        L.dsf_bwd_workspace_offsets.restype = ctypes.c_int
         _lib = L
     return _lib
 
 
 def status_string(code: int) -> str:
     return lib().dsf_status_string(int(code)).decode()
+
+
+def read_status(status, stream=None) -> int:
+    """The DSF_FLAG_* bits in a device status word, once the work queued on
+    the stream so far has finished (dsf_read_status)."""
+    out = ctypes.c_int32(0)
+    _check(lib().dsf_read_status(_dptr(status), ctypes.byref(out), _stream_ptr(stream)), "dsf_read_status")
+    return int(out.value)
 
 
 def _check(rc: int, where: str) -> None:
@@ -422,6 +435,25 @@ class BwdWorkspace:
         if self.nbytes == 0:
             raise DsfError(DSF_EINVAL, "dsf_bwd_workspace_bytes")
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        off = (ctypes.c_int64 * 6)()
+        _check(lib().dsf_bwd_workspace_offsets(int(B), int(n_values), int(n_per_key), int(D),
+                                               ctypes.cast(off, _vp)), "dsf_bwd_workspace_offsets")
+        self.offsets = list(off)
+        self.D = int(D)
+
+    def views(self, P: int, bf16: bool):
+        """The intermediates the last din_sparse_bwd left in this workspace,
+        over the first P positions: x, h1, h2 (h1 W2^T), dh2, g (dh2 W2),
+        dh1, as tensors viewing the buffer."""
+        K1 = 12 * self.D
+        op = torch.bfloat16 if bf16 else torch.float32
+        out = {}
+        for i, (name, width, dt) in enumerate((("x", K1, op), ("h1", 256, op), ("h2", 64, torch.float32),
+                                               ("dh2", 64, op), ("g", 256, torch.float32), ("dh1", 256, op))):
+            es = 2 if dt == torch.bfloat16 else 4
+            o = self.offsets[i]
+            out[name] = self.buf[o:o + P * width * es].view(dt).view(P, width)
+        return out
 
 
 def din_sparse_bwd(tables: EmbeddingTables, values, lengths, seq_values, seq_lengths, max_len: int, q_feat,

@@ -238,6 +238,16 @@ const char* dsf_status_string(int code) {
   }
 }
 
+int dsf_read_status(const int32_t* status_dev, int32_t* status_host, void* stream) {
+  if (!status_dev || !status_host) return DSF_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, status_dev, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DSF_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSF_ECUDA;
+  *status_host = v;
+  return DSF_OK;
+}
+
 int32_t dsf_grid_size(int32_t D, int32_t dtype, int32_t mode, int32_t with_attention) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -885,6 +885,15 @@ extern "C" size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_values, int64_t n
   return bwd::layout(B, n_values, n_per_key, kMaxF, D).total;
 }
 
+extern "C" int dsf_bwd_workspace_offsets(int32_t B, int64_t n_values, int64_t n_per_key, int32_t D,
+                                         int64_t* offsets) {
+  if (!offsets || dsf_bwd_workspace_bytes(B, n_values, n_per_key, D) == 0) return DSF_EINVAL;
+  const bwd::Layout L = bwd::layout(B, n_values, n_per_key, kMaxF, D);
+  const size_t at[6] = {L.X, L.H1, L.H2, L.dH2, L.G1, L.dH1};
+  for (int i = 0; i < 6; ++i) offsets[i] = static_cast<int64_t>(at[i]);
+  return DSF_OK;
+}
+
 extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq, const int32_t* q_feat,
                               const int32_t* seq_table, int32_t B, const dsf_mlp* mlp, const float* pooled_dev,
                               const float* dpooled_dev, const float* ddin_dev, const dsf_mlp_grads* mg,

@@ -4,17 +4,23 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fwd_kernel.cuh"
 
 namespace dsf {
 
 constexpr int kMaxDevices = 64;
 
+// The grid size is computed on the first launch per device and cached; host
+// threads may race on that first computation (each gets the same value), so
+// the cache words are atomics.
 template <class C>
 int grid_for_device(int dev) {
-  static int cache[kMaxDevices] = {0};
+  static std::atomic<int> cache[kMaxDevices];
   if (dev < 0 || dev >= kMaxDevices) return 0;
-  if (cache[dev] > 0) return cache[dev];
+  const int known = cache[dev].load(std::memory_order_acquire);
+  if (known > 0) return known;
   constexpr int smem = smem_bytes<C>();
   static_assert(smem <= 227 * 1024, "shared memory per block above the sm_100-family limit");
   int optin = 0, nsm = 0;
@@ -30,7 +36,7 @@ int grid_for_device(int dev) {
   if (occ < 1) return 0;
   int g = nsm * occ;
   if (g > kMaxG) g = kMaxG;
-  cache[dev] = g;
+  cache[dev].store(g, std::memory_order_release);
   return g;
 }
 

@@ -176,3 +176,28 @@ def test_no_fallback_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         binding.lib()
+
+
+def test_read_status_rejects_null_pointers(L):
+    out = ctypes.c_int32(7)
+    assert L.dsf_read_status(None, ctypes.byref(out), None) == binding.DSF_EINVAL
+    assert L.dsf_read_status(4096, None, None) == binding.DSF_EINVAL
+    assert out.value == 7
+
+
+def test_bwd_workspace_offsets(L):
+    """The six intermediates lie inside the workspace, 256-byte aligned, each
+    with room for its [n_per_key, width] fp32 rows, without overlap."""
+    for B, nv, npk, D in ((8192, 200000, 40000, 16), (3, 0, 0, 64), (0, 5, 7, 16)):
+        off = (ctypes.c_int64 * 6)()
+        assert L.dsf_bwd_workspace_offsets(B, nv, npk, D, off) == binding.DSF_OK
+        total = L.dsf_bwd_workspace_bytes(B, nv, npk, D)
+        widths = (12 * D, 256, 64, 64, 256, 256)
+        spans = sorted((off[i], off[i] + npk * widths[i] * 4) for i in range(6))
+        for (a, e), (a2, _) in zip(spans, spans[1:]):
+            assert e <= a2
+        assert all(o % 256 == 0 for o in off) and spans[-1][1] <= total
+    off = (ctypes.c_int64 * 6)()
+    assert L.dsf_bwd_workspace_offsets(4, 1, 1, 32, off) == binding.DSF_EINVAL
+    assert L.dsf_bwd_workspace_offsets(4, -1, 1, 16, off) == binding.DSF_EINVAL
+    assert L.dsf_bwd_workspace_offsets(4, 1, 1, 16, None) == binding.DSF_EINVAL

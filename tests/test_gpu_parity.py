@@ -218,3 +218,21 @@ def test_mean_pooling_deep_and_query_tables():
     c = _custom_batch(list(rng.integers(0, 40, size=120)), bags_len=lens)
     c.pooling = pooling
     check_batch(c)
+
+
+def test_read_status_through_the_c_abi():
+    """dsf_read_status returns the device word once the stream's earlier work
+    is done: a flag a forward call sets, and a value written on a side stream."""
+    b = _custom_batch([4, 6, 3])
+    b.values[3] = 10 ** 12
+    run = DeviceRun(b)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        binding.emb_bag_pool(run.db.tables, run.db.values, run.db.lengths, b.B,
+                             torch.empty(b.B, b.F * b.D, device="cuda"), run.ws, status=st, stream=s)
+    assert binding.read_status(st, stream=s) == binding.FLAG_ID_RANGE
+    with torch.cuda.stream(s):
+        st.fill_(0x1234)
+    assert binding.read_status(st, stream=s) == 0x1234
