@@ -14,10 +14,17 @@ the path has no cross-sample exchange, so there is no collective in a step.
 The reference arm (--impl reference) is the CPU oracle, timed on the host
 cores on a bounded sample of the same workload.
 
+The K timed steps run inside a window of about a second of identical steps,
+over which the SM clocks are sampled; the line reports the K-step mean (the
+headline), the per-step median and spread, and the window's statistics.
+
 Side legs, reported under their own keys of the same JSON line: the forward
-over a stream of distinct batches without L2 flushes, the pooling stage alone
-(taobao, and the B=65536 gather-stress workload), the forward over hashed
-tables, the dense towers and one training step.
+on every workload at full size (configs: tiny, taobao, long_multihot,
+gather_stress, wide_bf16, each with its roofline), the forward over a stream
+of distinct batches without L2 flushes, the pooling stage alone (taobao, and
+the B=65536 gather-stress workload), the forward over hashed tables, the
+dense towers and one training step; and on the host, the oracle on all cores
+(cpu_baseline), on one core, and the padded flow on one core.
 """
 from __future__ import annotations
 
@@ -42,6 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 E2E_GRAPH = 20    # pipelined end-to-end steps per captured graph
+CLOCK_WINDOW_S = 1.2  # steps run around the timed ones while the clocks are sampled
 KERNEL_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "hash.cuh", "launch.cuh", "fwd_attn_tc.cu"]
 
 
@@ -102,6 +110,47 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def step_stats(us):
+    """Per-step times (us): mean, median and spread."""
+    a = np.asarray(us, dtype=np.float64)
+    if a.size == 0:
+        return None
+    return {"mean": float(a.mean()), "median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "min": float(a.min()), "max": float(a.max()), "n": int(a.size)}
+
+
+def time_flushed(run, flush, steps, stream):
+    """Per-step us of run() on stream, each step bracketed by its own pair of
+    CUDA events, with L2 flushed (a 512 MB write) before each step, outside
+    the events."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(float(i & 7))
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+
+def roofline(nbytes, flops, us):
+    """HBM and tensor fractions of one launch of a kernel timed alone (the
+    burst tensor peak), the binding one first."""
+    hbm, tfs, _, src = peaks()
+    t = us * 1e-6
+    ach_gbs, ach_tfs = nbytes / t / 1e9, flops / t / 1e12
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tfs * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {"bound": bound, "achieved": ach_gbs if bound == "hbm" else ach_tfs,
+            "peak": hbm if bound == "hbm" else tfs, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": ach_gbs / hbm if bound == "hbm" else ach_tfs / tfs,
+            "hbm_frac": ach_gbs / hbm, "tensor_achieved_tflops": ach_tfs, "tensor_frac": ach_tfs / tfs,
+            "combined_frac": max(t_hbm, t_tc) / t, "algorithmic_bytes_per_launch": nbytes,
+            "flops_per_launch": flops, "peak_source": src, "tensor_peak_kind": "burst (kernel timed alone)"}
+
+
 def pool_bytes(batch):
     """Algorithmic bytes of the pooling stage alone (rows a1-a2): 8 B per id +
     4 B per bag length + one table row per id + the pooled output row."""
@@ -127,23 +176,18 @@ def time_pool_only(binding, db, wsp, flush, steps, batch, ws, workload="taobao B
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        stream.synchronize()
-        for i in range(steps):
-            flush.fill_(float(i & 7))
-            ev[i][0].record(stream)
-            g.replay()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+    stream.synchronize()
+    per = time_flushed(g.replay, flush, steps, stream)
     if int(status.item()):
         raise RuntimeError("pool-only status 0x%x" % int(status.item()))
-    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), ws, flush.device)
+    total_ms = max_over_ranks(sum(per) / 1e3, ws, flush.device)
     us = total_ms * 1e3 / steps
     nbytes = pool_bytes(batch)
     hbm, _, _, src = peaks()
     ach = nbytes / (us * 1e-6) / 1e9
     return {"what": "emb_bag_pool: KJT offsets and the pooled gather of all 16 tables (rows a1-a2)",
-            "workload": workload, "us_per_step": us, "samples_per_s": weak_rate(B * steps, total_ms, ws),
+            "workload": workload, "us_per_step": us, "us_stats": step_stats(per),
+            "samples_per_s": weak_rate(B * steps, total_ms, ws),
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "algorithmic_bytes_per_launch": nbytes, "peak_source": src}}
 
@@ -211,6 +255,58 @@ def algorithmic_work(batch):
     return deep + din, flops, P
 
 
+CONFIG_STEPS = {"tiny": 400, "long_multihot": 200, "gather_stress": 20, "wide_bf16": 60}
+
+
+def time_configs(binding, synth, dev, mode, flush, scale, headline):
+    """din_sparse_fwd, captured in a CUDA graph, on every workload at its full
+    size (taobao: the headline's figures): per-step times with L2 flushed
+    between steps, and each one's roofline from its algorithmic bytes and
+    FLOPs."""
+    import torch
+    from recsys_sparse_embedding_gb300.device_batch import to_device
+    out = {}
+    for name in synth.WORKLOAD_ORDER:
+        if name == WORKLOAD:
+            out[name] = headline
+            continue
+        b = synth.generate(name, seed=0)
+        db = to_device(b, dev)
+        B, D, F = db.B, db.D, db.F
+        mlp = db.mlp(mode)
+        wsp = binding.Workspace(B, D, device=dev)
+        wsp.prepare(mlp)
+        pooled = torch.empty(B, F * D, device=dev)
+        din = torch.empty(B, 3 * D, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+
+        def step():
+            binding.din_sparse_fwd(db.tables, db.values, db.lengths, db.seq_values, db.seq_lengths,
+                                   db.max_len, db.q_feat, db.seq_table, B, mlp, pooled, din, wsp,
+                                   status=status, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+        stream.synchronize()
+        us = time_flushed(g.replay, flush, max(3, int(CONFIG_STEPS[name] * scale)), stream)
+        st = int(status.item())
+        if st & ~binding.FLAG_SEQ_TRUNC:
+            raise RuntimeError("%s: status 0x%x" % (name, st))
+        nbytes, flops, P = algorithmic_work(b)
+        stats = step_stats(us)
+        out[name] = {"B": B, "D": D, "dtype": b.wl.dtype, "valid_positions": P, "us_per_step": stats,
+                     "samples_per_s": B / (stats["mean"] * 1e-6),
+                     "roofline": roofline(nbytes, flops, stats["mean"])}
+        del g, db, wsp, pooled, din, b
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def hashed_lookups(batch):
     """Lookups served by the hash table in one batch: the deep ids of the
     hashed features and the sequence ids of hashed sub-features."""
@@ -256,6 +352,7 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.t0 = time.perf_counter()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
@@ -266,6 +363,7 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
+        self.seconds = time.perf_counter() - self.t0
         self.lines = []
         if self.proc is not None:
             self.proc.terminate()
@@ -326,18 +424,11 @@ def time_dynamic_emb(binding, synth, batch, dev, mode, flush, steps, ws):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        stream.synchronize()
-        for i in range(steps):
-            flush.fill_(float(i & 7))
-            ev[i][0].record(stream)
-            g.replay()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+    stream.synchronize()
+    per = time_flushed(g.replay, flush, steps, stream)
     if int(status.item()):
         raise RuntimeError("hashed step status 0x%x" % int(status.item()))
-    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), ws, dev)
+    total_ms = max_over_ranks(sum(per) / 1e3, ws, dev)
     us = total_ms * 1e3 / steps
     nbytes, flops, _ = algorithmic_work(hb)
     nh = hashed_lookups(hb)
@@ -346,7 +437,7 @@ def time_dynamic_emb(binding, synth, batch, dev, mode, flush, steps, ws):
     ht = db.tables.hash
     return {"what": "din_sparse_fwd with user_id, adgroup_id, campaign_id, brand, customer in one "
                     "hash table (raw 56-bit keys, 300K admitted per table, unseen keys read zero)",
-            "us_per_step": us, "samples_per_s": weak_rate(B * steps, total_ms, ws),
+            "us_per_step": us, "us_stats": step_stats(per), "samples_per_s": weak_rate(B * steps, total_ms, ws),
             "hashed_lookups_per_step": nh, "hash_workspace_bytes": ht.nbytes,
             "hash_capacity": int(ht.c.capacity),
             "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e-6) / 1e9, "peak": hbm,
@@ -400,15 +491,17 @@ def time_train_step(binding, db, mlp, wsp, pooled, din, status, flush, steps, ba
         torch.cuda.synchronize()
     if int(status.item()):
         raise RuntimeError("train step status 0x%x" % int(status.item()))
-    f_us = sum(e[0].elapsed_time(e[1]) for e in ev) * 1e3 / steps
-    b_us = sum(e[1].elapsed_time(e[2]) for e in ev) * 1e3 / steps
-    u_us = sum(e[2].elapsed_time(e[3]) for e in ev) * 1e3 / steps
+    f_l = [e[0].elapsed_time(e[1]) * 1e3 for e in ev]
+    b_l = [e[1].elapsed_time(e[2]) * 1e3 for e in ev]
+    u_l = [e[2].elapsed_time(e[3]) * 1e3 for e in ev]
+    f_us, b_us, u_us = (sum(x) / steps for x in (f_l, b_l, u_l))
     step_us = f_us + b_us + u_us
     _, _, P = algorithmic_work(batch)
     flops = BWD_FLOPS_PER_POSITION_D16 * P if D == 16 else None
     _, tfs, _, src = peaks()
     out = {"what": "din_sparse_fwd + din_sparse_bwd (upstream gradients dpooled, ddin) + emb_adagrad_update",
            "us_per_step": step_us, "fwd_us": f_us, "bwd_us": b_us, "adagrad_us": u_us,
+           "fwd_stats": step_stats(f_l), "bwd_stats": step_stats(b_l), "adagrad_stats": step_stats(u_l),
            "samples_per_s": B / (step_us * 1e-6)}
     if flops:
         ach = flops / (b_us * 1e-6) / 1e12
@@ -479,6 +572,39 @@ def cpu_oracle_rate(batch, samples_per_pass, passes, threads):
     return samples_per_pass * passes / dt, dt, cpu_s
 
 
+def cpu_oracle_rate_padded(batch, samples_per_pass, passes):
+    """The pages' padded flow as the oracle states it (every sequence padded
+    to max_len, the MLP run on every padded position, masked before the
+    softmax), single-threaded."""
+    import oracle
+    samples = np.arange(samples_per_pass, dtype=np.int32) % batch.B
+    oracle.lib()
+    t0 = time.perf_counter()
+    for _ in range(passes):
+        oracle.pool_batch(batch, samples)
+        oracle.din_batch(batch, samples, padded=True)
+    dt = time.perf_counter() - t0
+    return samples_per_pass * passes / dt, dt
+
+
+def cpu_baselines(synth, batch, single_samples, padded_samples):
+    """The oracle on one host thread, and the padded flow on one thread for
+    the tiny and taobao workloads."""
+    rate1, dt1, _ = cpu_oracle_rate(batch, single_samples, 1, 1)
+    out = {"oracle_1thread": {"value": rate1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                              "sample": "%d samples of the B=%d batch (%.1f s)" % (single_samples, batch.B, dt1)},
+           "padded_flow_1thread": {}}
+    for name, n in (("tiny", 64 * 8), (WORKLOAD, padded_samples)):
+        b = batch if name == WORKLOAD else synth.generate(name, seed=0)
+        per = min(n, b.B)
+        rate, dt = cpu_oracle_rate_padded(b, per, max(1, n // per))
+        out["padded_flow_1thread"][name] = {
+            "value": rate, "unit": UNIT, "cores": 1, "kind": "oracle, padded flow",
+            "sample": "%d samples of the B=%d batch, sequences padded to %d (%.1f s)"
+                      % (per * max(1, n // per), b.B, b.max_len, dt)}
+    return out
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -530,6 +656,10 @@ def main():
     ap.add_argument("--train-steps", type=int, default=100)
     ap.add_argument("--dynemb-steps", type=int, default=500)
     ap.add_argument("--towers-steps", type=int, default=300)
+    ap.add_argument("--skip-configs", action="store_true")
+    ap.add_argument("--config-scale", type=float, default=1.0)
+    ap.add_argument("--cpu-single-sample", type=int, default=4096)
+    ap.add_argument("--cpu-padded-sample", type=int, default=512)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -586,24 +716,27 @@ def main():
                 torch.cuda.synchronize()
         run = graph.replay if graph is not None else step
 
+        # The K timed steps sit inside a window of at least CLOCK_WINDOW_S of
+        # identical steps, over which nvidia-smi samples the clocks (a short
+        # timed region alone would end before its first sample).
         K = args.steps
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-        if ws > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
+        window_us = []
         with ClockSampler(local) as clk:
-            for i in range(K):
-                flush.fill_(float(i & 7))
-                ev[i][0].record(stream)
-                run()
-                ev[i][1].record(stream)
+            t_end = time.perf_counter() + CLOCK_WINDOW_S / 2
+            while time.perf_counter() < t_end:
+                window_us += time_flushed(run, flush, 100, stream)
+            if ws > 1:
+                dist.barrier()
             torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
-        times_ms = [a.elapsed_time(b) for a, b in ev]
+            times_us = time_flushed(run, flush, K, stream)
+            if ws > 1:
+                dist.barrier()
+            t_end = time.perf_counter() + CLOCK_WINDOW_S / 2
+            while time.perf_counter() < t_end:
+                window_us += time_flushed(run, flush, 100, stream)
+        window_s = clk.seconds
         st = int(status.item())
-        total_ms = max_over_ranks(sum(times_ms), ws, dev)
+        total_ms = max_over_ranks(sum(times_us) / 1e3, ws, dev)
         value = weak_rate(B * K, total_ms, ws)
         ms_step = total_ms / K
 
@@ -705,28 +838,17 @@ def main():
     if rank == 0 and not args.skip_towers:
         towers = time_towers(binding, synth, pooled, din, B, dev, flush, args.towers_steps)
 
-    # roofline of the fused kernel (the only kernel of a step)
+    # roofline of the fused kernel (the only kernel of a step), timed alone:
+    # the burst tensor peak
     nbytes, flops, P = algorithmic_work(batch)
-    hbm, tfs, tfs_s, src = peaks()
-    t_s = ms_step / 1e3
-    ach_gbs = nbytes / t_s / 1e9
-    ach_tfs = flops / t_s / 1e12
-    t_hbm = nbytes / (hbm * 1e9)
-    t_tc = flops / (tfs_s * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    roof = {"bound": bound,
-            "achieved": ach_gbs if bound == "hbm" else ach_tfs,
-            "peak": hbm if bound == "hbm" else tfs_s,
-            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-            "frac": (ach_gbs / hbm) if bound == "hbm" else (ach_tfs / tfs_s),
-            "traffic": traffic_record(),
-            "peak_source": src,
-            "algorithmic_bytes_per_launch": nbytes,
-            "flops_per_launch": flops,
-            "tensor_achieved_tflops": ach_tfs,
-            "tensor_frac": ach_tfs / tfs_s,
-            "combined_frac": max(t_hbm, t_tc) / t_s,
-            "valid_positions": P}
+    roof = roofline(nbytes, flops, ms_step * 1e3)
+    roof["traffic"] = traffic_record()
+    roof["valid_positions"] = P
+    headline = {"B": B, "D": D, "dtype": batch.wl.dtype, "valid_positions": P,
+                "us_per_step": step_stats(times_us), "samples_per_s": value, "roofline": roof}
+    configs = None
+    if rank == 0 and not args.skip_configs:
+        configs = time_configs(binding, synth, dev, mode, flush, args.config_scale, headline)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.skip_cpu:
@@ -735,7 +857,11 @@ def main():
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%d passes over %d samples of the B=%d batch (%.1f s wall, %.1f s of CPU time)"
                % (args.cpu_passes, args.cpu_sample, B, dt, cpu_s)}
+        cpu.update(cpu_baselines(synth, batch, args.cpu_single_sample, args.cpu_padded_sample))
 
+    clocks = clk.summary()
+    if clocks.get("sm_mhz"):
+        clocks["us_x_mhz_median"] = step_stats(times_us)["median"] * clocks["sm_mhz"]
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -754,7 +880,13 @@ def main():
                               "graph, %d steps timed; no L2 flush (tables 201 MB > 129 MB L2)"
                               % (E2E_GRAPH, E)},
             "gpu_launches": args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
+            "us_per_step": step_stats(times_us),
+            "clock_window": {"seconds": window_s, "steps": len(window_us) + K,
+                             "us_per_step": step_stats(window_us + times_us),
+                             "what": "the K timed steps and identical flushed steps around them, "
+                                     "run while nvidia-smi samples the clocks every 100 ms"},
+            "configs": configs,
             "status": st,
             "towers": towers,
             "steady_state": steady,
