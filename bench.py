@@ -159,9 +159,11 @@ def pool_bytes(batch):
     return 8 * n_ids + 4 * batch.F * batch.B + batch.D * es * n_ids + 4 * batch.F * batch.D * batch.B
 
 
-def time_pool_only(binding, db, wsp, flush, steps, batch, ws, workload="taobao B=8192"):
+def time_pool_only(binding, db, wsp, flush, steps, batch, ws, workload="taobao B=8192", also_unflushed=False):
     """emb_bag_pool alone (the KJT offsets scan and the pooled gather), graph
-    replays with L2 flushed between steps, against the HBM peak."""
+    replays with L2 flushed between steps, against the HBM peak; with
+    also_unflushed, the same steps back to back without the flush as well (for
+    a workload whose tables are far larger than L2)."""
     import torch
     B, F, D = db.B, db.F, db.D
     pooled = torch.empty(B, F * D, device=flush.device)
@@ -178,6 +180,16 @@ def time_pool_only(binding, db, wsp, flush, steps, batch, ws, workload="taobao B
             step()
     stream.synchronize()
     per = time_flushed(g.replay, flush, steps, stream)
+    per_nf = None
+    if also_unflushed:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        torch.cuda.synchronize()
+        per_nf = [a.elapsed_time(b) * 1e3 for a, b in ev]
     if int(status.item()):
         raise RuntimeError("pool-only status 0x%x" % int(status.item()))
     total_ms = max_over_ranks(sum(per) / 1e3, ws, flush.device)
@@ -185,11 +197,20 @@ def time_pool_only(binding, db, wsp, flush, steps, batch, ws, workload="taobao B
     nbytes = pool_bytes(batch)
     hbm, _, _, src = peaks()
     ach = nbytes / (us * 1e-6) / 1e9
-    return {"what": "emb_bag_pool: KJT offsets and the pooled gather of all 16 tables (rows a1-a2)",
+    out = {"what": "emb_bag_pool: KJT offsets and the pooled gather of all 16 tables (rows a1-a2)",
             "workload": workload, "us_per_step": us, "us_stats": step_stats(per),
             "samples_per_s": weak_rate(B * steps, total_ms, ws),
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "algorithmic_bytes_per_launch": nbytes, "peak_source": src}}
+    if per_nf is not None:
+        st = step_stats(per_nf)
+        a_nf = nbytes / (st["mean"] * 1e-6) / 1e9
+        out["unflushed"] = {"what": "the same launches back to back, L2 not flushed: the tables (%.2f GB) "
+                                    "are far larger than L2, ids uniform" % (sum(int(t.numel()) * t.element_size()
+                                                                                for t in db.tables.tables) / 1e9),
+                            "us_stats": st, "roofline": {"bound": "hbm", "achieved": a_nf, "peak": hbm,
+                                                         "unit": "GB/s", "frac": a_nf / hbm}}
+    return out
 
 
 def time_steady_state(binding, synth, db, mlp, wsp, status, dev, n_batches, reps):
@@ -823,7 +844,8 @@ def main():
         sdb = to_device(sb, dev)
         swsp = binding.Workspace(sb.B, sb.D, device=dev)
         pool_stress = time_pool_only(binding, sdb, swsp, flush, args.pool_stress_steps, sb, ws,
-                                     workload="gather_stress B=65536, 1.92 GB fp32 tables, uniform ids")
+                                     workload="gather_stress B=65536, 1.92 GB fp32 tables, uniform ids",
+                                     also_unflushed=True)
         del sdb, swsp, sb
 
     dynemb = None

@@ -236,9 +236,9 @@ int din_sparse_fwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* 
  * It takes no workspace: the cross-CTA exchange state (a header and one partial
  * sum per CTA and table) lives in a fixed 262,400-byte array compiled into the
  * library, which every GPU that loads the library holds until the process
- * exits. Limits: F <= DSF_MAX_TABLES (32); the kernel grid is capped at 1024
- * CTAs (the array's rows), so a device with room for more resident CTAs runs
- * 1024 of them; B is not limited by the array.
+ * exits. Limits: F <= DSF_MAX_TABLES (32); the pooling grid is capped at
+ * 32,768 CTAs (one tagged word each in the array), far above any device's
+ * resident CTAs; B is not limited by the array.
  * The first call on a device, made with that device current, looks up the
  * array's device address and clears it on `stream`; make that first call
  * before any stream capture (later calls may be captured into a graph and

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdinsparse.so")
 
-UNITS = ["abi.cu", "fwd_pool.cu", "fwd_attn_tc.cu", "fwd_attn_f32.cu", "towers.cu", "hash.cu", "bwd.cu"]
+UNITS = ["abi.cu", "bag.cu", "fwd_attn_tc.cu", "fwd_attn_f32.cu", "towers.cu", "hash.cu", "bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -312,8 +312,8 @@ int emb_bag_pool_noalloc(const dsf_tables* tables, const dsf_kjt* kjt, int32_t B
   if (cudaGetDevice(&dev) != cudaSuccess) return DSF_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return DSF_EUNSUPPORTED;
   const bool bf16 = tables->dtype == DSF_BF16;
-  const int G = grid_pool(tables->D, bf16, dev);
-  if (G <= 0 || G > kMaxG) return DSF_EUNSUPPORTED;  // scratch holds kMaxG CTAs
+  // (the pooling grid is capped at the scratch's tagged words, one per CTA)
+  if (grid_pool(tables->D, bf16, dev) <= 0) return DSF_EUNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
   if ((rc = static_scratch(dev, s, &scratch)) != DSF_OK) return rc;

@@ -83,7 +83,7 @@ struct FwdParams {
   unsigned int hash_mask;
   unsigned char kspace[kMaxF];
   unsigned int* epoch;           // launch counter, tags the partials
-  unsigned long long* partials;  // [G][kMaxF]: (epoch + 1) << 32 | length total
+  unsigned long long* partials;  // (epoch + 1) << 32 | length total: [G][kMaxF] here, [G] for pooling alone
   int* status;
 };
 

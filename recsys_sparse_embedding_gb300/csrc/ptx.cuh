@@ -80,6 +80,10 @@ __device__ __forceinline__ void cp_async_commit() {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Wait until at most one of this thread's cp.async groups is still in flight.
+__device__ __forceinline__ void cp_async_wait_one_pending() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- bulk copy
 // Untiled bulk copy global -> shared; completes tx bytes on the mbarrier.
