@@ -19,9 +19,10 @@
 // checks on the way); while window k is summed, one bag per lane group, from
 // shared memory, the rows of window k+1 and the ids of window k+2 are in
 // flight. A chunk whose bags all hold one value (one id per feature, the
-// common case) goes straight through the stage: each lane group copies its
-// bags' rows into its own slots and stores them from there, two batches of
-// rows and the next batch's ids in flight. Bags are summed in value order from zero, as the
+// common case) goes straight through the stage: one thread per bag works out
+// the row and output addresses, then each lane group copies rows into its own
+// stage slots and stores them from there, two batches of rows and the next
+// batch's ids in flight. Bags are summed in value order from zero, as the
 // fused kernel and the oracle do, so the results are identical.
 #pragma once
 #include <cstdint>
@@ -33,7 +34,7 @@ namespace bag {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 2048;        // bags per chunk (offsets staged in shared memory)
+constexpr int kChunk = 1024;        // bags per chunk (offsets staged in shared memory)
 constexpr int kStageBytes = 32768;  // row stage: two windows' rows
 constexpr long long kMaxWords = (long long)(kWsPartBytes / 8);  // range totals the workspace holds
 
@@ -52,12 +53,20 @@ struct Cfg {
 
 template <class C>
 struct Smem {
-  alignas(16) uint8_t stage[2][kStageBytes / 2];  // two windows' rows, in value order
-  long long ids[C::CV];                           // the window being issued
+  alignas(16) uint8_t stage[2][kStageBytes / 2];  // two windows' (batches') rows
+  union {
+    struct {
+      long long ids[C::CV];  // the window being issued
+      uint8_t feat[C::CV];
+    } win;
+    struct {
+      const uint8_t* src[3][kThreads];  // a batch's row addresses (null: zero row)
+      float* dst[3][kThreads];          // its output rows (null: no bag)
+    } cp;
+  } u;
   long long offs[kChunk + 1];
   long long red[kWarps];
   long long scan[kWarps];
-  uint8_t feat[C::CV];
   int flags;
 };
 
@@ -99,7 +108,22 @@ __global__ void __launch_bounds__(kThreads) bag_totals_kernel(const __grid_const
   if (threadIdx.x == 0) sm_flags = 0;
   int flags = 0;
   long long tot = 0;
-  for (long long g = g0 + threadIdx.x; g < g1; g += kThreads) tot += bag_len(p, g, flags);
+  // eight loads in flight per thread per round
+  for (long long g = g0 + threadIdx.x; g < g1; g += 8 * kThreads) {
+    int v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const long long gk = g + (long long)k * kThreads;
+      v[k] = gk < g1 ? __ldg(p.lengths + gk) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      int x = v[k];
+      if (x < 0) { flags |= DSF_FLAG_NEG_LENGTH; x = 0; }
+      if (x > kMaxBagLen) { flags |= DSF_FLAG_COUNT; x = kMaxBagLen; }
+      tot += x;
+    }
+  }
   tot = block_sum(tot, red);
   if (threadIdx.x == 0) p.partials[c] = static_cast<unsigned long long>(tot);
   report(p, flags, &sm_flags);
@@ -165,88 +189,135 @@ __global__ void __launch_bounds__(kThreads, 4) bag_kernel(const __grid_constant_
     if (all_ones) {
       // Every bag of the chunk holds one value: bag i is value vb + i, and its
       // pooled row is that row (a sum of one; a mean over one). Batches of
-      // RB * NG bags; in batch j, lane group gi owns bags j * RB * NG + u * NG
-      // + gi (u < RB) and stage slots u * NG + gi of half j % 2: it copies
-      // their rows into its slots (cp.async) and later stores them from there,
-      // so no barrier is needed. While batch j is stored, the rows of batch
-      // j + 1 and the ids of batch j + 2 are in flight. (f, b) of each slot
-      // advance by one batch per step.
-      constexpr int RB = (kStageBytes / 2) / (C::NG * C::ROWB);
-      constexpr int PB = RB * C::NG;  // bags per batch
+      // PB bags (as many as half the stage holds, at most one per thread).
+      // For batch j, thread t < PB works out bag t's row
+      // address and output address (its id loaded one batch ahead) into a
+      // ring of three metadata slots; after a barrier, lane group gi copies
+      // rows gi, gi + NG, ... of the batch into its stage slots (cp.async),
+      // and later stores those same rows from there, so the copies need no
+      // further barrier. While batch j is stored, the rows of batch j + 1 and
+      // the ids of batch j + 2 are in flight.
+      constexpr int PB = (kStageBytes / 2) / C::ROWB < kThreads ? (kStageBytes / 2) / C::ROWB : kThreads;
+      constexpr int RB = PB / C::NG;  // rows per lane group per batch
+      static_assert(RB >= 1 && RB * C::NG == PB, "a batch is a whole number of rows per lane group");
       const long long vb = sm.offs[0];
+      const bool in_range = vb + n <= p.n_values;  // (else per-bag checks below)
       const int nbatch = (n + PB - 1) / PB;
-      long long idn[RB];
-      int fi[RB], bi[RB], fs[RB], bs_[RB];  // (feature, sample) of the slots at issue / at store
-#pragma unroll
-      for (int u = 0; u < RB; ++u) {
-        const unsigned x = unsigned(b0) + unsigned(u * C::NG + gi);
-        fi[u] = fs[u] = f0 + int(x / unsigned(B));
-        bi[u] = bs_[u] = int(x % unsigned(B));
+      // bag tid + j * PB: (feature, sample) at the metadata step (fr, br) and
+      // at the L2-prefetch step one batch later (fp, bp), advanced by PB per batch
+      int fr, br;
+      {
+        const unsigned x = unsigned(b0) + unsigned(tid);
+        fr = f0 + int(x / unsigned(B));
+        br = int(x % unsigned(B));
       }
-      auto advance = [&](int* f, int* b) {
-#pragma unroll
-        for (int u = 0; u < RB; ++u) {
-          b[u] += PB;
-          while (b[u] >= B) { b[u] -= int(B); ++f[u]; }
-        }
+      int fp = fr, bp = br;
+      auto load_id = [&](int j) -> long long {
+        const int i = j * PB + tid;
+        long long id = -1;
+        if (tid < PB && i < n && (in_range || vb + i < p.n_values)) id = __ldg(p.values + vb + i);
+        return id;
       };
-      auto load_ids = [&](int j) {
-#pragma unroll
-        for (int u = 0; u < RB; ++u) {
-          const int i = j * PB + u * C::NG + gi;
-          idn[u] = -1;
-          if (i < n) {
-            if (vb + i < p.n_values) idn[u] = __ldg(p.values + vb + i);
-            else if (sub == 0) flags |= DSF_FLAG_COUNT;
+      // bring the row of batch j's bag tid into L2 (plain tables only), two
+      // batches before its copy is issued, so that the copy sees L2 latency
+      auto prefetch = [&](int j, long long id) {
+        if (tid >= PB) return;
+        const int i = j * PB + tid;
+        if (i < n && !((p.hash_mask >> fp) & 1u) && id >= 0 && id < p.rows[fp])
+          prefetch_l2(static_cast<const uint8_t*>(p.tables[fp]) + id * C::ROWB);
+        bp += PB;
+        while (bp >= B) { bp -= int(B); ++fp; }
+      };
+      long long idn = -1;
+      auto meta = [&](int j) {
+        if (tid >= PB) return;
+        const int i = j * PB + tid;
+        const int m = j % 3;
+        const uint8_t* src = nullptr;
+        float* dst = nullptr;
+        if (i < n) {
+          if (in_range || vb + i < p.n_values) {
+            long long v = idn;
+            if ((p.hash_mask >> fr) & 1u) v = hash::find(p.hkeys, p.hbmask, p.kspace[fr], v);
+            if (v >= 0 && v < p.rows[fr]) src = static_cast<const uint8_t*>(p.tables[fr]) + v * C::ROWB;
+            else flags |= DSF_FLAG_ID_RANGE;
+          } else {
+            flags |= DSF_FLAG_COUNT;
           }
+          dst = p.pooled + (long long)br * (F * C::D) + fr * C::D;
         }
+        sm.u.cp.src[m][tid] = src;
+        sm.u.cp.dst[m][tid] = dst;
+        br += PB;
+        while (br >= B) { br -= int(B); ++fr; }
       };
+      // (all of a step's shared-memory loads first, so that their latencies
+      // overlap; rows past the chunk have a null output address)
       auto issue = [&](int j) {
         uint8_t* st = sm.stage[j & 1];
+        const int m = j % 3;
+        const uint8_t* src[RB];
+        bool live[RB];
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
-          const int i = j * PB + u * C::NG + gi;
-          if (i < n) {
-            long long v = idn[u];
-            const int f = fi[u];
-            bool ok = false;
-            if (vb + i < p.n_values) {
-              if ((p.hash_mask >> f) & 1u) v = hash::find(p.hkeys, p.hbmask, p.kspace[f], v);
-              ok = v >= 0 && v < p.rows[f];
-              if (!ok && sub == 0) flags |= DSF_FLAG_ID_RANGE;
-            }
-            const uint8_t* src = static_cast<const uint8_t*>(p.tables[f]) + (ok ? v : 0) * C::ROWB + sub * 16;
-            cp_async_16_ca(st + (u * C::NG + gi) * C::ROWB + sub * 16, src, ok ? 16u : 0u);
-          }
+          const int r = u * C::NG + gi;
+          src[u] = sm.u.cp.src[m][r];
+          live[u] = sm.u.cp.dst[m][r] != nullptr;
+        }
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+          const int r = u * C::NG + gi;
+          if (live[u])
+            cp_async_16_ca(st + r * C::ROWB + sub * 16, src[u] ? src[u] + sub * 16 : p.tables[0], src[u] ? 16u : 0u);
         }
         cp_async_commit();
-        advance(fi, bi);
       };
       auto store = [&](int j) {
         const uint8_t* st = sm.stage[j & 1];
+        const int m = j % 3;
+        float* o[RB];
+        uint4 v[RB];
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
-          const int i = j * PB + u * C::NG + gi;
-          if (i < n) {
+          const int r = u * C::NG + gi;
+          o[u] = sm.u.cp.dst[m][r];
+          v[u] = *reinterpret_cast<const uint4*>(st + r * C::ROWB + sub * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+          if (o[u] != nullptr) {
             float x[C::EPL];
-            widen16<C::BF16>(st + (u * C::NG + gi) * C::ROWB + sub * 16, x);
-            float* o = p.pooled + (long long)bs_[u] * (F * C::D) + fs[u] * C::D + sub * C::EPL;
+            widen16v<C::BF16>(v[u], x);
+            float* q = o[u] + sub * C::EPL;
 #pragma unroll
             for (int e = 0; e < C::EPL; e += 4)
-              *reinterpret_cast<float4*>(o + e) = make_float4(0.f + x[e], 0.f + x[e + 1], 0.f + x[e + 2], 0.f + x[e + 3]);
+              *reinterpret_cast<float4*>(q + e) = make_float4(0.f + x[e], 0.f + x[e + 1], 0.f + x[e + 2], 0.f + x[e + 3]);
           }
         }
-        advance(fs, bs_);
       };
-      load_ids(0);
+      // ids of batches j + 1 (ida) and j + 2 (idb) at the top of step j
+      idn = load_id(0);
+      long long ida = load_id(1), idb = load_id(2);
+      prefetch(0, idn);
+      prefetch(1, ida);
+      meta(0);
+      __syncthreads();
       issue(0);
-      if (nbatch > 1) load_ids(1);
       for (int j = 0; j < nbatch; ++j) {
-        if (j + 1 < nbatch) issue(j + 1);
-        if (j + 2 < nbatch) load_ids(j + 2);
-        if (j + 1 < nbatch) cp_async_wait_one_pending();
-        else cp_async_wait_all();
+        if (j + 2 < nbatch) prefetch(j + 2, idb);
+        const long long idc = load_id(j + 3);
+        if (j + 1 < nbatch) {
+          idn = ida;
+          meta(j + 1);   // slot (j + 1) % 3: not read by anyone now
+          __syncthreads();
+          issue(j + 1);
+          cp_async_wait_one_pending();
+        } else {
+          cp_async_wait_all();
+        }
         store(j);
+        ida = idb;
+        idb = idc;
       }
       __syncthreads();  // before the next chunk's offsets
       continue;
@@ -288,22 +359,22 @@ __global__ void __launch_bounds__(kThreads, 4) bag_kernel(const __grid_constant_
 #pragma unroll
       for (int j = 0; j < IPT; ++j) {
         const int q = tid + j * kThreads;
-        if (q < nv) sm.ids[q] = idr[j];
+        if (q < nv) sm.u.win.ids[q] = idr[j];
       }
       for (int i = i0 + tid; i < i1 && nv > 0; i += kThreads) {
         int f;
         long long b;
         bag_fb(i, f, b);
         const long long ve = min(sm.offs[i + 1], vs + nv);
-        for (long long q = sm.offs[i]; q < ve; ++q) sm.feat[q - vs] = uint8_t(f);
+        for (long long q = sm.offs[i]; q < ve; ++q) sm.u.win.feat[q - vs] = uint8_t(f);
       }
     };
     // every row copy of a window goes out (one cp.async group)
     auto issue_rows = [&](int i0, int i1, int st) {
       const int nv = nvals(i0, i1);
       for (int q = gi; q < nv; q += C::NG) {
-        const int f = sm.feat[q];
-        long long id = sm.ids[q];
+        const int f = sm.u.win.feat[q];
+        long long id = sm.u.win.ids[q];
         if ((p.hash_mask >> f) & 1u) id = hash::find(p.hkeys, p.hbmask, p.kspace[f], id);
         const bool ok = id >= 0 && id < p.rows[f];
         if (!ok && sub == 0) flags |= DSF_FLAG_ID_RANGE;
