@@ -317,12 +317,14 @@ int ctr_towers_fwd(const float* pooled_dev, const float* din_dev, int32_t B, con
  *     dW1 [256, 12D], db1 [256], dW2 [64, 256], db2 [64], dw3 [64], db3 [1]);
  *   - every touched row's summed gradient, accumulated into dsf_row_grads.
  * The MLP runs as in the forward's mode (mlp->mode): bf16 GEMM operands with
- * fp32 accumulation, or fp32 throughout. Its six GEMMs are library GEMMs
- * (cuBLAS) over the valid positions only; the rest are this library's
- * kernels. Row gradients are summed with fp32 atomics, so their rounding
- * order varies between runs. Gradients of unseen hash keys and of invalid ids
- * are dropped. emb_adagrad_update then applies AdaGrad to the touched rows
- * and leaves the row-gradient state zero for the next step.
+ * fp32 accumulation, or fp32 throughout. Its six matrix products are this
+ * library's GEMMs (tcgen05 tensor cores for bf16 operands, CUDA cores in the
+ * fp32 mode) over the sequence values' length (rows past the valid count are
+ * zero); the rest are this library's kernels. Row gradients are summed with
+ * fp32 atomics, so their rounding order varies between runs. Gradients of
+ * unseen hash keys and of invalid ids are dropped. emb_adagrad_update then
+ * applies AdaGrad to the touched rows and leaves the row-gradient state zero
+ * for the next step.
  *
  * Row-gradient state, caller-owned: host arrays [F] of device pointers, per
  * table f: grad[f] fp32 [rows_f, D] and touched[f] int32 [rows_f], zero

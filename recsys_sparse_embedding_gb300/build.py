@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdinsparse.so")
 
-UNITS = ["abi.cu", "bag.cu", "fwd_attn_tc.cu", "fwd_attn_f32.cu", "towers.cu", "hash.cu", "bwd.cu"]
+UNITS = ["abi.cu", "bag.cu", "fwd_attn_tc.cu", "fwd_attn_f32.cu", "towers.cu", "hash.cu", "bwd.cu", "gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
@@ -75,7 +75,7 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         raise RuntimeError("nvcc failed for " + ", ".join(failed))
     if jobs or _stale(LIB, objs):
         tmp = LIB + ".tmp.%d" % os.getpid()
-        cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"]
+        cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

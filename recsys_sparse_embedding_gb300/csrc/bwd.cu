@@ -13,28 +13,31 @@
 //   scatter    per sample: dq = sum_t (dx_q + dx_d + dx_p s_t), ds_t += dx_s -
 //              dx_d + dx_p q; row gradients: ds_t slices into the sequence
 //              rows, dpooled + dq slices into every value of the bags
-// The six GEMMs are plain library GEMMs (cuBLAS) over the valid positions,
-// sized by the sequence values' length (rows past the valid count are zero).
+// The six products are this library's GEMMs (gemm.cuh: tcgen05 with bf16
+// operands, CUDA cores in the fp32 check mode), all in the A B^T form: the
+// weights' transposes are packed per call, and the operands of the two
+// weight gradients (sums over positions, split over K and reduced in order)
+// are transposed into position-major rows. They run over the sequence
+// values' length (rows past the valid count are zero).
 // Row gradients are summed with vector fp32 atomics into caller-owned
 // per-table buffers; the first contribution to a row appends it to a list,
 // which the AdaGrad step walks.
-#include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdint>
-#include <mutex>
 
 #include "abi_checks.cuh"
 #include "dinsparse.h"
+#include "gemm.cuh"
 #include "hash.cuh"
 
 namespace dsf {
 namespace bwd {
 namespace {
 
-constexpr size_t kCublasWs = size_t(32) << 20;
+constexpr int kSplitCtas = 152;  // CTAs of the two weight-gradient products (K-splits x M-tiles)
 constexpr int kRowBits = 40;
 constexpr int kWarpsPerBlock = 8;
 constexpr int kScanThreads = 256, kScanRounds = 8, kScanTile = kScanThreads * kScanRounds;
@@ -47,8 +50,8 @@ constexpr unsigned long long kNoKey = ~0ull;
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, gbag, okey, osrc, w1b, w2b, X, S, G1, H1, H2, dH2, dH1, dX, dS, cublas,
-      total;
+  size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, gbag, okey, osrc, w1b, w2b, w1t, w2t, X, S, G1, H1, H2, dH2,
+      dH1, dX, dS, XT, H1T, dH2T, dH1T, split, total;
 };
 
 // Every buffer is sized for fp32 elements, so the layout does not depend on
@@ -85,7 +88,19 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.dH1 = take(P * kN1 * 4);
   L.dX = take(P * K1 * 4);
   L.dS = take(P * Q * 4);
-  L.cublas = take(kCublasWs);
+  // transposed weights; position-major copies of x, h1, dh2, dh1 (rows of
+  // P8 = P rounded up to 8 elements, 16-byte aligned); split-K partials
+  const size_t P8 = (P + 7) / 8 * 8;
+  L.w1t = take(K1 * size_t(kN1) * 4);
+  L.w2t = take(size_t(kN1) * kN2 * 4);
+  L.XT = take(K1 * P8 * 4);
+  L.H1T = take(size_t(kN1) * P8 * 4);
+  L.dH2T = take(size_t(kN2) * P8 * 4);
+  L.dH1T = take(size_t(kN1) * P8 * 4);
+  {
+    const size_t w1 = size_t(kSplitCtas / 2) * kN1 * K1, w2 = size_t(kSplitCtas) * kN2 * kN1;
+    L.split = take((w1 > w2 ? w1 : w2) * 4);
+  }
   L.total = o;
   return L;
 }
@@ -297,13 +312,6 @@ __global__ void __launch_bounds__(256) reduce_cols_kernel(const RedJobs r) {
   }
 }
 
-__global__ void pack_kernel(const float* __restrict__ W1, const float* __restrict__ W2, int n1, int n2,
-                            __nv_bfloat16* w1b, __nv_bfloat16* w2b) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n1 + n2; i += gridDim.x * blockDim.x) {
-    if (i < n1) w1b[i] = __float2bfloat16_rn(W1[i]);
-    else w2b[i - n1] = __float2bfloat16_rn(W2[i - n1]);
-  }
-}
 
 template <class T>
 __device__ __forceinline__ void store4(T* dst, float a, float b, float c, float d);
@@ -408,6 +416,28 @@ template <>
 __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// The MLP weights as the products read them: W1 [256, K1] and W2 [64, 256]
+// as given, and their transposes W1^T [K1, 256], W2^T [256, 64], in the
+// operand type T (bf16: rounded to nearest even).
+template <class T>
+__global__ void pack_kernel(const float* __restrict__ W1, const float* __restrict__ W2, int K1, T* w1, T* w2,
+                            T* w1t, T* w2t) {
+  const int n1 = kN1 * K1, n2 = kN2 * kN1;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n1 + n2; i += gridDim.x * blockDim.x) {
+    if (i < n1) {
+      const int o = i / K1, k = i - o * K1;
+      const T v = from_f<T>(W1[i]);
+      if (w1) w1[i] = v;
+      w1t[(long long)k * kN1 + o] = v;
+    } else {
+      const int j = i - n1, o = j / kN1, k = j - o * kN1;
+      const T v = from_f<T>(W2[j]);
+      if (w2) w2[j] = v;
+      w2t[(long long)k * kN2 + o] = v;
+    }
+  }
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -794,30 +824,6 @@ __global__ void update_kernel(const Upd u) {
 __global__ void reset_count_kernel(int* count) { *count = 0; }
 
 // ---------------------------------------------------------------- host
-cublasHandle_t handle_for(int dev) {
-  static std::mutex mu;
-  static cublasHandle_t h[64] = {};
-  std::lock_guard<std::mutex> g(mu);
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!h[dev] && cublasCreate(&h[dev]) != CUBLAS_STATUS_SUCCESS) h[dev] = nullptr;
-  return h[dev];
-}
-std::mutex& call_mutex() {
-  static std::mutex m;
-  return m;
-}
-
-// Row-major C[M, N] = op(A) op(B) (fp32 output), A, B row-major with leading
-// dimensions lda, ldb: the column-major product C^T = op(B)^T op(A)^T.
-bool gemm_rm(cublasHandle_t h, bool ta, bool tb, long long M, long long N, long long K, const void* A, long long lda,
-             const void* B, long long ldb, float* C, long long ldc, bool bf16) {
-  const float alpha = 1.f, beta = 0.f;
-  const cudaDataType_t it = bf16 ? CUDA_R_16BF : CUDA_R_32F;
-  return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, int(N), int(M), int(K),
-                      &alpha, B, it, int(ldb), A, it, int(lda), &beta, C, CUDA_R_32F, int(ldc), CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
-}
-
 int grid_for(long long n, int threads, int cap = 152 * 16) {
   long long g = (n + threads - 1) / threads;
   if (g < 1) g = 1;
@@ -918,11 +924,6 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   if (!workspace_dev || !aligned(workspace_dev, 256) || ws_bytes < L.total) return DSF_EWORKSPACE;
   if (B == 0) return DSF_OK;
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSF_ECUDA;
-  cublasHandle_t h = handle_for(dev);
-  if (!h) return DSF_ECUDA;
-  std::lock_guard<std::mutex> lock(call_mutex());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(workspace_dev);
   const int D = tables->D, F = tables->F, K1 = 12 * D;
@@ -977,13 +978,70 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     scan_apply_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
   }
   if (bf) {
-    pack_kernel<<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
-        mlp->W1, mlp->W2, kN1 * K1, kN2 * kN1, reinterpret_cast<__nv_bfloat16*>(w + L.w1b),
-        reinterpret_cast<__nv_bfloat16*>(w + L.w2b));
+    pack_kernel<__nv_bfloat16><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
+        mlp->W1, mlp->W2, K1, reinterpret_cast<__nv_bfloat16*>(w + L.w1b), reinterpret_cast<__nv_bfloat16*>(w + L.w2b),
+        reinterpret_cast<__nv_bfloat16*>(w + L.w1t), reinterpret_cast<__nv_bfloat16*>(w + L.w2t));
     W1 = w + L.w1b;
     W2 = w + L.w2b;
+  } else {
+    pack_kernel<float><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
+        mlp->W1, mlp->W2, K1, nullptr, nullptr, reinterpret_cast<float*>(w + L.w1t), reinterpret_cast<float*>(w + L.w2t));
   }
+  const void* W1T = w + L.w1t;
+  const void* W2T = w + L.w2t;
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
+  // D = A B^T (both row-major with K contiguous), on this library's GEMMs;
+  // splits > 1 writes per-split partials to the split buffer
+  const int esz = bf ? 2 : 4;
+  auto mm = [&](const void* A, long long lda, const void* Bm, long long ldb, float* D, long long ldd, long long M,
+                int N, long long K, int splits, const gemm::TnArgs* epi = nullptr) -> bool {
+    gemm::TnArgs g = epi ? *epi : gemm::TnArgs{};
+    g.A = A;
+    g.lda = lda;
+    g.B = Bm;
+    g.ldb = ldb;
+    g.D = D;
+    g.ldd = ldd;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.k_per_split = ((K + splits - 1) / splits + 63) / 64 * 64;
+    if (g.k_per_split < 64) g.k_per_split = 64;
+    g.split_stride = M * ldd;
+    g.status = status_dev;
+    const int n_split = int((K + g.k_per_split - 1) / g.k_per_split);
+    return gemm::tn(g, n_split < 1 ? 1 : n_split, bf, s);
+  };
+  // a sum over all positions: split over K, partials reduced in split order
+  // bf16 mode: ReLU and mask inside the products' epilogues (while db1's
+  // partial sums, one row per 128-position tile, fit their buffer)
+  const long long P8 = (Pc + 7) / 8 * 8;
+  const bool fuse = bf && (Pc + 127) / 128 <= kMaxBlocks;
+  auto mm_splitk = [&](const void* A, const void* Bm, long long P8, float* D, int M, int N, long long K) -> bool {
+    // K-splits of at least 256 positions, about kSplitCtas CTAs in all
+    const int mt = (M + 127) / 128;
+    int splits = int((K + 255) / 256);
+    if (splits > kSplitCtas / mt) splits = kSplitCtas / mt;
+    if (splits < 1) splits = 1;
+    const long long kps = ((K + splits - 1) / splits + 63) / 64 * 64;
+    splits = int((K + kps - 1) / kps);
+    if (splits < 1) splits = 1;
+    float* part = reinterpret_cast<float*>(w + L.split);
+    gemm::TnArgs g{};
+    g.A = A;
+    g.lda = P8;
+    g.B = Bm;
+    g.ldb = P8;
+    g.D = part;
+    g.ldd = N;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.k_per_split = kps;
+    g.split_stride = (long long)M * N;
+    g.status = status_dev;
+    return gemm::tn(g, splits, bf, s) && gemm::reduce(part, (long long)M * N, splits, N, D, N, M, N, s);
+  };
   if (Pc > 0) {
     const int gb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
     if (bf)
@@ -993,17 +1051,28 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       gather_kernel<float><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
                                                               S, Pc);
     if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
-    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
-        cublasSetWorkspace(h, w + L.cublas, kCublasWs) != CUBLAS_STATUS_SUCCESS)
-      return DSF_ECUDA;
-    // recompute: h1 = ReLU(x W1^T + b1), then the layer-2 pre-activation
-    if (!gemm_rm(h, false, true, Pc, kN1, K1, X, K1, W1, K1, G1, kN1, bf)) return DSF_ECUDA;
-    if (bf)
-      relu1_kernel<__nv_bfloat16><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1,
-                                                                               static_cast<__nv_bfloat16*>(H1), Pc * kN1 / 4);
-    else
-      relu1_kernel<float><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1, static_cast<float*>(H1), Pc * kN1 / 4);
-    if (!gemm_rm(h, false, true, Pc, kN2, kN1, H1, kN1, W2, kN1, H2, kN2, bf)) return DSF_ECUDA;
+    // recompute: h1 = ReLU(x W1^T + b1) (in bf16 mode inside the product's
+    // epilogue, which also writes h1's position-major copy), then the layer-2
+    // pre-activation
+    if (fuse) {
+      gemm::TnArgs e{};
+      e.epi = gemm::kEpiReluBias;
+      e.bias = mlp->b1;
+      e.H = H1;
+      e.ldh = kN1;
+      e.HT = w + L.H1T;
+      e.ldt = P8;
+      if (!mm(X, K1, W1, K1, nullptr, kN1, Pc, kN1, K1, 1, &e)) return DSF_ECUDA;
+    } else {
+      if (!mm(X, K1, W1, K1, G1, kN1, Pc, kN1, K1, 1)) return DSF_ECUDA;
+      if (bf)
+        relu1_kernel<__nv_bfloat16><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(
+            G1, mlp->b1, static_cast<__nv_bfloat16*>(H1), Pc * kN1 / 4);
+      else
+        relu1_kernel<float><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1, static_cast<float*>(H1),
+                                                                        Pc * kN1 / 4);
+    }
+    if (!mm(H1, kN1, W2, kN1, H2, kN2, Pc, kN2, kN1, 1)) return DSF_ECUDA;
   }
   const int sb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
   if (bf)
@@ -1014,19 +1083,46 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
                                                                  zb, dab, static_cast<float*>(dH2), dS, part1, Pc);
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   if (Pc > 0) {
-    if (!gemm_rm(h, false, false, Pc, kN1, kN2, dH2, kN2, W2, kN1, G1, kN1, bf)) return DSF_ECUDA;
-    const int rb = grid_for(Pc, 1, kMaxBlocks);
-    if (bf)
-      relu1_bwd_kernel<__nv_bfloat16><<<rb, kN1, 0, s>>>(G1, static_cast<const __nv_bfloat16*>(H1),
-                                                          static_cast<__nv_bfloat16*>(dH1), part2, Pc);
-    else
-      relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
-                                                 Pc);
+    // dh1 = (dh2 W2) [h1 > 0] and db1's partial sums (in bf16 mode inside the
+    // product's epilogue, with dh1's position-major copy)
+    int rb;
+    if (fuse) {
+      gemm::TnArgs e{};
+      e.epi = gemm::kEpiMask;
+      e.H = dH1;
+      e.ldh = kN1;
+      e.Hin = H1;
+      e.HT = w + L.dH1T;
+      e.ldt = P8;
+      e.part = part2;
+      if (!mm(dH2, kN2, W2T, kN2, G1, kN1, Pc, kN1, kN2, 1, &e)) return DSF_ECUDA;
+      rb = int((Pc + 127) / 128);
+    } else {
+      if (!mm(dH2, kN2, W2T, kN2, G1, kN1, Pc, kN1, kN2, 1)) return DSF_ECUDA;
+      rb = grid_for(Pc, 1, kMaxBlocks);
+      if (bf)
+        relu1_bwd_kernel<__nv_bfloat16><<<rb, kN1, 0, s>>>(G1, static_cast<const __nv_bfloat16*>(H1),
+                                                            static_cast<__nv_bfloat16*>(dH1), part2, Pc);
+      else
+        relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
+                                                   Pc);
+    }
     reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s>>>(
         RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
-    if (!gemm_rm(h, false, false, Pc, K1, kN1, dH1, kN1, W1, K1, dX, K1, bf)) return DSF_ECUDA;
-    if (!gemm_rm(h, true, false, kN1, K1, Pc, dH1, kN1, X, K1, mg->dW1, K1, bf)) return DSF_ECUDA;
-    if (!gemm_rm(h, true, false, kN2, kN1, Pc, dH2, kN2, H1, kN1, mg->dW2, kN1, bf)) return DSF_ECUDA;
+    if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
+    // the weight gradients sum over positions: their operands, position-major
+    // (h1's and dh1's copies came from the fused epilogues)
+    void* XT = w + L.XT;
+    void* H1T = w + L.H1T;
+    void* dH2T = w + L.dH2T;
+    void* dH1T = w + L.dH1T;
+    if (!gemm::transpose(X, K1, Pc, K1, XT, P8, esz, s) || !gemm::transpose(dH2, kN2, Pc, kN2, dH2T, P8, esz, s))
+      return DSF_ECUDA;
+    if (!fuse && (!gemm::transpose(dH1, kN1, Pc, kN1, dH1T, P8, esz, s) ||
+                  !gemm::transpose(H1, kN1, Pc, kN1, H1T, P8, esz, s)))
+      return DSF_ECUDA;
+    if (!mm_splitk(dH1T, XT, P8, mg->dW1, kN1, K1, Pc)) return DSF_ECUDA;
+    if (!mm_splitk(dH2T, H1T, P8, mg->dW2, kN2, kN1, Pc)) return DSF_ECUDA;
   } else {
     if (cudaMemsetAsync(mg->dW1, 0, size_t(kN1) * K1 * 4, s) != cudaSuccess ||
         cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess ||

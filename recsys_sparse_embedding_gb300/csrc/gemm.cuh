@@ -1,0 +1,81 @@
+// The backward's matrix products, as this library's own kernels: D = A B^T
+// with both operands K-major ("TN"), fp32 results.
+//
+//   bf16 operands: tcgen05 MMA (kind::f16, fp32 accumulation in tensor
+//   memory), 128 threads per CTA, a 128-row tile of D with the whole N
+//   (<= 256) in one accumulator. Two kernels:
+//   - B resident (K <= 256, no split: the products with a weight matrix):
+//     persistent CTAs, one per SM, hold B in shared memory (K-major, 128-byte
+//     swizzle) and walk the row tiles of A; the next tile's A loads while the
+//     current tile's epilogue runs;
+//   - streaming (split-K): a three-stage ring of 64-wide K-blocks of A and B.
+//   Operands arrive by cp.async from all threads; one thread issues the MMAs
+//   and commits them to an mbarrier. The epilogue reads each thread's row of
+//   the accumulator from tensor memory and stores it from registers, with the
+//   ReLU or the mask of the backward fused in (Epi).
+//   fp32 operands (the check mode): CUDA-core tiles of 64 x 64.
+//
+// Both take split-K: split z covers K-range [z * k_per_split, ...) and writes
+// its partial product to D + z * split_stride; reduce() then adds the
+// splits in a fixed order (deterministic).
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace dsf {
+namespace gemm {
+
+// What the bf16 kernel's epilogue writes (the fp32 kernel: kEpiF32 only).
+enum Epi {
+  kEpiF32 = 0,       // D = A B^T (fp32)
+  kEpiReluBias = 1,  // H = bf16(ReLU(A B^T + bias)) and its transpose HT
+  kEpiMask = 2,      // D = A B^T; v = D where Hin > 0, else 0; H = bf16(v) and
+                     // HT; part[tile][n] = the tile's column sums of v
+};
+
+struct TnArgs {
+  const void* A;      // [M][K] (row stride lda elements), bf16 or fp32
+  long long lda;
+  const void* B;      // [N][K] (row stride ldb elements)
+  long long ldb;
+  float* D;           // [M][N] (row stride ldd), per split at D + z * split_stride
+  long long ldd;
+  long long M;
+  int N;              // a multiple of 16 (larger N runs in chunks of 256; kEpiF32 only)
+  long long K;
+  long long k_per_split;  // a multiple of 64
+  long long split_stride;
+  int* status;        // DSF_FLAG_TIMEOUT on a wait that ran out (nullable)
+  int epi;            // Epi (bf16 only)
+  const float* bias;  // kEpiReluBias: [N]
+  void* H;            // bf16 [M][ldh]
+  long long ldh;
+  const void* Hin;    // kEpiMask: bf16 [M][ldh], the mask's source
+  void* HT;           // bf16 [N][ldt]: element (m, n) at n * ldt + m
+  long long ldt;
+  float* part;        // kEpiMask: [M tiles][N]
+};
+
+// Launches D = A B^T over `splits` K-splits on `stream`. bf16 selects the
+// operand type. Returns false if the shape is unsupported or a launch fails.
+// Rows of A / B must start 16-byte aligned (lda, ldb multiples of 8 bf16 or
+// 4 fp32 elements; A, B 16-byte aligned).
+bool tn(const TnArgs& a, int splits, bool bf16, cudaStream_t stream);
+
+// D[m][n] = sum over s of P[s][m][n] (row strides ldp / ldd, split stride
+// split_stride), in a fixed order: eight interleaved groups of splits
+// (z mod 8), each summed in increasing z, then the groups in order.
+bool reduce(const float* P, long long split_stride, int splits, long long ldp, float* D, long long ldd,
+            long long M, int N, cudaStream_t stream);
+
+// out[c][r] = in[r][c] for r < rows, c < cols (element size 2 or 4 bytes);
+// row strides ld_in / ld_out in elements.
+bool transpose(const void* in, long long ld_in, long long rows, int cols, void* out, long long ld_out, int esize,
+               cudaStream_t stream);
+
+// Dynamic shared memory of the tcgen05 kernel for an N-wide tile.
+size_t tn_bf16_smem_bytes(int N);
+
+}  // namespace gemm
+}  // namespace dsf
