@@ -51,7 +51,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
   size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, gbag, okey, osrc, w1b, w2b, w1t, w2t, X, S, G1, H1, H2, dH2,
-      dH1, dX, dS, XT, H1T, dH2T, dH1T, split, total;
+      dH1, dX, dS, XT, H1T, dH2T, dH1T, M1, split, total;
 };
 
 // Every buffer is sized for fp32 elements, so the layout does not depend on
@@ -73,7 +73,7 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.zb = take(P * 4);
   L.dab = take(P * 4);
   L.part1 = take(size_t(kMaxBlocks) * kRedCols * 4);
-  L.part2 = take(size_t(kMaxBlocks) * kN1 * 4);
+  L.part2 = take(size_t(4) * kMaxBlocks * kN1 * 4);  // (the fused mask epilogue: 4 rows per 128-position tile)
   L.gbag = take(size_t(B) * F * D * 4);
   L.okey = take((size_t(NV) + 3 * P) * 8);
   L.osrc = take((size_t(NV) + 3 * P) * 8);
@@ -97,6 +97,7 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.H1T = take(size_t(kN1) * P8 * 4);
   L.dH2T = take(size_t(kN2) * P8 * 4);
   L.dH1T = take(size_t(kN1) * P8 * 4);
+  L.M1 = take(P * (kN1 / 32) * 4);  // h1 > 0 as bits, one word per 32 columns
   {
     const size_t w1 = size_t(kSplitCtas / 2) * kN1 * K1, w2 = size_t(kSplitCtas) * kN2 * kN1;
     L.split = take((w1 > w2 ? w1 : w2) * 4);
@@ -1014,7 +1015,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   };
   // a sum over all positions: split over K, partials reduced in split order
   // bf16 mode: ReLU and mask inside the products' epilogues (while db1's
-  // partial sums, one row per 128-position tile, fit their buffer)
+  // partial sums, four rows per 128-position tile, fit their buffer)
   const long long P8 = (Pc + 7) / 8 * 8;
   const bool fuse = bf && (Pc + 127) / 128 <= kMaxBlocks;
   auto mm_splitk = [&](const void* A, const void* Bm, long long P8, float* D, int M, int N, long long K) -> bool {
@@ -1062,6 +1063,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       e.ldh = kN1;
       e.HT = w + L.H1T;
       e.ldt = P8;
+      e.mask = reinterpret_cast<uint32_t*>(w + L.M1);
+      e.ldm = kN1 / 32;
       if (!mm(X, K1, W1, K1, nullptr, kN1, Pc, kN1, K1, 1, &e)) return DSF_ECUDA;
     } else {
       if (!mm(X, K1, W1, K1, G1, kN1, Pc, kN1, K1, 1)) return DSF_ECUDA;
@@ -1091,12 +1094,13 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       e.epi = gemm::kEpiMask;
       e.H = dH1;
       e.ldh = kN1;
-      e.Hin = H1;
+      e.mask = reinterpret_cast<uint32_t*>(w + L.M1);
+      e.ldm = kN1 / 32;
       e.HT = w + L.dH1T;
       e.ldt = P8;
       e.part = part2;
       if (!mm(dH2, kN2, W2T, kN2, G1, kN1, Pc, kN1, kN2, 1, &e)) return DSF_ECUDA;
-      rb = int((Pc + 127) / 128);
+      rb = int(4 * ((Pc + 127) / 128));
     } else {
       if (!mm(dH2, kN2, W2T, kN2, G1, kN1, Pc, kN1, kN2, 1)) return DSF_ECUDA;
       rb = grid_for(Pc, 1, kMaxBlocks);

@@ -1,7 +1,11 @@
 // The backward's matrix products (see gemm.cuh).
 #include "gemm.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
+#include <mutex>
 
 #include "dinsparse.h"
 #include "ptx.cuh"
@@ -10,8 +14,9 @@ namespace dsf {
 namespace gemm {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps, one per tensor-memory lane quarter
+constexpr int kWarps = 16, kThreads = 32 * kWarps;  // four warps per tensor-memory lane quarter
 constexpr int kBM = 128, kBK = 64, kStages = 3;
+constexpr int kStgBytes = 32 * 64;  // a warp's epilogue staging: 32 rows x 64 bytes
 constexpr int kMaxGridY = 65535;
 
 __device__ __forceinline__ void set_flag(int* status, int bits) {
@@ -23,11 +28,11 @@ struct Tile {
   static constexpr int A_BYTES = kBM * 128;  // a 128 x 64 bf16 K-block
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int EPI_BYTES = 4 * BN * 4;  // the epilogue's per-warp column sums
+  static constexpr int EPI_BYTES = kWarps * kStgBytes;  // the epilogue's staging
   static constexpr int BODY = kStages * STAGE > EPI_BYTES ? kStages * STAGE : EPI_BYTES;
   static constexpr int SMEM = BODY + 1024;  // + alignment slack
   static constexpr uint32_t TCOLS = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
-  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "tcgen05 N for M = 128");
+  static_assert(BN % 64 == 0 && BN <= 256, "tcgen05 N for M = 128, whole 16-column chunks per warp group");
   static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle-atom alignment");
 };
 
@@ -38,91 +43,150 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Staging offsets (bytes) of 16-byte slot k of row r in a warp's block:
+// fp32 rows of 64 bytes (4 slots), bf16 rows of 32 bytes (2 slots, 32 bytes
+// of padding after every 8 rows). The slot is XOR-swizzled by row so that 8
+// lanes storing one slot of 8 rows, and 8 lanes loading whole rows, each
+// touch 8 different bank groups; the padding puts rows r and r + 8 (read
+// together by the transposed copy) in different bank groups.
+__device__ __forceinline__ int stg32(int r, int k) { return r * 64 + ((k ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ int stg16(int r, int k) { return r * 32 + (r >> 3) * 32 + ((k ^ ((r >> 2) & 1)) << 4); }
+
 // The epilogue of one 128-row tile whose accumulator (BN columns) starts at
-// tensor-memory column tbase. Thread t owns row t of the tile (its lane of
-// tensor memory) and walks its row 16 columns at a time, straight from
-// registers: the fp32 row of D (nullable), the fused transform of a.epi, the
-// bf16 row of H, and its transposed copy HT (2-byte stores: the 32 lanes of a
-// warp hold 32 consecutive rows, so each store instruction writes 64
-// contiguous bytes of one HT row). kEpiMask's column sums go through a
-// fixed-order shuffle tree per warp and a four-warp sum in shared memory
-// (csum: 4 * BN floats). have_acc false: the product is zero.
-template <int BN>
-__device__ __forceinline__ void epilogue(const TnArgs& a, float* csum, uint32_t tbase, long long m0, long long tile,
-                                         float* D, bool have_acc) {
+// tensor-memory column tbase. Warp w reads rows 32 (w % 4) .. + 31 (its lane
+// quarter of tensor memory), one row per lane, over the 16-column chunks
+// w / 4, w / 4 + 4, ... Every output goes through the warp's staging block
+// in shared memory, so that each store instruction writes whole 32-byte
+// sectors: D (fp32) and H (bf16) as row segments, HT (H transposed) as
+// 16-row column segments. Column sums (kEpiMask) add down the staged block
+// (rows 0-15 and 16-31 in two lanes, then the two) and go out per lane
+// quarter. This call covers columns n0 .. n0 + W - 1 of the tile, whose
+// accumulator starts at tensor-memory column tcol. E: kWarps staging blocks.
+// have_acc false: the product is zero.
+// bias: kEpiReluBias's bias (global or shared). mpre >= 0: the chunk's mask
+// bits, loaded by the caller (kEpiMask, one chunk per warp). work false:
+// nothing (a run that gave up).
+template <int BN, int W>
+__device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t tcol, long long m0, int n0,
+                                         long long tile, float* D, bool have_acc, const float* bias = nullptr,
+                                         long long mpre = -1, bool work = true) {
+  constexpr int NCH = W / 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long row = m0 + tid;
+  const int q = warp & 3, grp = warp >> 2;
+  uint8_t* stg = E + warp * kStgBytes;
+  const long long rbase = m0 + q * 32, row = rbase + lane;
   const bool live = row < a.M;
   __nv_bfloat16* H = static_cast<__nv_bfloat16*>(a.H);
-  __nv_bfloat16* HT = static_cast<__nv_bfloat16*>(a.HT);
-  const __nv_bfloat16* Hin = static_cast<const __nv_bfloat16*>(a.Hin);
-  const int nlim = a.N < BN ? a.N : BN;
-#pragma unroll 1
-  for (int c0 = 0; c0 < nlim; c0 += 16) {
+  uint16_t* HT = static_cast<uint16_t*>(a.HT);
+  uint16_t* mrow = a.mask ? reinterpret_cast<uint16_t*>(a.mask + (live ? row : 0) * a.ldm) : nullptr;
+#pragma unroll
+  for (int ch = grp; ch < NCH; ch += 4) {
+    const int c0 = n0 + ch * 16;
+    if (c0 >= a.N || !work) break;
+    const uint32_t mbits =
+        mpre >= 0 ? uint32_t(mpre) : ((a.epi == kEpiMask && live) ? uint32_t(mrow[c0 >> 4]) : 0u);  // (before the wait below)
     float v[16];
-    uint4 hin0 = make_uint4(0u, 0u, 0u, 0u), hin1 = hin0;
-    if (a.epi == kEpiMask && live) {  // (issued before the tensor-memory load)
-      hin0 = *reinterpret_cast<const uint4*>(Hin + row * a.ldh + c0);
-      hin1 = *reinterpret_cast<const uint4*>(Hin + row * a.ldh + c0 + 8);
-    }
     if (have_acc) {
-      tmem_ld16(tbase + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+      tmem_ld16(tcol + (uint32_t(q * 32) << 16) + uint32_t(ch * 16), v);
       tmem_ld_wait();
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = 0.f;
     }
-    const bool full = c0 + 16 <= a.N;
-    if (D && live) {
-      float* d = D + row * a.ldd + c0;
-      if (full && (reinterpret_cast<uintptr_t>(d) & 15) == 0) {
+    if (D) {  // fp32: 64-byte row segments
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(d + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      } else {
-        for (int j = 0; j < 16 && c0 + j < a.N; ++j) d[j] = v[j];
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float4*>(stg + stg32(lane, k)) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int r = it * 8 + (lane >> 2), k = lane & 3;
+        const long long gr = rbase + r;
+        if (gr < a.M && c0 + 4 * k < a.N)
+          *reinterpret_cast<float4*>(D + gr * a.ldd + c0 + 4 * k) = *reinterpret_cast<const float4*>(stg + stg32(r, k));
       }
+      __syncwarp();
     }
     if (a.epi == kEpiF32) continue;
     if (a.epi == kEpiReluBias) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j] + __ldg(a.bias + c0 + j), 0.f);
+      for (int k = 0; k < 4; ++k) {
+        const float4 b = reinterpret_cast<const float4*>((bias ? bias : a.bias) + c0)[k];
+        v[4 * k] = fmaxf(v[4 * k] + b.x, 0.f);
+        v[4 * k + 1] = fmaxf(v[4 * k + 1] + b.y, 0.f);
+        v[4 * k + 2] = fmaxf(v[4 * k + 2] + b.z, 0.f);
+        v[4 * k + 3] = fmaxf(v[4 * k + 3] + b.w, 0.f);
+      }
     } else {
-      const uint32_t hw[8] = {hin0.x, hin0.y, hin0.z, hin0.w, hin1.x, hin1.y, hin1.z, hin1.w};
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (!((mbits >> j) & 1u)) v[j] = 0.f;
+    }
+    uint32_t p[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) p[t] = bf16x2(v[2 * t], v[2 * t + 1]);
+    if (a.epi == kEpiReluBias && mrow && live) {
+      // bit j: bf16 value j is > 0 (ReLU outputs are >= 0 or -0); a half h
+      // of x = p & 0x7fff7fff is nonzero iff h + 0x7fff carries into its
+      // top bit
+      uint32_t bits = 0;
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        if (!(bf16_lo(hw[t]) > 0.f)) v[2 * t] = 0.f;
-        if (!(bf16_hi(hw[t]) > 0.f)) v[2 * t + 1] = 0.f;
+        const uint32_t y = (p[t] & 0x7fff7fffu) + 0x7fff7fffu;
+        bits |= ((y >> 15) & 1u) << (2 * t) | (y >> 31) << (2 * t + 1);
+      }
+      mrow[c0 >> 4] = uint16_t(bits);
+    }
+    // bf16: 32-byte row segments, then 16-row segments of HT's rows
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      *reinterpret_cast<uint4*>(stg + stg16(lane, k)) = make_uint4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int r = it * 16 + (lane >> 1), k = lane & 1;
+      const long long gr = rbase + r;
+      if (gr < a.M && c0 + 8 * k < a.N)
+        *reinterpret_cast<uint4*>(H + gr * a.ldh + c0 + 8 * k) = *reinterpret_cast<const uint4*>(stg + stg16(r, k));
+    }
+    {
+      // lane pair (2j, 2j + 1): column j, rows 8 (2i + hb) .. + 7 of the
+      // block (one 32-byte sector of HT's row per lane pair)
+      const int j = lane >> 1, hb = lane & 1;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r0 = 16 * i + 8 * hb;
+        uint16_t e[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          e[t] = *reinterpret_cast<const uint16_t*>(stg + stg16(r0 + t, j >> 3) + ((j & 7) << 1));
+        if (rbase + r0 < a.M && c0 + j < a.N)
+          *reinterpret_cast<uint4*>(HT + (long long)(c0 + j) * a.ldt + rbase + r0) =
+              make_uint4(uint32_t(e[0]) | uint32_t(e[1]) << 16, uint32_t(e[2]) | uint32_t(e[3]) << 16,
+                         uint32_t(e[4]) | uint32_t(e[5]) << 16, uint32_t(e[6]) | uint32_t(e[7]) << 16);
       }
     }
-    uint32_t packed[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) packed[t] = bf16x2(v[2 * t], v[2 * t + 1]);
-    if (live) {
-      *reinterpret_cast<uint4*>(H + row * a.ldh + c0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      *reinterpret_cast<uint4*>(H + row * a.ldh + c0 + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint16_t b16 = uint16_t(j & 1 ? packed[j >> 1] >> 16 : packed[j >> 1] & 0xffffu);
-        reinterpret_cast<uint16_t*>(HT)[(long long)(c0 + j) * a.ldt + row] = b16;
-      }
-    }
+    __syncwarp();
     if (a.epi == kEpiMask && a.part) {
-      // the warp's column sums of the masked values (rows past M are zero),
-      // a fixed-order tree over the lanes
+      // the masked fp32 block; lane l adds column l % 16 down rows
+      // 16 (l / 16) .. + 15 (the upper lanes rotated by one row: another
+      // bank group), then the lower lane adds the upper lane's sum and
+      // stores the column sum of the warp's 32 rows
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float x = v[j];
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float4*>(stg + stg32(lane, k)) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      __syncwarp();
+      const int c = lane & 15, hb = lane >> 4;
+      float sum = 0.f;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) csum[warp * BN + c0 + j] = x;
+      for (int t = 0; t < 16; ++t) {
+        const int rr = 16 * hb + ((t + hb) & 15);
+        sum += *reinterpret_cast<const float*>(stg + stg32(rr, c >> 2) + ((c & 3) << 2));
       }
+      sum += __shfl_down_sync(0xffffffffu, sum, 16);
+      if (lane < 16 && c0 + lane < a.N) a.part[(tile * 4 + q) * a.N + c0 + lane] = sum;
+      __syncwarp();
     }
-  }
-  if (a.epi == kEpiMask && a.part) {
-    __syncthreads();
-    for (int c = tid; c < nlim; c += kThreads)
-      a.part[tile * a.N + c] = ((csum[c] + csum[BN + c]) + csum[2 * BN + c]) + csum[3 * BN + c];
-    __syncthreads();
   }
 }
 
@@ -222,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_bf16_kernel(const TnArgs a) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (!abort_) epilogue<BN>(a, reinterpret_cast<float*>(sm), tbase, m0, blockIdx.x, D, nkb > 0);
+  if (!abort_) epilogue<BN, BN>(a, sm, tbase, m0, 0, blockIdx.x, D, nkb > 0);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, T::TCOLS);
@@ -230,39 +294,59 @@ __global__ void __launch_bounds__(kThreads, 1) tn_bf16_kernel(const TnArgs a) {
 }
 
 // B resident: D = A B^T with N <= 256 and K <= 64 * KB <= 256 (B, the MLP
-// weights, fits shared memory whole). Persistent CTAs, one per SM, walk the
-// 128-row tiles of A; B is loaded once. Per tile: the tile's A has landed ->
-// its MMAs -> the next tile's A starts loading -> this tile's epilogue
-// (overlapping that load).
+// weights, fits shared memory whole). Work units of 128 rows x 64 columns
+// (unit u: row tile u / NU, columns 64 (u % NU) ..), NU = BN / 64 per tile;
+// persistent CTAs, one per SM, each take a contiguous run of units (runs
+// differ by at most one unit; a row tile's A is loaded once per CTA that
+// touches it). Warp-specialised: warp kWarps loads A and issues the MMAs
+// (one thread) into two 64-column accumulators in tensor memory; warps
+// 0 .. kWarps - 1 run the epilogue. They hand over through mbarriers:
+// full[b] (the unit's MMAs committed) and empty[b] (every epilogue warp has
+// read accumulator b), so the MMAs and A loads of later units overlap the
+// epilogue of earlier ones and the epilogue warps never wait for each other.
 template <int BN, int KB>
 struct RTile {
+  static constexpr int UN = 64;  // columns per work unit
+  static constexpr int NU = BN / UN;
   static constexpr int B_BYTES = KB * BN * 128;
   static constexpr int A_BYTES = KB * kBM * 128;
-  static constexpr int E_BYTES = 4 * BN * 4;
-  static constexpr int SMEM = B_BYTES + A_BYTES + E_BYTES + 1024;
-  static constexpr uint32_t TCOLS = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
+  static constexpr int E_BYTES = kWarps * kStgBytes;
+  static constexpr int BIAS_BYTES = BN * 4;
+  static constexpr int SMEM = B_BYTES + A_BYTES + E_BYTES + BIAS_BYTES + 1024;
+  static constexpr uint32_t TCOLS = 2 * UN;
   static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1024-byte swizzle-atom alignment");
+  static_assert(BN % UN == 0 && BN <= 256 && UN == 4 * 16, "one 16-column chunk per epilogue warp and unit");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 template <int BN, int KB>
-__global__ void __launch_bounds__(kThreads, 1) tn_bf16_resident_kernel(const TnArgs a) {
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    tn_bf16_resident_kernel(const TnArgs a, const __grid_constant__ CUtensorMap mapA,
+                            const __grid_constant__ CUtensorMap mapB) {
   using T = RTile<BN, KB>;
+  constexpr int UN = T::UN, NU = T::NU;
+  constexpr uint32_t A_TX = KB * kBM * 128, B_TX = KB * BN * 128;
   extern __shared__ uint8_t dyn[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = sm;
   uint8_t* sA = sm + T::B_BYTES;
   uint8_t* sE = sA + T::A_BYTES;
-  __shared__ uint64_t bar;
+  float* sBias = reinterpret_cast<float*>(sE + T::E_BYTES);
+  __shared__ uint64_t full[2], empty[2], abar, bbar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long tiles = (a.M + kBM - 1) / kBM;
-  if ((long long)blockIdx.x >= tiles) return;
-  const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(a.A);
-  const __nv_bfloat16* Bm = static_cast<const __nv_bfloat16*>(a.B);
+  const long long units = tiles * NU;
+  const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+  if (u0 >= u1) return;
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], kWarps);
+    }
+    mbar_init(&abar, 1);
+    mbar_init(&bbar, 1);
     fence_mbarrier_init();
     abort_ = 0;
   }
@@ -270,63 +354,99 @@ __global__ void __launch_bounds__(kThreads, 1) tn_bf16_resident_kernel(const TnA
     tmem_alloc(&tmem_slot, T::TCOLS);
     tmem_relinquish();
   }
+  if (a.epi == kEpiReluBias)
+    for (int c = tid; c < BN; c += blockDim.x) sBias[c] = c < a.N ? a.bias[c] : 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
-  // 16-byte chunks in the 128-byte swizzle layout, K-block by K-block;
-  // rows past M / N and elements past K are zero-filled
-  for (int q = tid; q < KB * BN * 8; q += kThreads) {
-    const int kb = q / (BN * 8), rem = q - kb * (BN * 8), r = rem >> 3, c = rem & 7;
-    const long long k = (long long)kb * kBK + c * 8;
-    long long v = r < a.N ? a.K - k : 0;
-    v = v < 0 ? 0 : (v > 8 ? 8 : v);
-    const __nv_bfloat16* src = v > 0 ? Bm + (long long)r * a.ldb + k : Bm;
-    cp_async_16_ca(sB + kb * (BN * 128) + r * 128 + ((c ^ (r & 7)) << 4), src, uint32_t(v * 2));
-  }
-  auto load_a = [&](long long t) {
-    for (int q = tid; q < KB * kBM * 8; q += kThreads) {
-      const int kb = q / (kBM * 8), rem = q - kb * (kBM * 8), r = rem >> 3, c = rem & 7;
-      const long long row = t * kBM + r, k = (long long)kb * kBK + c * 8;
-      long long v = row < a.M ? a.K - k : 0;
-      v = v < 0 ? 0 : (v > 8 ? 8 : v);
-      const __nv_bfloat16* src = v > 0 ? A + row * a.lda + k : A;
-      cp_async_16_ca(sA + kb * (kBM * 128) + r * 128 + ((c ^ (r & 7)) << 4), src, uint32_t(v * 2));
+
+  if (warp == kWarps) {
+    // ------------------------------------------------ producer (one thread):
+    // TMA loads of B (once) and of each row tile's A, MMAs of every unit
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(kBM, UN);
+      uint32_t inflight = 0;             // accumulators with a commit not yet waited for
+      long long last0 = -1, last1 = -1;  // the last unit committed to full[0] / full[1]
+      uint32_t na = 0;                   // A loads issued (abar's phases)
+      bool a_pending = false, ok = true;
+      mbar_arrive_expect_tx(&bbar, B_TX);
+      for (int kb = 0; kb < KB; ++kb) tma_load_2d(sB + kb * (BN * 128), &mapB, kb * kBK, 0, &bbar);
+      auto load_a = [&](long long t) {
+        mbar_arrive_expect_tx(&abar, A_TX);
+        for (int kb = 0; kb < KB; ++kb) tma_load_2d(sA + kb * (kBM * 128), &mapA, kb * kBK, int(t * kBM), &abar);
+        ++na;
+        a_pending = true;
+      };
+      load_a(u0 / NU);
+      ok = mbar_wait(&bbar, 0);
+      for (long long u = u0; u < u1 && ok; ++u) {
+        const int b = int(u & 1);
+        const long long k = u - u0;
+        if (a_pending) {
+          if (!(ok = mbar_wait(&abar, (na - 1) & 1u))) break;
+          a_pending = false;
+        }
+        if (k >= 2 && !(ok = mbar_wait(&empty[b], uint32_t(((k - 2) >> 1) & 1)))) break;
+        tc_fence_after();
+        const uint32_t d = tbase + uint32_t(b) * UN;
+        const int nq = int(u % NU);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_f16(d, sw128_kmajor_desc(smem_u32(sA + kb * (kBM * 128)) + kk * 32),
+                       sw128_kmajor_desc(smem_u32(sB + kb * (BN * 128) + nq * (UN * 128)) + kk * 32), IDESC,
+                       (kb > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&full[b]);
+        inflight |= 1u << b;
+        (b ? last1 : last0) = u;
+        if (u + 1 < u1 && (u + 1) % NU == 0) {
+          // the next unit starts a row tile: its A loads once this unit's MMAs
+          // (the last readers of the current A) are done
+          if (!(ok = mbar_wait(&full[b], uint32_t((k >> 1) & 1)))) break;
+          load_a((u + 1) / NU);
+        }
+      }
+      if (!ok) {
+        atomicExch(&abort_, 1);
+        // (copies and MMAs that may still run: wait, bounded, before the
+        // buffers and accumulators are released)
+        if (a_pending) mbar_wait(&abar, (na - 1) & 1u);
+        if ((inflight & 1u) && last0 >= 0) mbar_wait(&full[0], uint32_t(((last0 - u0) >> 1) & 1));
+        if ((inflight & 2u) && last1 >= 0) mbar_wait(&full[1], uint32_t(((last1 - u0) >> 1) & 1));
+      }
     }
-  };
-  load_a(blockIdx.x);
-  cp_async_commit();
-  constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN);
-  uint32_t phase = 0;
-  for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (abort_) break;
-    if (tid == 0) {
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int q = warp & 3, grp = warp >> 2;
+    // the mask bits of this warp's chunk in unit u (kEpiMask), loaded a unit ahead
+    auto mask_of = [&](long long u) -> long long {
+      if (a.epi != kEpiMask || u >= u1) return 0;
+      const long long row = (u / NU) * kBM + q * 32 + lane;
+      const int c0 = int(u % NU) * UN + grp * 16;
+      return (row < a.M && c0 < a.N) ? (long long)reinterpret_cast<const uint16_t*>(a.mask + row * a.ldm)[c0 >> 4]
+                                     : 0;
+    };
+    long long mnext = mask_of(u0);
+    for (long long u = u0; u < u1; ++u) {
+      const int b = int(u & 1);
+      const long long k = u - u0;
+      bool ok = !*reinterpret_cast<volatile int*>(&abort_);
+      if (ok && lane == 0) ok = mbar_wait(&full[b], uint32_t((k >> 1) & 1));
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok && lane == 0) atomicExch(&abort_, 1);
       tc_fence_after();
-#pragma unroll
-      for (int kb = 0; kb < KB; ++kb)
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma_f16(tbase, sw128_kmajor_desc(smem_u32(sA + kb * (kBM * 128)) + kk * 32),
-                     sw128_kmajor_desc(smem_u32(sB + kb * (BN * 128)) + kk * 32), IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(&bar);
-      if (!mbar_wait(&bar, phase)) abort_ = 1;
+      const long long mcur = mnext;
+      mnext = mask_of(u + 1);
+      epilogue<BN, UN>(a, sE, tbase + uint32_t(b) * UN, (u / NU) * kBM, int(u % NU) * UN, u / NU, a.D, true, sBias,
+                       a.epi == kEpiMask ? mcur : -1, ok);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[b]);
     }
-    phase ^= 1u;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (abort_) break;
-    // the next tile's A streams in while this tile's epilogue runs
-    if (t + gridDim.x < tiles) load_a(t + gridDim.x);
-    cp_async_commit();
-    epilogue<BN>(a, reinterpret_cast<float*>(sE), tbase, t * kBM, t, a.D, true);
-    tc_fence_before();  // (this tile's tensor-memory reads before the next tile's MMAs)
   }
-  cp_async_wait_all();
-  tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, T::TCOLS);
   if (tid == 0 && abort_) set_flag(a.status, DSF_FLAG_TIMEOUT);
@@ -501,6 +621,35 @@ bool launch_bf16(const TnArgs& a, int splits, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A 2-D bf16 tensor map over rows x cols (row stride ld elements) whose box is
+// 64 columns (128 bytes, the 128-byte swizzle span) by box_rows rows; reads
+// past the tensor's edge fill with zeros.
+bool tensor_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+  if (!fn || rows <= 0 || cols <= 0 || box_rows <= 0 || box_rows > 256) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+  const cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, int KB>
 int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
   using T = RTile<BN, KB>;
@@ -515,10 +664,12 @@ int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
       return 0;
     attr_set[dev] = true;
   }
-  const long long tiles = (a.M + kBM - 1) / kBM;
-  const long long g = tiles < nsm[dev] ? tiles : nsm[dev];
+  const long long units = (a.M + kBM - 1) / kBM * T::NU;
+  const long long g = units < nsm[dev] ? units : nsm[dev];
   if (g <= 0) return 1;
-  tn_bf16_resident_kernel<BN, KB><<<unsigned(g), kThreads, T::SMEM, s>>>(a);
+  CUtensorMap mapA, mapB;
+  if (!tensor_map(&mapA, a.A, a.M, a.K, a.lda, kBM) || !tensor_map(&mapB, a.B, a.N, a.K, a.ldb, BN)) return 0;
+  tn_bf16_resident_kernel<BN, KB><<<unsigned(g), kThreads + 32, T::SMEM, s>>>(a, mapA, mapB);
   return cudaGetLastError() == cudaSuccess ? 1 : 0;
 }
 
@@ -545,8 +696,14 @@ bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
     tn_f32_kernel<<<dim3(unsigned(mt), unsigned(splits), unsigned(nt)), 256, 0, s>>>(a0, 0);
     return cudaGetLastError() == cudaSuccess;
   }
-  if (a0.epi != kEpiF32 && (a0.N > 256 || a0.N % 32 != 0 || !a0.H || !a0.HT || a0.ldh % 8 || a0.ldt % 8))
+  if (a0.epi != kEpiF32 &&
+      (a0.N > 256 || a0.N % 32 != 0 || !a0.H || !a0.HT || a0.ldh % 8 || (reinterpret_cast<uintptr_t>(a0.H) & 15) ||
+       a0.ldt % 8 || a0.ldt < (a0.M + 7) / 8 * 8 || (reinterpret_cast<uintptr_t>(a0.HT) & 15) ||
+       (a0.epi == kEpiMask && !a0.mask) || (a0.mask && a0.ldm < a0.N / 32) ||
+       (a0.epi == kEpiReluBias && (!a0.bias || (reinterpret_cast<uintptr_t>(a0.bias) & 15)))))
     return false;
+  // (the epilogue's fp32 stores are 16-byte vectors)
+  if (a0.D && ((reinterpret_cast<uintptr_t>(a0.D) & 15) || a0.ldd % 4 || a0.split_stride % 4)) return false;
   // B resident (the products with a weight matrix as B): persistent CTAs
   if (splits == 1 && a0.K <= 4 * kBK && a0.N <= 256) {
     const int kb = int((a0.K + kBK - 1) / kBK);
@@ -556,7 +713,6 @@ bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
     else if (bn == 256 && kb == 3) r = launch_resident<256, 3>(a0, s);
     else if (bn == 256 && kb == 1) r = launch_resident<256, 1>(a0, s);
     else if (bn == 192 && kb == 4) r = launch_resident<192, 4>(a0, s);
-    else if (bn == 256 && kb == 4) r = launch_resident<256, 4>(a0, s);
     if (r >= 0) return r == 1;
   }
   // N in chunks of at most 256 columns: B's rows and D's columns move on

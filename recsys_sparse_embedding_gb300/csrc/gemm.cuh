@@ -2,7 +2,7 @@
 // with both operands K-major ("TN"), fp32 results.
 //
 //   bf16 operands: tcgen05 MMA (kind::f16, fp32 accumulation in tensor
-//   memory), 128 threads per CTA, a 128-row tile of D with the whole N
+//   memory), 256 threads per CTA, a 128-row tile of D with the whole N
 //   (<= 256) in one accumulator. Two kernels:
 //   - B resident (K <= 256, no split: the products with a weight matrix):
 //     persistent CTAs, one per SM, hold B in shared memory (K-major, 128-byte
@@ -10,9 +10,10 @@
 //     current tile's epilogue runs;
 //   - streaming (split-K): a three-stage ring of 64-wide K-blocks of A and B.
 //   Operands arrive by cp.async from all threads; one thread issues the MMAs
-//   and commits them to an mbarrier. The epilogue reads each thread's row of
-//   the accumulator from tensor memory and stores it from registers, with the
-//   ReLU or the mask of the backward fused in (Epi).
+//   and commits them to an mbarrier. In the epilogue each warp reads 32 rows
+//   of the accumulator from tensor memory (one row per lane), applies the
+//   ReLU or the mask of the backward (Epi) and stores whole row segments
+//   through a per-warp staging block in shared memory.
 //   fp32 operands (the check mode): CUDA-core tiles of 64 x 64.
 //
 // Both take split-K: split z covers K-range [z * k_per_split, ...) and writes
@@ -29,9 +30,13 @@ namespace gemm {
 // What the bf16 kernel's epilogue writes (the fp32 kernel: kEpiF32 only).
 enum Epi {
   kEpiF32 = 0,       // D = A B^T (fp32)
-  kEpiReluBias = 1,  // H = bf16(ReLU(A B^T + bias)) and its transpose HT
-  kEpiMask = 2,      // D = A B^T; v = D where Hin > 0, else 0; H = bf16(v) and
-                     // HT; part[tile][n] = the tile's column sums of v
+  kEpiReluBias = 1,  // H = bf16(ReLU(A B^T + bias)) and its transpose HT;
+                     // mask (nullable): bit n % 32 of word n / 32 of row m
+                     // set where H[m][n] > 0
+  kEpiMask = 2,      // D = A B^T; v = D where mask's bit is set, else 0;
+                     // H = bf16(v) and HT; part[4 tile + j][n] = the column
+                     // sums of v over rows 32 j .. 32 j + 31 of 128-row tile
+                     // `tile`
 };
 
 struct TnArgs {
@@ -39,7 +44,8 @@ struct TnArgs {
   long long lda;
   const void* B;      // [N][K] (row stride ldb elements)
   long long ldb;
-  float* D;           // [M][N] (row stride ldd), per split at D + z * split_stride
+  float* D;           // [M][N] (row stride ldd), per split at D + z * split_stride;
+                      // 16-byte aligned, ldd and split_stride multiples of 4
   long long ldd;
   long long M;
   int N;              // a multiple of 16 (larger N runs in chunks of 256; kEpiF32 only)
@@ -48,13 +54,17 @@ struct TnArgs {
   long long split_stride;
   int* status;        // DSF_FLAG_TIMEOUT on a wait that ran out (nullable)
   int epi;            // Epi (bf16 only)
-  const float* bias;  // kEpiReluBias: [N]
-  void* H;            // bf16 [M][ldh]
+  const float* bias;  // kEpiReluBias: [N], 16-byte aligned
+  void* H;            // bf16 [M][ldh], 16-byte aligned, ldh a multiple of 8
   long long ldh;
-  const void* Hin;    // kEpiMask: bf16 [M][ldh], the mask's source
-  void* HT;           // bf16 [N][ldt]: element (m, n) at n * ldt + m
+  uint32_t* mask;     // [M][ldm] words (ldm >= N / 32): written by kEpiReluBias
+                      // (nullable), read by kEpiMask
+  long long ldm;
+  void* HT;           // bf16 [N][ldt]: element (m, n) at n * ldt + m; 16-byte
+                      // aligned, ldt a multiple of 8 and >= M rounded up to 8
+                      // (entries M .. that bound of each row are overwritten)
   long long ldt;
-  float* part;        // kEpiMask: [M tiles][N]
+  float* part;        // kEpiMask: [4 x M tiles][N]
 };
 
 // Launches D = A B^T over `splits` K-splits on `stream`. bf16 selects the
