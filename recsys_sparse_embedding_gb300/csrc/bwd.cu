@@ -88,8 +88,9 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.dH1 = take(P * kN1 * 4);
   L.dX = take(P * K1 * 4);
   L.dS = take(P * Q * 4);
-  // transposed weights; position-major copies of x, h1, dh2, dh1 (rows of
-  // P8 = P rounded up to 8 elements, 16-byte aligned); split-K partials
+  // transposed weights; transposed copies of x, h1, dh2, dh1 for the fp32
+  // weight gradients (positions contiguous: rows of P8 = P rounded up to 8
+  // elements, 16-byte aligned); split-K partials
   const size_t P8 = (P + 7) / 8 * 8;
   L.w1t = take(K1 * size_t(kN1) * 4);
   L.w2t = take(size_t(kN1) * kN2 * 4);
@@ -1018,7 +1019,11 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   // partial sums, four rows per 128-position tile, fit their buffer)
   const long long P8 = (Pc + 7) / 8 * 8;
   const bool fuse = bf && (Pc + 127) / 128 <= kMaxBlocks;
-  auto mm_splitk = [&](const void* A, const void* Bm, long long P8, float* D, int M, int N, long long K) -> bool {
+  // D [M][N] = A^T B over the K = P positions: bf16 reads the activations as
+  // stored, one row per position (A [K][lda], B [K][ldb]); fp32 takes their
+  // transposes (A [M][P8], B [N][P8]) on the CUDA cores
+  auto mm_splitk = [&](const void* A, long long lda, const void* Bm, long long ldb, float* D, int M, int N,
+                       long long K) -> bool {
     // K-splits of at least 256 positions, about kSplitCtas CTAs in all
     const int mt = (M + 127) / 128;
     int splits = int((K + 255) / 256);
@@ -1030,9 +1035,9 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     float* part = reinterpret_cast<float*>(w + L.split);
     gemm::TnArgs g{};
     g.A = A;
-    g.lda = P8;
+    g.lda = lda;
     g.B = Bm;
-    g.ldb = P8;
+    g.ldb = ldb;
     g.D = part;
     g.ldd = N;
     g.M = M;
@@ -1041,7 +1046,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     g.k_per_split = kps;
     g.split_stride = (long long)M * N;
     g.status = status_dev;
-    return gemm::tn(g, splits, bf, s) && gemm::reduce(part, (long long)M * N, splits, N, D, N, M, N, s);
+    const bool ok = bf ? gemm::atb(g, splits, s) : gemm::tn(g, splits, false, s);
+    return ok && gemm::reduce(part, (long long)M * N, splits, N, D, N, M, N, s);
   };
   if (Pc > 0) {
     const int gb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
@@ -1053,7 +1059,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
                                                               S, Pc);
     if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
     // recompute: h1 = ReLU(x W1^T + b1) (in bf16 mode inside the product's
-    // epilogue, which also writes h1's position-major copy), then the layer-2
+    // epilogue, which also records h1 > 0 as bits), then the layer-2
     // pre-activation
     if (fuse) {
       gemm::TnArgs e{};
@@ -1061,8 +1067,6 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       e.bias = mlp->b1;
       e.H = H1;
       e.ldh = kN1;
-      e.HT = w + L.H1T;
-      e.ldt = P8;
       e.mask = reinterpret_cast<uint32_t*>(w + L.M1);
       e.ldm = kN1 / 32;
       if (!mm(X, K1, W1, K1, nullptr, kN1, Pc, kN1, K1, 1, &e)) return DSF_ECUDA;
@@ -1087,7 +1091,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   if (Pc > 0) {
     // dh1 = (dh2 W2) [h1 > 0] and db1's partial sums (in bf16 mode inside the
-    // product's epilogue, with dh1's position-major copy)
+    // product's epilogue)
     int rb;
     if (fuse) {
       gemm::TnArgs e{};
@@ -1096,8 +1100,6 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       e.ldh = kN1;
       e.mask = reinterpret_cast<uint32_t*>(w + L.M1);
       e.ldm = kN1 / 32;
-      e.HT = w + L.dH1T;
-      e.ldt = P8;
       e.part = part2;
       if (!mm(dH2, kN2, W2T, kN2, G1, kN1, Pc, kN1, kN2, 1, &e)) return DSF_ECUDA;
       rb = int(4 * ((Pc + 127) / 128));
@@ -1114,19 +1116,21 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s>>>(
         RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
     if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
-    // the weight gradients sum over positions: their operands, position-major
-    // (h1's and dh1's copies came from the fused epilogues)
-    void* XT = w + L.XT;
-    void* H1T = w + L.H1T;
-    void* dH2T = w + L.dH2T;
-    void* dH1T = w + L.dH1T;
-    if (!gemm::transpose(X, K1, Pc, K1, XT, P8, esz, s) || !gemm::transpose(dH2, kN2, Pc, kN2, dH2T, P8, esz, s))
-      return DSF_ECUDA;
-    if (!fuse && (!gemm::transpose(dH1, kN1, Pc, kN1, dH1T, P8, esz, s) ||
-                  !gemm::transpose(H1, kN1, Pc, kN1, H1T, P8, esz, s)))
-      return DSF_ECUDA;
-    if (!mm_splitk(dH1T, XT, P8, mg->dW1, kN1, K1, Pc)) return DSF_ECUDA;
-    if (!mm_splitk(dH2T, H1T, P8, mg->dW2, kN2, kN1, Pc)) return DSF_ECUDA;
+    // the weight gradients sum over positions (fp32: on transposed copies)
+    if (bf) {
+      if (!mm_splitk(dH1, kN1, X, K1, mg->dW1, kN1, K1, Pc)) return DSF_ECUDA;
+      if (!mm_splitk(dH2, kN2, H1, kN1, mg->dW2, kN2, kN1, Pc)) return DSF_ECUDA;
+    } else {
+      void* XT = w + L.XT;
+      void* H1T = w + L.H1T;
+      void* dH2T = w + L.dH2T;
+      void* dH1T = w + L.dH1T;
+      if (!gemm::transpose(X, K1, Pc, K1, XT, P8, esz, s) || !gemm::transpose(dH2, kN2, Pc, kN2, dH2T, P8, esz, s) ||
+          !gemm::transpose(dH1, kN1, Pc, kN1, dH1T, P8, esz, s) || !gemm::transpose(H1, kN1, Pc, kN1, H1T, P8, esz, s))
+        return DSF_ECUDA;
+      if (!mm_splitk(dH1T, P8, XT, P8, mg->dW1, kN1, K1, Pc)) return DSF_ECUDA;
+      if (!mm_splitk(dH2T, P8, H1T, P8, mg->dW2, kN2, kN1, Pc)) return DSF_ECUDA;
+    }
   } else {
     if (cudaMemsetAsync(mg->dW1, 0, size_t(kN1) * K1 * 4, s) != cudaSuccess ||
         cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess ||

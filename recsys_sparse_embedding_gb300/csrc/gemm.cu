@@ -149,7 +149,7 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
       if (gr < a.M && c0 + 8 * k < a.N)
         *reinterpret_cast<uint4*>(H + gr * a.ldh + c0 + 8 * k) = *reinterpret_cast<const uint4*>(stg + stg16(r, k));
     }
-    {
+    if (HT) {
       // lane pair (2j, 2j + 1): column j, rows 8 (2i + hb) .. + 7 of the
       // block (one 32-byte sector of HT's row per lane pair)
       const int j = lane >> 1, hb = lane & 1;
@@ -452,6 +452,119 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   if (tid == 0 && abort_) set_flag(a.status, DSF_FLAG_TIMEOUT);
 }
 
+// D (+ split) = A^T B with both operands stored one row per K index (A
+// [K][M], B [K][N]): the weight gradients' sums over positions, read from
+// the activations as they are stored. A CTA computes a 128 x BN
+// tile over its K-split. Operand tiles arrive by TMA as 64 x 64 boxes in the
+// 128-byte swizzle (rows of 64 M- or N-elements, one row per position), which
+// is the MN-major canonical layout: atoms of 8 positions x 64 elements
+// (1024 bytes; SBO, along K), the next 64 elements 8 KB further (LBO, along
+// M or N). One thread keeps kAStages K-blocks in flight and issues the MMAs;
+// all warps run the epilogue.
+constexpr int kAStages = 4;
+
+template <int BN>
+struct ATile {
+  static constexpr int NB = BN / 64;
+  static constexpr int A_BYTES = 2 * 8192, B_BYTES = NB * 8192, STAGE = A_BYTES + B_BYTES;
+  static constexpr int SMEM = kAStages * STAGE + kWarps * kStgBytes + 1024;
+  static constexpr uint32_t TCOLS = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
+  static_assert(BN % 64 == 0 && BN <= 256, "whole 64-element atoms along N");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;  // LBO: the next 64 elements along M / N
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;  // SBO: the next 8 positions along K
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;  // 128-byte swizzle
+  return d;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    atb_bf16_kernel(const TnArgs a, const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB) {
+  using T = ATile<BN>;
+  extern __shared__ uint8_t dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sE = sm + kAStages * T::STAGE;
+  __shared__ uint64_t full[kAStages], done[kAStages];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const long long m0 = (long long)blockIdx.x * kBM;
+  const long long k0 = (long long)blockIdx.y * a.k_per_split;
+  const long long k1 = k0 + a.k_per_split < a.K ? k0 + a.k_per_split : a.K;
+  const int nkb = k1 > k0 ? int((k1 - k0 + kBK - 1) / kBK) : 0;
+  float* D = a.D + (long long)blockIdx.y * a.split_stride;
+  if (tid == 0) {
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&done[i], 1);
+    }
+    fence_mbarrier_init();
+    abort_ = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, T::TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+  if (tid == 0 && nkb > 0) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN) | (1u << 15) | (1u << 16);  // A and B MN-major
+    auto load = [&](int kb) {
+      uint8_t* st = sm + (kb % kAStages) * T::STAGE;
+      uint64_t* bar = &full[kb % kAStages];
+      const int y = int(k0 + (long long)kb * kBK);
+      mbar_arrive_expect_tx(bar, T::STAGE);
+      for (int j = 0; j < 2; ++j) tma_load_2d(st + j * 8192, &mapA, int(m0) + 64 * j, y, bar);
+      for (int j = 0; j < T::NB; ++j) tma_load_2d(st + T::A_BYTES + j * 8192, &mapB, 64 * j, y, bar);
+    };
+    bool ok = true;
+    int issued = 0;  // K-blocks whose loads were issued
+    for (; issued < kAStages && issued < nkb; ++issued) load(issued);
+    int last = -1;  // the last K-block whose MMAs were committed
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+      const int st = kb % kAStages;
+      const uint32_t par = uint32_t((kb / kAStages) & 1);
+      if (!(ok = mbar_wait(&full[st], par))) break;
+      tc_fence_after();
+      const uint32_t sa = smem_u32(sm + st * T::STAGE), sb = sa + T::A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        tc_mma_f16(tbase, sw128_mnmajor_desc(sa + kk * 2048), sw128_mnmajor_desc(sb + kk * 2048), IDESC,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&done[st]);
+      last = kb;
+      if (issued < nkb) {
+        // block `issued` reuses this stage once these MMAs are done
+        if (!(ok = mbar_wait(&done[st], par))) break;
+        load(issued++);
+      }
+    }
+    // every MMA done (a commit covers all earlier MMAs of the thread); on a
+    // timeout, the copies still in flight are waited for too (bounded)
+    if (last >= 0) ok = mbar_wait(&done[last % kAStages], uint32_t((last / kAStages) & 1)) && ok;
+    if (!ok) {
+      abort_ = 1;
+      for (int kb = last + 1; kb < issued; ++kb) mbar_wait(&full[kb % kAStages], uint32_t((kb / kAStages) & 1));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (!abort_) epilogue<BN, BN>(a, sE, tbase, m0, 0, blockIdx.x, D, nkb > 0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, T::TCOLS);
+  if (tid == 0 && abort_) set_flag(a.status, DSF_FLAG_TIMEOUT);
+}
+
 // fp32 operands on the CUDA cores: 64 x 64 tiles of D, 256 threads, 4 x 4
 // results each; K-steps of 16 staged in shared memory.
 __global__ void __launch_bounds__(256) tn_f32_kernel(const TnArgs a, int n0) {
@@ -673,6 +786,25 @@ int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
   return cudaGetLastError() == cudaSuccess ? 1 : 0;
 }
 
+template <int BN>
+bool launch_atb(const TnArgs& a, int splits, cudaStream_t s) {
+  using T = ATile<BN>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(atb_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) != cudaSuccess)
+      return false;
+    attr_set[dev] = true;
+  }
+  const long long mt = (a.M + kBM - 1) / kBM;
+  if (mt <= 0 || mt > 0x7fffffff || splits < 1 || splits > kMaxGridY) return false;
+  CUtensorMap mapA, mapB;
+  if (!tensor_map(&mapA, a.A, a.K, a.M, a.lda, 64) || !tensor_map(&mapB, a.B, a.K, a.N, a.ldb, 64)) return false;
+  atb_bf16_kernel<BN><<<dim3(unsigned(mt), unsigned(splits)), kThreads, T::SMEM, s>>>(a, mapA, mapB);
+  return cudaGetLastError() == cudaSuccess;
+}
+
 }  // namespace
 
 size_t tn_bf16_smem_bytes(int N) {
@@ -697,8 +829,8 @@ bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess;
   }
   if (a0.epi != kEpiF32 &&
-      (a0.N > 256 || a0.N % 32 != 0 || !a0.H || !a0.HT || a0.ldh % 8 || (reinterpret_cast<uintptr_t>(a0.H) & 15) ||
-       a0.ldt % 8 || a0.ldt < (a0.M + 7) / 8 * 8 || (reinterpret_cast<uintptr_t>(a0.HT) & 15) ||
+      (a0.N > 256 || a0.N % 32 != 0 || !a0.H || a0.ldh % 8 || (reinterpret_cast<uintptr_t>(a0.H) & 15) ||
+       (a0.HT && (a0.ldt % 8 || a0.ldt < (a0.M + 7) / 8 * 8 || (reinterpret_cast<uintptr_t>(a0.HT) & 15))) ||
        (a0.epi == kEpiMask && !a0.mask) || (a0.mask && a0.ldm < a0.N / 32) ||
        (a0.epi == kEpiReluBias && (!a0.bias || (reinterpret_cast<uintptr_t>(a0.bias) & 15)))))
     return false;
@@ -726,6 +858,36 @@ bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
     else if (a.N <= 128) ok = launch_bf16<128>(a, splits, s);
     else if (a.N <= 192) ok = launch_bf16<192>(a, splits, s);
     else ok = launch_bf16<256>(a, splits, s);
+    if (!ok) return false;
+  }
+  return true;
+}
+
+bool atb(const TnArgs& a0, int splits, cudaStream_t s) {
+  if (a0.M <= 0 || a0.N <= 0 || a0.K < 0 || splits < 1) return a0.M <= 0 || a0.N <= 0;
+  if (a0.k_per_split <= 0 || a0.k_per_split % kBK != 0 || !a0.D) return false;
+  if ((reinterpret_cast<uintptr_t>(a0.A) & 15) || (reinterpret_cast<uintptr_t>(a0.B) & 15) || a0.lda % 8 ||
+      a0.ldb % 8 || a0.lda < a0.M || a0.ldb < a0.N)
+    return false;
+  if ((reinterpret_cast<uintptr_t>(a0.D) & 15) || a0.ldd % 4 || a0.split_stride % 4) return false;
+  if (a0.K == 0) {
+    for (int z = 0; z < splits; ++z)
+      for (long long m = 0; m < a0.M; ++m)
+        if (cudaMemsetAsync(a0.D + z * a0.split_stride + m * a0.ldd, 0, size_t(a0.N) * 4, s) != cudaSuccess) return false;
+    return true;
+  }
+  // N in chunks of at most 256 columns: B's columns and D's columns move on
+  for (int n0 = 0; n0 < a0.N; n0 += 256) {
+    TnArgs a = a0;
+    a.N = a0.N - n0 < 256 ? a0.N - n0 : 256;
+    a.B = static_cast<const __nv_bfloat16*>(a0.B) + n0;
+    a.D = a0.D + n0;
+    a.epi = kEpiF32;
+    bool ok;
+    if (a.N <= 64) ok = launch_atb<64>(a, splits, s);
+    else if (a.N <= 128) ok = launch_atb<128>(a, splits, s);
+    else if (a.N <= 192) ok = launch_atb<192>(a, splits, s);
+    else ok = launch_atb<256>(a, splits, s);
     if (!ok) return false;
   }
   return true;

@@ -60,7 +60,7 @@ struct TnArgs {
   uint32_t* mask;     // [M][ldm] words (ldm >= N / 32): written by kEpiReluBias
                       // (nullable), read by kEpiMask
   long long ldm;
-  void* HT;           // bf16 [N][ldt]: element (m, n) at n * ldt + m; 16-byte
+  void* HT;           // bf16 [N][ldt] (nullable): element (m, n) at n * ldt + m; 16-byte
                       // aligned, ldt a multiple of 8 and >= M rounded up to 8
                       // (entries M .. that bound of each row are overwritten)
   long long ldt;
@@ -72,6 +72,14 @@ struct TnArgs {
 // Rows of A / B must start 16-byte aligned (lda, ldb multiples of 8 bf16 or
 // 4 fp32 elements; A, B 16-byte aligned).
 bool tn(const TnArgs& a, int splits, bool bf16, cudaStream_t stream);
+
+// D (+ split z) = A^T B in bf16 over `splits` K-splits, both operands stored
+// one row per K index: A [K][M] (row stride lda >= M), B [K][N] (ldb >= N), 16-byte
+// aligned, strides multiples of 8 elements; fp32 results at D + z *
+// split_stride, [M][ldd] (16-byte aligned, ldd and split_stride multiples of
+// 4). K = 0 writes zeros. Returns false if the shape is unsupported or a
+// launch fails.
+bool atb(const TnArgs& a, int splits, cudaStream_t stream);
 
 // D[m][n] = sum over s of P[s][m][n] (row strides ldp / ldd, split stride
 // split_stride), in a fixed order: eight interleaved groups of splits
