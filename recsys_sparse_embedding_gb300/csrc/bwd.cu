@@ -100,8 +100,11 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.dH1T = take(size_t(kN1) * P8 * 4);
   L.M1 = take(P * (kN1 / 32) * 4);  // h1 > 0 as bits, one word per 32 columns
   {
+    // one product alone (fp32) or both in one launch (bf16, kSplitCtas / 3 splits each)
     const size_t w1 = size_t(kSplitCtas / 2) * kN1 * K1, w2 = size_t(kSplitCtas) * kN2 * kN1;
-    L.split = take((w1 > w2 ? w1 : w2) * 4);
+    const size_t both = size_t(kSplitCtas / 3) * (size_t(kN1) * K1 + size_t(kN2) * kN1);
+    const size_t m = w1 > w2 ? w1 : w2;
+    L.split = take((m > both ? m : both) * 4);
   }
   L.total = o;
   return L;
@@ -254,7 +257,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(const ScanJobs
 }
 
 // Pass 2: each tile adds the sums of the tiles before it and scans its own
-// entries; the last tile writes the totals at index n.
+// entries, kScanRounds consecutive ones per thread (one block scan of the
+// threads' sums); the last tile writes the totals at index n.
 __global__ void __launch_bounds__(kScanThreads) scan_apply_kernel(const ScanJobs jobs) {
   int tile;
   const ScanJob& J = job_of(jobs, tile);
@@ -265,20 +269,31 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply_kernel(const ScanJobs
     block_scan2(ca, cb, ta, tb);
     ca = ta, cb = tb;
   }
+  const long long k0 = (long long)tile * kScanTile + (long long)threadIdx.x * kScanRounds;
+  int v[kScanRounds];
+  long long a = 0, b = 0;
+#pragma unroll
   for (int r = 0; r < kScanRounds; ++r) {
-    const long long k = (long long)tile * kScanTile + r * kScanThreads + threadIdx.x;
-    const int v = k < J.n ? max(J.len[k], 0) : 0;
-    long long a = v, b = min(v, J.clamp), ta, tb;
-    block_scan2(a, b, ta, tb);
-    if (k < J.n) {
-      J.raw[k] = ca + a - v;
-      if (J.clp) J.clp[k] = cb + b - min(v, J.clamp);
+    v[r] = k0 + r < J.n ? max(J.len[k0 + r], 0) : 0;
+    a += v[r];
+    b += min(v[r], J.clamp);
+  }
+  const long long own_a = a, own_b = b;
+  long long ta, tb;
+  block_scan2(a, b, ta, tb);
+  long long ea = ca + a - own_a, eb = cb + b - own_b;  // the exclusive prefix at entry k0
+#pragma unroll
+  for (int r = 0; r < kScanRounds; ++r) {
+    if (k0 + r < J.n) {
+      J.raw[k0 + r] = ea;
+      if (J.clp) J.clp[k0 + r] = eb;
     }
-    ca += ta, cb += tb;
+    ea += v[r];
+    eb += min(v[r], J.clamp);
   }
   if (tile == J.tiles - 1 && threadIdx.x == 0) {
-    J.raw[J.n] = ca;
-    if (J.clp) J.clp[J.n] = cb;
+    J.raw[J.n] = ca + ta;
+    if (J.clp) J.clp[J.n] = cb + tb;
   }
 }
 
@@ -1118,8 +1133,30 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
     // the weight gradients sum over positions (fp32: on transposed copies)
     if (bf) {
-      if (!mm_splitk(dH1, kN1, X, K1, mg->dW1, kN1, K1, Pc)) return DSF_ECUDA;
-      if (!mm_splitk(dH2, kN2, H1, kN1, mg->dW2, kN2, kN1, Pc)) return DSF_ECUDA;
+      // both products in one launch, kSplitCtas / 3 K-splits each (about
+      // kSplitCtas CTAs with equal K-blocks: dW1 has two row tiles, dW2 one),
+      // then both reductions in one launch
+      int splits = int((Pc + 255) / 256);
+      if (splits > kSplitCtas / 3) splits = kSplitCtas / 3;
+      if (splits < 1) splits = 1;
+      const long long kps = ((Pc + splits - 1) / splits + 63) / 64 * 64;
+      splits = int((Pc + kps - 1) / kps);
+      if (splits < 1) splits = 1;
+      float* part0 = reinterpret_cast<float*>(w + L.split);
+      float* part1 = part0 + size_t(splits) * kN1 * K1;
+      gemm::TnArgs g0{}, g1{};
+      g0.A = dH1, g0.lda = kN1, g0.B = X, g0.ldb = K1, g0.D = part0, g0.ldd = K1, g0.M = kN1, g0.N = K1;
+      g1.A = dH2, g1.lda = kN2, g1.B = H1, g1.ldb = kN1, g1.D = part1, g1.ldd = kN1, g1.M = kN2, g1.N = kN1;
+      for (gemm::TnArgs* g : {&g0, &g1}) {
+        g->K = Pc;
+        g->k_per_split = kps;
+        g->split_stride = g->M * g->N;
+        g->status = status_dev;
+      }
+      if (!gemm::atb2(g0, splits, g1, splits, s) ||
+          !gemm::reduce2(part0, g0.split_stride, splits, K1, mg->dW1, K1, kN1, K1, part1, g1.split_stride, splits, kN1,
+                         mg->dW2, kN1, kN2, kN1, s))
+        return DSF_ECUDA;
     } else {
       void* XT = w + L.XT;
       void* H1T = w + L.H1T;

@@ -483,10 +483,20 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Up to two independent products in one launch: CTAs [0, g0) take job 0
+// (mt0 row tiles x its splits, tile-minor), the rest job 1.
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    atb_bf16_kernel(const TnArgs a, const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB) {
+    atb_bf16_kernel(const __grid_constant__ TnArgs a0, const __grid_constant__ TnArgs a1, int g0, int mt0, int mt1,
+                    const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapB0,
+                    const __grid_constant__ CUtensorMap mapA1, const __grid_constant__ CUtensorMap mapB1) {
   using T = ATile<BN>;
+  const bool j1 = int(blockIdx.x) >= g0;
+  const TnArgs& a = j1 ? a1 : a0;
+  const CUtensorMap* mapA = j1 ? &mapA1 : &mapA0;
+  const CUtensorMap* mapB = j1 ? &mapB1 : &mapB0;
+  const int local = int(blockIdx.x) - (j1 ? g0 : 0), mt = j1 ? mt1 : mt0;
+  const int mtile = local % mt, split = local / mt;
   extern __shared__ uint8_t dyn[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
   uint8_t* sE = sm + kAStages * T::STAGE;
@@ -494,11 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const long long m0 = (long long)blockIdx.x * kBM;
-  const long long k0 = (long long)blockIdx.y * a.k_per_split;
+  const long long m0 = (long long)mtile * kBM;
+  const long long k0 = (long long)split * a.k_per_split;
   const long long k1 = k0 + a.k_per_split < a.K ? k0 + a.k_per_split : a.K;
   const int nkb = k1 > k0 ? int((k1 - k0 + kBK - 1) / kBK) : 0;
-  float* D = a.D + (long long)blockIdx.y * a.split_stride;
+  float* D = a.D + (long long)split * a.split_stride;
   if (tid == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&full[i], 1);
@@ -517,13 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = tmem_slot;
   if (tid == 0 && nkb > 0) {
     constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN) | (1u << 15) | (1u << 16);  // A and B MN-major
+    // boxes wholly past M or N are not loaded: the accumulator rows and
+    // columns they feed are never stored
+    const long long mrem = a.M - m0;
+    const int na = mrem > 64 ? 2 : 1, nb = int((a.N + 63) / 64) < T::NB ? int((a.N + 63) / 64) : T::NB;
+    const uint32_t tx = uint32_t(na + nb) * 8192u;
     auto load = [&](int kb) {
       uint8_t* st = sm + (kb % kAStages) * T::STAGE;
       uint64_t* bar = &full[kb % kAStages];
       const int y = int(k0 + (long long)kb * kBK);
-      mbar_arrive_expect_tx(bar, T::STAGE);
-      for (int j = 0; j < 2; ++j) tma_load_2d(st + j * 8192, &mapA, int(m0) + 64 * j, y, bar);
-      for (int j = 0; j < T::NB; ++j) tma_load_2d(st + T::A_BYTES + j * 8192, &mapB, 64 * j, y, bar);
+      mbar_arrive_expect_tx(bar, tx);
+      for (int j = 0; j < na; ++j) tma_load_2d(st + j * 8192, mapA, int(m0) + 64 * j, y, bar);
+      for (int j = 0; j < nb; ++j) tma_load_2d(st + T::A_BYTES + j * 8192, mapB, 64 * j, y, bar);
     };
     bool ok = true;
     int issued = 0;  // K-blocks whose loads were issued
@@ -558,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (!abort_) epilogue<BN, BN>(a, sE, tbase, m0, 0, blockIdx.x, D, nkb > 0);
+  if (!abort_) epilogue<BN, BN>(a, sE, tbase, m0, 0, mtile, D, nkb > 0);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, T::TCOLS);
@@ -622,26 +637,34 @@ __global__ void __launch_bounds__(256) tn_f32_kernel(const TnArgs a, int n0) {
 // 32 consecutive outputs per block of 256 threads: warp g adds splits g,
 // g + 8, g + 16, ... in increasing order (eight loads in flight), then warp
 // 0 adds the eight warps' sums in warp order. The order is fixed, so the
-// result is deterministic.
-__global__ void __launch_bounds__(256) reduce_kernel(const float* P, long long split_stride, int splits, long long ldp,
-                                                     float* D, long long ldd, long long M, int N) {
+// result is deterministic. Blocks [0, b0) take job 0, the rest job 1.
+struct RedJob {
+  const float* P;
+  long long split_stride, ldp, ldd, M;
+  float* D;
+  int splits, N;
+};
+__global__ void __launch_bounds__(256) reduce_kernel(const RedJob j0, const RedJob j1, int b0) {
   __shared__ float part[8][33];
+  const bool second = int(blockIdx.x) >= b0;
+  const RedJob& J = second ? j1 : j0;
+  const int nblk = second ? int(gridDim.x) - b0 : b0, blk = int(blockIdx.x) - (second ? b0 : 0);
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
-  const long long total = M * N;
-  for (long long base = blockIdx.x * 32LL; base < total; base += gridDim.x * 32LL) {
+  const long long total = J.M * J.N;
+  for (long long base = blk * 32LL; base < total; base += nblk * 32LL) {
     const long long i = base + lane;
-    const long long m = i < total ? i / N : 0;
-    const int n = int(i - m * N);
+    const long long m = i < total ? i / J.N : 0;
+    const int n = int(i - m * J.N);
     float s = 0.f;
     if (i < total) {
-      const float* q = P + m * ldp + n;
-      for (int z0 = g; z0 < splits; z0 += 64) {
+      const float* q = J.P + m * J.ldp + n;
+      for (int z0 = g; z0 < J.splits; z0 += 64) {
         float v[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = z0 + 8 * t < splits ? q[(long long)(z0 + 8 * t) * split_stride] : 0.f;
+        for (int t = 0; t < 8; ++t) v[t] = z0 + 8 * t < J.splits ? q[(long long)(z0 + 8 * t) * J.split_stride] : 0.f;
 #pragma unroll
         for (int t = 0; t < 8; ++t)
-          if (z0 + 8 * t < splits) s += v[t];
+          if (z0 + 8 * t < J.splits) s += v[t];
       }
     }
     part[g][lane] = s;
@@ -650,7 +673,50 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float* P, long long s
       float r = part[0][lane];
 #pragma unroll
       for (int k = 1; k < 8; ++k) r += part[k][lane];
-      D[m * ldd + n] = r;
+      J.D[m * J.ldd + n] = r;
+    }
+    __syncthreads();
+  }
+}
+
+// The same sums four outputs at a time (N, ldp, ldd and split_stride
+// multiples of 4; P and D 16-byte aligned): 128 consecutive outputs per
+// block, float4 loads, the same fixed order per output.
+__global__ void __launch_bounds__(256) reduce4_kernel(const RedJob j0, const RedJob j1, int b0) {
+  __shared__ float4 part[8][32];
+  const bool second = int(blockIdx.x) >= b0;
+  const RedJob& J = second ? j1 : j0;
+  const int nblk = second ? int(gridDim.x) - b0 : b0, blk = int(blockIdx.x) - (second ? b0 : 0);
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const long long total4 = J.M * J.N / 4;
+  for (long long base = blk * 32LL; base < total4; base += nblk * 32LL) {
+    const long long i = base + lane;
+    const long long m = i < total4 ? (4 * i) / J.N : 0;
+    const int n = int(4 * i - m * J.N);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < total4) {
+      const float* q = J.P + m * J.ldp + n;
+      for (int z0 = g; z0 < J.splits; z0 += 64) {
+        float4 v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          v[t] = z0 + 8 * t < J.splits ? *reinterpret_cast<const float4*>(q + (long long)(z0 + 8 * t) * J.split_stride)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (z0 + 8 * t < J.splits) s.x += v[t].x, s.y += v[t].y, s.z += v[t].z, s.w += v[t].w;
+      }
+    }
+    part[g][lane] = s;
+    __syncthreads();
+    if (g == 0 && i < total4) {
+      float4 r = part[0][lane];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) {
+        const float4 x = part[k][lane];
+        r.x += x.x, r.y += x.y, r.z += x.z, r.w += x.w;
+      }
+      *reinterpret_cast<float4*>(J.D + m * J.ldd + n) = r;
     }
     __syncthreads();
   }
@@ -786,8 +852,9 @@ int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
   return cudaGetLastError() == cudaSuccess ? 1 : 0;
 }
 
+// Job 1 (a1 non-null) runs in the same launch as job 0.
 template <int BN>
-bool launch_atb(const TnArgs& a, int splits, cudaStream_t s) {
+bool launch_atb(const TnArgs& a0, int s0, const TnArgs* a1, int s1, cudaStream_t s) {
   using T = ATile<BN>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -797,11 +864,20 @@ bool launch_atb(const TnArgs& a, int splits, cudaStream_t s) {
       return false;
     attr_set[dev] = true;
   }
-  const long long mt = (a.M + kBM - 1) / kBM;
-  if (mt <= 0 || mt > 0x7fffffff || splits < 1 || splits > kMaxGridY) return false;
-  CUtensorMap mapA, mapB;
-  if (!tensor_map(&mapA, a.A, a.K, a.M, a.lda, 64) || !tensor_map(&mapB, a.B, a.K, a.N, a.ldb, 64)) return false;
-  atb_bf16_kernel<BN><<<dim3(unsigned(mt), unsigned(splits)), kThreads, T::SMEM, s>>>(a, mapA, mapB);
+  const long long mt0 = (a0.M + kBM - 1) / kBM, mt1 = a1 ? (a1->M + kBM - 1) / kBM : 1;
+  const long long g0 = mt0 * s0, g1 = a1 ? mt1 * s1 : 0;
+  if (mt0 <= 0 || mt1 <= 0 || s0 < 1 || (a1 && s1 < 1) || g0 + g1 > 0x7fffffff) return false;
+  CUtensorMap mA0, mB0, mA1, mB1;
+  if (!tensor_map(&mA0, a0.A, a0.K, a0.M, a0.lda, 64) || !tensor_map(&mB0, a0.B, a0.K, a0.N, a0.ldb, 64)) return false;
+  if (a1) {
+    if (!tensor_map(&mA1, a1->A, a1->K, a1->M, a1->lda, 64) || !tensor_map(&mB1, a1->B, a1->K, a1->N, a1->ldb, 64))
+      return false;
+  } else {
+    mA1 = mA0;
+    mB1 = mB0;
+  }
+  atb_bf16_kernel<BN><<<unsigned(g0 + g1), kThreads, T::SMEM, s>>>(a0, a1 ? *a1 : a0, int(g0), int(mt0), int(mt1),
+                                                                    mA0, mB0, mA1, mB1);
   return cudaGetLastError() == cudaSuccess;
 }
 
@@ -863,19 +939,24 @@ bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
   return true;
 }
 
+namespace {
+bool atb_ok(const TnArgs& a) {
+  return a.k_per_split > 0 && a.k_per_split % kBK == 0 && a.D && !(reinterpret_cast<uintptr_t>(a.A) & 15) &&
+         !(reinterpret_cast<uintptr_t>(a.B) & 15) && a.lda % 8 == 0 && a.ldb % 8 == 0 && a.lda >= a.M &&
+         a.ldb >= a.N && !(reinterpret_cast<uintptr_t>(a.D) & 15) && a.ldd % 4 == 0 && a.split_stride % 4 == 0;
+}
+bool zero_splits(const TnArgs& a, int splits, cudaStream_t s) {
+  for (int z = 0; z < splits; ++z)
+    for (long long m = 0; m < a.M; ++m)
+      if (cudaMemsetAsync(a.D + z * a.split_stride + m * a.ldd, 0, size_t(a.N) * 4, s) != cudaSuccess) return false;
+  return true;
+}
+}  // namespace
+
 bool atb(const TnArgs& a0, int splits, cudaStream_t s) {
   if (a0.M <= 0 || a0.N <= 0 || a0.K < 0 || splits < 1) return a0.M <= 0 || a0.N <= 0;
-  if (a0.k_per_split <= 0 || a0.k_per_split % kBK != 0 || !a0.D) return false;
-  if ((reinterpret_cast<uintptr_t>(a0.A) & 15) || (reinterpret_cast<uintptr_t>(a0.B) & 15) || a0.lda % 8 ||
-      a0.ldb % 8 || a0.lda < a0.M || a0.ldb < a0.N)
-    return false;
-  if ((reinterpret_cast<uintptr_t>(a0.D) & 15) || a0.ldd % 4 || a0.split_stride % 4) return false;
-  if (a0.K == 0) {
-    for (int z = 0; z < splits; ++z)
-      for (long long m = 0; m < a0.M; ++m)
-        if (cudaMemsetAsync(a0.D + z * a0.split_stride + m * a0.ldd, 0, size_t(a0.N) * 4, s) != cudaSuccess) return false;
-    return true;
-  }
+  if (!atb_ok(a0)) return false;
+  if (a0.K == 0) return zero_splits(a0, splits, s);
   // N in chunks of at most 256 columns: B's columns and D's columns move on
   for (int n0 = 0; n0 < a0.N; n0 += 256) {
     TnArgs a = a0;
@@ -884,22 +965,57 @@ bool atb(const TnArgs& a0, int splits, cudaStream_t s) {
     a.D = a0.D + n0;
     a.epi = kEpiF32;
     bool ok;
-    if (a.N <= 64) ok = launch_atb<64>(a, splits, s);
-    else if (a.N <= 128) ok = launch_atb<128>(a, splits, s);
-    else if (a.N <= 192) ok = launch_atb<192>(a, splits, s);
-    else ok = launch_atb<256>(a, splits, s);
+    if (a.N <= 64) ok = launch_atb<64>(a, splits, nullptr, 0, s);
+    else if (a.N <= 128) ok = launch_atb<128>(a, splits, nullptr, 0, s);
+    else if (a.N <= 192) ok = launch_atb<192>(a, splits, nullptr, 0, s);
+    else ok = launch_atb<256>(a, splits, nullptr, 0, s);
     if (!ok) return false;
   }
   return true;
 }
 
+bool atb2(const TnArgs& a0, int s0, const TnArgs& a1, int s1, cudaStream_t s) {
+  const bool e0 = a0.M <= 0 || a0.N <= 0, e1 = a1.M <= 0 || a1.N <= 0;
+  if (e0 || e1 || a0.N > 256 || a1.N > 256 || a0.K <= 0 || a1.K <= 0)
+    return atb(a0, s0, s) && atb(a1, s1, s);
+  if (s0 < 1 || s1 < 1 || !atb_ok(a0) || !atb_ok(a1)) return false;
+  TnArgs b0 = a0, b1 = a1;
+  b0.epi = b1.epi = kEpiF32;
+  return launch_atb<256>(b0, s0, &b1, s1, s);
+}
+
 bool reduce(const float* P, long long split_stride, int splits, long long ldp, float* D, long long ldd, long long M,
             int N, cudaStream_t s) {
-  const long long total = M * N;
-  if (total <= 0) return true;
-  long long g = (total + 31) / 32;
-  if (g > 152 * 8) g = 152 * 8;
-  reduce_kernel<<<unsigned(g), 256, 0, s>>>(P, split_stride, splits, ldp, D, ldd, M, N);
+  return reduce2(P, split_stride, splits, ldp, D, ldd, M, N, nullptr, 0, 0, 0, nullptr, 0, 0, 0, s);
+}
+
+bool reduce2(const float* P0, long long ss0, int splits0, long long ldp0, float* D0, long long ldd0, long long M0,
+             int N0, const float* P1, long long ss1, int splits1, long long ldp1, float* D1, long long ldd1,
+             long long M1, int N1, cudaStream_t s) {
+  const long long t0 = M0 * N0, t1 = P1 ? M1 * N1 : 0;
+  if (t0 <= 0 && t1 <= 0) return true;
+  // blocks in proportion to the outputs, about 8 per SM in all
+  auto blocks = [](long long t) { return t <= 0 ? 0LL : ((t + 31) / 32 < 152 * 8 ? (t + 31) / 32 : 152LL * 8); };
+  long long b0 = blocks(t0), b1 = blocks(t1);
+  if (b0 + b1 > 152 * 8 && t0 > 0 && t1 > 0) {
+    b0 = 152 * 8 * t0 / (t0 + t1);
+    b0 = b0 < 1 ? 1 : b0;
+    b1 = 152 * 8 - b0;
+    b1 = b1 < 1 ? 1 : b1;
+  }
+  const RedJob j0{P0, ss0, ldp0, ldd0, t0 > 0 ? M0 : 0, D0, splits0, N0 > 0 ? N0 : 1};
+  const RedJob j1{P1, ss1, ldp1, ldd1, t1 > 0 ? M1 : 0, D1, splits1, N1 > 0 ? N1 : 1};
+  auto vec = [](const RedJob& j) {
+    return j.M == 0 || (j.N % 4 == 0 && j.ldp % 4 == 0 && j.ldd % 4 == 0 && j.split_stride % 4 == 0 &&
+                        !(reinterpret_cast<uintptr_t>(j.P) & 15) && !(reinterpret_cast<uintptr_t>(j.D) & 15));
+  };
+  if (vec(j0) && vec(j1)) {
+    auto blocks4 = [](long long t) { return t <= 0 ? 0LL : ((t / 4 + 31) / 32 < 152 * 4 ? (t / 4 + 31) / 32 : 152LL * 4); };
+    long long c0 = blocks4(t0), c1 = blocks4(t1);
+    reduce4_kernel<<<unsigned(c0 + c1), 256, 0, s>>>(j0, j1, int(c0));
+  } else {
+    reduce_kernel<<<unsigned(b0 + b1), 256, 0, s>>>(j0, j1, int(b0));
+  }
   return cudaGetLastError() == cudaSuccess;
 }
 

@@ -81,11 +81,20 @@ bool tn(const TnArgs& a, int splits, bool bf16, cudaStream_t stream);
 // launch fails.
 bool atb(const TnArgs& a, int splits, cudaStream_t stream);
 
+// Two independent atb products (N <= 256 each) in one launch; other shapes
+// run as two atb calls.
+bool atb2(const TnArgs& a0, int splits0, const TnArgs& a1, int splits1, cudaStream_t stream);
+
 // D[m][n] = sum over s of P[s][m][n] (row strides ldp / ldd, split stride
 // split_stride), in a fixed order: eight interleaved groups of splits
 // (z mod 8), each summed in increasing z, then the groups in order.
 bool reduce(const float* P, long long split_stride, int splits, long long ldp, float* D, long long ldd,
             long long M, int N, cudaStream_t stream);
+
+// Two reductions as above in one launch (P1 null: the first alone).
+bool reduce2(const float* P0, long long split_stride0, int splits0, long long ldp0, float* D0, long long ldd0,
+             long long M0, int N0, const float* P1, long long split_stride1, int splits1, long long ldp1, float* D1,
+             long long ldd1, long long M1, int N1, cudaStream_t stream);
 
 // out[c][r] = in[r][c] for r < rows, c < cols (element size 2 or 4 bytes);
 // row strides ld_in / ld_out in elements.
