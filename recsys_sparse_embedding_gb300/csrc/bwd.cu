@@ -689,7 +689,9 @@ __device__ __forceinline__ float4 shfl_up4(float4 v, int o) {
 
 // Row gradients of a tile of kTile id occurrences (the KJT's values at
 // [0, n_values), the sequence ids at n_values + 3 * position + k): the tile's
-// (key, source) pairs sorted by key in shared memory (bitonic network), then
+// keys sorted with their tile indices (bitonic network, two elements per
+// thread: registers, shuffles, and shared memory only for distances of 64
+// and more), then
 // per 4-element piece a segmented inclusive scan over the sorted order (two
 // elements per thread, shuffles within warps, a carry across warps) gives each
 // run's sum at its last element, which issues one vector reduction into the
@@ -700,37 +702,63 @@ __global__ void __launch_bounds__(kRowThreads) rowgrad_kernel(
     const unsigned long long* __restrict__ okey, const long long* __restrict__ osrc, const float* __restrict__ gbag,
     const float* __restrict__ dS) {
   constexpr int NW = kRowThreads / 32;
+  static_assert(kTile == 2 * kRowThreads && kTile <= 1024, "two elements per thread; tile index in 10 bits");
   __shared__ unsigned long long key[kTile];
   __shared__ long long src[kTile];
+  __shared__ uint16_t sidx[kTile];
   __shared__ float4 wagg[NW];
   __shared__ int whead[NW];
   const int D = p.D, Q = 3 * D, pieces = D / 4, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const long long nv = min(boff[(long long)p.F * p.B], p.n_values), P = min(soff[p.B], Pc);
   const long long o0 = (long long)blockIdx.x * kTile;
-  for (int i = tid; i < kTile; i += kRowThreads) {
+  // sort words: key << 10 | tile index (keys hold at most 45 bits; an
+  // occurrence with no parameter row sorts last as all ones). Equal keys
+  // keep their occurrence order, so each run is summed in that order.
+  unsigned long long v[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int i = 2 * tid + e;
     const long long o = o0 + i;
     const bool ok = o < p.n_values ? o < nv : (o - p.n_values) < 3 * P;
-    key[i] = ok ? okey[o] : kNoKey;
+    const unsigned long long k = ok ? okey[o] : kNoKey;
     src[i] = ok ? osrc[o] : 0;
+    v[e] = k == kNoKey ? ~0ull : (k << 10) | unsigned(i);
   }
-  __syncthreads();
+  // bitonic network over positions 2 tid + e: distance 1 within the thread,
+  // 2 .. 32 across lanes (shuffles), 64 and up through shared memory
   for (int k = 2; k <= kTile; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < kTile; i += kRowThreads) {
-        const int l = i ^ j;
-        if (l > i) {
-          const bool up = (i & k) == 0;
-          const unsigned long long a = key[i], b = key[l];
-          if ((a > b) == up) {
-            key[i] = b, key[l] = a;
-            const long long t = src[i];
-            src[i] = src[l], src[l] = t;
-          }
-        }
+      unsigned long long q[2];
+      if (j == 1) {
+        q[0] = v[1];
+        q[1] = v[0];
+      } else if (j <= 32) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) q[e] = __shfl_xor_sync(0xffffffffu, v[e], j >> 1);
+      } else {
+        __syncthreads();  // (the previous stage's reads are done)
+        key[2 * tid] = v[0];
+        key[2 * tid + 1] = v[1];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) q[e] = key[(2 * tid + e) ^ j];
       }
-      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = 2 * tid + e;
+        const bool up = (i & k) == 0, low = (i & j) == 0;
+        const unsigned long long lo = v[e] < q[e] ? v[e] : q[e], hi = v[e] < q[e] ? q[e] : v[e];
+        v[e] = (low == up) ? lo : hi;
+      }
     }
   }
+  __syncthreads();  // (the last shared-memory stage's reads are done)
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    key[2 * tid + e] = v[e] == ~0ull ? kNoKey : v[e] >> 10;
+    sidx[2 * tid + e] = uint16_t(v[e] & 1023u);
+  }
+  __syncthreads();
   const int ia = 2 * tid, ib = ia + 1;
   const unsigned long long ka = key[ia], kb = key[ib];
   const unsigned long long kn = ib + 1 < kTile ? key[ib + 1] : kNoKey;
@@ -743,8 +771,8 @@ __global__ void __launch_bounds__(kRowThreads) rowgrad_kernel(
   };
   int flags = 0;
   for (int c = 0; c < pieces; ++c) {
-    const float4 xa = va ? piece(src[ia], c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 xb = vb ? piece(src[ib], c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 xa = va ? piece(src[sidx[ia]], c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 xb = vb ? piece(src[sidx[ib]], c) : make_float4(0.f, 0.f, 0.f, 0.f);
     // this thread's trailing segment (from its last run start, or all of it)
     float4 agg = sb ? xb : xa + xb;
     bool head = sa || sb;
