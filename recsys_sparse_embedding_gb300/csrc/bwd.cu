@@ -73,7 +73,12 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.zb = take(P * 4);
   L.dab = take(P * 4);
   L.part1 = take(size_t(kMaxBlocks) * kRedCols * 4);
-  L.part2 = take(size_t(4) * kMaxBlocks * kN1 * 4);  // (the fused mask epilogue: 4 rows per 128-position tile)
+  {
+    // db1's partial sums: a row per block of the fp32 mask kernel, or four
+    // per 128-position tile from the bf16 products' mask epilogue
+    const size_t rows = size_t(4) * ((P + 127) / 128);
+    L.part2 = take((rows > size_t(kMaxBlocks) ? rows : size_t(kMaxBlocks)) * kN1 * 4);
+  }
   L.gbag = take(size_t(B) * F * D * 4);
   L.okey = take((size_t(NV) + 3 * P) * 8);
   L.osrc = take((size_t(NV) + 3 * P) * 8);
@@ -409,7 +414,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
   flag(p.status, flags);
 }
 
-// h1 = ReLU(G1 + b1) in the MLP operand type, over [Pc, 256].
+// h1 = ReLU(G1 + b1) in the MLP operand type, over [Pc, 256] (the fp32 check
+// mode; bf16 mode does it in the product's epilogue).
 template <class T>
 __global__ void relu1_kernel(const float* __restrict__ G1, const float* __restrict__ b1, T* H1, long long n4) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
@@ -424,8 +430,6 @@ template <class T>
 __device__ __forceinline__ float to_f(T v);
 template <>
 __device__ __forceinline__ float to_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 template <class T>
 __device__ __forceinline__ T from_f(float v);
@@ -565,7 +569,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
 }
 
 // dh1 = G (dh2 W2) * [h1 > 0], over [Pc, 256] with one column per thread;
-// db1 sums the masked values.
+// db1 sums the masked values (the fp32 check mode; bf16 mode does it in the
+// product's epilogue).
 template <class T>
 __global__ void __launch_bounds__(kN1) relu1_bwd_kernel(const float* __restrict__ G, const T* __restrict__ H1,
                                                        T* dH1, float* part, long long Pc) {
@@ -1058,10 +1063,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     return gemm::tn(g, n_split < 1 ? 1 : n_split, bf, s);
   };
   // a sum over all positions: split over K, partials reduced in split order
-  // bf16 mode: ReLU and mask inside the products' epilogues (while db1's
-  // partial sums, four rows per 128-position tile, fit their buffer)
   const long long P8 = (Pc + 7) / 8 * 8;
-  const bool fuse = bf && (Pc + 127) / 128 <= kMaxBlocks;
   // D [M][N] = A^T B over the K = P positions: bf16 reads the activations as
   // stored, one row per position (A [K][lda], B [K][ldb]); fp32 takes their
   // transposes (A [M][P8], B [N][P8]) on the CUDA cores
@@ -1104,7 +1106,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     // recompute: h1 = ReLU(x W1^T + b1) (in bf16 mode inside the product's
     // epilogue, which also records h1 > 0 as bits), then the layer-2
     // pre-activation
-    if (fuse) {
+    if (bf) {
       gemm::TnArgs e{};
       e.epi = gemm::kEpiReluBias;
       e.bias = mlp->b1;
@@ -1115,12 +1117,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       if (!mm(X, K1, W1, K1, nullptr, kN1, Pc, kN1, K1, 1, &e)) return DSF_ECUDA;
     } else {
       if (!mm(X, K1, W1, K1, G1, kN1, Pc, kN1, K1, 1)) return DSF_ECUDA;
-      if (bf)
-        relu1_kernel<__nv_bfloat16><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(
-            G1, mlp->b1, static_cast<__nv_bfloat16*>(H1), Pc * kN1 / 4);
-      else
-        relu1_kernel<float><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1, static_cast<float*>(H1),
-                                                                        Pc * kN1 / 4);
+      relu1_kernel<float><<<grid_for(Pc * kN1 / 4, 256), 256, 0, s>>>(G1, mlp->b1, static_cast<float*>(H1),
+                                                                      Pc * kN1 / 4);
     }
     if (!mm(H1, kN1, W2, kN1, H2, kN2, Pc, kN2, kN1, 1)) return DSF_ECUDA;
   }
@@ -1136,7 +1134,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     // dh1 = (dh2 W2) [h1 > 0] and db1's partial sums (in bf16 mode inside the
     // product's epilogue)
     int rb;
-    if (fuse) {
+    if (bf) {
       gemm::TnArgs e{};
       e.epi = gemm::kEpiMask;
       e.H = dH1;
@@ -1149,12 +1147,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     } else {
       if (!mm(dH2, kN2, W2T, kN2, G1, kN1, Pc, kN1, kN2, 1)) return DSF_ECUDA;
       rb = grid_for(Pc, 1, kMaxBlocks);
-      if (bf)
-        relu1_bwd_kernel<__nv_bfloat16><<<rb, kN1, 0, s>>>(G1, static_cast<const __nv_bfloat16*>(H1),
-                                                            static_cast<__nv_bfloat16*>(dH1), part2, Pc);
-      else
-        relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
-                                                   Pc);
+      relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
+                                                 Pc);
     }
     reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s>>>(
         RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});

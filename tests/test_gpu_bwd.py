@@ -122,6 +122,15 @@ def test_backward_taobao_full_size():
     run_case(synth.generate("taobao", seed=0), modes=(TC,), seed=3)
 
 
+def test_backward_taobao_many_positions():
+    """B = 36,000 (about 180 K valid positions, over 1,400 row tiles): db1's
+    partial sums, four rows per 128-position tile, fill a buffer sized by the
+    position count, several times the rows of the other column sums."""
+    b = synth.generate("taobao", seed=4, B=36000)
+    assert int(np.minimum(b.seq_lengths, b.max_len).sum()) > 155_648
+    run_case(b, modes=(TC,), seed=21)
+
+
 def test_backward_mean_pooling_and_long_bags():
     rng = np.random.default_rng(4)
     lens = rng.integers(0, 12, size=(16, 200)).astype(np.int32)
