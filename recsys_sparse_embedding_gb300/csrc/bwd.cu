@@ -440,17 +440,20 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return
 
 // The MLP weights as the products read them: W1 [256, K1] and W2 [64, 256]
 // as given, and their transposes W1^T [K1, 256], W2^T [256, 64], in the
-// operand type T (bf16: rounded to nearest even).
+// operand type T (bf16: rounded to nearest even). perm: W1^T's row for
+// column g Q + d of x (part g of cat[q, s, q - s, q s], dim d) is 4 d + g,
+// so that the dx product's columns come four per dim (the dq/ds epilogue).
 template <class T>
 __global__ void pack_kernel(const float* __restrict__ W1, const float* __restrict__ W2, int K1, T* w1, T* w2,
-                            T* w1t, T* w2t) {
-  const int n1 = kN1 * K1, n2 = kN2 * kN1;
+                            T* w1t, T* w2t, bool perm) {
+  const int n1 = kN1 * K1, n2 = kN2 * kN1, Q = K1 / 4;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n1 + n2; i += gridDim.x * blockDim.x) {
     if (i < n1) {
       const int o = i / K1, k = i - o * K1;
       const T v = from_f<T>(W1[i]);
       if (w1) w1[i] = v;
-      w1t[(long long)k * kN1 + o] = v;
+      const int r = perm ? 4 * (k % Q) + k / Q : k;
+      w1t[(long long)r * kN1 + o] = v;
     } else {
       const int j = i - n1, o = j / kN1, k = j - o * kN1;
       const T v = from_f<T>(W2[j]);
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
     const long long* __restrict__ roff, long long Pc, const float* __restrict__ pooled,
     const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S,
     float* __restrict__ dS, float* __restrict__ gbag, unsigned long long* __restrict__ okey,
-    long long* __restrict__ osrc) {
+    long long* __restrict__ osrc, const float* __restrict__ dqc) {
   __shared__ float dqs[kWarpsPerBlock][3 * 64];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
@@ -630,6 +633,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
                                                      : kNoKey;
             osrc[o] = -(3 * q + k) - 1;
           }
+        }
+        if (dqc) {  // (ds and the dq terms came from the dx product's epilogue)
+#pragma unroll
+          for (int i = 0; i < kPG; ++i)
+            if (g0 + i < nc) dq[i] = dq[i] + f4(dqc + q * Q + 4 * (g0 + i));
+          continue;
         }
         const float* dx = dX + q * K1;
 #pragma unroll
@@ -1027,15 +1036,19 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     scan_tiles_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
     scan_apply_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
   }
+  // bf16 with x at most 256 wide (D = 16): ds and the dq terms in the dx
+  // product's epilogue (dx itself is not written)
+  const bool fuse_dsdq = bf && K1 <= 256;
   if (bf) {
     pack_kernel<__nv_bfloat16><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
         mlp->W1, mlp->W2, K1, reinterpret_cast<__nv_bfloat16*>(w + L.w1b), reinterpret_cast<__nv_bfloat16*>(w + L.w2b),
-        reinterpret_cast<__nv_bfloat16*>(w + L.w1t), reinterpret_cast<__nv_bfloat16*>(w + L.w2t));
+        reinterpret_cast<__nv_bfloat16*>(w + L.w1t), reinterpret_cast<__nv_bfloat16*>(w + L.w2t), fuse_dsdq);
     W1 = w + L.w1b;
     W2 = w + L.w2b;
   } else {
     pack_kernel<float><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
-        mlp->W1, mlp->W2, K1, nullptr, nullptr, reinterpret_cast<float*>(w + L.w1t), reinterpret_cast<float*>(w + L.w2t));
+        mlp->W1, mlp->W2, K1, nullptr, nullptr, reinterpret_cast<float*>(w + L.w1t), reinterpret_cast<float*>(w + L.w2t),
+        false);
   }
   const void* W1T = w + L.w1t;
   const void* W2T = w + L.w2t;
@@ -1152,7 +1165,22 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     }
     reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s>>>(
         RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
-    if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
+    if (fuse_dsdq) {
+      gemm::TnArgs e{};
+      e.epi = gemm::kEpiDsDq;
+      e.nvalid = soff + B;
+      e.samp = samp;
+      e.S = S;
+      e.dS = dS;
+      e.dqc = dX;  // (the dq terms, [Pc][Q], in dx's buffer)
+      e.pooled = pooled_dev;
+      e.pooled_ld = F * D;
+      e.dim = D;
+      for (int k = 0; k < 3; ++k) e.qoff[k] = q_feat[k] * D;
+      if (!mm(dH1, kN1, W1T, kN1, nullptr, K1, Pc, K1, kN1, 1, &e)) return DSF_ECUDA;
+    } else {
+      if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
+    }
     // the weight gradients sum over positions (fp32: on transposed copies)
     if (bf) {
       // both products in one launch, kSplitCtas / 3 K-splits each (about
@@ -1202,7 +1230,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     unsigned long long* okey = reinterpret_cast<unsigned long long*>(w + L.okey);
     long long* osrc = reinterpret_cast<long long*>(w + L.osrc);
     dsdq_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS, gbag,
-                                                   okey, osrc);
+                                                   okey, osrc, fuse_dsdq && Pc > 0 ? dX : nullptr);
     const long long nocc = kjt->n_values + 3 * Pc;
     if (nocc > 0)
       rowgrad_kernel<<<int((nocc + kTile - 1) / kTile), kRowThreads, 0, s>>>(p, boff, soff, Pc, okey, osrc, gbag, dS);

@@ -40,8 +40,6 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // Staging offsets (bytes) of 16-byte slot k of row r in a warp's block:
 // fp32 rows of 64 bytes (4 slots), bf16 rows of 32 bytes (2 slots, 32 bytes
@@ -79,12 +77,25 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
   __nv_bfloat16* H = static_cast<__nv_bfloat16*>(a.H);
   uint16_t* HT = static_cast<uint16_t*>(a.HT);
   uint16_t* mrow = a.mask ? reinterpret_cast<uint16_t*>(a.mask + (live ? row : 0) * a.ldm) : nullptr;
+  long long ds_rows = 0;  // kEpiDsDq: rows below this are valid
+  if (a.epi == kEpiDsDq) {
+    const long long nv = __ldg(a.nvalid);
+    ds_rows = nv < a.M ? nv : a.M;
+  }
 #pragma unroll
   for (int ch = grp; ch < NCH; ch += 4) {
     const int c0 = n0 + ch * 16;
     if (c0 >= a.N || !work) break;
     const uint32_t mbits =
         mpre >= 0 ? uint32_t(mpre) : ((a.epi == kEpiMask && live) ? uint32_t(mrow[c0 >> 4]) : 0u);  // (before the wait below)
+    // kEpiDsDq: the row's sample, s and ds for dims c0 / 4 .. + 3 (before the wait below)
+    int ds_samp = 0;
+    float4 ds_s = make_float4(0.f, 0.f, 0.f, 0.f), ds_d = ds_s;
+    if (a.epi == kEpiDsDq && row < ds_rows) {
+      ds_samp = __ldg(a.samp + row);
+      ds_s = __ldg(reinterpret_cast<const float4*>(a.S + row * (a.N / 4) + (c0 >> 2)));
+      ds_d = *reinterpret_cast<const float4*>(a.dS + row * (a.N / 4) + (c0 >> 2));
+    }
     float v[16];
     if (have_acc) {
       tmem_ld16(tcol + (uint32_t(q * 32) << 16) + uint32_t(ch * 16), v);
@@ -108,6 +119,27 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
       __syncwarp();
     }
     if (a.epi == kEpiF32) continue;
+    if (a.epi == kEpiDsDq) {
+      // columns c0 .. c0 + 15: dims d0 .. d0 + 3, four columns each
+      const int d0 = c0 >> 2;
+      if (row < ds_rows) {
+        const int part = d0 / a.dim, e = d0 - part * a.dim;
+        const float4 q4 = __ldg(reinterpret_cast<const float4*>(a.pooled + (long long)ds_samp * a.pooled_ld +
+                                                                a.qoff[part] + e));
+        const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, sv[4] = {ds_s.x, ds_s.y, ds_s.z, ds_s.w};
+        const float dv[4] = {ds_d.x, ds_d.y, ds_d.z, ds_d.w};
+        float o[4], g[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float xq = v[4 * t], xs = v[4 * t + 1], xd = v[4 * t + 2], xp = v[4 * t + 3];
+          o[t] = dv[t] + xs - xd + xp * qv[t];
+          g[t] = xq + xd + xp * sv[t];
+        }
+        *reinterpret_cast<float4*>(a.dS + row * (a.N / 4) + d0) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(a.dqc + row * (a.N / 4) + d0) = make_float4(g[0], g[1], g[2], g[3]);
+      }
+      continue;
+    }
     if (a.epi == kEpiReluBias) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -200,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_bf16_kernel(const TnArgs a) {
   __shared__ uint64_t bar[kStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const long long m0 = (long long)blockIdx.x * kBM;
   const long long k0 = (long long)blockIdx.y * a.k_per_split;
   const long long k1 = k0 + a.k_per_split < a.K ? k0 + a.k_per_split : a.K;
@@ -904,7 +936,14 @@ bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
     tn_f32_kernel<<<dim3(unsigned(mt), unsigned(splits), unsigned(nt)), 256, 0, s>>>(a0, 0);
     return cudaGetLastError() == cudaSuccess;
   }
-  if (a0.epi != kEpiF32 &&
+  if (a0.epi == kEpiDsDq &&
+      (a0.N > 256 || a0.N % 16 != 0 || !a0.nvalid || !a0.samp || !a0.S || !a0.dS || !a0.dqc || !a0.pooled ||
+       a0.dim % 4 != 0 || a0.dim <= 0 || a0.N != 12 * a0.dim || a0.pooled_ld % 4 != 0 ||
+       (reinterpret_cast<uintptr_t>(a0.S) & 15) || (reinterpret_cast<uintptr_t>(a0.dS) & 15) ||
+       (reinterpret_cast<uintptr_t>(a0.dqc) & 15) || (reinterpret_cast<uintptr_t>(a0.pooled) & 15) ||
+       a0.qoff[0] % 4 || a0.qoff[1] % 4 || a0.qoff[2] % 4))
+    return false;
+  if ((a0.epi == kEpiReluBias || a0.epi == kEpiMask) &&
       (a0.N > 256 || a0.N % 32 != 0 || !a0.H || a0.ldh % 8 || (reinterpret_cast<uintptr_t>(a0.H) & 15) ||
        (a0.HT && (a0.ldt % 8 || a0.ldt < (a0.M + 7) / 8 * 8 || (reinterpret_cast<uintptr_t>(a0.HT) & 15))) ||
        (a0.epi == kEpiMask && !a0.mask) || (a0.mask && a0.ldm < a0.N / 32) ||

@@ -37,6 +37,12 @@ enum Epi {
                      // H = bf16(v) and HT; part[4 tile + j][n] = the column
                      // sums of v over rows 32 j .. 32 j + 31 of 128-row tile
                      // `tile`
+  kEpiDsDq = 3,      // the dx product of the DIN backward, B's rows permuted
+                     // so that columns 4d .. 4d + 3 are (dx_q, dx_s, dx_d,
+                     // dx_p) of dim d: for rows m < *nvalid, ds[m][d] +=
+                     // dx_s - dx_d + dx_p q and dqc[m][d] = dx_q + dx_d +
+                     // dx_p s[m][d] (q: the pooled query slice of row m's
+                     // sample); D is not written
 };
 
 struct TnArgs {
@@ -65,6 +71,15 @@ struct TnArgs {
                       // (entries M .. that bound of each row are overwritten)
   long long ldt;
   float* part;        // kEpiMask: [4 x M tiles][N]
+  // kEpiDsDq (N = 4 Q): Q = 3 x dim
+  const long long* nvalid;  // valid rows (device)
+  const int* samp;          // [M] row -> sample
+  const float* S;           // [M][Q] s
+  float* dS;                // [M][Q] ds, updated in place
+  float* dqc;               // [M][Q] out: the row's dq term
+  const float* pooled;      // [B][pooled_ld]
+  int pooled_ld, dim;
+  int qoff[3];              // pooled column of the query slice of part k of s
 };
 
 // Launches D = A B^T over `splits` K-splits on `stream`. bf16 selects the
