@@ -318,9 +318,10 @@ int ctr_towers_fwd(const float* pooled_dev, const float* din_dev, int32_t B, con
  *   - every touched row's summed gradient, accumulated into dsf_row_grads.
  * The MLP runs as in the forward's mode (mlp->mode): bf16 GEMM operands with
  * fp32 accumulation, or fp32 throughout. Its six matrix products are this
- * library's GEMMs (tcgen05 tensor cores for bf16 operands, CUDA cores in the
- * fp32 mode) over the sequence values' length (rows past the valid count are
- * zero); the rest are this library's kernels. Row gradients are summed with
+ * library's GEMMs (tcgen05 tensor cores fed by TMA for bf16 operands, CUDA
+ * cores in the fp32 mode) over the sequence values' length (rows past the
+ * valid count are zero), with the ReLU, the mask and (at D = 16) ds fused
+ * into their epilogues; the rest are this library's kernels. Row gradients are summed with
  * fp32 atomics, so their rounding order varies between runs. Gradients of
  * unseen hash keys and of invalid ids are dropped. emb_adagrad_update then
  * applies AdaGrad to the touched rows and leaves the row-gradient state zero
@@ -370,9 +371,11 @@ size_t dsf_bwd_workspace_bytes(int32_t B, int64_t n_values, int64_t n_per_key, i
 int dsf_bwd_workspace_offsets(int32_t B, int64_t n_values, int64_t n_per_key, int32_t D, int64_t* offsets);
 
 /* Returns DSF_EINVAL / DSF_EUNSUPPORTED / DSF_EWORKSPACE for bad arguments
- * (as din_sparse_fwd), DSF_ECUDA when a launch or a library call fails.
+ * (as din_sparse_fwd), DSF_ECUDA when a launch or a CUDA call fails (the
+ * products' TMA tensor maps are encoded through the driver at each call).
  * Device data errors set bits in *status_dev (nullable). Asynchronous on
- * stream; the GEMMs run on the same stream with this workspace as theirs. */
+ * stream: every kernel, the matrix products included, runs on that stream
+ * in this workspace. */
 int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
                    const int32_t* q_feat, const int32_t* seq_table, int32_t B, const dsf_mlp* mlp,
                    const float* pooled_dev, const float* dpooled_dev, const float* ddin_dev,

@@ -915,13 +915,6 @@ bool launch_atb(const TnArgs& a0, int s0, const TnArgs* a1, int s1, cudaStream_t
 
 }  // namespace
 
-size_t tn_bf16_smem_bytes(int N) {
-  if (N <= 64) return Tile<64>::SMEM;
-  if (N <= 128) return Tile<128>::SMEM;
-  if (N <= 192) return Tile<192>::SMEM;
-  return Tile<256>::SMEM;
-}
-
 bool tn(const TnArgs& a0, int splits, bool bf16, cudaStream_t s) {
   if (a0.M <= 0 || a0.N <= 0 || a0.K < 0 || splits < 1) return a0.M <= 0 || a0.N <= 0;
   if (a0.k_per_split <= 0 || a0.k_per_split % kBK != 0) return false;

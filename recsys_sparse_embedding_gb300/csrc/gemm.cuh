@@ -116,8 +116,6 @@ bool reduce2(const float* P0, long long split_stride0, int splits0, long long ld
 bool transpose(const void* in, long long ld_in, long long rows, int cols, void* out, long long ld_out, int esize,
                cudaStream_t stream);
 
-// Dynamic shared memory of the tcgen05 kernel for an N-wide tile.
-size_t tn_bf16_smem_bytes(int N);
 
 }  // namespace gemm
 }  // namespace dsf
