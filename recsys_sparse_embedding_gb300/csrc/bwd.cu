@@ -27,11 +27,13 @@
 
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "abi_checks.cuh"
 #include "dinsparse.h"
 #include "gemm.cuh"
 #include "hash.cuh"
+#include "launch.cuh"
 
 namespace dsf {
 namespace bwd {
@@ -48,6 +50,32 @@ constexpr unsigned long long kNoKey = ~0ull;
 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// A second stream per device for the backward's steps that no next step
+// needs (the KJT offsets, the weight packing, the bias-gradient columns).
+// Work moves to it and back through events, so a graph capture of the call
+// records the fork and the join. Null if it cannot be had: every step then
+// runs on the call's stream.
+cudaStream_t side_stream(int dev) {
+  static std::mutex mu;
+  static cudaStream_t cache[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev] && cudaStreamCreateWithFlags(&cache[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    cache[dev] = nullptr;
+    (void)cudaGetLastError();
+  }
+  return cache[dev];
+}
+// `to` waits for everything enqueued on `from` so far.
+bool follow(cudaStream_t to, cudaStream_t from) {
+  if (to == from) return true;
+  cudaEvent_t e;
+  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+  const bool ok = cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
+  cudaEventDestroy(e);  // (released once the record completes)
+  return ok;
+}
 
 struct Layout {
   size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, gbag, okey, osrc, w1b, w2b, w1t, w2t, X, S, G1, H1, H2, dH2,
@@ -1028,25 +1056,34 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   long long* tsum = reinterpret_cast<long long*>(w + L.tsum);
   float* part1 = reinterpret_cast<float*>(w + L.part1);
   float* part2 = reinterpret_cast<float*>(w + L.part2);
-  {  // bag offsets of the KJT; raw and clamped sequence offsets
+  // the side stream (s2) takes the KJT offsets and the weight packing; the
+  // call's stream joins it before the first product
+  int dev = 0;
+  cudaStream_t s2 = cudaGetDevice(&dev) == cudaSuccess ? side_stream(dev) : nullptr;
+  if (!s2 || !follow(s2, s)) s2 = s;
+  {  // bag offsets of the KJT (s2); raw and clamped sequence offsets (s)
     const int nk = F * B, tk = (nk + kScanTile - 1) / kScanTile, ts = (B + kScanTile - 1) / kScanTile;
-    ScanJobs jobs;
-    jobs.j[0] = ScanJob{kjt->lengths_dev, nk, INT_MAX, tk, tsum, boff, nullptr};
-    jobs.j[1] = ScanJob{seq->lengths_dev, B, seq->max_len, ts, tsum + 2 * (tk + 1), roff, soff};
-    scan_tiles_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
-    scan_apply_kernel<<<tk + ts, kScanThreads, 0, s>>>(jobs);
+    ScanJobs kj{}, sj{};
+    kj.j[0] = ScanJob{kjt->lengths_dev, nk, INT_MAX, tk, tsum, boff, nullptr};
+    sj.j[0] = ScanJob{seq->lengths_dev, B, seq->max_len, ts, tsum + 2 * (tk + 1), roff, soff};
+    if (tk > 0) {
+      scan_tiles_kernel<<<tk, kScanThreads, 0, s2>>>(kj);
+      scan_apply_kernel<<<tk, kScanThreads, 0, s2>>>(kj);
+    }
+    scan_tiles_kernel<<<ts, kScanThreads, 0, s>>>(sj);
+    scan_apply_kernel<<<ts, kScanThreads, 0, s>>>(sj);
   }
   // bf16 with x at most 256 wide (D = 16): ds and the dq terms in the dx
   // product's epilogue (dx itself is not written)
   const bool fuse_dsdq = bf && K1 <= 256;
   if (bf) {
-    pack_kernel<__nv_bfloat16><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
+    pack_kernel<__nv_bfloat16><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s2>>>(
         mlp->W1, mlp->W2, K1, reinterpret_cast<__nv_bfloat16*>(w + L.w1b), reinterpret_cast<__nv_bfloat16*>(w + L.w2b),
         reinterpret_cast<__nv_bfloat16*>(w + L.w1t), reinterpret_cast<__nv_bfloat16*>(w + L.w2t), fuse_dsdq);
     W1 = w + L.w1b;
     W2 = w + L.w2b;
   } else {
-    pack_kernel<float><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s>>>(
+    pack_kernel<float><<<grid_for(kN1 * K1 + kN2 * kN1, 256), 256, 0, s2>>>(
         mlp->W1, mlp->W2, K1, nullptr, nullptr, reinterpret_cast<float*>(w + L.w1t), reinterpret_cast<float*>(w + L.w2t),
         false);
   }
@@ -1116,6 +1153,9 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       gather_kernel<float><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
                                                               S, Pc);
     if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
+  }
+  if (!follow(s, s2)) return DSF_ECUDA;  // (the packed weights and the KJT offsets)
+  if (Pc > 0) {
     // recompute: h1 = ReLU(x W1^T + b1) (in bf16 mode inside the product's
     // epilogue, which also records h1 > 0 as bits), then the layer-2
     // pre-activation
@@ -1163,7 +1203,9 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
                                                  Pc);
     }
-    reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s>>>(
+    // the bias-gradient columns beside the remaining products (s2)
+    if (!follow(s2, s)) return DSF_ECUDA;
+    reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s2>>>(
         RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
     if (fuse_dsdq) {
       gemm::TnArgs e{};
@@ -1235,7 +1277,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     if (nocc > 0)
       rowgrad_kernel<<<int((nocc + kTile - 1) / kTile), kRowThreads, 0, s>>>(p, boff, soff, Pc, okey, osrc, gbag, dS);
   }
-  return cudaGetLastError() == cudaSuccess ? DSF_OK : DSF_ECUDA;
+  if (cudaGetLastError() != cudaSuccess || !follow(s, s2)) return DSF_ECUDA;
+  return DSF_OK;
 }
 
 extern "C" int emb_adagrad_update(const dsf_tables* tables, float* const* accum, const dsf_row_grads* rg, float lr,
