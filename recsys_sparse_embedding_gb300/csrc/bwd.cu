@@ -1245,9 +1245,10 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
         g->split_stride = g->M * g->N;
         g->status = status_dev;
       }
-      if (!gemm::atb2(g0, splits, g1, splits, s) ||
+      // (the reduction beside dq/ds and the row gradients, on s2)
+      if (!gemm::atb2(g0, splits, g1, splits, s) || !follow(s2, s) ||
           !gemm::reduce2(part0, g0.split_stride, splits, K1, mg->dW1, K1, kN1, K1, part1, g1.split_stride, splits, kN1,
-                         mg->dW2, kN1, kN2, kN1, s))
+                         mg->dW2, kN1, kN2, kN1, s2))
         return DSF_ECUDA;
     } else {
       void* XT = w + L.XT;
