@@ -1203,27 +1203,12 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
       relu1_bwd_kernel<float><<<rb, kN1, 0, s>>>(G1, static_cast<const float*>(H1), static_cast<float*>(dH1), part2,
                                                  Pc);
     }
-    // the bias-gradient columns beside the remaining products (s2)
+    // the bias-gradient columns beside the remaining steps (s2)
     if (!follow(s2, s)) return DSF_ECUDA;
     reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s2>>>(
         RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
-    if (fuse_dsdq) {
-      gemm::TnArgs e{};
-      e.epi = gemm::kEpiDsDq;
-      e.nvalid = soff + B;
-      e.samp = samp;
-      e.S = S;
-      e.dS = dS;
-      e.dqc = dX;  // (the dq terms, [Pc][Q], in dx's buffer)
-      e.pooled = pooled_dev;
-      e.pooled_ld = F * D;
-      e.dim = D;
-      for (int k = 0; k < 3; ++k) e.qoff[k] = q_feat[k] * D;
-      if (!mm(dH1, kN1, W1T, kN1, nullptr, K1, Pc, K1, kN1, 1, &e)) return DSF_ECUDA;
-    } else {
-      if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
-    }
-    // the weight gradients sum over positions (fp32: on transposed copies)
+    // bf16: the weight gradients (their operands are all written by now) on
+    // s2 as well, beside dx, dq/ds and the row gradients
     if (bf) {
       // both products in one launch, kSplitCtas / 3 K-splits each (about
       // kSplitCtas CTAs with equal K-blocks: dW1 has two row tiles, dW2 one),
@@ -1245,12 +1230,29 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
         g->split_stride = g->M * g->N;
         g->status = status_dev;
       }
-      // (the reduction beside dq/ds and the row gradients, on s2)
-      if (!gemm::atb2(g0, splits, g1, splits, s) || !follow(s2, s) ||
+      if (!gemm::atb2(g0, splits, g1, splits, s2) ||
           !gemm::reduce2(part0, g0.split_stride, splits, K1, mg->dW1, K1, kN1, K1, part1, g1.split_stride, splits, kN1,
                          mg->dW2, kN1, kN2, kN1, s2))
         return DSF_ECUDA;
+    }
+    if (fuse_dsdq) {
+      gemm::TnArgs e{};
+      e.epi = gemm::kEpiDsDq;
+      e.nvalid = soff + B;
+      e.samp = samp;
+      e.S = S;
+      e.dS = dS;
+      e.dqc = dX;  // (the dq terms, [Pc][Q], in dx's buffer)
+      e.pooled = pooled_dev;
+      e.pooled_ld = F * D;
+      e.dim = D;
+      for (int k = 0; k < 3; ++k) e.qoff[k] = q_feat[k] * D;
+      if (!mm(dH1, kN1, W1T, kN1, nullptr, K1, Pc, K1, kN1, 1, &e)) return DSF_ECUDA;
     } else {
+      if (!mm(dH1, kN1, W1T, kN1, dX, K1, Pc, K1, kN1, 1)) return DSF_ECUDA;
+    }
+    // the weight gradients (fp32: on transposed copies; bf16: on s2, above)
+    if (!bf) {
       void* XT = w + L.XT;
       void* H1T = w + L.H1T;
       void* dH2T = w + L.dH2T;
