@@ -377,6 +377,24 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
   u.y = *reinterpret_cast<const uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(dst) = u;
 }
+// 8 consecutive elements (16-byte aligned for bf16: one 16-byte store)
+template <class T>
+__device__ __forceinline__ void store8(T* dst, const float* v);
+template <>
+__device__ __forceinline__ void store8<float>(float* dst, const float* v) {
+  *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    u[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(dst) = make_uint4(u[0], u[1], u[2], u[3]);
+}
 
 // One warp per sample, one lane per position: its sample, s (fp32) and
 // x = [q, s, q - s, q * s] (the MLP operand type). Rows past the valid count
@@ -426,12 +444,18 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
         for (int h = 0; h < 4; ++h) {
           const int i = 4 * h;
           *reinterpret_cast<float4*>(sd + i) = make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
-          store4<T>(x + c * 16 + i, q[i], q[i + 1], q[i + 2], q[i + 3]);
-          store4<T>(x + Q + c * 16 + i, sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
-          store4<T>(x + 2 * Q + c * 16 + i, q[i] - sv[i], q[i + 1] - sv[i + 1], q[i + 2] - sv[i + 2],
-                    q[i + 3] - sv[i + 3]);
-          store4<T>(x + 3 * Q + c * 16 + i, q[i] * sv[i], q[i + 1] * sv[i + 1], q[i + 2] * sv[i + 2],
-                    q[i + 3] * sv[i + 3]);
+        }
+        // x's four parts, eight elements per store
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 8 * h;
+          float dq[8], pq[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) dq[t] = q[i + t] - sv[i + t], pq[t] = q[i + t] * sv[i + t];
+          store8<T>(x + c * 16 + i, q + i);
+          store8<T>(x + Q + c * 16 + i, sv + i);
+          store8<T>(x + 2 * Q + c * 16 + i, dq);
+          store8<T>(x + 3 * Q + c * 16 + i, pq);
         }
       }
     }
