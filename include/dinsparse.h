@@ -374,8 +374,12 @@ int dsf_bwd_workspace_offsets(int32_t B, int64_t n_values, int64_t n_per_key, in
  * (as din_sparse_fwd), DSF_ECUDA when a launch or a CUDA call fails (the
  * products' TMA tensor maps are encoded through the driver at each call).
  * Device data errors set bits in *status_dev (nullable). Asynchronous on
- * stream: every kernel, the matrix products included, runs on that stream
- * in this workspace. */
+ * stream, in this workspace: steps that no next step needs run on a second
+ * stream of the library's (one per device, made by the first call that is
+ * not being captured into a CUDA graph), forked from and joined back to
+ * `stream` by events before the call returns; a captured call records that
+ * fork and join, or, with no second stream yet, runs every step on
+ * `stream`. */
 int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, const dsf_seq* seq,
                    const int32_t* q_feat, const int32_t* seq_table, int32_t B, const dsf_mlp* mlp,
                    const float* pooled_dev, const float* dpooled_dev, const float* ddin_dev,

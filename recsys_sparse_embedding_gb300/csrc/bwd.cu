@@ -54,14 +54,15 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // A second stream per device for the backward's steps that no next step
 // needs (the KJT offsets, the weight packing, the bias-gradient columns).
 // Work moves to it and back through events, so a graph capture of the call
-// records the fork and the join. Null if it cannot be had: every step then
-// runs on the call's stream.
-cudaStream_t side_stream(int dev) {
+// records the fork and the join. It is created by the first call that is not
+// being captured (create false: only an existing one is returned). Null if
+// it cannot be had: every step then runs on the call's stream.
+cudaStream_t side_stream(int dev, bool create) {
   static std::mutex mu;
   static cudaStream_t cache[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev] && cudaStreamCreateWithFlags(&cache[dev], cudaStreamNonBlocking) != cudaSuccess) {
+  if (!cache[dev] && create && cudaStreamCreateWithFlags(&cache[dev], cudaStreamNonBlocking) != cudaSuccess) {
     cache[dev] = nullptr;
     (void)cudaGetLastError();
   }
@@ -1083,7 +1084,10 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   // the side stream (s2) takes the KJT offsets and the weight packing; the
   // call's stream joins it before the first product
   int dev = 0;
-  cudaStream_t s2 = cudaGetDevice(&dev) == cudaSuccess ? side_stream(dev) : nullptr;
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &capturing) != cudaSuccess) return DSF_ECUDA;
+  cudaStream_t s2 =
+      cudaGetDevice(&dev) == cudaSuccess ? side_stream(dev, capturing == cudaStreamCaptureStatusNone) : nullptr;
   if (!s2 || !follow(s2, s)) s2 = s;
   {  // bag offsets of the KJT (s2); raw and clamped sequence offsets (s)
     const int nk = F * B, tk = (nk + kScanTile - 1) / kScanTile, ts = (B + kScanTile - 1) / kScanTile;
