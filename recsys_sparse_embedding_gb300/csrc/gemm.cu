@@ -64,10 +64,11 @@ __device__ __forceinline__ int stg16(int r, int k) { return r * 32 + (r >> 3) * 
 // bias: kEpiReluBias's bias (global or shared). mpre >= 0: the chunk's mask
 // bits, loaded by the caller (kEpiMask, one chunk per warp). work false:
 // nothing (a run that gave up).
-template <int BN, int W>
+template <int BN, int W, int EPI = -1>
 __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t tcol, long long m0, int n0,
                                          long long tile, float* D, bool have_acc, const float* bias = nullptr,
                                          long long mpre = -1, bool work = true) {
+  const int epi = EPI >= 0 ? EPI : a.epi;  // (compile-time where the caller knows it)
   constexpr int NCH = W / 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = warp & 3, grp = warp >> 2;
@@ -78,7 +79,7 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
   uint16_t* HT = static_cast<uint16_t*>(a.HT);
   uint16_t* mrow = a.mask ? reinterpret_cast<uint16_t*>(a.mask + (live ? row : 0) * a.ldm) : nullptr;
   long long ds_rows = 0;  // kEpiDsDq: rows below this are valid
-  if (a.epi == kEpiDsDq) {
+  if (epi == kEpiDsDq) {
     const long long nv = __ldg(a.nvalid);
     ds_rows = nv < a.M ? nv : a.M;
   }
@@ -87,11 +88,11 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
     const int c0 = n0 + ch * 16;
     if (c0 >= a.N || !work) break;
     const uint32_t mbits =
-        mpre >= 0 ? uint32_t(mpre) : ((a.epi == kEpiMask && live) ? uint32_t(mrow[c0 >> 4]) : 0u);  // (before the wait below)
+        mpre >= 0 ? uint32_t(mpre) : ((epi == kEpiMask && live) ? uint32_t(mrow[c0 >> 4]) : 0u);  // (before the wait below)
     // kEpiDsDq: the row's sample, s and ds for dims c0 / 4 .. + 3 (before the wait below)
     int ds_samp = 0;
     float4 ds_s = make_float4(0.f, 0.f, 0.f, 0.f), ds_d = ds_s;
-    if (a.epi == kEpiDsDq && row < ds_rows) {
+    if (epi == kEpiDsDq && row < ds_rows) {
       ds_samp = __ldg(a.samp + row);
       ds_s = __ldg(reinterpret_cast<const float4*>(a.S + row * (a.N / 4) + (c0 >> 2)));
       ds_d = *reinterpret_cast<const float4*>(a.dS + row * (a.N / 4) + (c0 >> 2));
@@ -118,8 +119,8 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
       }
       __syncwarp();
     }
-    if (a.epi == kEpiF32) continue;
-    if (a.epi == kEpiDsDq) {
+    if (epi == kEpiF32) continue;
+    if (epi == kEpiDsDq) {
       // columns c0 .. c0 + 15: dims d0 .. d0 + 3, four columns each
       const int d0 = c0 >> 2;
       if (row < ds_rows) {
@@ -140,7 +141,7 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
       }
       continue;
     }
-    if (a.epi == kEpiReluBias) {
+    if (epi == kEpiReluBias) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float4 b = reinterpret_cast<const float4*>((bias ? bias : a.bias) + c0)[k];
@@ -157,7 +158,7 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
     uint32_t p[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) p[t] = bf16x2(v[2 * t], v[2 * t + 1]);
-    if (a.epi == kEpiReluBias && mrow && live) {
+    if (epi == kEpiReluBias && mrow && live) {
       // bit j: bf16 value j is > 0 (ReLU outputs are >= 0 or -0); a half h
       // of x = p & 0x7fff7fff is nonzero iff h + 0x7fff carries into its
       // top bit
@@ -199,7 +200,7 @@ __device__ __forceinline__ void epilogue(const TnArgs& a, uint8_t* E, uint32_t t
       }
     }
     __syncwarp();
-    if (a.epi == kEpiMask && a.part) {
+    if (epi == kEpiMask && a.part) {
       // the masked fp32 block; lane l adds column l % 16 down rows
       // 16 (l / 16) .. + 15 (the upper lanes rotated by one row: another
       // bank group), then the lower lane adds the upper lane's sum and
@@ -351,7 +352,7 @@ struct RTile {
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int BN, int KB>
+template <int BN, int KB, int EPI>
 __global__ void __launch_bounds__(kThreads + 32, 1)
     tn_bf16_resident_kernel(const TnArgs a, const __grid_constant__ CUtensorMap mapA,
                             const __grid_constant__ CUtensorMap mapB) {
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     tmem_alloc(&tmem_slot, T::TCOLS);
     tmem_relinquish();
   }
-  if (a.epi == kEpiReluBias)
+  if (EPI == kEpiReluBias)
     for (int c = tid; c < BN; c += blockDim.x) sBias[c] = c < a.N ? a.bias[c] : 0.f;
   tc_fence_before();
   __syncthreads();
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int q = warp & 3, grp = warp >> 2;
     // the mask bits of this warp's chunk in unit u (kEpiMask), loaded a unit ahead
     auto mask_of = [&](long long u) -> long long {
-      if (a.epi != kEpiMask || u >= u1) return 0;
+      if (EPI != kEpiMask || u >= u1) return 0;
       const long long row = (u / NU) * kBM + q * 32 + lane;
       const int c0 = int(u % NU) * UN + grp * 16;
       return (row < a.M && c0 < a.N) ? (long long)reinterpret_cast<const uint16_t*>(a.mask + row * a.ldm)[c0 >> 4]
@@ -472,8 +473,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       tc_fence_after();
       const long long mcur = mnext;
       mnext = mask_of(u + 1);
-      epilogue<BN, UN>(a, sE, tbase + uint32_t(b) * UN, (u / NU) * kBM, int(u % NU) * UN, u / NU, a.D, true, sBias,
-                       a.epi == kEpiMask ? mcur : -1, ok);
+      epilogue<BN, UN, EPI>(a, sE, tbase + uint32_t(b) * UN, (u / NU) * kBM, int(u % NU) * UN, u / NU, a.D, true, sBias,
+                       EPI == kEpiMask ? mcur : -1, ok);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[b]);
@@ -861,15 +862,15 @@ bool tensor_map(CUtensorMap* m, const void* base, long long rows, long long cols
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int KB>
-int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
+template <int BN, int KB, int EPI>
+int launch_resident_e(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
   using T = RTile<BN, KB>;
   static bool attr_set[64] = {};
   static int nsm[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(tn_bf16_resident_kernel<BN, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
+    if (cudaFuncSetAttribute(tn_bf16_resident_kernel<BN, KB, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
             cudaSuccess ||
         cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return 0;
@@ -880,8 +881,19 @@ int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
   if (g <= 0) return 1;
   CUtensorMap mapA, mapB;
   if (!tensor_map(&mapA, a.A, a.M, a.K, a.lda, kBM) || !tensor_map(&mapB, a.B, a.N, a.K, a.ldb, BN)) return 0;
-  tn_bf16_resident_kernel<BN, KB><<<unsigned(g), kThreads + 32, T::SMEM, s>>>(a, mapA, mapB);
+  tn_bf16_resident_kernel<BN, KB, EPI><<<unsigned(g), kThreads + 32, T::SMEM, s>>>(a, mapA, mapB);
   return cudaGetLastError() == cudaSuccess ? 1 : 0;
+}
+
+template <int BN, int KB>
+int launch_resident(const TnArgs& a, cudaStream_t s) {  // 1 ok, 0 failed
+  switch (a.epi) {
+    case kEpiF32: return launch_resident_e<BN, KB, kEpiF32>(a, s);
+    case kEpiReluBias: return launch_resident_e<BN, KB, kEpiReluBias>(a, s);
+    case kEpiMask: return launch_resident_e<BN, KB, kEpiMask>(a, s);
+    case kEpiDsDq: return launch_resident_e<BN, KB, kEpiDsDq>(a, s);
+    default: return 0;
+  }
 }
 
 // Job 1 (a1 non-null) runs in the same launch as job 0.
