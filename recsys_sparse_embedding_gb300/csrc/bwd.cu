@@ -397,13 +397,14 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const 
   *reinterpret_cast<uint4*>(dst) = make_uint4(u[0], u[1], u[2], u[3]);
 }
 
-// One warp per sample, one lane per position: its sample, s (fp32) and
-// x = [q, s, q - s, q * s] (the MLP operand type). Rows past the valid count
-// are zeroed.
+// One warp per sample, one lane per position: its sample, s (fp32), x =
+// [q, s, q - s, q * s] (the MLP operand type) and the occurrence keys of its
+// three sequence ids. Rows past the valid count are zeroed.
 template <class T>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
     const Params p, const float* __restrict__ pooled, const long long* __restrict__ soff,
-    const long long* __restrict__ roff, int* samp, T* X, float* S, long long Pc) {
+    const long long* __restrict__ roff, int* samp, T* X, float* S, long long Pc, unsigned long long* __restrict__ okey,
+    long long* __restrict__ osrc) {
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D;
   const int lane = threadIdx.x & 31;
   const long long P = min(soff[p.B], Pc);
@@ -426,6 +427,13 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
         ok[k] = id >= 0 && id < p.rows[tb];
         if (!ok[k] && j < p.n_seq) flags |= DSF_FLAG_ID_RANGE;
         row[k] = ok[k] ? id : 0;
+        // the occurrence of this sequence id (its gradient is row 3 pos + k
+        // of ds): storage << 40 | row, or none
+        const long long o = p.n_values + 3 * pos + k;
+        okey[o] = (id >= 0 && id < p.glimit[tb])
+                      ? (static_cast<unsigned long long>(p.sid[tb]) << kRowBits) | static_cast<unsigned long long>(id)
+                      : kNoKey;
+        osrc[o] = -(3 * pos + k) - 1;
       }
       for (int c = 0; c < Q / 16; ++c) {
         const int k = (c * 16) / D, e = (c * 16) % D;
@@ -649,19 +657,17 @@ __device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4
 
 // One warp per sample, no atomics. Positions, a lane each: the final ds =
 // dS + dx_s - dx_d + dx_p q (in place) and the lane's share of dq = sum_t
-// (dx_q + dx_d + dx_p s_t), reduced over the lanes afterwards; the position's
-// three sequence ids become occurrences (storage << 40 | row, and where their
-// gradient is). Then the bags, one (feature, 4-element piece) per lane step:
-// g = dpooled + dq (over L for mean pooling) into the bag-gradient rows, and
-// every value of the bag becomes an occurrence. Pieces of x are handled kPG
-// at a time so the dq shares stay in registers.
+// (dx_q + dx_d + dx_p s_t), reduced over the lanes afterwards. Then the bags,
+// one (feature, 4-element piece) per lane step: g = dpooled + dq (over L for
+// mean pooling) into the bag-gradient rows. Pieces of x are handled kPG at a
+// time so the dq shares stay in registers. (The occurrence keys come from the
+// gather and from kjt_keys_kernel.)
 constexpr int kPG = 4;
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
     const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
     const long long* __restrict__ roff, long long Pc, const float* __restrict__ pooled,
     const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S,
-    float* __restrict__ dS, float* __restrict__ gbag, unsigned long long* __restrict__ okey,
-    long long* __restrict__ osrc, const float* __restrict__ dqc) {
+    float* __restrict__ dS, float* __restrict__ gbag, const float* __restrict__ dqc) {
   __shared__ float dqs[kWarpsPerBlock][3 * 64];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
@@ -674,19 +680,6 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
 #pragma unroll
       for (int i = 0; i < kPG; ++i) dq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (long long q = p0 + lane; q < p1; q += 32) {
-        const long long j = roff[b] + (q - soff[b]);
-        if (g0 == 0) {
-#pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            const int tb = p.seq_table[k];
-            const long long id = j < p.n_seq ? rid(p, tb, p.seq_values[k * p.n_seq + j]) : -1;
-            const long long o = p.n_values + 3 * q + k;
-            okey[o] = (id >= 0 && id < p.glimit[tb]) ? (static_cast<unsigned long long>(p.sid[tb]) << kRowBits) |
-                                                           static_cast<unsigned long long>(id)
-                                                     : kNoKey;
-            osrc[o] = -(3 * q + k) - 1;
-          }
-        }
         if (dqc) {  // (ds and the dq terms came from the dx product's epilogue)
 #pragma unroll
           for (int i = 0; i < kPG; ++i)
@@ -731,20 +724,35 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
       const long long v0 = boff[(long long)f * p.B + b], v1 = boff[(long long)f * p.B + b + 1];
       if (v1 > v0 && ((p.mean_mask >> f) & 1u)) g = scale4(g, 1.f / float(v1 - v0));
       *reinterpret_cast<float4*>(gbag + (long long)b * FD + f * D + e) = g;
-      if (e != 0) continue;
-      for (long long v = v0; v < v1; ++v) {
-        if (v >= p.n_values) {
-          flags |= DSF_FLAG_COUNT;
-          break;
-        }
-        const long long id = rid(p, f, p.values[v]);
-        okey[v] = (id >= 0 && id < p.glimit[f])
-                      ? (static_cast<unsigned long long>(p.sid[f]) << kRowBits) | static_cast<unsigned long long>(id)
-                      : kNoKey;
-        osrc[v] = (long long)b * p.F + f;
-      }
     }
     __syncwarp();
+  }
+  flag(p.status, flags);
+}
+
+// The occurrences of the KJT's values, one thread per bag: value v of bag
+// (f, b) gets the key storage << 40 | row (or none) and its gradient row
+// b F + f of the bag gradients.
+__global__ void __launch_bounds__(256) kjt_keys_kernel(const Params p, const long long* __restrict__ boff,
+                                                       unsigned long long* __restrict__ okey,
+                                                       long long* __restrict__ osrc) {
+  int flags = 0;
+  const long long nb = (long long)p.F * p.B;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < nb; g += (long long)gridDim.x * blockDim.x) {
+    const int f = int(g / p.B);
+    const long long b = g - (long long)f * p.B;
+    const long long v0 = boff[g], v1 = boff[g + 1];
+    for (long long v = v0; v < v1; ++v) {
+      if (v >= p.n_values) {
+        flags |= DSF_FLAG_COUNT;
+        break;
+      }
+      const long long id = rid(p, f, p.values[v]);
+      okey[v] = (id >= 0 && id < p.glimit[f])
+                    ? (static_cast<unsigned long long>(p.sid[f]) << kRowBits) | static_cast<unsigned long long>(id)
+                    : kNoKey;
+      osrc[v] = b * p.F + f;
+    }
   }
   flag(p.status, flags);
 }
@@ -1078,6 +1086,9 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   const void* W1 = mlp->W1;
   const void* W2 = mlp->W2;
 
+  float* gbag = reinterpret_cast<float*>(w + L.gbag);
+  unsigned long long* okey = reinterpret_cast<unsigned long long*>(w + L.okey);
+  long long* osrc = reinterpret_cast<long long*>(w + L.osrc);
   long long* tsum = reinterpret_cast<long long*>(w + L.tsum);
   float* part1 = reinterpret_cast<float*>(w + L.part1);
   float* part2 = reinterpret_cast<float*>(w + L.part2);
@@ -1097,6 +1108,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     if (tk > 0) {
       scan_tiles_kernel<<<tk, kScanThreads, 0, s2>>>(kj);
       scan_apply_kernel<<<tk, kScanThreads, 0, s2>>>(kj);
+      // the occurrence keys of the KJT's values (for the row gradients)
+      kjt_keys_kernel<<<grid_for(nk, 256, kMaxBlocks), 256, 0, s2>>>(p, boff, okey, osrc);
     }
     scan_tiles_kernel<<<ts, kScanThreads, 0, s>>>(sj);
     scan_apply_kernel<<<ts, kScanThreads, 0, s>>>(sj);
@@ -1176,13 +1189,13 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     const int gb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
     if (bf)
       gather_kernel<__nv_bfloat16><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp,
-                                                                      static_cast<__nv_bfloat16*>(X), S, Pc);
+                                                                      static_cast<__nv_bfloat16*>(X), S, Pc, okey, osrc);
     else
       gather_kernel<float><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
-                                                              S, Pc);
+                                                              S, Pc, okey, osrc);
     if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   }
-  if (!follow(s, s2)) return DSF_ECUDA;  // (the packed weights and the KJT offsets)
+  if (!follow(s, s2)) return DSF_ECUDA;  // (the packed weights, the KJT offsets and keys)
   if (Pc > 0) {
     // recompute: h1 = ReLU(x W1^T + b1) (in bf16 mode inside the product's
     // epilogue, which also records h1 > 0 as bits), then the layer-2
@@ -1299,11 +1312,8 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     reduce_cols_kernel<<<kRedCols, 256, 0, s>>>(RedJobs{part1, sb, nullptr, 0, mg->dw3, mg->db2, mg->db3, nullptr});
   }
   {
-    float* gbag = reinterpret_cast<float*>(w + L.gbag);
-    unsigned long long* okey = reinterpret_cast<unsigned long long*>(w + L.okey);
-    long long* osrc = reinterpret_cast<long long*>(w + L.osrc);
     dsdq_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS, gbag,
-                                                   okey, osrc, fuse_dsdq && Pc > 0 ? dX : nullptr);
+                                                   fuse_dsdq && Pc > 0 ? dX : nullptr);
     const long long nocc = kjt->n_values + 3 * Pc;
     if (nocc > 0)
       rowgrad_kernel<<<int((nocc + kTile - 1) / kTile), kRowThreads, 0, s>>>(p, boff, soff, Pc, okey, osrc, gbag, dS);
