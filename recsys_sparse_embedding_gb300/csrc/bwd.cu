@@ -41,10 +41,14 @@ namespace {
 
 constexpr int kSplitCtas = 152;  // CTAs of the two weight-gradient products (K-splits x M-tiles)
 constexpr int kRowBits = 40;
-constexpr int kWarpsPerBlock = 8;
+// The per-sample kernels (gather, softmax backward, dq/ds) take one warp per
+// block: a block whose sample holds a long sequence then keeps only its own
+// warp, and the freed warp slots take new blocks at once.
+constexpr int kSampleWarps = 1, kSampleBlocks = 152 * 64;
 constexpr int kScanThreads = 256, kScanRounds = 8, kScanTile = kScanThreads * kScanRounds;
 constexpr int kMaxBlocks = 152 * 8;  // grid cap of the grid-stride kernels (their partial sums)
 constexpr int kRedCols = 2 * 64 + 1;  // dw3 | db2 | db3 partials of the softmax kernel
+constexpr int kRedChunks = 32;        // chunks of the column sums' first step
 constexpr int kTile = 1024, kRowThreads = 512;  // row-gradient tiles (id occurrences) and their blocks
 constexpr unsigned long long kNoKey = ~0ull;
 
@@ -80,7 +84,7 @@ bool follow(cudaStream_t to, cudaStream_t from) {
 
 struct Layout {
   size_t boff, soff, roff, tsum, samp, zb, dab, part1, part2, gbag, okey, osrc, w1b, w2b, w1t, w2t, X, S, G1, H1, H2, dH2,
-      dH1, dX, dS, XT, H1T, dH2T, dH1T, M1, split, total;
+      dH1, dX, dS, XT, H1T, dH2T, dH1T, M1, split, red, total;
 };
 
 // Every buffer is sized for fp32 elements, so the layout does not depend on
@@ -101,7 +105,7 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
   L.samp = take(P * 4);
   L.zb = take(P * 4);
   L.dab = take(P * 4);
-  L.part1 = take(size_t(kMaxBlocks) * kRedCols * 4);
+  L.part1 = take(size_t(kSampleBlocks) * kRedCols * 4);
   {
     // db1's partial sums: a row per block of the fp32 mask kernel, or four
     // per 128-position tile from the bf16 products' mask epilogue
@@ -140,6 +144,7 @@ Layout layout(long long B, long long NV, long long Pc, int F, int D) {
     const size_t m = w1 > w2 ? w1 : w2;
     L.split = take((m > both ? m : both) * 4);
   }
+  L.red = take(size_t(kRedChunks) * (kRedCols + kN1) * 4);  // the column sums' chunk sums
   L.total = o;
   return L;
 }
@@ -332,8 +337,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply_kernel(const ScanJobs
 }
 
 // Column sums over the rows of [rows, cols] fp32 partial-sum arrays, in a
-// fixed order, one block per column: blocks [0, c0) sum part0 into dw3 | db2
-// | db3, the blocks after them (when part1 is given) part1 into db1.
+// fixed order: part0 ([rows0, kRedCols]) into dw3 | db2 | db3 and, when given,
+// part1 ([rows1, kN1]) into db1. Two steps: chunk sums (reduce_chunks_kernel)
+// and then one block per column over the chunks (reduce_cols_kernel).
 struct RedJobs {
   const float* part0;
   int rows0;
@@ -341,6 +347,35 @@ struct RedJobs {
   int rows1;
   float *dw3, *db2, *db3, *db1;
 };
+// Step 1: block (group g, chunk k) sums 32 columns of rows [k rows / 32,
+// (k + 1) rows / 32), eight rows at a time (each warp reads a row's 128
+// bytes), and writes the chunk's sums to row k of out0 (part0's columns) or
+// out1 (part1's). Blocks [0, 5) x 32 take part0, the rest part1.
+__global__ void __launch_bounds__(256) reduce_chunks_kernel(const RedJobs r, float* __restrict__ out0,
+                                                             float* __restrict__ out1) {
+  constexpr int G0 = (kRedCols + 31) / 32;
+  __shared__ float sh[8][33];
+  const bool first = int(blockIdx.x) < G0;
+  const int g = first ? int(blockIdx.x) : int(blockIdx.x) - G0;
+  const float* part = first ? r.part0 : r.part1;
+  const int rows = first ? r.rows0 : r.rows1, cols = first ? kRedCols : kN1;
+  float* out = first ? out0 : out1;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5, c = g * 32 + tx, k = blockIdx.y;
+  const long long r0 = (long long)rows * k / kRedChunks, r1 = (long long)rows * (k + 1) / kRedChunks;
+  float v = 0.f;
+  if (c < cols) {
+#pragma unroll 8
+    for (long long i = r0 + ty; i < r1; i += 8) v += part[i * cols + c];
+  }
+  sh[ty][tx] = v;
+  __syncthreads();
+  if (ty == 0 && c < cols) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += sh[w][tx];
+    out[(long long)k * cols + c] = t;
+  }
+}
 __global__ void __launch_bounds__(256) reduce_cols_kernel(const RedJobs r) {
   __shared__ float sh[256];
   const bool first = int(blockIdx.x) < kRedCols;
@@ -401,7 +436,7 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const 
 // [q, s, q - s, q * s] (the MLP operand type) and the occurrence keys of its
 // three sequence ids. Rows past the valid count are zeroed.
 template <class T>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
+__global__ void __launch_bounds__(kSampleWarps * 32, 32 / kSampleWarps) gather_kernel(
     const Params p, const float* __restrict__ pooled, const long long* __restrict__ soff,
     const long long* __restrict__ roff, int* samp, T* X, float* S, long long Pc, unsigned long long* __restrict__ okey,
     long long* __restrict__ osrc) {
@@ -409,8 +444,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) gather_kernel(
   const int lane = threadIdx.x & 31;
   const long long P = min(soff[p.B], Pc);
   int flags = (soff[p.B] > Pc && blockIdx.x == 0 && threadIdx.x == 0) ? DSF_FLAG_COUNT : 0;
-  const int nwarps = gridDim.x * kWarpsPerBlock;
-  for (int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); b < p.B; b += nwarps) {
+  const int nwarps = gridDim.x * kSampleWarps;
+  for (int b = blockIdx.x * kSampleWarps + (threadIdx.x >> 5); b < p.B; b += nwarps) {
     const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
     for (long long pos = p0 + lane; pos < p1; pos += 32) {
       T* x = X + pos * K1;
@@ -530,26 +565,26 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One warp per sample: softmax and score backward over its positions. z and
-// da = ddin.s take one lane per position; dH2, dS and the sums of dw3, db2,
-// db3 take one position per step with the lanes over dimensions (steps are
-// independent). Writes each block's partial sums (dw3 | db2 | db3); rows
-// of dH2 past the valid count are zeroed.
+// One warp per sample (and per block, as in the gather): softmax and score
+// backward over the sample's positions. z and da = ddin.s take one lane per
+// position; dH2, dS and the sums of dw3, db2, db3 take one position per step
+// with the lanes over dimensions (steps are independent). Writes each
+// block's partial sums (dw3 | db2 | db3) as a row; rows of dH2 past the valid
+// count are zeroed.
 template <class T>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
+__global__ void __launch_bounds__(32, 32) softmax_bwd_kernel(
     const Params p, const long long* __restrict__ soff, const float* __restrict__ H2, const float* __restrict__ S,
     const float* __restrict__ ddin, const float* __restrict__ b2, const float* __restrict__ w3,
     const float* __restrict__ b3, float* __restrict__ zb, float* __restrict__ dab, T* __restrict__ dH2,
     float* __restrict__ dS, float* __restrict__ part, long long Pc) {
-  __shared__ float red[kWarpsPerBlock][kRedCols];
   __shared__ float sw3[kN2], sb2[kN2];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x;
   const int Q = 3 * p.D;
-  for (int i = threadIdx.x; i < kN2; i += blockDim.x) sw3[i] = w3[i], sb2[i] = b2[i];
-  __syncthreads();
+  for (int i = lane; i < kN2; i += 32) sw3[i] = w3[i], sb2[i] = b2[i];
+  __syncwarp();
   const float bb3 = __ldg(b3);
   float acc_w3[2] = {0.f, 0.f}, acc_b2[2] = {0.f, 0.f}, acc_b3 = 0.f;
-  for (int b = blockIdx.x * kWarpsPerBlock + warp; b < p.B; b += gridDim.x * kWarpsPerBlock) {
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
     const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
     if (p1 <= p0) continue;
     const float* dd = ddin + (long long)b * Q;
@@ -613,18 +648,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) softmax_bwd_kernel(
       }
     }
   }
-  red[warp][lane] = acc_w3[0];
-  red[warp][lane + 32] = acc_w3[1];
-  red[warp][lane + 64] = acc_b2[0];
-  red[warp][lane + 96] = acc_b2[1];
-  if (lane == 0) red[warp][2 * kN2] = acc_b3;
-  __syncthreads();
-  for (int i = threadIdx.x; i < kRedCols; i += blockDim.x) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerBlock; ++w) v += red[w][i];
-    part[(long long)blockIdx.x * kRedCols + i] = v;
-  }
+  float* row = part + (long long)blockIdx.x * kRedCols;
+  row[lane] = acc_w3[0];
+  row[lane + 32] = acc_w3[1];
+  row[lane + 64] = acc_b2[0];
+  row[lane + 96] = acc_b2[1];
+  if (lane == 0) row[2 * kN2] = acc_b3;
   // rows past the valid count: zero gradient
   const long long P = min(soff[p.B], Pc);
   for (long long i = P * kN2 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < Pc * kN2;
@@ -663,16 +692,16 @@ __device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4
 // time so the dq shares stay in registers. (The occurrence keys come from the
 // gather and from kjt_keys_kernel.)
 constexpr int kPG = 4;
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) dsdq_kernel(
+__global__ void __launch_bounds__(kSampleWarps * 32, 32 / kSampleWarps) dsdq_kernel(
     const Params p, const long long* __restrict__ boff, const long long* __restrict__ soff,
     const long long* __restrict__ roff, long long Pc, const float* __restrict__ pooled,
     const float* __restrict__ dpooled, const float* __restrict__ dX, const float* __restrict__ S,
     float* __restrict__ dS, float* __restrict__ gbag, const float* __restrict__ dqc) {
-  __shared__ float dqs[kWarpsPerBlock][3 * 64];
+  __shared__ float dqs[kSampleWarps][3 * 64];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int D = p.D, Q = 3 * D, K1 = 4 * Q, FD = p.F * D, nc = Q / 4;
   int flags = 0;
-  for (int b = blockIdx.x * kWarpsPerBlock + warp; b < p.B; b += gridDim.x * kWarpsPerBlock) {
+  for (int b = blockIdx.x * kSampleWarps + warp; b < p.B; b += gridDim.x * kSampleWarps) {
     const long long p0 = min(soff[b], Pc), p1 = min(soff[b + 1], Pc);
     const float* qrow = pooled + (long long)b * FD;
     for (int g0 = 0; g0 < nc; g0 += kPG) {
@@ -951,6 +980,20 @@ int grid_for(long long n, int threads, int cap = 152 * 16) {
   return int(g);
 }
 
+// The column sums of the partial-sum arrays (two launches on st; red holds
+// the chunk sums).
+bool col_sums(const RedJobs& r, float* red, cudaStream_t st) {
+  float *out0 = red, *out1 = red + size_t(kRedChunks) * kRedCols;
+  const int g = (kRedCols + 31) / 32 + (r.part1 ? kN1 / 32 : 0);
+  reduce_chunks_kernel<<<dim3(g, kRedChunks), 256, 0, st>>>(r, out0, out1);
+  RedJobs c = r;
+  c.part0 = out0;
+  c.rows0 = kRedChunks;
+  if (r.part1) c.part1 = out1, c.rows1 = kRedChunks;
+  reduce_cols_kernel<<<kRedCols + (r.part1 ? kN1 : 0), 256, 0, st>>>(c);
+  return cudaGetLastError() == cudaSuccess;
+}
+
 // Storage of table f: hash-table tables share the first such table's index.
 int storage_of(const dsf_tables* t, int f) {
   if (!hashed(t, f)) return f;
@@ -1091,6 +1134,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
   long long* osrc = reinterpret_cast<long long*>(w + L.osrc);
   long long* tsum = reinterpret_cast<long long*>(w + L.tsum);
   float* part1 = reinterpret_cast<float*>(w + L.part1);
+  float* red = reinterpret_cast<float*>(w + L.red);
   float* part2 = reinterpret_cast<float*>(w + L.part2);
   // the side stream (s2) takes the KJT offsets and the weight packing; the
   // call's stream joins it before the first product
@@ -1186,12 +1230,12 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     return ok && gemm::reduce(part, (long long)M * N, splits, N, D, N, M, N, s);
   };
   if (Pc > 0) {
-    const int gb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
+    const int gb = grid_for(B, kSampleWarps, kSampleBlocks);
     if (bf)
-      gather_kernel<__nv_bfloat16><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp,
+      gather_kernel<__nv_bfloat16><<<gb, kSampleWarps * 32, 0, s>>>(p, pooled_dev, soff, roff, samp,
                                                                       static_cast<__nv_bfloat16*>(X), S, Pc, okey, osrc);
     else
-      gather_kernel<float><<<gb, kWarpsPerBlock * 32, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
+      gather_kernel<float><<<gb, kSampleWarps * 32, 0, s>>>(p, pooled_dev, soff, roff, samp, static_cast<float*>(X),
                                                               S, Pc, okey, osrc);
     if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   }
@@ -1216,13 +1260,13 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     }
     if (!mm(H1, kN1, W2, kN1, H2, kN2, Pc, kN2, kN1, 1)) return DSF_ECUDA;
   }
-  const int sb = grid_for(B, kWarpsPerBlock, kMaxBlocks);
+  const int smb = grid_for(B, 1, kSampleBlocks);  // (one warp per block)
   if (bf)
-    softmax_bwd_kernel<__nv_bfloat16><<<sb, kWarpsPerBlock * 32, 0, s>>>(
-        p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3, zb, dab, static_cast<__nv_bfloat16*>(dH2), dS, part1, Pc);
+    softmax_bwd_kernel<__nv_bfloat16><<<smb, 32, 0, s>>>(p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3, zb, dab,
+                                                         static_cast<__nv_bfloat16*>(dH2), dS, part1, Pc);
   else
-    softmax_bwd_kernel<float><<<sb, kWarpsPerBlock * 32, 0, s>>>(p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3,
-                                                                 zb, dab, static_cast<float*>(dH2), dS, part1, Pc);
+    softmax_bwd_kernel<float><<<smb, 32, 0, s>>>(p, soff, H2, S, ddin_dev, mlp->b2, mlp->w3, mlp->b3, zb, dab,
+                                                 static_cast<float*>(dH2), dS, part1, Pc);
   if (cudaGetLastError() != cudaSuccess) return DSF_ECUDA;
   if (Pc > 0) {
     // dh1 = (dh2 W2) [h1 > 0] and db1's partial sums (in bf16 mode inside the
@@ -1246,8 +1290,7 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
     }
     // the bias-gradient columns beside the remaining steps (s2)
     if (!follow(s2, s)) return DSF_ECUDA;
-    reduce_cols_kernel<<<kRedCols + kN1, 256, 0, s2>>>(
-        RedJobs{part1, sb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1});
+    if (!col_sums(RedJobs{part1, smb, part2, rb, mg->dw3, mg->db2, mg->db3, mg->db1}, red, s2)) return DSF_ECUDA;
     // bf16: the weight gradients (their operands are all written by now) on
     // s2 as well, beside dx, dq/ds and the row gradients
     if (bf) {
@@ -1309,10 +1352,10 @@ extern "C" int din_sparse_bwd(const dsf_tables* tables, const dsf_kjt* kjt, cons
         cudaMemsetAsync(mg->dW2, 0, size_t(kN2) * kN1 * 4, s) != cudaSuccess ||
         cudaMemsetAsync(mg->db1, 0, size_t(kN1) * 4, s) != cudaSuccess)
       return DSF_ECUDA;
-    reduce_cols_kernel<<<kRedCols, 256, 0, s>>>(RedJobs{part1, sb, nullptr, 0, mg->dw3, mg->db2, mg->db3, nullptr});
+    if (!col_sums(RedJobs{part1, smb, nullptr, 0, mg->dw3, mg->db2, mg->db3, nullptr}, red, s)) return DSF_ECUDA;
   }
   {
-    dsdq_kernel<<<sb, kWarpsPerBlock * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS, gbag,
+    dsdq_kernel<<<grid_for(B, kSampleWarps, kSampleBlocks), kSampleWarps * 32, 0, s>>>(p, boff, soff, roff, Pc, pooled_dev, dpooled_dev, dX, S, dS, gbag,
                                                    fuse_dsdq && Pc > 0 ? dX : nullptr);
     const long long nocc = kjt->n_values + 3 * Pc;
     if (nocc > 0)
